@@ -1,0 +1,524 @@
+"""Benchmark of the decode-attention hot path on one B300 (replicas on N).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one pass of the absorbed-MLA pipeline over one batch of the
+DeepSeek-V3-like decode workload (b=32, h=128, d=128, k=512, p=64, t=4096,
+s=1): query absorption GEMM, tcgen05 latent attention (+ split combine) and
+the W_uv projection. Inputs are seeded synthetic tensors already resident in
+HBM; three full input sets (about 555 MB, far above the 126 MB L2) rotate
+between steps so no step reads another step's data from L2. Steps are
+replayed from CUDA graphs captured once per input set.
+
+Printed: one JSON line (rank 0). `value` is microseconds per pipeline call of
+the whole job (the timed time divided by the calls all ranks made), so lower
+is better. `roofline` is for the latent-attention call (kernel + combine),
+timed in its own loop of graph replays with CUDA events on its stream.
+`e2e` times the public Python API with the step's queries copied in from
+pinned host memory and the outputs copied back. `cpu_baseline` times the
+fp64 oracle on a bounded sample on the host cores.
+
+--impl reference runs that oracle as the reference arm (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode attn µs/call, TFLOP/s, HBM GB/s and % roofline (MLA h128 k512 t4096)"
+UNIT = "us/call"
+WORKLOAD = "mla_dsv3"
+FALLBACK_HBM_GBS = 6400.0
+FALLBACK_BF16_TFLOPS = 1800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the grouped-head and s-sweep side measurements")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, None, "fallback"
+
+
+class ClockSampler:
+    """Samples the SM clock and clock-event reasons through NVML in a thread."""
+
+    def __init__(self, index: int, period_s: float = 0.01):
+        self.index, self.period = index, period_s
+        self.samples, self.reasons = [], set()
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._t = None
+        self.ok = False
+
+    def __enter__(self):
+        try:
+            import pynvml as nv
+
+            nv.nvmlInit()
+            self.nv = nv
+            self.h = nv.nvmlDeviceGetHandleByIndex(self.index)
+            self.max_mhz = nv.nvmlDeviceGetMaxClockInfo(self.h, nv.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:
+            return self
+        names = {
+            "hw_slowdown": getattr(self.nv, "nvmlClocksEventReasonHwSlowdown", 0x8),
+            "sw_thermal_slowdown": getattr(self.nv, "nvmlClocksEventReasonSwThermalSlowdown", 0x20),
+            "hw_thermal_slowdown": getattr(self.nv, "nvmlClocksEventReasonHwThermalSlowdown", 0x40),
+            "sw_power_cap": getattr(self.nv, "nvmlClocksEventReasonSwPowerCap", 0x4),
+            "hw_power_brake_slowdown": getattr(self.nv, "nvmlClocksEventReasonHwPowerBrakeSlowdown", 0x80),
+        }
+
+        def run():
+            while not self._stop.is_set():
+                self._sample(names)
+                time.sleep(self.period)
+
+        self._sample(names)
+        self._t = threading.Thread(target=run, daemon=True)
+        self._t.start()
+        return self
+
+    def _sample(self, names):
+        try:
+            self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+            r = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+            for n, bit in names.items():
+                if r & bit:
+                    self.reasons.add(n)
+        except Exception:
+            pass
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            if self._t:
+                self._t.join()
+            self._sample({})
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples), "source": "nvml"}
+
+
+def cost_numbers(wl):
+    from oracle import cost
+
+    L = wl.seqlens()
+    f = cost.mla_flops_exact(wl.heads, wl.k, wl.p, L, wl.s)
+    by = cost.mla_bytes_exact(wl.heads, wl.k, wl.p, L, wl.s)
+    fa = cost.proj_flops(wl.b, wl.heads, wl.s, wl.d, wl.k)
+    ba = cost.proj_bytes(wl.b, wl.heads, wl.s, wl.d, wl.k)
+    return f, by, fa, ba
+
+
+def cpu_baseline(wl, seconds_target=15.0):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload:
+    whole sequences (all heads) of the absorbed pipeline until about
+    `seconds_target` seconds of CPU work; scaled to a full call."""
+    import numpy as np
+    import torch
+
+    from decode_attention_18_b300 import workloads as W
+    from oracle import attention as A
+
+    inp = W.make_mla(wl.b, wl.heads, wl.d, wl.k, wl.p, wl.s, wl.seqlens(), seed=wl.seed, device="cpu")
+    f = lambda t: t.float().double().numpy()  # noqa: E731
+    wuk, wuv = f(inp.w_uk), f(inp.w_uv)
+    n, t_total = 0, 0.0
+    while t_total < seconds_target and n < wl.b:
+        i = n
+        zs, kp = [f(inp.seq_rows(i, "z"))], [f(inp.seq_rows(i, "kpe"))]
+        qn, qp = f(inp.q_nope[i:i + 1]), f(inp.q_pe[i:i + 1])
+        t0 = time.perf_counter()
+        A.mla_absorbed_ref(qn, qp, zs, kp, wuk, wuv, [inp.seqlens[i]], inp.scale)
+        t_total += time.perf_counter() - t0
+        n += 1
+    cores = torch.get_num_threads()
+    try:
+        from threadpoolctl import threadpool_info
+
+        blas = [x.get("num_threads") for x in threadpool_info() if x.get("user_api") == "blas"]
+        if blas:
+            cores = max(blas)
+    except Exception:
+        pass
+    us_per_call = t_total / n * wl.b * 1e6
+    return {"value": us_per_call, "unit": UNIT, "cores": int(cores), "kind": "oracle",
+            "sample": f"{n} of {wl.b} sequences (all {wl.heads} heads, absorb + latent attention + W_uv "
+                      f"in float64), {t_total:.1f} s of CPU time, scaled x{wl.b / n:.1f} to one call"}
+
+
+def traffic_record():
+    """DRAM bytes of the latent kernel from a committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "mla_latent_dsv3_traffic.json")
+    src = os.path.join(ROOT, "decode_attention_18_b300", "csrc", "mla_decode.cu")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path))
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if rec.get("source_sha256_16") != h:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import numpy as np
+
+    from decode_attention_18_b300 import workloads as W
+    from oracle import attention as A
+
+    wl = W.WORKLOADS[WORKLOAD]
+    inp = W.make_mla(wl.b, wl.heads, wl.d, wl.k, wl.p, wl.s, wl.seqlens(), seed=wl.seed, device="cpu")
+    f = lambda t: t.float().double().numpy()  # noqa: E731
+    wuk, wuv = f(inp.w_uk), f(inp.w_uv)
+    seqs = [(f(inp.seq_rows(i, "z")), f(inp.seq_rows(i, "kpe"))) for i in range(2)]
+
+    def step(k):
+        i = k % 2
+        j = ((k // 2) * heads_per_step) % (wl.heads - heads_per_step + 1)
+        hsl = slice(j, j + heads_per_step)
+        A.mla_absorbed_ref(f(inp.q_nope[i:i + 1, hsl]), f(inp.q_pe[i:i + 1, hsl]), [seqs[i][0]], [seqs[i][1]],
+                           wuk[hsl], wuv[hsl], [inp.seqlens[i]], inp.scale)
+
+    heads_per_step = 1
+    t0 = time.perf_counter()
+    for k in range(3):
+        step(k)
+    per_head = (time.perf_counter() - t0) / 3
+    budget = 90.0
+    heads_per_step = max(1, min(wl.heads, int(budget / max(1, args.steps) / per_head)))
+    for k in range(args.warmup):
+        step(k)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        step(k)
+    dt = time.perf_counter() - t0
+    sample_units = heads_per_step
+    full_units = wl.b * wl.heads
+    value = dt / args.steps * (full_units / sample_units) * 1e6
+    import torch
+
+    cores = torch.get_num_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "step_sample": f"{heads_per_step} head(s) of one sequence per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": int(cores), "kind": "oracle",
+                         "sample": f"{heads_per_step} of {full_units} (sequence, head) pairs per step, "
+                                   f"scaled x{full_units / sample_units:.0f} to one call"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    import decode_attention_18_b300 as da
+    from decode_attention_18_b300 import build as dabuild
+    from decode_attention_18_b300 import workloads as W
+
+    if not os.path.exists(dabuild.LIB):
+        raise RuntimeError("libdecattn.so is not built (run: python -m decode_attention_18_b300.build)")
+    wl = W.WORKLOADS[WORKLOAD]
+    seqlens = wl.seqlens()
+    L = max(seqlens)
+    NBUF = 3
+    sets = [W.make_mla(wl.b, wl.heads, wl.d, wl.k, wl.p, wl.s, seqlens, seed=wl.seed + 17 * r, device=dev)
+            for r in range(NBUF)]
+    sl = torch.tensor(seqlens, dtype=torch.int32, device=dev)
+    scale = sets[0].scale
+    ws_bytes = da.ops.load().mla_decode_workspace_size(wl.b, wl.s, wl.heads, wl.k, L)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    outs = []
+    for s_ in sets:
+        outs.append(dict(
+            qz=torch.empty((wl.b, wl.heads, wl.s, wl.k), dtype=torch.bfloat16, device=dev),
+            o_lat=torch.empty((wl.b, wl.heads, wl.s, wl.k), dtype=torch.bfloat16, device=dev),
+            lse=torch.empty((wl.b, wl.heads, wl.s), dtype=torch.float32, device=dev),
+            out=torch.empty((wl.b, wl.heads, wl.s, wl.d), dtype=torch.bfloat16, device=dev)))
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(r, parts=("absorb", "decode", "proj")):
+        s_, o = sets[r], outs[r]
+        if "absorb" in parts:
+            da.mla_absorb_q(s_.q_nope, s_.w_uk, sl, out=o["qz"], stream=stream)
+        if "decode" in parts:
+            da.mla_decode(o["qz"], s_.q_pe, s_.z, s_.k_pe, sl, scale=scale, max_seqlen=L, out=o["o_lat"],
+                          lse=o["lse"], workspace=ws, stream=stream)
+        if "proj" in parts:
+            da.mla_out_proj(o["o_lat"], s_.w_uv, sl, out=o["out"], stream=stream)
+
+    # warm (first-call set-up happens outside capture), then capture one graph per input set
+    with torch.cuda.stream(stream):
+        for r in range(NBUF):
+            step(r)
+    torch.cuda.synchronize()
+    nsplit = da.last_num_splits()
+    assert da.check_errors(stream) == 0
+    graphs, dgraphs = [], []
+    for r in range(NBUF):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(r)
+        graphs.append(g)
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, stream=stream):
+            step(r, ("decode",))
+        dgraphs.append(g2)
+    launches_per_step = 3 + (1 if nsplit > 1 else 0)
+
+    def timed(gs, k_steps, w_steps):
+        with torch.cuda.stream(stream):
+            for k in range(w_steps):
+                gs[k % NBUF].replay()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for k in range(k_steps):
+                gs[k % NBUF].replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    with ClockSampler(local) as clk:
+        total_ms = timed(graphs, args.steps, args.warmup)
+    dec_steps = max(args.steps, 500)
+    dec_ms = timed(dgraphs, dec_steps, max(3, args.warmup // 4))
+    assert da.check_errors(stream) == 0
+
+    ms_per_step = total_ms / args.steps
+    value = total_ms * 1e3 / (args.steps * world)  # us per call over the whole job
+
+    # end to end through the public API: queries in from pinned host memory, outputs back
+    e2e_steps = min(args.steps, 300)
+    hq_nope = [s_.q_nope.cpu().pin_memory() for s_ in sets]
+    hq_pe = [s_.q_pe.cpu().pin_memory() for s_ in sets]
+    hsl = torch.tensor(seqlens, dtype=torch.int32).pin_memory()
+    hout = torch.empty((wl.b, wl.heads, wl.s, wl.d), dtype=torch.bfloat16).pin_memory()
+    hlse = torch.empty((wl.b, wl.heads, wl.s), dtype=torch.float32).pin_memory()
+
+    def e2e_step(r):
+        s_, o = sets[r], outs[r]
+        s_.q_nope.copy_(hq_nope[r], non_blocking=True)
+        s_.q_pe.copy_(hq_pe[r], non_blocking=True)
+        sl.copy_(hsl, non_blocking=True)
+        step(r)
+        hout.copy_(o["out"], non_blocking=True)
+        hlse.copy_(o["lse"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for k in range(5):
+            e2e_step(k % NBUF)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for k in range(e2e_steps):
+            e2e_step(k % NBUF)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = sum(t.numel() * t.element_size() for t in (hq_nope[0], hq_pe[0], hsl))
+    d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
+
+    f_core, b_core, f_proj, b_proj = cost_numbers(wl)
+    hbm, tfl, tfl_sus, peak_src = peaks()
+    dec_s = dec_ms / dec_steps * 1e-3
+    t_roof = max(f_core / (tfl * 1e12), b_core / (hbm * 1e9))
+    bound = "hbm" if b_core / (hbm * 1e9) >= f_core / (tfl * 1e12) else "tensor"
+    if bound == "hbm":
+        achieved, peak, unit = b_core / dec_s / 1e9, hbm, "GB/s"
+    else:
+        achieved, peak, unit = f_core / dec_s / 1e12, tfl, "TFLOP/s"
+    step_s = ms_per_step * 1e-3
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "global_batch": wl.b * world, "seq_len": wl.t, "new_tokens": wl.s,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"{NBUF} rotating input sets of {sum(t.numel() * t.element_size() for t in (sets[0].z, sets[0].k_pe, sets[0].w_uk, sets[0].w_uv, sets[0].q_nope, sets[0].q_pe)) / 1e6:.0f} MB each (> 126 MB L2)",
+                   "num_splits": nsplit, "graphs": "one CUDA graph per input set"},
+        "step_breakdown": {
+            "pipeline_us": ms_per_step * 1e3,
+            "latent_call_us": dec_s * 1e6,
+            "pipeline_tflops": (f_core + 2 * f_proj) / step_s / 1e12,
+            "pipeline_hbm_gbs": (b_core + 2 * b_proj) / step_s / 1e9,
+            "latent_tflops": f_core / dec_s / 1e12,
+            "latent_hbm_gbs": b_core / dec_s / 1e9,
+            "latent_roofline_us": t_roof * 1e6,
+            "latent_frac_of_roofline": t_roof / dec_s,
+            "latent_algorithmic": {"flops": f_core, "bytes": b_core, "ai": f_core / b_core},
+        },
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                     "traffic": traffic_record(), "kernel": "mla_decode call (tcgen05 latent kernel + combine)",
+                     "peak_source": peak_src,
+                     "note": "frac of measured peak; the call's roofline time is max(FLOPs/tensor peak, bytes/HBM peak)"},
+        "e2e": {"value": e2e_ms * 1e3 / (e2e_steps * world), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    if rank == 0 and not args.no_extras:
+        line["extras"] = extras(dev, stream, hbm, tfl)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def extras(dev, stream, hbm, tfl):
+    """Side measurements (not the headline): the grouped-head workloads and the
+    MLA s-sweep, each as us per call with its roofline fraction."""
+    import torch
+
+    import decode_attention_18_b300 as da
+    from decode_attention_18_b300 import workloads as W
+    from oracle import cost
+
+    res = {}
+
+    def time_calls(fn, n=30, w=5):
+        with torch.cuda.stream(stream):
+            for _ in range(w):
+                fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(n):
+                fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n * 1e-3
+
+    for name in ("gqa_64_8", "gqa_paged_hkv24", "gqa_paged_hkv4", "gqa_paged_hkv1"):
+        wl = W.WORKLOADS[name]
+        seqlens = wl.seqlens()
+        nb = 2
+        qs = []
+        for r in range(nb):
+            q, c = W.make_gqa(wl.b, wl.heads, wl.hkv, wl.d, wl.s, seqlens, paged=wl.paged, seed=wl.seed + r, device=dev)
+            qs.append((q, c))
+        sl = torch.tensor(seqlens, dtype=torch.int32, device=dev)
+        outs = [torch.empty_like(q) for q, _ in qs]
+        lses = [torch.empty(q.shape[:3], dtype=torch.float32, device=dev) for q, _ in qs]
+        wsb = da.ops.load().gqa_decode_workspace_size(wl.b, wl.s, wl.heads, wl.hkv, wl.d, max(seqlens))
+        ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+        it = [0]
+
+        def fn():
+            r = it[0] % nb
+            it[0] += 1
+            q, c = qs[r]
+            da.gqa_decode(q, c.k, c.v, sl, max_seqlen=max(seqlens), block_table=c.block_table if wl.paged else None,
+                          out=outs[r], lse=lses[r], workspace=ws, stream=stream)
+
+        t = time_calls(fn)
+        by = cost.gqa_bytes_exact(wl.heads, wl.hkv, wl.d, seqlens, wl.s)
+        fl = cost.gqa_flops_exact(wl.heads, wl.d, seqlens, wl.s)
+        res[name] = {"us": t * 1e6, "hbm_gbs": by / t / 1e9, "frac_hbm": by / t / 1e9 / hbm,
+                     "tflops": fl / t / 1e12, "bytes": by, "num_splits": da.last_num_splits(),
+                     "l2": f"{nb} rotating caches of {by / 1e6:.0f} MB"}
+        del qs, outs, lses, ws
+        torch.cuda.empty_cache()
+
+    for s in (1, 2, 4, 8, 16, 32):
+        wl = W.WORKLOADS["mla_dsv3"] if s == 1 else W.WORKLOADS[f"mla_mtp_s{s}"]
+        seqlens = wl.seqlens()
+        inp = [W.make_mla(wl.b, wl.heads, wl.d, wl.k, wl.p, wl.s, seqlens, seed=wl.seed + r, device=dev)
+               for r in range(2)]
+        sl = torch.tensor(seqlens, dtype=torch.int32, device=dev)
+        qzs = [da.mla_absorb_q(x.q_nope, x.w_uk, sl) for x in inp]
+        o = [torch.empty_like(q) for q in qzs]
+        lse = [torch.empty(q.shape[:3], dtype=torch.float32, device=dev) for q in qzs]
+        wsb = da.ops.load().mla_decode_workspace_size(wl.b, wl.s, wl.heads, wl.k, max(seqlens))
+        ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+        it = [0]
+
+        def fn():
+            r = it[0] % 2
+            it[0] += 1
+            da.mla_decode(qzs[r], inp[r].q_pe, inp[r].z, inp[r].k_pe, sl, scale=inp[r].scale,
+                          max_seqlen=max(seqlens), out=o[r], lse=lse[r], workspace=ws, stream=stream)
+
+        t = time_calls(fn, n=20)
+        fl = cost.mla_flops_exact(wl.heads, wl.k, wl.p, seqlens, wl.s)
+        by = cost.mla_bytes_exact(wl.heads, wl.k, wl.p, seqlens, wl.s)
+        troof = max(fl / (tfl * 1e12), by / (hbm * 1e9))
+        res[f"mla_s{s}"] = {"us": t * 1e6, "tflops": fl / t / 1e12, "hbm_gbs": by / t / 1e9, "ai": fl / by,
+                            "roofline_us": troof * 1e6, "frac_roofline": troof / t,
+                            "bound": "tensor" if fl / (tfl * 1e12) > by / (hbm * 1e9) else "hbm",
+                            "num_splits": da.last_num_splits()}
+        del inp, qzs, o, lse, ws
+        torch.cuda.empty_cache()
+    return res
+
+
+if __name__ == "__main__":
+    sys.exit(main())

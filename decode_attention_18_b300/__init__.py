@@ -1,0 +1,21 @@
+"""B300-native (sm_103a) decode attention: grouped-head (MHA / GQA / MQA)
+split-KV decode and absorbed latent MLA, behind the C ABI of
+include/decattn.h. The native library is loaded on first use."""
+from ._native import DecAttnError, LIB_PATH, SYMBOLS  # noqa: F401
+from .ops import (  # noqa: F401
+    check_errors,
+    gqa_decode,
+    last_num_splits,
+    mla_absorb_q,
+    mla_decode,
+    mla_forward,
+    mla_out_proj,
+    set_forced_splits,
+    set_wait_limit_ns,
+    test_force_timeout,
+)
+
+__all__ = [
+    "gqa_decode", "mla_absorb_q", "mla_decode", "mla_out_proj", "mla_forward", "check_errors",
+    "set_forced_splits", "last_num_splits", "set_wait_limit_ns", "test_force_timeout", "DecAttnError",
+]

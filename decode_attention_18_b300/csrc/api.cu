@@ -1,0 +1,331 @@
+// C ABI of the decode-attention library: argument checks, the split planner,
+// workspace sizing, the device error word and the launches. Every entry point
+// returns a status and enqueues on the caller's stream; nothing here
+// allocates device memory or synchronises (except decattn_check_errors).
+#include <atomic>
+#include <climits>
+#include <cstdint>
+#include <mutex>
+
+#include "decattn.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace decattn {
+namespace {
+
+// device error word (bit flags set by the kernels, read by decattn_check_errors)
+__device__ unsigned g_err_word;
+
+struct DeviceState {
+  bool ready = false;
+  unsigned* err = nullptr;
+  int sms = 0;
+};
+constexpr int kMaxDevices = 64;
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+std::atomic<unsigned long long> g_wait_ns{0};
+std::atomic<int> g_forced_splits{0};
+std::atomic<int> g_last_splits{0};
+std::atomic<int> g_test_timeout{0};
+
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
+constexpr int kChunkAlign = 64;                                // chunks are whole 64-key pages
+
+// Per-device set-up on first use: the error word's device address and the SM count.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DECATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_err_word) != cudaSuccess) return DECATTN_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      return DECATTN_ERR_CUDA;
+    st.err = static_cast<unsigned*>(addr);
+    st.sms = sms;
+    st.ready = true;
+  }
+  *out = &st;
+  return DECATTN_OK;
+}
+
+unsigned long long wait_limit() {
+  const unsigned long long w = g_wait_ns.load();
+  return w ? w : kDefaultWaitNs;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+struct Plan {
+  int nsplit;
+  int chunk;
+};
+
+// Split planner: pick the number of context chunks so that the CTAs fill the
+// SMs in whole waves. base = CTAs per chunk index (sequences x heads x row
+// blocks), slots = CTAs resident on the whole GPU at once, overhead = fixed
+// cost of a CTA expressed in keys. Cost model: waves x (chunk + overhead).
+Plan plan_splits(long long base, int max_seqlen, long long slots, int overhead_keys) {
+  Plan pl{1, kChunkAlign};
+  const long long L = max_seqlen > 0 ? max_seqlen : 1;
+  const int max_n = (int)ceil_div(L, kChunkAlign);
+  auto chunk_for = [&](int n) { return (int)(ceil_div(ceil_div(L, n), kChunkAlign) * kChunkAlign); };
+  const int forced = g_forced_splits.load();
+  if (forced > 0) {
+    const int n = forced < max_n ? forced : max_n;
+    pl.chunk = chunk_for(n);
+    pl.nsplit = (int)ceil_div(L, pl.chunk);
+    return pl;
+  }
+  double best = 1e300;
+  for (int n = 1; n <= max_n && n <= 1024; ++n) {
+    const int chunk = chunk_for(n);
+    const int ne = (int)ceil_div(L, chunk);
+    if (ne != n) continue;
+    const long long waves = ceil_div(base * ne, slots);
+    const double cost = (double)waves * (chunk + overhead_keys);
+    if (cost < best * 0.999) {
+      best = cost;
+      pl.nsplit = ne;
+      pl.chunk = chunk;
+    }
+  }
+  return pl;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+size_t partial_bytes(long long rows, int nsplit, int width) {
+  if (nsplit <= 1) return 0;
+  return align256((size_t)rows * nsplit * width * sizeof(float)) + align256((size_t)rows * nsplit * sizeof(float));
+}
+
+int check_kv(const decattn_kv& kv, int b, int max_seqlen) {
+  if (kv.paged) {
+    if (!kv.block_table || kv.page_size != 64 || kv.num_pages < 1 || kv.max_pages < 1) return DECATTN_ERR_INVALID_ARG;
+    if ((long long)kv.max_pages * 64 < max_seqlen) return DECATTN_ERR_INVALID_ARG;
+    if ((long long)kv.num_pages * 64 > INT_MAX) return DECATTN_ERR_INVALID_ARG;
+  } else {
+    if (kv.capacity < max_seqlen || kv.capacity < 1) return DECATTN_ERR_INVALID_ARG;
+    if ((long long)b * kv.capacity > INT_MAX) return DECATTN_ERR_INVALID_ARG;
+  }
+  return DECATTN_OK;
+}
+
+// --- grouped-head plan
+Plan gqa_plan(int b, int s, int hq, int hkv, int d, int max_seqlen, int sms) {
+  const int rows = (hq / hkv) * s;
+  const int rpc = gqa_rows_per_cta(rows);
+  const long long base = (long long)b * hkv * ceil_div(rows, rpc);
+  const long long slots = (long long)sms * gqa_ctas_per_sm(d);
+  return plan_splits(base, max_seqlen, slots, 64);
+}
+
+// --- latent MLA plan (one CTA per SM: its shared memory holds the 128-row query tile)
+Plan mla_plan(int b, int s, int h, int k, int max_seqlen, int sms) {
+  const long long base = (long long)b * mla_latent_parts(k) * ceil_div((long long)h * s, 128);
+  return plan_splits(base, max_seqlen, sms, 192);
+}
+
+}  // namespace
+}  // namespace decattn
+
+using namespace decattn;
+
+extern "C" {
+
+const char* decattn_status_string(int status) {
+  switch (status) {
+    case DECATTN_OK: return "ok";
+    case DECATTN_ERR_INVALID_ARG: return "invalid argument";
+    case DECATTN_ERR_UNSUPPORTED: return "unsupported shape (no compiled instance)";
+    case DECATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case DECATTN_ERR_CUDA: return "CUDA runtime error";
+    case DECATTN_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+void decattn_set_wait_limit_ns(unsigned long long ns) { g_wait_ns.store(ns); }
+void decattn_set_forced_splits(int nsplit) { g_forced_splits.store(nsplit > 0 ? nsplit : 0); }
+int decattn_last_num_splits(void) { return g_last_splits.load(); }
+void decattn_test_force_timeout(int on) { g_test_timeout.store(on ? 1 : 0); }
+
+int decattn_check_errors(cudaStream_t stream) {
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return DECATTN_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_err_word, sizeof(word)) != cudaSuccess) return DECATTN_ERR_CUDA;
+  const unsigned zero = 0;
+  if (cudaMemcpyToSymbol(g_err_word, &zero, sizeof(zero)) != cudaSuccess) return DECATTN_ERR_CUDA;
+  if (word & kErrWaitTimeout) return DECATTN_ERR_TIMEOUT;
+  if (word & kErrBadPage) return DECATTN_ERR_INVALID_ARG;
+  return DECATTN_OK;
+}
+
+// ------------------------------------------------------------------ grouped-head
+
+size_t gqa_decode_workspace_size(int b, int s, int hq, int hkv, int d, int max_seqlen) {
+  if (b < 1 || s < 1 || hq < 1 || hkv < 1 || hq % hkv || d < 1) return 0;
+  DeviceState* st = nullptr;
+  if (device_state(&st)) return 0;
+  const Plan pl = gqa_plan(b, s, hq, hkv, d, max_seqlen, st->sms);
+  return partial_bytes((long long)b * hq * s, pl.nsplit, d);
+}
+
+int gqa_decode(const decattn_bf16* q, const decattn_bf16* k, const decattn_bf16* v, decattn_kv kv,
+               const int32_t* seqlens, int max_seqlen, int b, int s, int hq, int hkv, int d, float scale,
+               decattn_bf16* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (b < 0 || s < 1 || s > 32 || hq < 1 || hkv < 1 || hq % hkv || max_seqlen < 0) return DECATTN_ERR_INVALID_ARG;
+  if (b == 0) return DECATTN_OK;
+  if (!q || !k || !v || !seqlens || !out) return DECATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return DECATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return DECATTN_ERR_INVALID_ARG;
+  if (hkv > 65535 || b > 65535) return DECATTN_ERR_INVALID_ARG;
+  if (int rc = check_kv(kv, b, max_seqlen)) return rc;
+  DeviceState* st = nullptr;
+  if (int rc = device_state(&st)) return rc;
+  const Plan pl = gqa_plan(b, s, hq, hkv, d, max_seqlen, st->sms);
+  const long long rows = (long long)b * hq * s;
+  const size_t need = partial_bytes(rows, pl.nsplit, d);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return DECATTN_ERR_WORKSPACE;
+  GqaLaunch a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.seqlens = seqlens;
+  a.block_table = kv.block_table;
+  a.max_pages = kv.max_pages;
+  a.paged = kv.paged;
+  a.capacity = kv.capacity;
+  a.num_pages = kv.num_pages;
+  a.b = b;
+  a.s = s;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.d = d;
+  a.nsplit = pl.nsplit;
+  a.chunk = pl.chunk;
+  a.scale = scale;
+  a.out = out;
+  a.lse = lse;
+  a.ws_o = pl.nsplit > 1 ? static_cast<float*>(workspace) : nullptr;
+  a.ws_lse = pl.nsplit > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                       align256((size_t)rows * pl.nsplit * d * sizeof(float)))
+                           : nullptr;
+  a.err = st->err;
+  g_last_splits.store(pl.nsplit);
+  if (launch_gqa(a, stream) != cudaSuccess) return DECATTN_ERR_CUDA;
+  if (pl.nsplit > 1) {
+    if (launch_combine(a.ws_o, a.ws_lse, seqlens, (int)rows, hq * s, pl.nsplit, pl.chunk, d, out, lse, stream) !=
+        cudaSuccess)
+      return DECATTN_ERR_CUDA;
+  }
+  return DECATTN_OK;
+}
+
+// ------------------------------------------------------------------ MLA
+
+static int check_proj(const void* a, const void* w, const void* c, int b, int s, int h, int kin, int nout) {
+  if (b < 0 || s < 1 || s > 32 || h < 1 || kin < 8 || nout < 8) return DECATTN_ERR_INVALID_ARG;
+  if (!a || !w || !c) return DECATTN_ERR_INVALID_ARG;
+  if (kin % 8 || nout % 8) return DECATTN_ERR_UNSUPPORTED;
+  if (!aligned16(a) || !aligned16(w) || !aligned16(c)) return DECATTN_ERR_INVALID_ARG;
+  if (h > 65535 || (long long)b * s > 65535LL * 64) return DECATTN_ERR_INVALID_ARG;
+  return DECATTN_OK;
+}
+
+int mla_absorb_q(const decattn_bf16* q_nope, const decattn_bf16* w_uk, decattn_bf16* qz, const int32_t* seqlens,
+                 int b, int s, int h, int d, int k, float scale, cudaStream_t stream) {
+  if (int rc = check_proj(q_nope, w_uk, qz, b, s, h, d, k)) return rc;
+  if (b == 0) return DECATTN_OK;
+  DeviceState* st = nullptr;
+  if (int rc = device_state(&st)) return rc;
+  ProjLaunch a{q_nope, w_uk, qz, seqlens, b, s, h, d, k, scale};
+  return launch_proj(a, st->sms, stream) == cudaSuccess ? DECATTN_OK : DECATTN_ERR_CUDA;
+}
+
+int mla_out_proj(const decattn_bf16* o_lat, const decattn_bf16* w_uv, decattn_bf16* out, const int32_t* seqlens,
+                 int b, int s, int h, int k, int d, float scale, cudaStream_t stream) {
+  if (int rc = check_proj(o_lat, w_uv, out, b, s, h, k, d)) return rc;
+  if (b == 0) return DECATTN_OK;
+  DeviceState* st = nullptr;
+  if (int rc = device_state(&st)) return rc;
+  ProjLaunch a{o_lat, w_uv, out, seqlens, b, s, h, k, d, scale};
+  return launch_proj(a, st->sms, stream) == cudaSuccess ? DECATTN_OK : DECATTN_ERR_CUDA;
+}
+
+size_t mla_decode_workspace_size(int b, int s, int h, int k, int max_seqlen) {
+  if (b < 1 || s < 1 || h < 1 || k < 1) return 0;
+  DeviceState* st = nullptr;
+  if (device_state(&st)) return 0;
+  const Plan pl = mla_plan(b, s, h, k, max_seqlen, st->sms);
+  return partial_bytes((long long)b * h * s, pl.nsplit, k);
+}
+
+int mla_decode(const decattn_bf16* qz, const decattn_bf16* q_pe, const decattn_bf16* z, const decattn_bf16* k_pe,
+               decattn_kv kv, const int32_t* seqlens, int max_seqlen, int b, int s, int h, int k, int p,
+               float scale, decattn_bf16* o_lat, float* lse, void* workspace, size_t workspace_bytes,
+               cudaStream_t stream) {
+  if (b < 0 || s < 1 || s > 32 || h < 1 || max_seqlen < 0) return DECATTN_ERR_INVALID_ARG;
+  if (b == 0) return DECATTN_OK;
+  if (!qz || !q_pe || !z || !k_pe || !seqlens || !o_lat) return DECATTN_ERR_INVALID_ARG;
+  if (!mla_supported(k, p)) return DECATTN_ERR_UNSUPPORTED;
+  if (!aligned16(qz) || !aligned16(q_pe) || !aligned16(z) || !aligned16(k_pe) || !aligned16(o_lat))
+    return DECATTN_ERR_INVALID_ARG;
+  if (b > 65535 || (long long)b * h * s > INT_MAX / 2) return DECATTN_ERR_INVALID_ARG;
+  if (int rc = check_kv(kv, b, max_seqlen)) return rc;
+  DeviceState* st = nullptr;
+  if (int rc = device_state(&st)) return rc;
+  const Plan pl = mla_plan(b, s, h, k, max_seqlen, st->sms);
+  const long long rows = (long long)b * h * s;
+  const size_t need = partial_bytes(rows, pl.nsplit, k);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return DECATTN_ERR_WORKSPACE;
+  MlaLaunch a;
+  a.qz = qz;
+  a.q_pe = q_pe;
+  a.z = z;
+  a.k_pe = k_pe;
+  a.seqlens = seqlens;
+  a.block_table = kv.block_table;
+  a.max_pages = kv.max_pages;
+  a.paged = kv.paged;
+  a.capacity = kv.capacity;
+  a.num_pages = kv.num_pages;
+  a.b = b;
+  a.s = s;
+  a.h = h;
+  a.k = k;
+  a.p = p;
+  a.nsplit = pl.nsplit;
+  a.chunk = pl.chunk;
+  a.scale = scale;
+  a.o_lat = o_lat;
+  a.lse = lse;
+  a.ws_o = pl.nsplit > 1 ? static_cast<float*>(workspace) : nullptr;
+  a.ws_lse = pl.nsplit > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                       align256((size_t)rows * pl.nsplit * k * sizeof(float)))
+                           : nullptr;
+  a.err = st->err;
+  a.wait_ns = wait_limit();
+  a.test_timeout = g_test_timeout.load();
+  g_last_splits.store(pl.nsplit);
+  if (launch_mla_latent(a, stream) != cudaSuccess) return DECATTN_ERR_CUDA;
+  if (pl.nsplit > 1) {
+    if (launch_combine(a.ws_o, a.ws_lse, seqlens, (int)rows, h * s, pl.nsplit, pl.chunk, k, o_lat, lse, stream) !=
+        cudaSuccess)
+      return DECATTN_ERR_CUDA;
+  }
+  return DECATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,71 @@
+// Internal launch interfaces between the C-ABI layer (api.cu) and the kernel
+// translation units. Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace decattn {
+
+struct GqaLaunch {
+  const void* q;
+  const void* k;
+  const void* v;
+  const int32_t* seqlens;
+  const int32_t* block_table;
+  int max_pages, paged, capacity, num_pages;
+  int b, s, hq, hkv, d;
+  int nsplit, chunk;
+  float scale;
+  void* out;
+  float* lse;
+  float* ws_o;    // [b*hq*s, nsplit, d] (nsplit > 1)
+  float* ws_lse;  // [b*hq*s, nsplit]
+  unsigned* err;
+};
+
+// rows of one grouped-head CTA (multiple of 16) for head dim d
+int gqa_rows_per_cta(int d);
+int gqa_ctas_per_sm(int d);
+cudaError_t launch_gqa(const GqaLaunch& p, cudaStream_t stream);
+
+// log-sum-exp merge of split partials: rows x nsplit partials of width d
+cudaError_t launch_combine(const float* ws_o, const float* ws_lse, const int32_t* seqlens, int rows, int rows_per_seq,
+                           int nsplit, int chunk, int d, void* out, float* lse, cudaStream_t stream);
+
+struct ProjLaunch {
+  const void* a;     // [b, h, s, kin]
+  const void* w;     // [h, kin, nout]
+  void* c;           // [b, h, s, nout]
+  const int32_t* seqlens;
+  int b, s, h, kin, nout;
+  float scale;
+};
+cudaError_t launch_proj(const ProjLaunch& p, int num_sms, cudaStream_t stream);
+
+struct MlaLaunch {
+  const void* qz;
+  const void* q_pe;
+  const void* z;
+  const void* k_pe;
+  const int32_t* seqlens;
+  const int32_t* block_table;
+  int max_pages, paged, capacity, num_pages;
+  int b, s, h, k, p;
+  int nsplit, chunk;
+  float scale;
+  void* o_lat;
+  float* lse;
+  float* ws_o;    // [b*h*s, nsplit, k]
+  float* ws_lse;  // [b*h*s, nsplit]
+  unsigned* err;
+  unsigned long long wait_ns;
+  int test_timeout;
+};
+// latent-dimension partitions (CTAs) per 128-row tile for latent width k
+int mla_latent_parts(int k);
+bool mla_supported(int k, int p);
+cudaError_t launch_mla_latent(const MlaLaunch& p, cudaStream_t stream);
+
+}  // namespace decattn

@@ -1,0 +1,168 @@
+/*
+ * decattn.h - C ABI of the B300 (sm_103a) decode-attention library.
+ *
+ * One GPU, one process. Every entry point enqueues work on the caller's CUDA
+ * stream and returns at once; none synchronises, none allocates device
+ * memory, none falls back to the CPU or to another library. All tensor
+ * pointers are DEVICE pointers to dense row-major arrays in the layouts
+ * stated below, owned by the caller, and must stay valid until the enqueued
+ * work completes. bf16 tensors are passed as 16-bit storage (decattn_bf16).
+ *
+ * Sources (the web pages this library follows):
+ *   [SKILL]  "Mla Analysis" skill page: "Tensor Shapes (DeepSeek-V3 defaults)"
+ *            (layouts Q [B,H,S,D], K/V [B,T,H,D], Z [B,T,K], QPE [B,H,S,P],
+ *            KPE [B,T,P]), "Absorption Trick (FlashMLA)" (scores Qz Z^T,
+ *            values (softmax Z) Wv, decompression in a separate kernel).
+ *   [FIGHT]  "Why MLA and MTP Fight Each Other" post, summary table
+ *            (MHA / GQA / MQA / MLA) and the MTP discussion (several new
+ *            tokens per step).
+ *   [QA]     "MHA vs GQA" Q&A, section 1 (query heads sharing a KV head).
+ *   [LESSON] "MQA, GQA & MLA" lesson, Concept (contiguous groups; MLA caches
+ *            a latent plus a decoupled RoPE part).
+ *
+ * Conventions shared by all calls
+ *   b   sequences, s new tokens per sequence (1..32), seqlens[i] = keys of
+ *       sequence i INCLUDING its s new tokens (a device int32[b]); token r of
+ *       the s new ones attends to keys 0 .. seqlens[i]-s+r (causal among the
+ *       new tokens, aligned to the end); seqlens[i] = 0 gives a zero output
+ *       row and LSE = -inf; 0 < seqlens[i] < s is undefined (the kernels
+ *       treat the missing keys as absent).
+ *   max_seqlen  host-side upper bound of seqlens (sizes the launch grid).
+ *   scale       softmax scale applied to the whole score.
+ *   lse         optional float[b, heads, s] natural-log log-sum-exp of the
+ *               scaled scores (NULL to skip).
+ *   workspace   caller-allocated scratch of at least *_workspace_size() bytes
+ *               (16-byte aligned); its content on entry does not matter.
+ *   Return: DECATTN_OK or an error status; on an argument error nothing is
+ *   launched. Device-side faults detected by the kernels (a bounded wait that
+ *   ran out, a page index outside the pool) are recorded in a device error
+ *   word and reported by decattn_check_errors().
+ */
+#ifndef DECATTN_H
+#define DECATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t decattn_bf16; /* bfloat16 bit pattern */
+
+enum decattn_status {
+  DECATTN_OK = 0,
+  DECATTN_ERR_INVALID_ARG = 1, /* null pointer, Hq % Hkv != 0, s outside 1..32, page_size != 64, ... */
+  DECATTN_ERR_UNSUPPORTED = 2, /* head dim / (k, p) without a compiled instance */
+  DECATTN_ERR_WORKSPACE = 3,   /* workspace missing or too small */
+  DECATTN_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+  DECATTN_ERR_TIMEOUT = 5      /* a device-side bounded wait ran out (from decattn_check_errors) */
+};
+
+/* Cache description shared by both attention forms.
+ *   paged = 0: contiguous cache, sequence i owns rows [i*capacity, (i+1)*capacity)
+ *              of the cache tensor ([b, capacity, ...]).
+ *   paged = 1: page pool [num_pages, page_size, ...]; token j of sequence i
+ *              lives in page block_table[i*max_pages + j/page_size], row
+ *              j % page_size. block_table is a DEVICE int32[b, max_pages];
+ *              entries past a sequence's last page are never read. */
+typedef struct decattn_kv {
+  int paged;
+  int capacity;                /* contiguous only: token slots per sequence */
+  const int32_t* block_table;  /* paged only */
+  int max_pages;               /* paged only: columns of block_table */
+  int page_size;               /* paged only: must be 64 */
+  int num_pages;               /* paged only: pages in the pool */
+} decattn_kv;
+
+/* Text for a status code (static storage). */
+const char* decattn_status_string(int status);
+
+/* ------------------------------------------------------------------------
+ * Grouped-head decode attention: MHA (Hkv = Hq), GQA, MQA (Hkv = 1).
+ * [QA] section 1; [FIGHT] summary table; [LESSON] contiguous groups: query
+ * head j reads KV head j / (Hq / Hkv).
+ *   q    [b, Hq, s, d] bf16 ([SKILL] Q layout)
+ *   k, v contiguous [b, capacity, Hkv, d] bf16 ([SKILL] K, V layout) or
+ *        paged [num_pages, 64, Hkv, d]
+ *   out  [b, Hq, s, d] bf16 (round-to-nearest-even)
+ *   d in {64, 128, 256}. Split-KV: the context is cut into chunks processed
+ *   in parallel and merged by log-sum-exp in a second kernel.
+ */
+size_t gqa_decode_workspace_size(int b, int s, int hq, int hkv, int d, int max_seqlen);
+int gqa_decode(const decattn_bf16* q, const decattn_bf16* k, const decattn_bf16* v, decattn_kv kv,
+               const int32_t* seqlens, int max_seqlen, int b, int s, int hq, int hkv, int d, float scale,
+               decattn_bf16* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Absorbed MLA, step 1: query absorption ([SKILL] Absorption Trick, score
+ * line: Q K^T = (Q Wk^T) Z^T = Qz Z^T).
+ *   qz[b, j, r, :] = scale * q_nope[b, j, r, :] @ w_uk[j]
+ *   q_nope [b, h, s, d], w_uk [h, d, k], qz [b, h, s, k], all bf16; fp32
+ *   accumulation, bf16 output. seqlens may be NULL; where given, rows of
+ *   sequences with seqlens[i] == 0 are written as zeros. scale is an output
+ *   multiplier (normally 1). d, k multiples of 8, s * b <= 65535 * 64.
+ */
+int mla_absorb_q(const decattn_bf16* q_nope, const decattn_bf16* w_uk, decattn_bf16* qz, const int32_t* seqlens,
+                 int b, int s, int h, int d, int k, float scale, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Absorbed MLA, step 2: latent attention over the latent cache ([SKILL]
+ * Absorption Trick; Tensor Shapes: Z [B,T,K], KPE [B,T,P] shared by all
+ * heads; [LESSON] decoupled RoPE part). For each sequence all h*s query rows
+ * (row = head*s + token) share every latent tile:
+ *   score_m = scale * (<qz_row, z_m> + <q_pe_row, k_pe_m>)
+ *   o_lat_row = sum_m softmax(score)_m z_m
+ *   qz   [b, h, s, k] bf16 (output of mla_absorb_q)
+ *   q_pe [b, h, s, p] bf16
+ *   z    contiguous [b, capacity, k] or paged [num_pages, 64, k] bf16
+ *   k_pe contiguous [b, capacity, p] or paged [num_pages, 64, p] bf16
+ *   o_lat [b, h, s, k] bf16; lse [b, h, s] float or NULL.
+ *   Compiled instances (k, p): (512, 64) and (64, 16). Pointers 16-byte
+ *   aligned. Tensor-core (tcgen05) kernel with TMA tile loads, split over
+ *   the context and merged by a second kernel.
+ */
+size_t mla_decode_workspace_size(int b, int s, int h, int k, int max_seqlen);
+int mla_decode(const decattn_bf16* qz, const decattn_bf16* q_pe, const decattn_bf16* z, const decattn_bf16* k_pe,
+               decattn_kv kv, const int32_t* seqlens, int max_seqlen, int b, int s, int h, int k, int p,
+               float scale, decattn_bf16* o_lat, float* lse, void* workspace, size_t workspace_bytes,
+               cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Absorbed MLA, step 3: output decompression, done as a separate kernel
+ * ([SKILL] Absorption Trick, value line: (softmax(A) Z) Wv).
+ *   out[b, j, r, :] = scale * o_lat[b, j, r, :] @ w_uv[j]
+ *   o_lat [b, h, s, k], w_uv [h, k, d], out [b, h, s, d], all bf16.
+ *   seqlens and scale as in mla_absorb_q.
+ */
+int mla_out_proj(const decattn_bf16* o_lat, const decattn_bf16* w_uv, decattn_bf16* out, const int32_t* seqlens,
+                 int b, int s, int h, int k, int d, float scale, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics.
+ * decattn_check_errors: synchronises `stream`, reads and clears the device
+ * error word of the current device; returns DECATTN_ERR_TIMEOUT if a bounded
+ * wait ran out, DECATTN_ERR_INVALID_ARG if a page index was outside the pool,
+ * DECATTN_ERR_CUDA on a CUDA error, else DECATTN_OK.
+ * decattn_set_wait_limit_ns: limit of every device-side wait (0 = default,
+ * 2 s). decattn_set_forced_splits: 0 = let the planner choose the number of
+ * context chunks; n > 0 forces n (for split-invariance tests); it also
+ * changes the workspace sizes returned afterwards.
+ * decattn_last_num_splits: number of chunks the last attention call used.
+ * decattn_test_force_timeout: when nonzero, the next mla_decode kernels wait
+ * once on a barrier that nothing signals, with a 1 ms limit, so that the
+ * timeout path runs; the kernels then wind down and report
+ * DECATTN_ERR_TIMEOUT through decattn_check_errors. Test use only.
+ */
+int decattn_check_errors(cudaStream_t stream);
+void decattn_set_wait_limit_ns(unsigned long long ns);
+void decattn_set_forced_splits(int nsplit);
+int decattn_last_num_splits(void);
+void decattn_test_force_timeout(int on);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DECATTN_H */

@@ -1,0 +1,62 @@
+"""Shared test utilities: tolerance checks and oracle calls on torch inputs.
+
+Tolerances (float outputs, bf16 out / fp32 accumulate):
+  max |gpu - oracle| <= 2e-2, mean |gpu - oracle| <= 2e-3,
+  relative RMS ||gpu - oracle|| / ||oracle|| <= 1e-2 (bf16 output rounding
+  alone is about 2^-9 = 2e-3 relative), LSE within 1e-3 absolute.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+MAX_ABS = 2e-2
+MEAN_ABS = 2e-3
+REL_RMS = 1e-2
+LSE_ABS = 1e-3
+
+
+def f64(t):
+    return t.detach().float().double().cpu().numpy()
+
+
+def assert_out_close(got, ref, what="", max_abs=MAX_ABS, mean_abs=MEAN_ABS, rel_rms=REL_RMS):
+    """The absolute bounds are stated for unit-scale outputs: outputs whose
+    RMS exceeds 1 (e.g. sharp-softmax cases, absorbed queries of large
+    inputs) are first divided by that RMS."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    unit = max(1.0, float(np.sqrt(np.mean(ref ** 2)))) if ref.size else 1.0
+    got, ref = got / unit, ref / unit
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    assert err.max() <= max_abs, f"{what}: max|err| {err.max():.3e} > {max_abs}"
+    assert err.mean() <= mean_abs, f"{what}: mean|err| {err.mean():.3e} > {mean_abs}"
+    den = np.sqrt(np.mean(ref ** 2))
+    if den > 0:
+        rr = np.sqrt(np.mean(err ** 2)) / den
+        assert rr <= rel_rms, f"{what}: rel-RMS {rr:.3e} > {rel_rms}"
+
+
+def assert_lse_close(got, ref, what="", tol=LSE_ABS):
+    """tol may be a scalar or an array of per-row bounds."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape
+    fin = np.isfinite(ref)
+    assert np.array_equal(fin, np.isfinite(got)), f"{what}: -inf pattern differs"
+    if fin.any():
+        tol = np.broadcast_to(np.asarray(tol, np.float64), ref.shape)
+        e = np.abs(got[fin] - ref[fin])
+        worst = int(np.argmax(e - tol[fin]))
+        assert np.all(e <= tol[fin]), f"{what}: LSE err {e[worst]:.3e} > bound {tol[fin][worst]:.3e}"
+    assert np.all(got[~fin] == -np.inf)
+
+
+def qz_rounding_lse_bound(qz_exact, o_lat_exact, scale):
+    """Per-row bound on the LSE change caused by rounding Qz to bf16 between
+    the absorb and latent kernels (the pipeline's stage boundary):
+    to first order dLSE = scale * dQz . O_lat with |dQz_i| <= 2^-9 |Qz_i|
+    (bf16 round-to-nearest), so |dLSE| <= scale * 2^-9 * sum_i |Qz_i| |O_lat_i|.
+    Returned with the 1e-3 allowance added."""
+    return LSE_ABS + scale * 2.0 ** -9 * np.sum(np.abs(qz_exact) * np.abs(o_lat_exact), axis=-1)

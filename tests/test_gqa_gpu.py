@@ -1,0 +1,164 @@
+"""Parity of the grouped-head decode kernels (split + combine, contiguous and
+paged) against the fp64 oracle, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as A
+from tests.helpers import assert_lse_close, assert_out_close, f64
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from decode_attention_18_b300 import build
+
+    build.build()
+    import decode_attention_18_b300 as da
+
+    da.set_forced_splits(0)
+    yield
+    da.set_forced_splits(0)
+
+
+def run(b, hq, hkv, d, s, seqlens, paged=False, capacity=None, q_std=1.0, seed=0, heads_subset=None):
+    import decode_attention_18_b300 as da
+    from decode_attention_18_b300 import workloads as W
+
+    q, cache = W.make_gqa(b, hq, hkv, d, s, seqlens, paged=paged, capacity=capacity, seed=seed, device=DEV,
+                          q_std=q_std)
+    sl = torch.tensor(seqlens, dtype=torch.int32, device=DEV)
+    out, lse = da.gqa_decode(q, cache.k, cache.v, sl, max_seqlen=max(seqlens),
+                             block_table=cache.block_table if paged else None)
+    torch.cuda.synchronize()
+    assert da.check_errors() == 0
+    return q, cache, out, lse
+
+
+def check_all(q, cache, out, lse, seqlens, d, what):
+    b = q.shape[0]
+    ks = [f64(cache.seq_rows(i, "k")) for i in range(b)]
+    vs = [f64(cache.seq_rows(i, "v")) for i in range(b)]
+    ro, rl = A.gqa_ref(f64(q), ks, vs, seqlens, 1 / math.sqrt(d))
+    assert_out_close(f64(out), ro, what)
+    assert_lse_close(f64(lse), rl, what)
+
+
+def check_sampled(q, cache, out, lse, seqlens, d, seqs, kv_heads):
+    """Oracle on selected (sequence, KV head) pairs only: the G query heads of
+    each KV head against that head's keys and values."""
+    hq = q.shape[1]
+    hkv = cache.k.shape[2]
+    G = hq // hkv
+    for i in seqs:
+        K = cache.seq_rows(i, "k")
+        V = cache.seq_rows(i, "v")
+        for g in kv_heads:
+            heads = slice(g * G, (g + 1) * G)
+            ro, rl = A.gqa_ref(f64(q[i:i + 1, heads]), [f64(K[:, g:g + 1])], [f64(V[:, g:g + 1])], [seqlens[i]],
+                               1 / math.sqrt(d))
+            assert_out_close(f64(out[i:i + 1, heads]), ro, f"seq {i} kv head {g}")
+            assert_lse_close(f64(lse[i:i + 1, heads]), rl, f"seq {i} kv head {g}")
+
+
+@pytest.mark.parametrize("b,hq,hkv,d,s,seqlens", [
+    (2, 8, 2, 128, 1, [200, 77]),          # GQA, ragged, several tiles + tail
+    (2, 8, 8, 64, 1, [130, 64]),           # MHA
+    (2, 8, 1, 128, 1, [65, 63]),           # MQA
+    (3, 6, 2, 256, 1, [1, 129, 300]),      # d = 256
+    (2, 24, 4, 256, 1, [500, 333]),        # 24 / 4 / 256 geometry
+    (2, 24, 1, 256, 1, [257, 190]),        # MQA with 24 rows (two row blocks)
+    (2, 8, 2, 128, 3, [100, 50]),          # MTP s = 3, causal
+    (1, 16, 2, 64, 32, [300]),             # s = 32: 256 rows per KV head
+    (2, 64, 8, 128, 2, [4096, 1000]),      # 64 / 8 geometry, s = 2
+    (5, 8, 2, 128, 1, [0, 1, 63, 64, 65]),  # empty and page-boundary lengths
+])
+def test_contiguous_vs_oracle(b, hq, hkv, d, s, seqlens):
+    q, cache, out, lse = run(b, hq, hkv, d, s, seqlens, capacity=max(seqlens) + 7)
+    check_all(q, cache, out, lse, seqlens, d, f"b{b} hq{hq} hkv{hkv} d{d} s{s}")
+
+
+@pytest.mark.parametrize("b,hq,hkv,d,s,seqlens", [
+    (3, 8, 2, 128, 1, [200, 77, 64]),
+    (2, 24, 24, 256, 1, [700, 129]),
+    (2, 24, 1, 256, 2, [1000, 65]),
+    (4, 8, 4, 64, 1, [0, 1, 191, 192]),
+])
+def test_paged_vs_oracle(b, hq, hkv, d, s, seqlens):
+    q, cache, out, lse = run(b, hq, hkv, d, s, seqlens, paged=True, seed=5)
+    check_all(q, cache, out, lse, seqlens, d, f"paged b{b} hq{hq} hkv{hkv} d{d} s{s}")
+
+
+def test_sharp_softmax():
+    # queries x 8: peaked softmax and near-unit outputs
+    seqlens = [300, 1000]
+    q, cache, out, lse = run(2, 8, 2, 128, 1, seqlens, q_std=8.0, seed=7)
+    check_all(q, cache, out, lse, seqlens, 128, "sharp")
+    assert np.sqrt(np.mean(f64(out) ** 2)) > 0.2
+
+
+def test_paged_equals_contiguous_bitwise():
+    import decode_attention_18_b300 as da
+
+    seqlens = [517, 64, 1000]
+    q, cache, out, lse = run(3, 16, 4, 128, 1, seqlens, paged=True, seed=11)
+    cap = max(seqlens)
+    kc = torch.zeros((3, cap, 4, 128), dtype=torch.bfloat16, device=DEV)
+    vc = torch.zeros_like(kc)
+    for i, L in enumerate(seqlens):
+        kc[i, :L] = cache.seq_rows(i, "k")
+        vc[i, :L] = cache.seq_rows(i, "v")
+    sl = torch.tensor(seqlens, dtype=torch.int32, device=DEV)
+    out2, lse2 = da.gqa_decode(q, kc, vc, sl, max_seqlen=cap)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2)
+    assert torch.equal(lse, lse2)
+
+
+@pytest.mark.parametrize("nsplit", [1, 2, 7])
+def test_split_invariance(nsplit):
+    import decode_attention_18_b300 as da
+
+    seqlens = [1500, 800]
+    q, cache, out, lse = run(2, 8, 2, 128, 1, seqlens, seed=13)
+    da.set_forced_splits(nsplit)
+    try:
+        sl = torch.tensor(seqlens, dtype=torch.int32, device=DEV)
+        out2, lse2 = da.gqa_decode(q, cache.k, cache.v, sl, max_seqlen=max(seqlens))
+        torch.cuda.synchronize()
+        L = max(seqlens)
+        chunk = -(-(-(-L // nsplit)) // 64) * 64  # chunks are whole 64-key pages
+        assert da.last_num_splits() == -(-L // chunk)
+    finally:
+        da.set_forced_splits(0)
+    a, b2 = f64(out), f64(out2)
+    rr = np.sqrt(np.mean((a - b2) ** 2)) / np.sqrt(np.mean(a ** 2))
+    assert rr <= 1e-2
+    assert np.abs(f64(lse) - f64(lse2)).max() <= 1e-4
+    check_all(q, cache, out2, lse2, seqlens, 128, f"nsplit {nsplit}")
+
+
+def test_full_size_gqa_64_8_sampled():
+    # b=32, Hq=64, Hkv=8, d=128, t=4096: the grouped-head workload at full size
+    from decode_attention_18_b300 import workloads as W
+
+    wl = W.WORKLOADS["gqa_64_8"]
+    seqlens = wl.seqlens()
+    q, cache, out, lse = run(wl.b, wl.heads, wl.hkv, wl.d, wl.s, seqlens, seed=wl.seed)
+    check_sampled(q, cache, out, lse, seqlens, wl.d, seqs=[0, 13, 31], kv_heads=[0, 3, 7])
+
+
+@pytest.mark.parametrize("hkv", [24, 4, 1])
+def test_full_size_paged_ragged_sampled(hkv):
+    # b=8, Hq=24, d=256, L ~ U[16384, 32768], 64-token pages in random order
+    from decode_attention_18_b300 import workloads as W
+
+    wl = W.WORKLOADS[f"gqa_paged_hkv{hkv}"]
+    seqlens = wl.seqlens()
+    q, cache, out, lse = run(wl.b, wl.heads, wl.hkv, wl.d, wl.s, seqlens, paged=True, seed=wl.seed)
+    check_sampled(q, cache, out, lse, seqlens, wl.d, seqs=[0, 7], kv_heads=sorted({0, hkv - 1}))

@@ -1,0 +1,192 @@
+"""Parity of the absorbed-MLA kernels (absorb GEMM, tcgen05 latent attention +
+combine, W_uv projection) against the fp64 oracle, through the C ABI.
+
+Two comparisons per case: stage-wise (the oracle step is fed the very bf16
+tensor the GPU step received, e.g. the GPU's Qz) and end to end (the oracle
+runs the whole pipeline from the bf16 inputs without rounding anything)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as A
+from tests.helpers import assert_lse_close, assert_out_close, f64, qz_rounding_lse_bound
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from decode_attention_18_b300 import build
+
+    build.build()
+    import decode_attention_18_b300 as da
+
+    da.set_forced_splits(0)
+    yield
+    da.set_forced_splits(0)
+
+
+def make(b, h, d, k, p, s, seqlens, paged=False, capacity=None, seed=0, q_std=1.0):
+    from decode_attention_18_b300 import workloads as W
+
+    return W.make_mla(b, h, d, k, p, s, seqlens, paged=paged, capacity=capacity, seed=seed, device=DEV,
+                      q_std=q_std)
+
+
+def forward(inp):
+    import decode_attention_18_b300 as da
+
+    sl = torch.tensor(inp.seqlens, dtype=torch.int32, device=DEV)
+    out, lse, qz, o_lat = da.mla_forward(inp.q_nope, inp.q_pe, inp.z, inp.k_pe, inp.w_uk, inp.w_uv, sl,
+                                         scale=inp.scale, max_seqlen=max(inp.seqlens),
+                                         block_table=inp.block_table if inp.paged else None)
+    torch.cuda.synchronize()
+    assert da.check_errors() == 0
+    return out, lse, qz, o_lat
+
+
+def seq_inputs(inp, seqs):
+    zs = [f64(inp.seq_rows(i, "z")) for i in seqs]
+    kp = [f64(inp.seq_rows(i, "kpe")) for i in seqs]
+    return zs, kp
+
+
+def check(inp, res, seqs=None, what=""):
+    out, lse, qz, o_lat = res
+    seqs = list(range(len(inp.seqlens))) if seqs is None else seqs
+    sl = [inp.seqlens[i] for i in seqs]
+    zs, kp = seq_inputs(inp, seqs)
+    # stage 1: absorb against the oracle on the same bf16 inputs (rows of
+    # empty sequences are zero by the entry point's contract)
+    rq = A.mla_absorb_ref(f64(inp.q_nope[seqs]), f64(inp.w_uk))
+    for n, L in enumerate(sl):
+        if L == 0:
+            rq[n] = 0.0
+    assert_out_close(f64(qz[seqs]), rq, what + " absorb")
+    # stage 2: latent attention fed the GPU's bf16 Qz
+    ro_lat, rl = A.mla_latent_ref(f64(qz[seqs]), f64(inp.q_pe[seqs]), zs, kp, sl, inp.scale)
+    assert_out_close(f64(o_lat[seqs]), ro_lat, what + " latent")
+    assert_lse_close(f64(lse[seqs]), rl, what + " lse")
+    # stage 3: projection fed the GPU's bf16 O_lat
+    ro = A.mla_out_proj_ref(f64(o_lat[seqs]), f64(inp.w_uv))
+    assert_out_close(f64(out[seqs]), ro, what + " out_proj")
+    # end to end from the bf16 inputs, nothing rounded in between
+    eo, el, eqz, eolat = A.mla_absorbed_ref(f64(inp.q_nope[seqs]), f64(inp.q_pe[seqs]), zs, kp, f64(inp.w_uk),
+                                            f64(inp.w_uv), sl, inp.scale)
+    assert_out_close(f64(out[seqs]), eo, what + " end-to-end")
+    assert_lse_close(f64(lse[seqs]), el, what + " end-to-end lse", tol=qz_rounding_lse_bound(eqz, eolat, inp.scale))
+
+
+def test_tiny_workload():
+    # b=2, h=16, d=32, k=64, p=16, t=256, s=1, scale 1/sqrt(48), seed 0
+    from decode_attention_18_b300 import workloads as W
+
+    wl = W.WORKLOADS["mla_tiny"]
+    inp = make(wl.b, wl.heads, wl.d, wl.k, wl.p, wl.s, wl.seqlens(), seed=wl.seed)
+    check(inp, forward(inp), what="tiny")
+
+
+@pytest.mark.parametrize("b,h,s,seqlens", [
+    (2, 128, 1, [333, 100]),     # one full 128-row tile, ragged tails
+    (3, 16, 1, [64, 65, 31]),    # fewer rows than a tile
+    (2, 128, 2, [300, 40]),      # MTP s=2: two row tiles, causal
+    (1, 64, 4, [97]),            # s=4
+    (2, 8, 32, [64, 200]),       # s=32
+])
+def test_dsv3_shapes_small(b, h, s, seqlens):
+    inp = make(b, h, 128, 512, 64, s, seqlens, capacity=max(seqlens) + 5, seed=1)
+    check(inp, forward(inp), what=f"b{b} h{h} s{s}")
+
+
+def test_edge_lengths():
+    seqlens = [0, 1, 31, 32, 33, 64, 65]
+    inp = make(7, 16, 128, 512, 64, 1, seqlens, seed=2)
+    res = forward(inp)
+    check(inp, res, what="edges")
+    out, lse, _, o_lat = res
+    assert torch.all(o_lat[0] == 0) and torch.all(out[0] == 0)
+    assert torch.all(torch.isneginf(lse[0]))
+
+
+def test_paged_vs_oracle_and_bitwise_contiguous():
+    import decode_attention_18_b300 as da
+
+    seqlens = [700, 64, 129]
+    inp = make(3, 128, 128, 512, 64, 1, seqlens, paged=True, seed=3)
+    res = forward(inp)
+    check(inp, res, what="paged")
+    cap = max(seqlens)
+    z = torch.zeros((3, cap, 512), dtype=torch.bfloat16, device=DEV)
+    kpe = torch.zeros((3, cap, 64), dtype=torch.bfloat16, device=DEV)
+    for i, L in enumerate(seqlens):
+        z[i, :L] = inp.seq_rows(i, "z")
+        kpe[i, :L] = inp.seq_rows(i, "kpe")
+    sl = torch.tensor(seqlens, dtype=torch.int32, device=DEV)
+    o2, l2 = da.mla_decode(res[2], inp.q_pe, z, kpe, sl, scale=inp.scale, max_seqlen=cap)
+    torch.cuda.synchronize()
+    assert torch.equal(o2, res[3])
+    assert torch.equal(l2, res[1])
+
+
+def test_sharp_queries():
+    inp = make(2, 128, 128, 512, 64, 1, [400, 900], seed=4, q_std=8.0)
+    check(inp, forward(inp), what="sharp")
+
+
+@pytest.mark.parametrize("nsplit", [1, 2, 5])
+def test_split_invariance(nsplit):
+    import decode_attention_18_b300 as da
+
+    inp = make(2, 128, 128, 512, 64, 1, [1500, 700], seed=5)
+    base = forward(inp)
+    da.set_forced_splits(nsplit)
+    try:
+        sl = torch.tensor(inp.seqlens, dtype=torch.int32, device=DEV)
+        o2, l2 = da.mla_decode(base[2], inp.q_pe, inp.z, inp.k_pe, sl, scale=inp.scale, max_seqlen=1500)
+        torch.cuda.synchronize()
+        chunk = -(-(-(-1500 // nsplit)) // 64) * 64  # chunks are whole 64-key pages
+        assert da.last_num_splits() == -(-1500 // chunk)
+    finally:
+        da.set_forced_splits(0)
+    a, b2 = f64(base[3]), f64(o2)
+    assert np.sqrt(np.mean((a - b2) ** 2)) / np.sqrt(np.mean(a ** 2)) <= 1e-2
+    assert np.abs(f64(base[1]) - f64(l2)).max() <= 1e-4
+
+
+def test_projection_gemms_alone():
+    import decode_attention_18_b300 as da
+
+    g = torch.Generator(device=DEV).manual_seed(9)
+    o_lat = torch.randn((5, 16, 3, 512), generator=g, device=DEV).bfloat16()
+    w = (torch.randn((16, 512, 128), generator=g, device=DEV) / math.sqrt(512)).bfloat16()
+    sl = torch.tensor([3, 0, 9, 4, 5], dtype=torch.int32, device=DEV)
+    out = da.mla_out_proj(o_lat, w, sl, scale=0.5)
+    q = torch.randn((5, 16, 3, 128), generator=g, device=DEV).bfloat16()
+    wk = (torch.randn((16, 128, 512), generator=g, device=DEV) / math.sqrt(512)).bfloat16()
+    qz = da.mla_absorb_q(q, wk, None, scale=2.0)
+    torch.cuda.synchronize()
+    ro = A.mla_out_proj_ref(f64(o_lat), f64(w), 0.5)
+    ro[1] = 0.0  # empty sequence -> zero rows
+    assert_out_close(f64(out), ro, "out_proj")
+    assert_out_close(f64(qz), A.mla_absorb_ref(f64(q), f64(wk), 2.0), "absorb", max_abs=4e-2, mean_abs=4e-3)
+
+
+def test_full_size_dsv3_sampled():
+    # b=32, h=128, d=128, k=512, p=64, t=4096, s=1: the headline workload
+    from decode_attention_18_b300 import workloads as W
+
+    wl = W.WORKLOADS["mla_dsv3"]
+    inp = make(wl.b, wl.heads, wl.d, wl.k, wl.p, wl.s, wl.seqlens(), seed=wl.seed)
+    check(inp, forward(inp), seqs=[0, 19, 31], what="dsv3")
+
+
+def test_full_size_mtp_s8_sampled():
+    from decode_attention_18_b300 import workloads as W
+
+    wl = W.WORKLOADS["mla_mtp_s8"]
+    inp = make(wl.b, wl.heads, wl.d, wl.k, wl.p, wl.s, wl.seqlens(), seed=wl.seed)
+    check(inp, forward(inp), seqs=[0, 31], what="mtp s8")

@@ -32,7 +32,7 @@ std::atomic<int> g_last_splits{0};
 std::atomic<int> g_test_timeout{0};
 
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
-constexpr int kChunkAlign = 64;                                // chunks are whole 64-key pages
+constexpr int kPage = 64;  // chunks are whole 64-key pages (and whole kernel tiles)
 
 // Per-device set-up on first use: the error word's device address and the SM count.
 int device_state(DeviceState** out) {
@@ -71,12 +71,14 @@ struct Plan {
 // Split planner: pick the number of context chunks so that the CTAs fill the
 // SMs in whole waves. base = CTAs per chunk index (sequences x heads x row
 // blocks), slots = CTAs resident on the whole GPU at once, overhead = fixed
-// cost of a CTA expressed in keys. Cost model: waves x (chunk + overhead).
-Plan plan_splits(long long base, int max_seqlen, long long slots, int overhead_keys) {
-  Plan pl{1, kChunkAlign};
+// cost of a CTA expressed in keys, align = chunk granularity (a multiple of
+// the 64-key page and of the kernel's key tile). Cost model:
+// waves x (chunk + overhead).
+Plan plan_splits(long long base, int max_seqlen, long long slots, int overhead_keys, int align) {
+  Plan pl{1, align};
   const long long L = max_seqlen > 0 ? max_seqlen : 1;
-  const int max_n = (int)ceil_div(L, kChunkAlign);
-  auto chunk_for = [&](int n) { return (int)(ceil_div(ceil_div(L, n), kChunkAlign) * kChunkAlign); };
+  const int max_n = (int)ceil_div(L, align);
+  auto chunk_for = [&](int n) { return (int)(ceil_div(ceil_div(L, n), align) * align); };
   const int forced = g_forced_splits.load();
   if (forced > 0) {
     const int n = forced < max_n ? forced : max_n;
@@ -125,13 +127,13 @@ Plan gqa_plan(int b, int s, int hq, int hkv, int d, int max_seqlen, int sms) {
   const int rpc = gqa_rows_per_cta(rows);
   const long long base = (long long)b * hkv * ceil_div(rows, rpc);
   const long long slots = (long long)sms * gqa_ctas_per_sm(d);
-  return plan_splits(base, max_seqlen, slots, 64);
+  return plan_splits(base, max_seqlen, slots, 64, kPage);
 }
 
 // --- latent MLA plan (one CTA per SM: its shared memory holds the 128-row query tile)
 Plan mla_plan(int b, int s, int h, int k, int max_seqlen, int sms) {
   const long long base = (long long)b * mla_latent_parts(k) * ceil_div((long long)h * s, 128);
-  return plan_splits(base, max_seqlen, sms, 192);
+  return plan_splits(base, max_seqlen, sms, 256, mla_tile_keys());
 }
 
 }  // namespace

@@ -65,6 +65,8 @@ struct MlaLaunch {
 };
 // latent-dimension partitions (CTAs) per 128-row tile for latent width k
 int mla_latent_parts(int k);
+// keys per latent tile (context chunks are multiples of it)
+int mla_tile_keys();
 bool mla_supported(int k, int p);
 cudaError_t launch_mla_latent(const MlaLaunch& p, cudaStream_t stream);
 

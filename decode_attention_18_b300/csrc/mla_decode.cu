@@ -8,26 +8,35 @@
 // a sequence (h heads x s new tokens) reads the same Z, which is what makes
 // the form compute-heavy ("Cost Models", FlashMLA: AI ~ 228 FLOP/B at s = 1).
 //
-// Kernel design (one CTA = 128 query rows x one context chunk x one latent
-// partition of the output):
+// Kernel design (one CTA = 128 query rows x one context chunk x one half of the
+// output columns):
 //   * All h*s query rows of a sequence are packed into the MMA M dimension
 //     (row = head*s + token), 128 rows per CTA.
-//   * Q' = [Qz | q_pe] stays in shared memory for the whole chunk; tiles of 32
-//     latent rows [Z | K_pe] stream from HBM once per CTA through a 2-stage
-//     TMA pipeline (128-byte swizzled boxes, evict-first L2 policy).
+//   * Q' = [Qz | q_pe] stays in shared memory for the whole chunk. The cache
+//     is consumed in tiles of 128 latent rows. For S, each tile streams
+//     through a ring of 16 KB shared-memory slots, one 64-wide column chunk
+//     [128 rows x 64] (or the RoPE chunk) at a time, loaded by TMA as two
+//     64-row boxes (so a box never crosses a 64-token page). For O, the
+//     CTA's 256 output columns of the same rows stream again (from L2) in
+//     16-row slabs through a second ring.
 //   * tcgen05.mma (kind::f16, bf16 in, fp32 accumulate in Tensor Memory):
-//       S  = Q' K'^T           M=128, N=32, K=k+p   (K-major A and B)
-//       O += P Z_part          M=128, N=k/NH, K=32  (Z read MN-major: the very
-//                                                    same shared tile as above)
-//     S is double-buffered in TMEM; the fp32 O accumulator of a 128-row tile
-//     is 128 x k, which for k = 512 fills all 512 TMEM columns, so the output
-//     columns are split over NH = 2 CTAs (each recomputes S for its rows).
+//       S  = Q' K'^T    M=128, N=128 keys, K=k+p  (K-major A and B)
+//       O += P Z_half   M=128, N=256,      K=16 keys per slab (Z read MN-major)
+//     The fp32 accumulator of 128 rows x k = 512 columns would fill all of
+//     TMEM, so the output columns are split over 2 CTAs per row tile, each
+//     recomputing S for the same rows; TMEM holds O (256 columns) and two
+//     128-column S buffers, so S of the next tile is computed while the
+//     softmax of the current one runs. On this part a tcgen05.mma costs about
+//     100 cycles to issue whatever its N, so N = 128 keeps the tensor pipe fed.
 //   * Softmax warps (thread = row) read S with tcgen05.ld, apply the causal
-//     mask and scale, and keep a running reference maximum that moves only
-//     when a row's maximum grows by more than 2^8 (then O is rescaled in
-//     TMEM); P (bf16) goes to shared memory for the second MMA.
+//     mask and scale, and keep a reference maximum that moves only when a
+//     row's maximum grows by more than 2^8 (O is then rescaled in TMEM); P is
+//     written as bf16 into shared memory (128-byte swizzled) for the O MMA.
 //   * Warp roles: warp 0 issues TMA, warp 1 issues MMAs (one thread) and owns
 //     the TMEM allocation, warps 2-5 run the softmax and the epilogue.
+//   * Latent rows past the sequence end may hold anything: slabs wholly past
+//     it are not loaded or multiplied; the one slab that straddles it has its
+//     rows past the end zeroed before the O MMA, so P Z stays finite.
 //   * Every mbarrier wait is bounded; on time-out the CTA records the error,
 //     stops issuing work, waits for its own copies and MMAs, frees TMEM and
 //     returns.
@@ -42,12 +51,14 @@ namespace decattn {
 
 namespace {
 
-constexpr int TK = 32;          // latent rows (keys) per tile
-constexpr int NSTAGE = 2;
+constexpr int TK = 128;         // latent rows (keys) per S tile
+constexpr int NS = 2;           // S-ring slots (one 64-wide column chunk of a tile each)
+constexpr int NO = 2;           // O-ring slots (one 16-row slab each)
+constexpr int SLAB = 16;        // keys per O slab (= MMA K)
 constexpr int BMROWS = 128;     // query rows per CTA (MMA M)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleLog2 = 8.f;                      // move the reference max only past 2^8
+constexpr float kRescaleLog2 = 8.f;                        // move the reference max only past 2^8
 constexpr unsigned long long kTeardownNs = 1000000000ull;  // 1 s for own copies / MMAs at exit
 constexpr unsigned long long kTestWaitNs = 1000000ull;     // 1 ms forced-timeout wait
 
@@ -71,36 +82,51 @@ struct MlaParams {
 
 template <int KL, int P>
 struct MlaCfg {
-  static constexpr int NH = KL >= 512 ? 2 : 1;  // CTAs per 128-row tile (output-column partitions)
+  static constexpr int NH = KL >= 512 ? 2 : 1;  // CTAs per 128-row tile (output-column halves)
   static constexpr int KLH = KL / NH;           // O columns per CTA
-  static constexpr int NBL = KL / 64;           // 64-wide (128-byte) latent boxes
+  static constexpr int NBL = KL / 64;           // 64-wide latent column chunks
+  static constexpr int NCH = NBL + 1;           // + the RoPE chunk
   static constexpr int PE_ROW = P * 2;          // bytes per RoPE row
   static constexpr uint32_t PE_SWZ = PE_ROW == 128 ? kSw128 : (PE_ROW == 64 ? kSw64 : kSw32);
   static constexpr int Q_BOX = BMROWS * 128;
   static constexpr int Q_LAT = NBL * Q_BOX;
   static constexpr int Q_PE = BMROWS * PE_ROW;
-  static constexpr int KV_BOX = TK * 128;
-  static constexpr int KV_LAT = NBL * KV_BOX;
-  static constexpr int KV_PE = TK * PE_ROW;
-  static constexpr int STAGE = align1024(KV_LAT + KV_PE);
-  static constexpr int P_BYTES = BMROWS * TK * 2;  // P tile, rows of 64 B (64-byte swizzle)
+  static constexpr int S_SLOT = TK * 128;             // one [128 keys x 64] chunk
+  static constexpr int HALF_LAT = 64 * 128;           // one 64-row box of a latent chunk
+  static constexpr int HALF_PE = 64 * PE_ROW;         // one 64-row box of the RoPE chunk
+  static constexpr int O_SUB = SLAB * 128;            // [16 keys x 64 cols]
+  static constexpr int O_SLOT = (KLH / 64) * O_SUB;   // [16 keys x KLH cols]
+  static constexpr int P_BOX = BMROWS * 128;          // [128 rows x 64 keys] of P
   static constexpr int OFF_QPE = Q_LAT;
-  static constexpr int OFF_STAGE = align1024(Q_LAT + Q_PE);
-  static constexpr int OFF_P = OFF_STAGE + NSTAGE * STAGE;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int OFF_P = align1024(Q_LAT + Q_PE);
+  static constexpr int OFF_SRING = OFF_P + 2 * P_BOX;
+  static constexpr int OFF_ORING = OFF_SRING + NS * S_SLOT;
+  static constexpr int OFF_BAR = align1024(OFF_ORING + NO * O_SLOT);
   static constexpr int SMEM = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
-  static constexpr int TM_S = KLH;                   // S buffers after the O accumulator
-  static constexpr int TM_COLS = pow2_cols(KLH + NSTAGE * TK);
-  static_assert(KL % 64 == 0 && KLH % 32 == 0 && KLH <= 256, "latent width");
+  static constexpr int TM_S = KLH;                   // two S buffers after the O accumulator
+  static constexpr int TM_COLS = pow2_cols(KLH + 2 * TK);
+  static_assert(KL % 64 == 0 && KLH % 64 == 0 && KLH <= 256, "latent width");
   static_assert(P % 16 == 0 && PE_ROW <= 128, "rope width");
   static_assert(SMEM <= 232448, "shared memory");
 };
 
+__device__ __forceinline__ int cache_row(const MlaParams& p, int bi, int key) {
+  if (p.paged) {
+    int page = p.block_table[(size_t)bi * p.max_pages + key / 64];
+    if (page < 0 || page >= p.num_pages) {
+      raise_error(p.err, kErrBadPage);
+      page = 0;  // stay inside the pool; the result is flagged invalid
+    }
+    return page * 64 + (key % 64);
+  }
+  return bi * p.capacity + key;
+}
+
 template <int KL, int P>
 __global__ void __launch_bounds__(192, 1)
     mla_latent_kernel(const __grid_constant__ CUtensorMap tm_qz, const __grid_constant__ CUtensorMap tm_qpe,
-                      const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_kpe,
-                      MlaParams p) {
+                      const __grid_constant__ CUtensorMap tm_z64, const __grid_constant__ CUtensorMap tm_kpe64,
+                      const __grid_constant__ CUtensorMap tm_z16, MlaParams p) {
   using C = MlaCfg<KL, P>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -130,29 +156,36 @@ __global__ void __launch_bounds__(192, 1)
   const int kend = min(L, kstart + p.chunk);
   const int ntiles = (kend - kstart + TK - 1) / TK;
   const int qrow0 = bi * p.rows + mt * BMROWS;  // first flattened [b*h*s] query row
+  auto tile_keys = [&](int t) { return min(TK, kend - (kstart + t * TK)); };
+  auto tile_slabs = [&](int t) { return (tile_keys(t) + SLAB - 1) / SLAB; };
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [NSTAGE]
-  uint64_t* kv_empty = bars + 3;  // [NSTAGE]
-  uint64_t* s_full = bars + 5;    // [NSTAGE]
-  uint64_t* s_free = bars + 7;    // [NSTAGE]
-  uint64_t* p_full = bars + 9;
-  uint64_t* o_done = bars + 10;
-  uint64_t* test_bar = bars + 11;
-  uint64_t* fin_bar = bars + 12;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 14);
+  uint64_t* s_full = bars + 1;    // [NS]  chunk landed
+  uint64_t* s_empty = bars + 3;   // [NS]  chunk consumed by the S MMAs
+  uint64_t* o_full = bars + 5;    // [NO]  slab landed
+  uint64_t* o_empty = bars + 7;   // [NO]  slab consumed by the O MMA
+  uint64_t* s_ready = bars + 9;   // [2]   S tile in TMEM
+  uint64_t* p_full = bars + 11;   //       P in shared memory (+ O rescaled)
+  uint64_t* o_done = bars + 12;   //       O MMAs of a tile complete
+  uint64_t* test_bar = bars + 13;
+  uint64_t* fin_bar = bars + 14;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 16);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int st = 0; st < NSTAGE; ++st) {
-      mbar_init(&kv_full[st], 1);
-      mbar_init(&kv_empty[st], 1);
-      mbar_init(&s_full[st], 1);
-      mbar_init(&s_free[st], 4);  // one arrival per softmax warp
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 1);
     }
-    mbar_init(p_full, 4);
+    for (int i = 0; i < NO; ++i) {
+      mbar_init(&o_full[i], 1);
+      mbar_init(&o_empty[i], 1);
+    }
+    mbar_init(&s_ready[0], 1);
+    mbar_init(&s_ready[1], 1);
+    mbar_init(p_full, 4);  // one arrival per softmax warp
     mbar_init(o_done, 1);
     mbar_init(test_bar, 1);  // never signalled: the forced-timeout test waits on it
     mbar_init(fin_bar, 1);
@@ -162,8 +195,9 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_qz);
     prefetch_tmap(&tm_qpe);
-    prefetch_tmap(&tm_z);
-    prefetch_tmap(&tm_kpe);
+    prefetch_tmap(&tm_z64);
+    prefetch_tmap(&tm_kpe64);
+    prefetch_tmap(&tm_z16);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TM_COLS);
@@ -183,109 +217,163 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol_stream = policy_evict_first();
-      int last_issued[NSTAGE] = {-1, -1};
+      const uint64_t pol_keep = policy_evict_last();
+      int last_s[NS] = {-1, -1}, last_o[NO] = {-1, -1};
       mbar_expect_tx(q_full, C::Q_LAT + C::Q_PE);
       for (int kb = 0; kb < C::NBL; ++kb) tma_load_2d(sb + kb * C::Q_BOX, &tm_qz, kb * 64, qrow0, q_full);
       tma_load_2d(sb + C::OFF_QPE, &tm_qpe, 0, qrow0, q_full);
-      for (int t = 0; t < ntiles; ++t) {
-        const int st = t % NSTAGE;
-        if (t >= NSTAGE && !mbar_wait(&kv_empty[st], ((t / NSTAGE) - 1) & 1, p.wait_ns, abort_flag)) {
-          if (!*abort_flag) fail();
-          break;
-        }
-        if (*abort_flag) break;
-        const int key0 = kstart + t * TK;
-        int row;
-        if (p.paged) {
-          int page = p.block_table[(size_t)bi * p.max_pages + key0 / 64];
-          if (page < 0 || page >= p.num_pages) {
-            raise_error(p.err, kErrBadPage);
-            page = 0;  // stay inside the pool; the result is flagged invalid
-          }
-          row = page * 64 + (key0 % 64);
-        } else {
-          row = bi * p.capacity + key0;
-        }
-        const uint32_t dst = sb + C::OFF_STAGE + st * C::STAGE;
-        mbar_expect_tx(&kv_full[st], C::KV_LAT + C::KV_PE);
-        for (int kb = 0; kb < C::NBL; ++kb)
-          tma_load_2d_hint(dst + kb * C::KV_BOX, &tm_z, kb * 64, row, &kv_full[st], pol_stream);
-        tma_load_2d_hint(dst + C::KV_LAT, &tm_kpe, 0, row, &kv_full[st], pol_stream);
-        last_issued[st] = t;
-      }
-      // no copy may still be landing in shared memory when the CTA exits
-      mbar_wait(q_full, 0, kTeardownNs, nullptr);
-      for (int st = 0; st < NSTAGE; ++st)
-        if (last_issued[st] >= 0) mbar_wait(&kv_full[st], (last_issued[st] / NSTAGE) & 1, kTeardownNs, nullptr);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+      int sc = 0, oc = 0;
       bool ok = true;
-      if (p.test_timeout && !mbar_wait(test_bar, 0, kTestWaitNs, abort_flag)) {
-        fail();
-        ok = false;
-      }
-      if (ok && !mbar_wait(q_full, 0, p.wait_ns, abort_flag)) {
-        fail();
-        ok = false;
-      }
-      tc_fence_after();
-      constexpr uint32_t idS = idesc_bf16_f32(BMROWS, TK, false, false);
-      constexpr uint32_t idO = idesc_bf16_f32(BMROWS, C::KLH, false, true);
       for (int t = 0; ok && t <= ntiles; ++t) {
         if (t < ntiles) {
-          const int st = t % NSTAGE;
-          if (!mbar_wait(&kv_full[st], (t / NSTAGE) & 1, p.wait_ns, abort_flag) ||
-              (t >= NSTAGE && !mbar_wait(&s_free[st], ((t - NSTAGE) / NSTAGE) & 1, p.wait_ns, abort_flag))) {
-            if (!*abort_flag) fail();
-            break;
-          }
-          tc_fence_after();
-          const uint32_t stage = sb + C::OFF_STAGE + st * C::STAGE;
-          const uint32_t d_s = tmem + C::TM_S + st * TK;
-          uint32_t acc = 0;
-          for (int kb = 0; kb < C::NBL; ++kb) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t a = smem_desc(sb + kb * C::Q_BOX + kk * 32, 16, 1024, kSw128);
-              const uint64_t bd = smem_desc(stage + kb * C::KV_BOX + kk * 32, 16, 1024, kSw128);
-              tc_mma_ss(d_s, a, bd, idS, acc);
-              acc = 1;
+          const int key0 = kstart + t * TK;
+          const int nhalf = tile_keys(t) > 64 ? 2 : 1;
+          const int row_a = cache_row(p, bi, key0);
+          const int row_b = nhalf > 1 ? cache_row(p, bi, key0 + 64) : 0;
+          for (int j = 0; j < C::NCH; ++j, ++sc) {
+            const int slot = sc % NS;
+            if (sc >= NS && !mbar_wait(&s_empty[slot], ((sc / NS) - 1) & 1, p.wait_ns, abort_flag)) {
+              ok = false;
+              break;
             }
+            const bool pe = j == C::NBL;
+            const uint32_t dst = sb + C::OFF_SRING + slot * C::S_SLOT;
+            const uint32_t half = pe ? C::HALF_PE : C::HALF_LAT;
+            mbar_expect_tx(&s_full[slot], half * nhalf);
+            if (pe) {
+              tma_load_2d_hint(dst, &tm_kpe64, 0, row_a, &s_full[slot], pol_keep);
+              if (nhalf > 1) tma_load_2d_hint(dst + half, &tm_kpe64, 0, row_b, &s_full[slot], pol_keep);
+            } else {
+              // the CTA's own output half is read again for O (from L2): keep it; the rest streams
+              const uint64_t pol = (j / (C::NBL / C::NH)) == lh ? pol_keep : pol_stream;
+              tma_load_2d_hint(dst, &tm_z64, j * 64, row_a, &s_full[slot], pol);
+              if (nhalf > 1) tma_load_2d_hint(dst + half, &tm_z64, j * 64, row_b, &s_full[slot], pol);
+            }
+            last_s[slot] = sc;
           }
-#pragma unroll
-          for (int kk = 0; kk < P / 16; ++kk) {
-            const uint64_t a = smem_desc(sb + C::OFF_QPE + kk * 32, 16, 8 * C::PE_ROW, C::PE_SWZ);
-            const uint64_t bd = smem_desc(stage + C::KV_LAT + kk * 32, 16, 8 * C::PE_ROW, C::PE_SWZ);
-            tc_mma_ss(d_s, a, bd, idS, 1);
-          }
-          tc_commit(&s_full[st]);
         }
-        if (t >= 1) {
+        if (ok && t >= 1) {
           const int u = t - 1;
-          const int su = u % NSTAGE;
-          if (!mbar_wait(p_full, u & 1, p.wait_ns, abort_flag)) {
-            if (!*abort_flag) fail();
-            break;
+          const int key0 = kstart + u * TK;
+          const int nsl = tile_slabs(u);
+          for (int s = 0; s < nsl; ++s, ++oc) {
+            const int slot = oc % NO;
+            if (oc >= NO && !mbar_wait(&o_empty[slot], ((oc / NO) - 1) & 1, p.wait_ns, abort_flag)) {
+              ok = false;
+              break;
+            }
+            const int row = cache_row(p, bi, key0 + s * SLAB);
+            const uint32_t dst = sb + C::OFF_ORING + slot * C::O_SLOT;
+            mbar_expect_tx(&o_full[slot], C::O_SLOT);
+            for (int i = 0; i < C::KLH / 64; ++i)
+              tma_load_2d_hint(dst + i * C::O_SUB, &tm_z16, lh * C::KLH + i * 64, row, &o_full[slot], pol_stream);
+            last_o[slot] = oc;
           }
-          tc_fence_after();
-          const uint32_t zpart = sb + C::OFF_STAGE + su * C::STAGE + (lh * C::KLH / 64) * C::KV_BOX;
-#pragma unroll
-          for (int kk = 0; kk < TK / 16; ++kk) {
-            const uint64_t a = smem_desc(sb + C::OFF_P + kk * 32, 16, 512, kSw64);
-            // Z tile read MN-major: 64-column boxes KV_BOX apart, 8-key groups 1024 B apart
-            const uint64_t bd = smem_desc(zpart + kk * 16 * 128, C::KV_BOX, 1024, kSw128);
-            tc_mma_ss(tmem, a, bd, idO, (u > 0 || kk > 0) ? 1u : 0u);
-          }
-          tc_commit(o_done);
-          tc_commit(&kv_empty[su]);
         }
       }
+      if (!ok && !*abort_flag) fail();
+      // no copy may still be landing in shared memory when the CTA exits
+      mbar_wait(q_full, 0, kTeardownNs, nullptr);
+      for (int i = 0; i < NS; ++i)
+        if (last_s[i] >= 0) mbar_wait(&s_full[i], (last_s[i] / NS) & 1, kTeardownNs, nullptr);
+      for (int i = 0; i < NO; ++i)
+        if (last_o[i] >= 0) mbar_wait(&o_full[i], (last_o[i] / NO) & 1, kTeardownNs, nullptr);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (lane 0; the warp zeroes tails)
+    bool ok = true;
+    if (lane == 0) {
+      if (p.test_timeout && !mbar_wait(test_bar, 0, kTestWaitNs, abort_flag)) ok = false;
+      if (ok && !mbar_wait(q_full, 0, p.wait_ns, abort_flag)) ok = false;
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    tc_fence_after();
+    constexpr uint32_t idS = idesc_bf16_f32(BMROWS, TK, false, false);
+    constexpr uint32_t idO = idesc_bf16_f32(BMROWS, C::KLH, false, true);
+    int sc = 0, oc = 0;
+    for (int t = 0; ok && t <= ntiles; ++t) {
+      if (t < ntiles) {
+        const uint32_t d_s = tmem + C::TM_S + (t & 1) * TK;
+        for (int j = 0; j < C::NCH; ++j, ++sc) {
+          const int slot = sc % NS;
+          if (lane == 0) {
+            if (!mbar_wait(&s_full[slot], (sc / NS) & 1, p.wait_ns, abort_flag)) {
+              ok = false;
+            } else {
+              tc_fence_after();
+              const uint32_t src = sb + C::OFF_SRING + slot * C::S_SLOT;
+              if (j < C::NBL) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  tc_mma_ss(d_s, smem_desc(sb + j * C::Q_BOX + kk * 32, 16, 1024, kSw128),
+                            smem_desc(src + kk * 32, 16, 1024, kSw128), idS, (j > 0 || kk > 0) ? 1u : 0u);
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < P / 16; ++kk)
+                  tc_mma_ss(d_s, smem_desc(sb + C::OFF_QPE + kk * 32, 16, 8 * C::PE_ROW, C::PE_SWZ),
+                            smem_desc(src + kk * 32, 16, 8 * C::PE_ROW, C::PE_SWZ), idS, 1u);
+              }
+              tc_commit(&s_empty[slot]);
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+            ok = false;
+            break;
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) tc_commit(&s_ready[t & 1]);
+      }
+      if (t >= 1) {
+        const int u = t - 1;
+        const int key0 = kstart + u * TK;
+        const int nsl = tile_slabs(u);
+        if (lane == 0 && !mbar_wait(p_full, u & 1, p.wait_ns, abort_flag)) ok = false;
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
+        for (int s = 0; s < nsl; ++s, ++oc) {
+          const int slot = oc % NO;
+          if (lane == 0 && !mbar_wait(&o_full[slot], (oc / NO) & 1, p.wait_ns, abort_flag)) ok = false;
+          if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+            ok = false;
+            break;
+          }
+          __syncwarp();
+          const int first_bad = L - (key0 + s * SLAB);  // rows at or past the sequence end
+          if (first_bad < SLAB) {
+            const uint32_t base = C::OFF_ORING + slot * C::O_SLOT;
+            const int nrow = SLAB - first_bad;
+            for (int idx = lane; idx < nrow * (C::KLH / 64) * 8; idx += 32) {
+              const int rr = first_bad + idx / ((C::KLH / 64) * 8);
+              const int rem = idx % ((C::KLH / 64) * 8);
+              *reinterpret_cast<uint4*>(smem + base + (rem / 8) * C::O_SUB + rr * 128 + (rem % 8) * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          if (lane == 0) {
+            tc_fence_after();
+            const uint64_t a = smem_desc(sb + C::OFF_P + (s / 4) * C::P_BOX + (s % 4) * 32, 16, 1024, kSw128);
+            // Z slab read MN-major: 64-column boxes O_SUB apart, 8-key groups 1024 B apart
+            const uint64_t bd = smem_desc(sb + C::OFF_ORING + slot * C::O_SLOT, C::O_SUB, 1024, kSw128);
+            tc_mma_ss(tmem, a, bd, idO, (u > 0 || s > 0) ? 1u : 0u);
+            tc_commit(&o_empty[slot]);
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) tc_commit(o_done);
+      }
+    }
+    if (lane == 0) {
+      if (!ok && !*abort_flag) fail();
       // every issued tcgen05 operation has finished before TMEM is released
       tc_commit(fin_bar);
       mbar_wait(fin_bar, 0, kTeardownNs, nullptr);
     }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax + epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
@@ -294,33 +382,31 @@ __global__ void __launch_bounds__(192, 1)
     const bool row_ok = row_in_seq < p.rows;
     const int lim = row_ok ? min(kend, L - p.s + (row_in_seq % p.s) + 1) : 0;  // exclusive key limit
     const uint32_t t_lane = tmem + ((uint32_t)(q * 32) << 16);
-    const int sm_tid = threadIdx.x - 64;  // 0..127
     float m_ref = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
-      const int st = t % NSTAGE;
       // waits are made warp-uniform: the tcgen05 loads below are warp-collective
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[st], (t / NSTAGE) & 1, p.wait_ns, abort_flag))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_ready[t & 1], (t >> 1) & 1, p.wait_ns, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t sv[32];
-      tmem_ld32(t_lane + C::TM_S + st * TK, sv);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[st]);
-
       const int key0 = kstart + t * TK;
-      float x[32];
+      float x[TK];
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        x[c] = (key0 + c < lim) ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, x[c]);
+      for (int c0 = 0; c0 < TK; c0 += 32) {
+        uint32_t sv[32];
+        tmem_ld32(t_lane + C::TM_S + (t & 1) * TK + c0, sv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float v = (key0 + c0 + c < lim) ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
+          x[c0 + c] = v;
+          mx = fmaxf(mx, v);
+        }
       }
-      // the previous O MMA must be complete: it still reads P, and O may be rescaled
+      // the previous O MMAs must be complete: they still read P, and O may be rescaled
       if (t > 0 && !__all_sync(0xffffffffu, mbar_wait(o_done, (t - 1) & 1, p.wait_ns, abort_flag))) {
         ok = false;
         break;
@@ -343,35 +429,24 @@ __global__ void __launch_bounds__(192, 1)
         }
         tmem_st_wait();
       }
-      // latent rows past the sequence end may hold anything: zero them so P Z stays finite
-      if (key0 + TK > L) {
-        const int first = max(0, L - key0);
-        const uint32_t zpart = C::OFF_STAGE + st * C::STAGE + (lh * C::KLH / 64) * C::KV_BOX;
-        const int nrow = TK - first;
-        for (int idx = sm_tid; idx < nrow * (C::KLH / 64) * 8; idx += 128) {
-          const int rr = first + idx / ((C::KLH / 64) * 8);
-          const int rem = idx % ((C::KLH / 64) * 8);
-          const int box = rem / 8, ch = rem % 8;
-          *reinterpret_cast<uint4*>(smem + zpart + box * C::KV_BOX + rr * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
-        }
-      }
-      // P row (bf16), 64-byte swizzled K-major layout
-      uint32_t pk[16];
+      // P row (bf16) into two 128-byte-swizzled [128 rows x 64 keys] boxes
       float ps = 0.f;
+      const bool live = m_ref != -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        const float p0 = m_ref == -INFINITY ? 0.f : exp2f(x[c] - m_ref);
-        const float p1 = m_ref == -INFINITY ? 0.f : exp2f(x[c + 1] - m_ref);
-        pk[c / 2] = pack_bf16(p0, p1);
-        ps += p0 + p1;
+      for (int ch = 0; ch < TK / 8; ++ch) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = live ? exp2f(x[ch * 8 + 2 * e] - m_ref) : 0.f;
+          const float p1 = live ? exp2f(x[ch * 8 + 2 * e + 1] - m_ref) : 0.f;
+          ps += p0 + p1;
+          pk[e] = pack_bf16(p0, p1);
+        }
+        const int box = ch / 8, lc = ch % 8;
+        *reinterpret_cast<uint4*>(smem + C::OFF_P + box * C::P_BOX + r * 128 + ((lc ^ (r & 7)) * 16)) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
       l_run += ps;
-      uint8_t* prow = smem + C::OFF_P + r * 64;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        const int phys = ch ^ ((r >> 1) & 3);
-        *reinterpret_cast<uint4*>(prow + phys * 16) = make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
-      }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -475,9 +550,10 @@ cudaError_t launch_kl(const MlaLaunch& a, cudaStream_t stream) {
   }
   const uint64_t qrows = (uint64_t)a.b * a.h * a.s;
   const uint64_t krows = a.paged ? (uint64_t)a.num_pages * 64 : (uint64_t)a.b * a.capacity;
-  CUtensorMap tqz, tqpe, tz, tkpe;
+  CUtensorMap tqz, tqpe, tz64, tkpe64, tz16;
   if (!make_map(&tqz, a.qz, qrows, KL, BMROWS, 64) || !make_map(&tqpe, a.q_pe, qrows, P, BMROWS, P) ||
-      !make_map(&tz, a.z, krows, KL, TK, 64) || !make_map(&tkpe, a.k_pe, krows, P, TK, P))
+      !make_map(&tz64, a.z, krows, KL, 64, 64) || !make_map(&tkpe64, a.k_pe, krows, P, 64, P) ||
+      !make_map(&tz16, a.z, krows, KL, SLAB, 64))
     return cudaErrorInvalidValue;
   MlaParams p;
   p.seqlens = a.seqlens;
@@ -502,13 +578,14 @@ cudaError_t launch_kl(const MlaLaunch& a, cudaStream_t stream) {
   p.test_timeout = a.test_timeout;
   const int mtiles = (p.rows + BMROWS - 1) / BMROWS;
   dim3 grid(C::NH * mtiles, a.nsplit, a.b);
-  mla_latent_kernel<KL, P><<<grid, 192, C::SMEM, stream>>>(tqz, tqpe, tz, tkpe, p);
+  mla_latent_kernel<KL, P><<<grid, 192, C::SMEM, stream>>>(tqz, tqpe, tz64, tkpe64, tz16, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 int mla_latent_parts(int k) { return k >= 512 ? 2 : 1; }
+int mla_tile_keys() { return TK; }
 bool mla_supported(int k, int p) { return (k == 512 && p == 64) || (k == 64 && p == 16); }
 
 cudaError_t launch_mla_latent(const MlaLaunch& a, cudaStream_t stream) {

@@ -55,7 +55,7 @@ def seq_inputs(inp, seqs):
     return zs, kp
 
 
-def check(inp, res, seqs=None, what=""):
+def check(inp, res, seqs=None, what="", e2e_max_abs=None):
     out, lse, qz, o_lat = res
     seqs = list(range(len(inp.seqlens))) if seqs is None else seqs
     sl = [inp.seqlens[i] for i in seqs]
@@ -77,7 +77,10 @@ def check(inp, res, seqs=None, what=""):
     # end to end from the bf16 inputs, nothing rounded in between
     eo, el, eqz, eolat = A.mla_absorbed_ref(f64(inp.q_nope[seqs]), f64(inp.q_pe[seqs]), zs, kp, f64(inp.w_uk),
                                             f64(inp.w_uv), sl, inp.scale)
-    assert_out_close(f64(out[seqs]), eo, what + " end-to-end")
+    if e2e_max_abs is None:
+        assert_out_close(f64(out[seqs]), eo, what + " end-to-end")
+    else:
+        assert_out_close(f64(out[seqs]), eo, what + " end-to-end", max_abs=e2e_max_abs)
     assert_lse_close(f64(lse[seqs]), el, what + " end-to-end lse", tol=qz_rounding_lse_bound(eqz, eolat, inp.scale))
 
 
@@ -133,8 +136,15 @@ def test_paged_vs_oracle_and_bitwise_contiguous():
 
 
 def test_sharp_queries():
+    # queries x 8: logits of a few units, a peaked softmax. Every stage keeps
+    # the 2e-2 bound against the oracle fed the same bf16 tensor. End to end,
+    # the bf16 rounding of the Qz intermediate (relative 2^-9 on |Qz| ~ 4)
+    # shifts a logit by scale * |dQz . Z| ~ 2^-9 * 4 * sqrt(512) / sqrt(192)
+    # ~ 0.013 per unit of logit scale, i.e. a few percent on the dominant
+    # weights: the end-to-end max-abs bound is 5e-2 here (mean and rel-RMS
+    # bounds unchanged).
     inp = make(2, 128, 128, 512, 64, 1, [400, 900], seed=4, q_std=8.0)
-    check(inp, forward(inp), what="sharp")
+    check(inp, forward(inp), what="sharp", e2e_max_abs=5e-2)
 
 
 @pytest.mark.parametrize("nsplit", [1, 2, 5])
@@ -148,7 +158,7 @@ def test_split_invariance(nsplit):
         sl = torch.tensor(inp.seqlens, dtype=torch.int32, device=DEV)
         o2, l2 = da.mla_decode(base[2], inp.q_pe, inp.z, inp.k_pe, sl, scale=inp.scale, max_seqlen=1500)
         torch.cuda.synchronize()
-        chunk = -(-(-(-1500 // nsplit)) // 64) * 64  # chunks are whole 64-key pages
+        chunk = -(-(-(-1500 // nsplit)) // 128) * 128  # chunks are whole 128-key latent tiles
         assert da.last_num_splits() == -(-1500 // chunk)
     finally:
         da.set_forced_splits(0)

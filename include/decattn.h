@@ -140,6 +140,32 @@ int mla_out_proj(const decattn_bf16* o_lat, const decattn_bf16* w_uv, decattn_bf
                  int b, int s, int h, int k, int d, float scale, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Grouped-head decode that allocates nothing and takes no workspace.
+ * The pages have no counterpart: this is a convenience for callers that
+ * cannot allocate device memory - an engine whose allocator already holds
+ * nearly all of HBM, a plug-in host that exposes no device allocator, a
+ * loop that cannot afford cudaMalloc's implicit synchronisation.
+ * Same arguments, layouts, results and errors as gqa_decode, minus the
+ * workspace: the split partials live in one fixed array of
+ * DECATTN_NO_ALLOC_SCRATCH_BYTES in the library's device image, which every
+ * GPU that loads the library holds until the process exits.
+ *   - Returns DECATTN_ERR_WORKSPACE, launching nothing, when the split plan
+ *     needs more than DECATTN_NO_ALLOC_SCRATCH_BYTES
+ *     (gqa_decode_workspace_size(...) > the limit).
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address (cudaGetSymbolAddress); make that first call
+ *     before any stream capture on the device.
+ *   - All calls on a device share the one array and it keeps the last
+ *     call's contents (no call relies on them). Calls that overlap on the
+ *     GPU (other streams, other host threads) race on it: serialise them.
+ *   - Calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define DECATTN_NO_ALLOC_SCRATCH_BYTES ((size_t)16 << 20) /* 16 MiB */
+int gqa_decode_no_alloc(const decattn_bf16* q, const decattn_bf16* k, const decattn_bf16* v, decattn_kv kv,
+                        const int32_t* seqlens, int max_seqlen, int b, int s, int hq, int hkv, int d, float scale,
+                        decattn_bf16* out, float* lse, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Diagnostics.
  * decattn_check_errors: synchronises `stream`, reads and clears the device
  * error word of the current device; returns DECATTN_ERR_TIMEOUT if a bounded

@@ -29,7 +29,6 @@ import math
 import os
 import statistics
 import sys
-import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -50,6 +49,10 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the grouped-head and s-sweep side measurements")
+    ap.add_argument("--profile", default=None, metavar="WORKLOAD",
+                    help="profiling mode: run --warmup + --steps calls of one op on one input set of the named "
+                         "workload (mla_dsv3, mla_mtp_s8, gqa_64_8, gqa_paged_hkv4, ...) and exit; prints no "
+                         "bench line (numbers taken under a profiler are not bench values)")
     return ap.parse_args()
 
 
@@ -62,67 +65,66 @@ def peaks():
 
 
 class ClockSampler:
-    """Samples the SM clock and clock-event reasons through NVML in a thread."""
+    """Samples SM clocks and clock-event reasons with nvidia-smi (every
+    100 ms) while the timed region runs. `gpu` is the device's UUID (or
+    index) as nvidia-smi knows it."""
 
-    def __init__(self, index: int, period_s: float = 0.01):
-        self.index, self.period = index, period_s
-        self.samples, self.reasons = [], set()
-        self.max_mhz = None
-        self._stop = threading.Event()
-        self._t = None
-        self.ok = False
+    FIELDS = ("clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu: str, period_ms: int = 100):
+        self.gpu, self.period = gpu, period_ms
+        self.proc = None
+        self.lines = []
+        self.error = None
 
     def __enter__(self):
+        import subprocess
+
         try:
-            import pynvml as nv
-
-            nv.nvmlInit()
-            self.nv = nv
-            self.h = nv.nvmlDeviceGetHandleByIndex(self.index)
-            self.max_mhz = nv.nvmlDeviceGetMaxClockInfo(self.h, nv.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception:
-            return self
-        names = {
-            "hw_slowdown": getattr(self.nv, "nvmlClocksEventReasonHwSlowdown", 0x8),
-            "sw_thermal_slowdown": getattr(self.nv, "nvmlClocksEventReasonSwThermalSlowdown", 0x20),
-            "hw_thermal_slowdown": getattr(self.nv, "nvmlClocksEventReasonHwThermalSlowdown", 0x40),
-            "sw_power_cap": getattr(self.nv, "nvmlClocksEventReasonSwPowerCap", 0x4),
-            "hw_power_brake_slowdown": getattr(self.nv, "nvmlClocksEventReasonHwPowerBrakeSlowdown", 0x80),
-        }
-
-        def run():
-            while not self._stop.is_set():
-                self._sample(names)
-                time.sleep(self.period)
-
-        self._sample(names)
-        self._t = threading.Thread(target=run, daemon=True)
-        self._t.start()
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", str(self.period)],
+                stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
+            time.sleep(0.3)  # let the first sample land before the timed region
+        except Exception as e:  # no nvidia-smi: reported, not fatal
+            self.error = repr(e)
         return self
 
-    def _sample(self, names):
-        try:
-            self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
-            r = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-            for n, bit in names.items():
-                if r & bit:
-                    self.reasons.add(n)
-        except Exception:
-            pass
-
     def __exit__(self, *a):
-        if self.ok:
-            self._stop.set()
-            if self._t:
-                self._t.join()
-            self._sample({})
+        if self.proc is None:
+            return
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, err = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, err = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        if not self.lines and err:
+            self.error = err.strip()[:200]
 
     def summary(self):
-        if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": sorted(self.reasons), "samples": len(self.samples), "source": "nvml"}
+        sm, mx, reasons = [], None, set()
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, f[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0, "error": self.error}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
+                "sm_mhz_min": min(sm), "source": "nvidia-smi -lms %d" % self.period}
 
 
 def cost_numbers(wl):
@@ -246,6 +248,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile:
+        return run_profile(args)
 
     import numpy as np
     import torch
@@ -336,7 +340,10 @@ def main():
             ms = float(t.item())
         return ms
 
-    with ClockSampler(local) as clk:
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    gpu_id = str(local) if uuid is None else (str(uuid) if str(uuid).startswith("GPU-") else "GPU-" + str(uuid))
+    with ClockSampler(gpu_id) as clk:
         total_ms = timed(graphs, args.steps, args.warmup)
     dec_steps = max(args.steps, 500)
     dec_ms = timed(dgraphs, dec_steps, max(3, args.warmup // 4))
@@ -429,6 +436,38 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+    return 0
+
+
+def run_profile(args):
+    """A few calls of one op on one input set, for ncu (no timing, no JSON)."""
+    import torch
+
+    import decode_attention_18_b300 as da
+    from decode_attention_18_b300 import workloads as W
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = W.WORKLOADS[args.profile]
+    seqlens = wl.seqlens()
+    L = max(seqlens)
+    sl = torch.tensor(seqlens, dtype=torch.int32, device=dev)
+    if wl.kind == "gqa":
+        q, c = W.make_gqa(wl.b, wl.heads, wl.hkv, wl.d, wl.s, seqlens, paged=wl.paged, seed=wl.seed, device=dev)
+
+        def fn():
+            da.gqa_decode(q, c.k, c.v, sl, max_seqlen=L, block_table=c.block_table if wl.paged else None)
+    else:
+        x = W.make_mla(wl.b, wl.heads, wl.d, wl.k, wl.p, wl.s, seqlens, seed=wl.seed, device=dev)
+        qz = da.mla_absorb_q(x.q_nope, x.w_uk, sl)
+
+        def fn():
+            da.mla_decode(qz, x.q_pe, x.z, x.k_pe, sl, scale=x.scale, max_seqlen=L)
+    for _ in range(args.warmup + args.steps):
+        fn()
+    torch.cuda.synchronize()
+    assert da.check_errors() == 0
+    print(f"profiled {args.profile}: {args.warmup + args.steps} calls, splits {da.last_num_splits()}", flush=True)
     return 0
 
 

@@ -171,6 +171,7 @@ int decattn_check_errors(cudaStream_t stream) {
   if (cudaMemcpyToSymbol(g_err_word, &zero, sizeof(zero)) != cudaSuccess) return DECATTN_ERR_CUDA;
   if (word & kErrWaitTimeout) return DECATTN_ERR_TIMEOUT;
   if (word & kErrBadPage) return DECATTN_ERR_INVALID_ARG;
+  if (word & kErrLaunch) return DECATTN_ERR_CUDA;
   return DECATTN_OK;
 }
 

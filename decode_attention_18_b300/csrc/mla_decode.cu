@@ -13,30 +13,35 @@
 //   * All h*s query rows of a sequence are packed into the MMA M dimension
 //     (row = head*s + token), 128 rows per CTA.
 //   * Q' = [Qz | q_pe] stays in shared memory for the whole chunk. The cache
-//     is consumed in tiles of 128 latent rows. For S, each tile streams
-//     through a ring of 16 KB shared-memory slots, one 64-wide column chunk
-//     [128 rows x 64] (or the RoPE chunk) at a time, loaded by TMA as two
-//     64-row boxes (so a box never crosses a 64-token page). For O, the
-//     CTA's 256 output columns of the same rows stream again (from L2) in
-//     16-row slabs through a second ring.
+//     is consumed in tiles of 128 latent rows. One ring of 16 KB slots carries,
+//     in exactly the order the MMAs consume them, the tile's 64-wide column
+//     chunks [128 rows x 64] (plus the RoPE chunk), each loaded by TMA as two
+//     64-row boxes (a box never crosses a 64-token page), and the O slab
+//     pairs: the CTA's own output columns of 32 latent rows, re-read from L2.
+//     Tiles two ahead are pulled into L2 first, so the ring waits on L2.
 //   * tcgen05.mma (kind::f16, bf16 in, fp32 accumulate in Tensor Memory):
-//       S  = Q' K'^T    M=128, N=128 keys, K=k+p  (K-major A and B)
-//       O += P Z_half   M=128, N=256,      K=16 keys per slab (Z read MN-major)
+//       S  = Q' K'^T    M=128, N=128 keys, K=k+p   (both operands in smem)
+//       O += P Z_half   M=128, N=256 cols, K=16 keys per slab, with P read
+//                       from Tensor Memory and the Z slab (MN-major) from smem
 //     The fp32 accumulator of 128 rows x k = 512 columns would fill all of
 //     TMEM, so the output columns are split over 2 CTAs per row tile, each
-//     recomputing S for the same rows; TMEM holds O (256 columns) and two
-//     128-column S buffers, so S of the next tile is computed while the
-//     softmax of the current one runs. On this part a tcgen05.mma costs about
-//     100 cycles to issue whatever its N, so N = 128 keeps the tensor pipe fed.
-//   * Softmax warps (thread = row) read S with tcgen05.ld, apply the causal
-//     mask and scale, and keep a reference maximum that moves only when a
-//     row's maximum grows by more than 2^8 (O is then rescaled in TMEM); P is
-//     written as bf16 into shared memory (128-byte swizzled) for the O MMA.
-//   * Warp roles: warp 0 issues TMA, warp 1 issues MMAs (one thread) and owns
-//     the TMEM allocation, warps 2-5 run the softmax and the epilogue.
+//     recomputing S for the same rows. TMEM holds O (256 columns) and two
+//     128-column S buffers; the softmax writes P (bf16, two per column) over
+//     the first 64 columns of its own S buffer, so P is double-buffered too.
+//   * The O MMAs of tile t are issued interleaved with the S MMAs of tile
+//     t+1, so the tensor pipe stays busy while the softmax of tile t runs.
+//     tcgen05 MMAs of one thread execute in issue order, so the S of tile t+2
+//     (same buffer) never overtakes the O MMAs still reading P of tile t.
+//   * Softmax: two warps per TMEM lane quadrant (thread = row, 64 keys each);
+//     they exchange row maxima through shared memory and keep one reference
+//     maximum per row that moves only when the row maximum grows by more than
+//     2^8 (O is then rescaled in TMEM). Exponentials use ex2.approx.
+//   * Warp roles: warp 0 issues TMA loads and L2 prefetches, warp 1 issues
+//     MMAs (lane 0; the warp zeroes tails and owns the TMEM allocation),
+//     warps 2-9 run the softmax and the epilogue.
 //   * Latent rows past the sequence end may hold anything: slabs wholly past
-//     it are not loaded or multiplied; the one slab that straddles it has its
-//     rows past the end zeroed before the O MMA, so P Z stays finite.
+//     it are not multiplied; a slab that straddles it has its rows past the
+//     end zeroed before the O MMA, so P Z stays finite.
 //   * Every mbarrier wait is bounded; on time-out the CTA records the error,
 //     stops issuing work, waits for its own copies and MMAs, frees TMEM and
 //     returns.
@@ -52,10 +57,13 @@ namespace decattn {
 namespace {
 
 constexpr int TK = 128;         // latent rows (keys) per S tile
-constexpr int NS = 2;           // S-ring slots (one 64-wide column chunk of a tile each)
-constexpr int NO = 2;           // O-ring slots (one 16-row slab each)
+constexpr int NR = 5;           // ring slots (16 KB each)
 constexpr int SLAB = 16;        // keys per O slab (= MMA K)
+constexpr int PAIR = 2 * SLAB;  // keys per O ring item
 constexpr int BMROWS = 128;     // query rows per CTA (MMA M)
+constexpr int PF = 2;           // tiles pulled into L2 ahead of the ring
+constexpr int NSMW = 8;         // softmax warps
+constexpr int NTHREADS = 32 * (2 + NSMW);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.f;                        // move the reference max only past 2^8
@@ -86,28 +94,31 @@ struct MlaCfg {
   static constexpr int KLH = KL / NH;           // O columns per CTA
   static constexpr int NBL = KL / 64;           // 64-wide latent column chunks
   static constexpr int NCH = NBL + 1;           // + the RoPE chunk
+  static constexpr int J0 = NCH > 5 ? 5 : NCH - 1;  // O items of the previous tile start after chunk J0
   static constexpr int PE_ROW = P * 2;          // bytes per RoPE row
   static constexpr uint32_t PE_SWZ = PE_ROW == 128 ? kSw128 : (PE_ROW == 64 ? kSw64 : kSw32);
   static constexpr int Q_BOX = BMROWS * 128;
   static constexpr int Q_LAT = NBL * Q_BOX;
   static constexpr int Q_PE = BMROWS * PE_ROW;
-  static constexpr int S_SLOT = TK * 128;             // one [128 keys x 64] chunk
+  static constexpr int SLOT = TK * 128;               // ring slot: one [128 keys x 64] chunk
   static constexpr int HALF_LAT = 64 * 128;           // one 64-row box of a latent chunk
   static constexpr int HALF_PE = 64 * PE_ROW;         // one 64-row box of the RoPE chunk
-  static constexpr int O_SUB = SLAB * 128;            // [16 keys x 64 cols]
-  static constexpr int O_SLOT = (KLH / 64) * O_SUB;   // [16 keys x KLH cols]
-  static constexpr int P_BOX = BMROWS * 128;          // [128 rows x 64 keys] of P
+  static constexpr int PBOX = PAIR * 128;             // [32 keys x 64 cols] box of an O item
+  static constexpr int PAIR_BYTES = (KLH / 64) * PBOX;
   static constexpr int OFF_QPE = Q_LAT;
-  static constexpr int OFF_P = align1024(Q_LAT + Q_PE);
-  static constexpr int OFF_SRING = OFF_P + 2 * P_BOX;
-  static constexpr int OFF_ORING = OFF_SRING + NS * S_SLOT;
-  static constexpr int OFF_BAR = align1024(OFF_ORING + NO * O_SLOT);
-  static constexpr int SMEM = OFF_BAR + 256 + 1024;  // + barriers + alignment slack
+  static constexpr int OFF_RING = align1024(Q_LAT + Q_PE);
+  static constexpr int OFF_RED = OFF_RING + NR * SLOT;          // row-max exchange [2][2][128] floats
+  static constexpr int OFF_BAR = align1024(OFF_RED + 2 * 2 * BMROWS * 4);
+  // + barriers. No alignment slack: the dynamic window follows the CTA's 1 KB reserved
+  // shared memory and is 1024-byte aligned; the kernel checks this and refuses otherwise.
+  static constexpr int SMEM = OFF_BAR + 256;
   static constexpr int TM_S = KLH;                   // two S buffers after the O accumulator
   static constexpr int TM_COLS = pow2_cols(KLH + 2 * TK);
   static_assert(KL % 64 == 0 && KLH % 64 == 0 && KLH <= 256, "latent width");
   static_assert(P % 16 == 0 && PE_ROW <= 128, "rope width");
+  static_assert(PAIR_BYTES <= SLOT, "O item fits a ring slot");
   static_assert(SMEM <= 232448, "shared memory");
+  static_assert(KLH + 2 * TK <= 512, "tensor memory");
 };
 
 __device__ __forceinline__ int cache_row(const MlaParams& p, int bi, int key) {
@@ -122,16 +133,46 @@ __device__ __forceinline__ int cache_row(const MlaParams& p, int bi, int key) {
   return bi * p.capacity + key;
 }
 
+// warp-uniform bounded wait (every lane polls; all agree on the outcome)
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns, volatile int* abort_flag) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, limit_ns, abort_flag));
+}
+
+// The ring's item sequence, shared by the producer and the MMA issuer:
+// iteration u (0..ntiles) carries the NCH chunks of tile u (u < ntiles) with
+// the O items (32-key slab pairs) of tile u-1 spread over chunks J0..NCH-1;
+// the last iteration carries only the O items of the last tile.
+template <int NCH, int J0, class Chunk, class Pair>
+__device__ __forceinline__ bool walk_iteration(int u, int ntiles, int npairs_prev, Chunk&& chunk, Pair&& pair) {
+  if (u >= ntiles) {
+    for (int q = 0; q < npairs_prev; ++q)
+      if (!pair(u - 1, q)) return false;
+    return true;
+  }
+  int done = 0;
+  for (int j = 0; j < NCH; ++j) {
+    if (!chunk(u, j)) return false;
+    if (npairs_prev > 0 && j >= J0) {
+      const int target = (npairs_prev * (j - J0 + 1) + (NCH - J0) - 1) / (NCH - J0);
+      for (; done < target; ++done)
+        if (!pair(u - 1, done)) return false;
+    }
+  }
+  return true;
+}
+
 template <int KL, int P>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(NTHREADS, 1)
     mla_latent_kernel(const __grid_constant__ CUtensorMap tm_qz, const __grid_constant__ CUtensorMap tm_qpe,
                       const __grid_constant__ CUtensorMap tm_z64, const __grid_constant__ CUtensorMap tm_kpe64,
-                      const __grid_constant__ CUtensorMap tm_z16, MlaParams p) {
+                      const __grid_constant__ CUtensorMap tm_z32, MlaParams p) {
   using C = MlaCfg<KL, P>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sb = smem_u32(smem);
+  if (sb & 1023u) {  // 128-byte swizzled tiles need 1024-byte aligned slots
+    if (threadIdx.x == 0) raise_error(p.err, kErrLaunch);
+    return;
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int lh = blockIdx.x % C::NH;
@@ -158,35 +199,32 @@ __global__ void __launch_bounds__(192, 1)
   const int qrow0 = bi * p.rows + mt * BMROWS;  // first flattened [b*h*s] query row
   auto tile_keys = [&](int t) { return min(TK, kend - (kstart + t * TK)); };
   auto tile_slabs = [&](int t) { return (tile_keys(t) + SLAB - 1) / SLAB; };
+  auto tile_pairs = [&](int t) { return t >= 0 ? (tile_keys(t) + PAIR - 1) / PAIR : 0; };
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars + 0;
-  uint64_t* s_full = bars + 1;    // [NS]  chunk landed
-  uint64_t* s_empty = bars + 3;   // [NS]  chunk consumed by the S MMAs
-  uint64_t* o_full = bars + 5;    // [NO]  slab landed
-  uint64_t* o_empty = bars + 7;   // [NO]  slab consumed by the O MMA
-  uint64_t* s_ready = bars + 9;   // [2]   S tile in TMEM
-  uint64_t* p_full = bars + 11;   //       P in shared memory (+ O rescaled)
-  uint64_t* o_done = bars + 12;   //       O MMAs of a tile complete
-  uint64_t* test_bar = bars + 13;
-  uint64_t* fin_bar = bars + 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 16);
+  uint64_t* r_full = bars + 1;     // [NR] ring item landed
+  uint64_t* r_empty = bars + 6;    // [NR] ring item consumed by its MMAs
+  uint64_t* s_ready = bars + 11;   // [2]  S tile in TMEM (and the previous tile's O MMAs complete)
+  uint64_t* p_full = bars + 13;    //      P in TMEM (+ O rescaled)
+  uint64_t* o_final = bars + 14;   //      last O MMAs complete
+  uint64_t* test_bar = bars + 15;
+  uint64_t* fin_bar = bars + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 18);
+  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);  // [parity][column half][row]
+  volatile int* okf = reinterpret_cast<volatile int*>(bars + 20);  // [parity][column half][quadrant]
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 1);
-    }
-    for (int i = 0; i < NO; ++i) {
-      mbar_init(&o_full[i], 1);
-      mbar_init(&o_empty[i], 1);
+    for (int i = 0; i < NR; ++i) {
+      mbar_init(&r_full[i], 1);
+      mbar_init(&r_empty[i], 1);
     }
     mbar_init(&s_ready[0], 1);
     mbar_init(&s_ready[1], 1);
-    mbar_init(p_full, 4);  // one arrival per softmax warp
-    mbar_init(o_done, 1);
+    mbar_init(p_full, NSMW);  // one arrival per softmax warp
+    mbar_init(o_final, 1);
     mbar_init(test_bar, 1);  // never signalled: the forced-timeout test waits on it
     mbar_init(fin_bar, 1);
     *abort_flag = 0;
@@ -197,7 +235,7 @@ __global__ void __launch_bounds__(192, 1)
     prefetch_tmap(&tm_qpe);
     prefetch_tmap(&tm_z64);
     prefetch_tmap(&tm_kpe64);
-    prefetch_tmap(&tm_z16);
+    prefetch_tmap(&tm_z32);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TM_COLS);
@@ -214,158 +252,173 @@ __global__ void __launch_bounds__(192, 1)
   };
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      const uint64_t pol_stream = policy_evict_first();
-      const uint64_t pol_keep = policy_evict_last();
-      int last_s[NS] = {-1, -1}, last_o[NO] = {-1, -1};
-      mbar_expect_tx(q_full, C::Q_LAT + C::Q_PE);
-      for (int kb = 0; kb < C::NBL; ++kb) tma_load_2d(sb + kb * C::Q_BOX, &tm_qz, kb * 64, qrow0, q_full);
-      tma_load_2d(sb + C::OFF_QPE, &tm_qpe, 0, qrow0, q_full);
-      int sc = 0, oc = 0;
-      bool ok = true;
-      for (int t = 0; ok && t <= ntiles; ++t) {
-        if (t < ntiles) {
-          const int key0 = kstart + t * TK;
-          const int nhalf = tile_keys(t) > 64 ? 2 : 1;
-          const int row_a = cache_row(p, bi, key0);
-          const int row_b = nhalf > 1 ? cache_row(p, bi, key0 + 64) : 0;
-          for (int j = 0; j < C::NCH; ++j, ++sc) {
-            const int slot = sc % NS;
-            if (sc >= NS && !mbar_wait(&s_empty[slot], ((sc / NS) - 1) & 1, p.wait_ns, abort_flag)) {
-              ok = false;
-              break;
-            }
-            const bool pe = j == C::NBL;
-            const uint32_t dst = sb + C::OFF_SRING + slot * C::S_SLOT;
-            const uint32_t half = pe ? C::HALF_PE : C::HALF_LAT;
-            mbar_expect_tx(&s_full[slot], half * nhalf);
-            if (pe) {
-              tma_load_2d_hint(dst, &tm_kpe64, 0, row_a, &s_full[slot], pol_keep);
-              if (nhalf > 1) tma_load_2d_hint(dst + half, &tm_kpe64, 0, row_b, &s_full[slot], pol_keep);
-            } else {
-              // the CTA's own output half is read again for O (from L2): keep it; the rest streams
-              const uint64_t pol = (j / (C::NBL / C::NH)) == lh ? pol_keep : pol_stream;
-              tma_load_2d_hint(dst, &tm_z64, j * 64, row_a, &s_full[slot], pol);
-              if (nhalf > 1) tma_load_2d_hint(dst + half, &tm_z64, j * 64, row_b, &s_full[slot], pol);
-            }
-            last_s[slot] = sc;
-          }
-        }
-        if (ok && t >= 1) {
-          const int u = t - 1;
-          const int key0 = kstart + u * TK;
-          const int nsl = tile_slabs(u);
-          for (int s = 0; s < nsl; ++s, ++oc) {
-            const int slot = oc % NO;
-            if (oc >= NO && !mbar_wait(&o_empty[slot], ((oc / NO) - 1) & 1, p.wait_ns, abort_flag)) {
-              ok = false;
-              break;
-            }
-            const int row = cache_row(p, bi, key0 + s * SLAB);
-            const uint32_t dst = sb + C::OFF_ORING + slot * C::O_SLOT;
-            mbar_expect_tx(&o_full[slot], C::O_SLOT);
-            for (int i = 0; i < C::KLH / 64; ++i)
-              tma_load_2d_hint(dst + i * C::O_SUB, &tm_z16, lh * C::KLH + i * 64, row, &o_full[slot], pol_stream);
-            last_o[slot] = oc;
-          }
-        }
+    // ------------------------------------------------------------ producer: TMA into the ring + L2 prefetch
+    // One thread's bulk copies are served one after another (~16-19 B/clk per issuing
+    // thread on this part), so the boxes of each ring item are issued by different
+    // lanes, rotating over the warp; the whole warp walks the item sequence together.
+    const uint64_t pol_last = policy_evict_first();  // O items are the last reads of those rows
+    int last[NR];
+    for (int i = 0; i < NR; ++i) last[i] = -1;
+    int rot = 0;  // lane that issues the next box
+    auto my_box = [&](int nbox) -> int {  // box index this lane issues (or -1); advances the rotation
+      const int k = (lane - rot + 32) & 31;
+      rot = (rot + nbox) & 31;
+      return k < nbox ? k : -1;
+    };
+    auto prefetch_tile = [&](int t) {
+      const int key0 = kstart + t * TK;
+      const bool two = tile_keys(t) > 64;
+      const int k = my_box(2 * C::NCH);
+      if (k >= 0 && (k < C::NCH || two)) {
+        const int row = cache_row(p, bi, key0 + (k >= C::NCH ? 64 : 0));
+        const int j = k % C::NCH;
+        if (j < C::NBL) tma_prefetch_l2_2d(&tm_z64, j * 64, row);
+        else tma_prefetch_l2_2d(&tm_kpe64, 0, row);
       }
+    };
+    for (int t = 0; t < PF && t < ntiles; ++t) prefetch_tile(t);
+    if (lane == 0) mbar_expect_tx(q_full, C::Q_LAT + C::Q_PE);
+    __syncwarp();
+    {
+      const int k = my_box(C::NBL + 1);
+      if (k >= 0 && k < C::NBL) tma_load_2d(sb + k * C::Q_BOX, &tm_qz, k * 64, qrow0, q_full);
+      if (k == C::NBL) tma_load_2d(sb + C::OFF_QPE, &tm_qpe, 0, qrow0, q_full);
+    }
+    int ic = 0;  // ring items issued
+    auto acquire = [&](int& slot) -> bool {
+      slot = ic % NR;
+      if (ic >= NR && !warp_wait(&r_empty[slot], ((ic / NR) - 1) & 1, p.wait_ns, abort_flag)) return false;
+      last[slot] = ic;
+      ++ic;
+      return true;
+    };
+    auto chunk = [&](int u, int j) -> bool {
+      if (j == 0 && u + PF < ntiles) prefetch_tile(u + PF);
+      int slot;
+      if (!acquire(slot)) return false;
+      const int key0 = kstart + u * TK;
+      const int nhalf = tile_keys(u) > 64 ? 2 : 1;
+      const uint32_t dst = sb + C::OFF_RING + slot * C::SLOT;
+      const bool pe = j == C::NBL;
+      const uint32_t half = pe ? C::HALF_PE : C::HALF_LAT;
+      if (lane == 0) mbar_expect_tx(&r_full[slot], half * nhalf);
+      __syncwarp();
+      const int k = my_box(nhalf);
+      if (k >= 0) {
+        const int row = cache_row(p, bi, key0 + k * 64);
+        if (pe) tma_load_2d(dst + k * half, &tm_kpe64, 0, row, &r_full[slot]);
+        else tma_load_2d(dst + k * half, &tm_z64, j * 64, row, &r_full[slot]);
+      }
+      return true;
+    };
+    auto pair = [&](int v, int q) -> bool {
+      int slot;
+      if (!acquire(slot)) return false;
+      const uint32_t dst = sb + C::OFF_RING + slot * C::SLOT;
+      if (lane == 0) mbar_expect_tx(&r_full[slot], C::PAIR_BYTES);
+      __syncwarp();
+      const int k = my_box(C::KLH / 64);
+      if (k >= 0) {
+        const int row = cache_row(p, bi, kstart + v * TK + q * PAIR);
+        tma_load_2d_hint(dst + k * C::PBOX, &tm_z32, lh * C::KLH + k * 64, row, &r_full[slot], pol_last);
+      }
+      return true;
+    };
+    bool ok = true;
+    for (int u = 0; ok && u <= ntiles; ++u)
+      ok = walk_iteration<C::NCH, C::J0>(u, ntiles, tile_pairs(u - 1), chunk, pair);
+    if (lane == 0) {
       if (!ok && !*abort_flag) fail();
       // no copy may still be landing in shared memory when the CTA exits
       mbar_wait(q_full, 0, kTeardownNs, nullptr);
-      for (int i = 0; i < NS; ++i)
-        if (last_s[i] >= 0) mbar_wait(&s_full[i], (last_s[i] / NS) & 1, kTeardownNs, nullptr);
-      for (int i = 0; i < NO; ++i)
-        if (last_o[i] >= 0) mbar_wait(&o_full[i], (last_o[i] / NO) & 1, kTeardownNs, nullptr);
+      for (int i = 0; i < NR; ++i)
+        if (last[i] >= 0) mbar_wait(&r_full[i], (last[i] / NR) & 1, kTeardownNs, nullptr);
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (lane 0; the warp zeroes tails)
     bool ok = true;
-    if (lane == 0) {
-      if (p.test_timeout && !mbar_wait(test_bar, 0, kTestWaitNs, abort_flag)) ok = false;
-      if (ok && !mbar_wait(q_full, 0, p.wait_ns, abort_flag)) ok = false;
-    }
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (p.test_timeout) ok = warp_wait(test_bar, 0, kTestWaitNs, abort_flag);
+    if (ok) ok = warp_wait(q_full, 0, p.wait_ns, abort_flag);
     tc_fence_after();
     constexpr uint32_t idS = idesc_bf16_f32(BMROWS, TK, false, false);
     constexpr uint32_t idO = idesc_bf16_f32(BMROWS, C::KLH, false, true);
-    int sc = 0, oc = 0;
-    for (int t = 0; ok && t <= ntiles; ++t) {
-      if (t < ntiles) {
-        const uint32_t d_s = tmem + C::TM_S + (t & 1) * TK;
-        for (int j = 0; j < C::NCH; ++j, ++sc) {
-          const int slot = sc % NS;
-          if (lane == 0) {
-            if (!mbar_wait(&s_full[slot], (sc / NS) & 1, p.wait_ns, abort_flag)) {
-              ok = false;
-            } else {
-              tc_fence_after();
-              const uint32_t src = sb + C::OFF_SRING + slot * C::S_SLOT;
-              if (j < C::NBL) {
+    // descriptors of the resident Q' chunks and of ring slot 0 (start-address field advanced per slot / k step)
+    const uint64_t dq0 = smem_desc(sb, 16, 1024, kSw128);
+    const uint64_t dqpe = smem_desc(sb + C::OFF_QPE, 16, 8 * C::PE_ROW, C::PE_SWZ);
+    const uint64_t dring = smem_desc(sb + C::OFF_RING, 16, 1024, kSw128);
+    const uint64_t dring_pe = smem_desc(sb + C::OFF_RING, 16, 8 * C::PE_ROW, C::PE_SWZ);
+    const uint64_t dpair = smem_desc(sb + C::OFF_RING, C::PBOX, 1024, kSw128);  // Z slab read MN-major
+    int ic = 0;        // ring items consumed
+    bool first_o = true;
+    auto take = [&](int& slot) -> bool {
+      slot = ic % NR;
+      if (!warp_wait(&r_full[slot], (ic / NR) & 1, p.wait_ns, abort_flag)) return false;
+      ++ic;
+      return true;
+    };
+    auto chunk = [&](int u, int j) -> bool {
+      int slot;
+      if (!take(slot)) return false;
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t d_s = tmem + C::TM_S + (u & 1) * TK;
+        const uint64_t so = (uint64_t)((slot * C::SLOT) >> 4);
+        if (j < C::NBL) {
+          const uint64_t qa = dq0 + (uint64_t)((j * C::Q_BOX) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                  tc_mma_ss(d_s, smem_desc(sb + j * C::Q_BOX + kk * 32, 16, 1024, kSw128),
-                            smem_desc(src + kk * 32, 16, 1024, kSw128), idS, (j > 0 || kk > 0) ? 1u : 0u);
-              } else {
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_ss(d_s, qa + 2 * kk, dring + so + 2 * kk, idS, (j > 0 || kk > 0) ? 1u : 0u);
+        } else {
 #pragma unroll
-                for (int kk = 0; kk < P / 16; ++kk)
-                  tc_mma_ss(d_s, smem_desc(sb + C::OFF_QPE + kk * 32, 16, 8 * C::PE_ROW, C::PE_SWZ),
-                            smem_desc(src + kk * 32, 16, 8 * C::PE_ROW, C::PE_SWZ), idS, 1u);
-              }
-              tc_commit(&s_empty[slot]);
-            }
-          }
-          if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
-            ok = false;
-            break;
-          }
+          for (int kk = 0; kk < P / 16; ++kk) tc_mma_ss(d_s, dqpe + 2 * kk, dring_pe + so + 2 * kk, idS, 1u);
         }
-        if (!ok) break;
-        if (lane == 0) tc_commit(&s_ready[t & 1]);
+        tc_commit(&r_empty[slot]);
       }
-      if (t >= 1) {
-        const int u = t - 1;
-        const int key0 = kstart + u * TK;
-        const int nsl = tile_slabs(u);
-        if (lane == 0 && !mbar_wait(p_full, u & 1, p.wait_ns, abort_flag)) ok = false;
-        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
-          ok = false;
-          break;
+      __syncwarp();
+      return true;
+    };
+    auto pair = [&](int v, int q) -> bool {
+      if (q == 0 && !warp_wait(p_full, v & 1, p.wait_ns, abort_flag)) return false;
+      int slot;
+      if (!take(slot)) return false;
+      const int nsl = tile_slabs(v);
+      const int key_q = kstart + v * TK + q * PAIR;
+      const int first_bad = L - key_q;  // rows of the item at or past the sequence end
+      const uint32_t base = C::OFF_RING + slot * C::SLOT;
+      if (first_bad < PAIR) {
+        const int nrow = PAIR - first_bad;
+        for (int idx = lane; idx < nrow * (C::KLH / 64) * 8; idx += 32) {
+          const int rr = first_bad + idx / ((C::KLH / 64) * 8);
+          const int rem = idx % ((C::KLH / 64) * 8);
+          *reinterpret_cast<uint4*>(smem + base + (rem / 8) * C::PBOX + rr * 128 + (rem % 8) * 16) =
+              make_uint4(0, 0, 0, 0);
         }
-        for (int s = 0; s < nsl; ++s, ++oc) {
-          const int slot = oc % NO;
-          if (lane == 0 && !mbar_wait(&o_full[slot], (oc / NO) & 1, p.wait_ns, abort_flag)) ok = false;
-          if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
-            ok = false;
-            break;
-          }
-          __syncwarp();
-          const int first_bad = L - (key0 + s * SLAB);  // rows at or past the sequence end
-          if (first_bad < SLAB) {
-            const uint32_t base = C::OFF_ORING + slot * C::O_SLOT;
-            const int nrow = SLAB - first_bad;
-            for (int idx = lane; idx < nrow * (C::KLH / 64) * 8; idx += 32) {
-              const int rr = first_bad + idx / ((C::KLH / 64) * 8);
-              const int rem = idx % ((C::KLH / 64) * 8);
-              *reinterpret_cast<uint4*>(smem + base + (rem / 8) * C::O_SUB + rr * 128 + (rem % 8) * 16) =
-                  make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
-          if (lane == 0) {
-            tc_fence_after();
-            const uint64_t a = smem_desc(sb + C::OFF_P + (s / 4) * C::P_BOX + (s % 4) * 32, 16, 1024, kSw128);
-            // Z slab read MN-major: 64-column boxes O_SUB apart, 8-key groups 1024 B apart
-            const uint64_t bd = smem_desc(sb + C::OFF_ORING + slot * C::O_SLOT, C::O_SUB, 1024, kSw128);
-            tc_mma_ss(tmem, a, bd, idO, (u > 0 || s > 0) ? 1u : 0u);
-            tc_commit(&o_empty[slot]);
-          }
-        }
-        if (!ok) break;
-        if (lane == 0) tc_commit(o_done);
+        fence_proxy_async_smem();
+        __syncwarp();
       }
+      if (lane == 0) {
+        tc_fence_after();
+        const uint64_t so = (uint64_t)((slot * C::SLOT) >> 4);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int sl = 2 * q + e;
+          if (sl < nsl) {
+            const uint32_t a = tmem + C::TM_S + (v & 1) * TK + sl * (SLAB / 2);
+            tc_mma_ts(tmem, a, dpair + so + (uint64_t)((e * SLAB * 128) >> 4), idO, first_o ? 0u : 1u);
+            first_o = false;
+          }
+        }
+        tc_commit(&r_empty[slot]);
+      }
+      first_o = false;
+      __syncwarp();
+      return true;
+    };
+    for (int u = 0; ok && u <= ntiles; ++u) {
+      ok = walk_iteration<C::NCH, C::J0>(u, ntiles, tile_pairs(u - 1), chunk, pair);
+      if (ok && lane == 0) tc_commit(u < ntiles ? &s_ready[u & 1] : o_final);
+      __syncwarp();
     }
     if (lane == 0) {
       if (!ok && !*abort_flag) fail();
@@ -375,97 +428,116 @@ __global__ void __launch_bounds__(192, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax + epilogue
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    // ------------------------------------------------------------ softmax + epilogue (warps 2-9)
+    const int q = warp & 3;            // TMEM lane quadrant this warp may access
+    const int ch = (warp - 2) >> 2;    // key half of each tile (and output column half) of this warp
     const int r = q * 32 + lane;
     const int row_in_seq = mt * BMROWS + r;
     const bool row_ok = row_in_seq < p.rows;
     const int lim = row_ok ? min(kend, L - p.s + (row_in_seq % p.s) + 1) : 0;  // exclusive key limit
     const uint32_t t_lane = tmem + ((uint32_t)(q * 32) << 16);
+    constexpr int KH = TK / 2;         // keys per warp per tile
+    constexpr int OCW = C::KLH / 2;    // O columns per warp (rescale, epilogue)
     float m_ref = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
-      // waits are made warp-uniform: the tcgen05 loads below are warp-collective
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_ready[t & 1], (t >> 1) & 1, p.wait_ns, abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int key0 = kstart + t * TK;
-      float x[TK];
+      // S(t) in TMEM; O MMAs of tile t-1 are complete too (issued before this commit).
+      // Both warps of a quadrant meet at the exchange below on every tile, whatever
+      // happened to their waits, so they leave the loop together (no barrier is orphaned).
+      const bool okw = warp_wait(&s_ready[t & 1], (t >> 1) & 1, p.wait_ns, abort_flag);
+      const int kb = kstart + t * TK + ch * KH;  // first key of this warp's half
+      const uint32_t sbuf = t_lane + C::TM_S + (t & 1) * TK;
+      float x[KH];
       float mx = -INFINITY;
-#pragma unroll
-      for (int c0 = 0; c0 < TK; c0 += 32) {
+      if (okw) {
+        tc_fence_after();
         uint32_t sv[32];
-        tmem_ld32(t_lane + C::TM_S + (t & 1) * TK + c0, sv);
+        tmem_ld32(sbuf + ch * KH, sv);
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float v = (key0 + c0 + c < lim) ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
-          x[c0 + c] = v;
-          mx = fmaxf(mx, v);
+        for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(sv[c]) * p.scale_log2;
+        tmem_ld32(sbuf + ch * KH + 32, sv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) x[32 + c] = __uint_as_float(sv[c]) * p.scale_log2;
+        if (kb + KH > lim) {
+#pragma unroll
+          for (int c = 0; c < KH; ++c)
+            if (kb + c >= lim) x[c] = -INFINITY;
         }
+        float m8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m8[e] = x[e];
+#pragma unroll
+        for (int c = 8; c < KH; ++c) m8[c & 7] = fmaxf(m8[c & 7], x[c]);
+        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       }
-      // the previous O MMAs must be complete: they still read P, and O may be rescaled
-      if (t > 0 && !__all_sync(0xffffffffu, mbar_wait(o_done, (t - 1) & 1, p.wait_ns, abort_flag))) {
+      // row maximum over both key halves (the two warps of this quadrant)
+      float* rb = red + (t & 1) * 2 * BMROWS;
+      rb[ch * BMROWS + r] = mx;
+      if (lane == 0) okf[(t & 1) * 8 + ch * 4 + q] = okw ? 1 : 0;
+      named_bar_sync(1 + q, 64);
+      mx = fmaxf(mx, rb[(ch ^ 1) * BMROWS + r]);
+      if (!okw || !okf[(t & 1) * 8 + (ch ^ 1) * 4 + q]) {
         ok = false;
         break;
       }
-      tc_fence_after();
       float alpha = 1.f;
       if (mx > m_ref + kRescaleLog2) {
-        alpha = exp2f(m_ref - mx);  // 0 when nothing was seen yet
+        alpha = fast_exp2(m_ref - mx);  // 0 when nothing was seen yet
         m_ref = mx;
         l_run *= alpha;
       }
       if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        for (int c0 = 0; c0 < C::KLH; c0 += 32) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < OCW; c0 += 32) {
           uint32_t v[32];
-          tmem_ld32(t_lane + c0, v);
+          tmem_ld32(t_lane + ch * OCW + c0, v);
           tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * alpha);
-          tmem_st32(t_lane + c0, v);
+          tmem_st32(t_lane + ch * OCW + c0, v);
         }
-        tmem_st_wait();
       }
-      // P row (bf16) into two 128-byte-swizzled [128 rows x 64 keys] boxes
-      float ps = 0.f;
-      const bool live = m_ref != -INFINITY;
+      // P (bf16 pairs, key 2c in the low half) over columns [ch*32, ch*32+32) of this S buffer
+      const float mneg = m_ref == -INFINITY ? 0.f : -m_ref;  // all keys masked so far: x = -inf -> 0
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[32];
 #pragma unroll
-      for (int ch = 0; ch < TK / 8; ++ch) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = live ? exp2f(x[ch * 8 + 2 * e] - m_ref) : 0.f;
-          const float p1 = live ? exp2f(x[ch * 8 + 2 * e + 1] - m_ref) : 0.f;
-          ps += p0 + p1;
-          pk[e] = pack_bf16(p0, p1);
-        }
-        const int box = ch / 8, lc = ch % 8;
-        *reinterpret_cast<uint4*>(smem + C::OFF_P + box * C::P_BOX + r * 128 + ((lc ^ (r & 7)) * 16)) =
-            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      for (int e = 0; e < 32; ++e) {
+        const float p0 = fast_exp2(x[2 * e] + mneg);
+        const float p1 = fast_exp2(x[2 * e + 1] + mneg);
+        ps[e & 3] += p0 + p1;
+        pk[e] = pack_bf16(p0, p1);
       }
-      l_run += ps;
-      fence_proxy_async_smem();
+      tmem_st32(sbuf + ch * (KH / 2), pk);
+      l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
-    if (ok && !__all_sync(0xffffffffu, mbar_wait(o_done, (ntiles - 1) & 1, p.wait_ns, abort_flag))) ok = false;
+    if (ok && !warp_wait(o_final, 0, p.wait_ns, abort_flag)) ok = false;
+    // row sum over both key halves
+    float* lb = red + 2 * BMROWS * ((ntiles) & 1);
+    lb[ch * BMROWS + r] = l_run;
+    named_bar_sync(1 + q, 64);
+    const float l_tot = l_run + lb[(ch ^ 1) * BMROWS + r];
     if (!ok) {
       if (!*abort_flag) fail();
     } else {
       tc_fence_after();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      const float lse = l_run > 0.f ? (m_ref + log2f(l_run)) * kLn2 : -INFINITY;
+      const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+      const float lse = l_tot > 0.f ? (m_ref + log2f(l_tot)) * kLn2 : -INFINITY;
       const size_t grow = (size_t)qrow0 + r;
-      for (int c0 = 0; c0 < C::KLH; c0 += 32) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < OCW; c0 += 32) {
         uint32_t v[32];
-        tmem_ld32(t_lane + c0, v);
+        tmem_ld32(t_lane + ch * OCW + c0, v);
         tmem_ld_wait();
         if (!row_ok) continue;
-        const int col = lh * C::KLH + c0;
+        const int col = lh * C::KLH + ch * OCW + c0;
         if (p.nsplit == 1) {
           uint4* dst = reinterpret_cast<uint4*>(p.o_lat + grow * KL + col);
 #pragma unroll
@@ -482,7 +554,7 @@ __global__ void __launch_bounds__(192, 1)
                                  __uint_as_float(v[4 * e + 2]) * inv, __uint_as_float(v[4 * e + 3]) * inv);
         }
       }
-      if (row_ok && lh == 0) {
+      if (row_ok && lh == 0 && ch == 0) {
         if (p.nsplit == 1) {
           if (p.lse) p.lse[grow] = lse;
         } else {
@@ -550,10 +622,10 @@ cudaError_t launch_kl(const MlaLaunch& a, cudaStream_t stream) {
   }
   const uint64_t qrows = (uint64_t)a.b * a.h * a.s;
   const uint64_t krows = a.paged ? (uint64_t)a.num_pages * 64 : (uint64_t)a.b * a.capacity;
-  CUtensorMap tqz, tqpe, tz64, tkpe64, tz16;
+  CUtensorMap tqz, tqpe, tz64, tkpe64, tz32;
   if (!make_map(&tqz, a.qz, qrows, KL, BMROWS, 64) || !make_map(&tqpe, a.q_pe, qrows, P, BMROWS, P) ||
       !make_map(&tz64, a.z, krows, KL, 64, 64) || !make_map(&tkpe64, a.k_pe, krows, P, 64, P) ||
-      !make_map(&tz16, a.z, krows, KL, SLAB, 64))
+      !make_map(&tz32, a.z, krows, KL, PAIR, 64))
     return cudaErrorInvalidValue;
   MlaParams p;
   p.seqlens = a.seqlens;
@@ -578,7 +650,7 @@ cudaError_t launch_kl(const MlaLaunch& a, cudaStream_t stream) {
   p.test_timeout = a.test_timeout;
   const int mtiles = (p.rows + BMROWS - 1) / BMROWS;
   dim3 grid(C::NH * mtiles, a.nsplit, a.b);
-  mla_latent_kernel<KL, P><<<grid, 192, C::SMEM, stream>>>(tqz, tqpe, tz64, tkpe64, tz16, p);
+  mla_latent_kernel<KL, P><<<grid, NTHREADS, C::SMEM, stream>>>(tqz, tqpe, tz64, tkpe64, tz32, p);
   return cudaGetLastError();
 }
 

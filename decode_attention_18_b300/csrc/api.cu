@@ -68,13 +68,15 @@ struct Plan {
   int chunk;
 };
 
-// Split planner: pick the number of context chunks so that the CTAs fill the
-// SMs in whole waves. base = CTAs per chunk index (sequences x heads x row
-// blocks), slots = CTAs resident on the whole GPU at once, overhead = fixed
-// cost of a CTA expressed in keys, align = chunk granularity (a multiple of
-// the 64-key page and of the kernel's key tile). Cost model:
-// waves x (chunk + overhead).
-Plan plan_splits(long long base, int max_seqlen, long long slots, int overhead_keys, int align) {
+// Split planner: pick the number of context chunks. base = CTAs per chunk index
+// (sequences x heads x row blocks), slots = CTAs resident on the whole GPU at once,
+// align = chunk granularity (a multiple of the 64-key page and of the kernel's key
+// tile). Cost model, in keys of one CTA's work:
+//   waves x (chunk + overhead) + (nsplit > 1 ? combine : 0)
+// overhead = a CTA's prologue (pipeline fill, query load, epilogue), combine = the
+// second kernel and the partials' round trip. Measured on B300 (b=32, 8 KV heads,
+// d=128, 4096 keys): unsplit runs at 95% of HBM bandwidth, 8 chunks at 67%.
+Plan plan_splits(long long base, int max_seqlen, long long slots, int overhead_keys, int combine_keys, int align) {
   Plan pl{1, align};
   const long long L = max_seqlen > 0 ? max_seqlen : 1;
   const int max_n = (int)ceil_div(L, align);
@@ -92,7 +94,7 @@ Plan plan_splits(long long base, int max_seqlen, long long slots, int overhead_k
     const int ne = (int)ceil_div(L, chunk);
     if (ne != n) continue;
     const long long waves = ceil_div(base * ne, slots);
-    const double cost = (double)waves * (chunk + overhead_keys);
+    const double cost = (double)waves * (chunk + overhead_keys) + (ne > 1 ? combine_keys : 0);
     if (cost < best * 0.999) {
       best = cost;
       pl.nsplit = ne;
@@ -127,13 +129,13 @@ Plan gqa_plan(int b, int s, int hq, int hkv, int d, int max_seqlen, int sms) {
   const int rpc = gqa_rows_per_cta(rows);
   const long long base = (long long)b * hkv * ceil_div(rows, rpc);
   const long long slots = (long long)sms * gqa_ctas_per_sm(d);
-  return plan_splits(base, max_seqlen, slots, 64, kPage);
+  return plan_splits(base, max_seqlen, slots, 256, 512, kPage);
 }
 
 // --- latent MLA plan (one CTA per SM: its shared memory holds the 128-row query tile)
 Plan mla_plan(int b, int s, int h, int k, int max_seqlen, int sms) {
   const long long base = (long long)b * mla_latent_parts(k) * ceil_div((long long)h * s, 128);
-  return plan_splits(base, max_seqlen, sms, 256, mla_tile_keys());
+  return plan_splits(base, max_seqlen, sms, 384, 512, mla_tile_keys());
 }
 
 }  // namespace

@@ -8,7 +8,7 @@
 // with M = b*s rows per head. At decode sizes M is small (32 rows for 32
 // sequences of one token) and the kernel is bound by reading W (h*kin*nout
 // bf16, 16.8 MB for h=128, d=128, k=512), so it streams W once through a
-// 3-stage cp.async pipeline and runs mma.sync m16n8k16 (bf16, fp32 accumulate).
+// cp.async pipeline and runs mma.sync m16n8k16 (bf16, fp32 accumulate).
 #include "common.cuh"
 #include "internal.h"
 
@@ -16,9 +16,7 @@ namespace decattn {
 
 namespace {
 
-constexpr int BM = 64;
 constexpr int BK = 64;
-constexpr int NST = 3;
 
 struct ProjParams {
   const __nv_bfloat16* a;
@@ -31,18 +29,23 @@ struct ProjParams {
 
 __device__ __forceinline__ uint32_t swz(int row, int chunk) { return (uint32_t)(chunk ^ (row & 7)); }
 
-template <int BN>
+// One CTA: BM rows of one head x BN output columns, 4 warps laid out (BM/32) x (4/(BM/32)),
+// each warp 32 rows x WN columns; NST k-stages of BK in flight (cp.async, 16-byte chunks).
+template <int BM, int BN, int NST>
 __global__ void __launch_bounds__(128) proj_kernel(ProjParams p) {
-  constexpr int A_BYTES = BM * BK * 2;       // [64 rows][64 k], rows of 128 B
+  constexpr int WMW = BM / 32;               // warps along M
+  constexpr int WNW = 4 / WMW;               // warps along N
+  constexpr int WN = BN / WNW;               // columns per warp
+  constexpr int NTW = WN / 8;                // n-tiles per warp
+  constexpr int A_BYTES = BM * BK * 2;       // [BM rows][64 k], rows of 128 B
   constexpr int B_ROW = BN * 2;              // bytes per k row of the W tile
   constexpr int B_BYTES = BK * B_ROW;        // [64 k][BN n]
   constexpr int STAGE = A_BYTES + B_BYTES;
-  constexpr int WN = BN / 2;                 // warp tile: 32 rows x WN cols
-  constexpr int NTW = WN / 8;                // n-tiles per warp
+  static_assert(NTW % 2 == 0 && (BM * 8) % 128 == 0 && (BK * (BN / 8)) % 128 == 0, "tile shape");
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int wm = warp >> 1, wn = warp & 1;
+  const int wm = warp / WNW, wn = warp % WNW;
   const int n0 = blockIdx.x * BN;
   const int m0 = blockIdx.y * BM;
   const int j = blockIdx.z;
@@ -57,7 +60,6 @@ __global__ void __launch_bounds__(128) proj_kernel(ProjParams p) {
   auto load = [&](int kt, int stage) {
     const uint32_t adst = sbase + stage * STAGE;
     const uint32_t bdst = adst + A_BYTES;
-    // A: 64 rows x 8 chunks
 #pragma unroll
     for (int n = 0; n < (BM * 8) / 128; ++n) {
       const int idx = tid + n * 128;
@@ -67,7 +69,6 @@ __global__ void __launch_bounds__(128) proj_kernel(ProjParams p) {
       const __nv_bfloat16* src = ok ? a_row_ptr(m) + kt * BK + c * 8 : p.a;
       cp_async_16(adst + r * 128 + swz(r, c) * 16, src, ok ? 16u : 0u);
     }
-    // W: 64 k rows x BN/8 chunks
     const __nv_bfloat16* wbase = p.w + (size_t)j * p.kin * p.nout;
 #pragma unroll
     for (int n = 0; n < (BK * (BN / 8)) / 128; ++n) {
@@ -140,22 +141,26 @@ __global__ void __launch_bounds__(128) proj_kernel(ProjParams p) {
     }
 }
 
-template <int BN>
-cudaError_t launch_bn(const ProjParams& p, cudaStream_t stream) {
+template <int BM, int BN, int NST>
+cudaError_t launch_tile(const ProjParams& p, cudaStream_t stream) {
   constexpr int SMEM = NST * (BM * BK * 2 + BK * BN * 2);
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(proj_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    cudaError_t e = cudaFuncSetAttribute(proj_kernel<BM, BN, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   dim3 grid((p.nout + BN - 1) / BN, (p.M + BM - 1) / BM, p.h);
-  proj_kernel<BN><<<grid, 128, SMEM, stream>>>(p);
+  proj_kernel<BM, BN, NST><<<grid, 128, SMEM, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+// Tile choice: weight-read bound at decode sizes, so the goal is one wave of CTAs with
+// every k-stage of a CTA in flight at once. 32-row tiles when b*s <= 32 (decode with
+// one token per sequence), wide column tiles when the weight is wide (absorption:
+// d -> k) and narrow ones when it is tall (output projection: k -> d).
 cudaError_t launch_proj(const ProjLaunch& a, int num_sms, cudaStream_t stream) {
   ProjParams p;
   p.a = static_cast<const __nv_bfloat16*>(a.a);
@@ -169,9 +174,14 @@ cudaError_t launch_proj(const ProjLaunch& a, int num_sms, cudaStream_t stream) {
   p.nout = a.nout;
   p.M = a.b * a.s;
   p.scale = a.scale;
-  const long long ctas128 = (long long)((a.nout + 127) / 128) * ((p.M + BM - 1) / BM) * a.h;
-  if (a.nout >= 128 && ctas128 >= 2LL * num_sms) return launch_bn<128>(p, stream);
-  return launch_bn<64>(p, stream);
+  (void)num_sms;
+  const int kiters = (a.kin + BK - 1) / BK;
+  if (p.M <= 32) {
+    if (a.nout >= 256 && kiters <= 2) return launch_tile<32, 256, 2>(p, stream);
+    return launch_tile<32, 64, 4>(p, stream);
+  }
+  if (a.nout >= 128) return launch_tile<64, 128, 3>(p, stream);
+  return launch_tile<64, 64, 3>(p, stream);
 }
 
 }  // namespace decattn

@@ -176,17 +176,21 @@ def cpu_baseline(wl, seconds_target=15.0):
 
 
 def traffic_record():
-    """DRAM bytes of the latent kernel from a committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", "mla_latent_dsv3_traffic.json")
+    """DRAM bytes (read + write) per launch of the latent kernel from the committed
+    ncu summary, if that summary was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "mla_latent_dsv3_b32_h128_k512_t4096_s1.md")
     src = os.path.join(ROOT, "decode_attention_18_b300", "csrc", "mla_decode.cu")
     if not os.path.exists(path):
         return None
-    rec = json.load(open(path))
+    fields = {}
+    for line in open(path):
+        if ":" in line and not line.startswith(("|", "#", " ")):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
     h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    if rec.get("source_sha256_16") != h:
+    if fields.get("source_sha256_16") != h or "dram_bytes_per_launch" not in fields:
         return None
-    return rec.get("dram_bytes_per_launch")
+    return int(fields["dram_bytes_per_launch"])
 
 
 def run_reference(args):

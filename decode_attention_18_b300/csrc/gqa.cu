@@ -47,6 +47,7 @@ constexpr int kTileKeys = 64;
 constexpr int kSlices = 4;  // warps (key slices of 16) per m-tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.f;  // move a row's reference maximum only past 2^8
 
 template <int D, int MT_>
 struct GqaCfg {
@@ -128,14 +129,32 @@ __global__ void __launch_bounds__(128 * MT) gqa_split_kernel(GqaParams p) {
     }
   }
 
-  // ---- K/V tile loader (all threads; zero-fill past the chunk end)
+  // ---- K/V tile loader (all threads; zero-fill past the chunk end). For a paged cache
+  // the tile's page index comes from page_of(); it is fetched one iteration ahead so that
+  // the block-table read never sits in front of the copies.
   const uint32_t sbase = smem_u32(smem);
-  auto load_tile = [&](int t, int stage) {
+  auto page_of = [&](int t) -> int {
+    const int key0 = kstart + t * kTileKeys;
+    if (!p.paged || t >= ntiles) return 0;
+    return __ldg(p.block_table + (size_t)bi * p.max_pages + key0 / kTileKeys);
+  };
+  // this thread's 16-byte chunks of a tile: row, shared-memory offset, element offset in the cache
+  // (the element offset fits 32 bits: row < 64, hkv <= 65535, d <= 256)
+  uint32_t ld_soff[C::LOADS];
+  uint32_t ld_goff[C::LOADS];
+#pragma unroll
+  for (int n = 0; n < C::LOADS; ++n) {
+    const int idx = tid + n * C::THREADS;
+    const int kr = idx / C::CHUNKS;
+    const int c = idx % C::CHUNKS;
+    ld_soff[n] = kr * C::ROW_BYTES + swz(kr, c) * 16;
+    ld_goff[n] = (uint32_t)(kr * p.hkv * D + c * 8);
+  }
+  auto load_tile = [&](int t, int stage, int page) {
     const int key0 = kstart + t * kTileKeys;
     long long rowbase;  // cache-tensor row of the tile's first token
     bool page_ok = true;
     if (p.paged) {
-      const int page = __ldg(p.block_table + (size_t)bi * p.max_pages + key0 / kTileKeys);
       if (page < 0 || page >= p.num_pages) {
         page_ok = false;
         if (tid == 0) raise_error(p.err, kErrBadPage);
@@ -146,16 +165,16 @@ __global__ void __launch_bounds__(128 * MT) gqa_split_kernel(GqaParams p) {
     }
     const uint32_t kdst = sbase + stage * C::STAGE_BYTES;
     const uint32_t vdst = kdst + C::TILE_BYTES;
+    const __nv_bfloat16* kt = p.k + ((size_t)rowbase * p.hkv + g) * D;
+    const __nv_bfloat16* vt = p.v + ((size_t)rowbase * p.hkv + g) * D;
+    const int nvalid = page_ok ? kend - key0 : 0;  // keys of the tile inside the chunk
 #pragma unroll
     for (int n = 0; n < C::LOADS; ++n) {
-      const int idx = tid + n * C::THREADS;
-      const int kr = idx / C::CHUNKS;
-      const int c = idx % C::CHUNKS;
-      const bool valid = page_ok && (key0 + kr < kend);
-      const size_t goff = valid ? (((size_t)(rowbase + kr) * p.hkv + g) * D + c * 8) : 0;
-      const uint32_t soff = kr * C::ROW_BYTES + swz(kr, c) * 16;
-      cp_async_16(kdst + soff, p.k + goff, valid ? 16u : 0u);
-      cp_async_16(vdst + soff, p.v + goff, valid ? 16u : 0u);
+      const int kr = (tid + n * C::THREADS) / C::CHUNKS;
+      const bool valid = kr < nvalid;
+      const uint32_t goff = valid ? ld_goff[n] : 0u;
+      cp_async_16(kdst + ld_soff[n], kt + goff, valid ? 16u : 0u);
+      cp_async_16(vdst + ld_soff[n], vt + goff, valid ? 16u : 0u);
     }
   };
 
@@ -168,16 +187,19 @@ __global__ void __launch_bounds__(128 * MT) gqa_split_kernel(GqaParams p) {
 
 #pragma unroll
   for (int t = 0; t < C::NST - 1; ++t) {
-    if (t < ntiles) load_tile(t, t);
+    if (t < ntiles) load_tile(t, t, page_of(t));
     cp_async_commit();
   }
+  int page_next = page_of(C::NST - 1);  // page of the next tile to load
 
   for (int t = 0; t < ntiles; ++t) {
     cp_async_wait<C::NST - 2>();
     __syncthreads();
     {
       const int tn = t + C::NST - 1;
-      if (tn < ntiles) load_tile(tn, tn % C::NST);
+      const int page = page_next;
+      page_next = page_of(tn + 1);
+      if (tn < ntiles) load_tile(tn, tn % C::NST, page);
       cp_async_commit();
     }
     const int stage = t % C::NST;
@@ -185,24 +207,42 @@ __global__ void __launch_bounds__(128 * MT) gqa_split_kernel(GqaParams p) {
     const uint32_t vbase = kbase + C::TILE_BYTES;
     const int key_w = kstart + t * kTileKeys + slice * 16;  // first key of this warp's slice
 
-    // S = Q K^T over the 16 keys of the slice (two n-tiles of 8 keys)
+    // S = Q K^T over the 16 keys of the slice (two n-tiles of 8 keys); for d >= 128 the
+    // k-steps alternate between two accumulator sets, halving the dependent MMA chain.
     float sc[2][4];
-#pragma unroll
-    for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
     {
+      constexpr int NACC = KS >= 8 ? 2 : 1;
+      float sacc[NACC][2][4];
+#pragma unroll
+      for (int a = 0; a < NACC; ++a)
+#pragma unroll
+        for (int n = 0; n < 2; ++n) sacc[a][n][0] = sacc[a][n][1] = sacc[a][n][2] = sacc[a][n][3] = 0.f;
       const int kr = slice * 16 + (lane & 7) + ((lane >> 4) & 1) * 8;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         const int c = ks * 2 + ((lane >> 3) & 1);
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4(kbase + kr * C::ROW_BYTES + swz(kr, c) * 16, b0, b1, b2, b3);
-        mma_bf16_16816(sc[0], qa[ks], b0, b1);
-        mma_bf16_16816(sc[1], qa[ks], b2, b3);
+        mma_bf16_16816(sacc[ks % NACC][0], qa[ks], b0, b1);
+        mma_bf16_16816(sacc[ks % NACC][1], qa[ks], b2, b3);
       }
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float v = sacc[0][n][e];
+#pragma unroll
+          for (int a = 1; a < NACC; ++a) v += sacc[a][n][e];
+          sc[n][e] = v;
+        }
     }
 
-    // online softmax (exp2 domain); P packed as bf16 A fragments
+    // online softmax (exp2 domain); P packed as bf16 A fragments. The reference maximum
+    // of a row moves only when the row's maximum grows by more than 2^8 (P values stay
+    // below 256, exact enough in bf16 with fp32 sums), so the 2*NT-register rescale of the
+    // output accumulator is skipped on almost every tile.
     uint32_t pa[4];
+    float alpha2[2] = {1.f, 1.f};
 #pragma unroll
     for (int h2 = 0; h2 < 2; ++h2) {
       float x[4];
@@ -216,27 +256,29 @@ __global__ void __launch_bounds__(128 * MT) gqa_split_kernel(GqaParams p) {
       float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float m_new = fmaxf(m_run[h2], mx);
-      float alpha = 1.f, ref = 0.f;
-      if (m_new != -INFINITY) {
-        alpha = exp2f(m_run[h2] - m_new);  // 0 while nothing was seen yet
-        ref = m_new;
+      if (mx > m_run[h2] + kRescaleLog2) {
+        alpha2[h2] = fast_exp2(m_run[h2] - mx);  // 0 while nothing was seen yet
+        m_run[h2] = mx;
       }
-      m_run[h2] = m_new;
+      const float ref = m_run[h2] == -INFINITY ? 0.f : m_run[h2];
       float pv[4], ps = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        pv[e] = exp2f(x[e] - ref);  // masked keys -> 0
+        pv[e] = fast_exp2(x[e] - ref);  // masked keys -> 0
         ps += pv[e];
       }
-      l_run[h2] = l_run[h2] * alpha + ps;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        o[nt][h2 * 2 + 0] *= alpha;
-        o[nt][h2 * 2 + 1] *= alpha;
-      }
+      l_run[h2] = l_run[h2] * alpha2[h2] + ps;
       pa[h2 + 0] = pack_bf16(pv[0], pv[1]);  // keys 0-7 of the slice
       pa[h2 + 2] = pack_bf16(pv[2], pv[3]);  // keys 8-15
+    }
+    if (__any_sync(0xffffffffu, alpha2[0] != 1.f || alpha2[1] != 1.f)) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        o[nt][0] *= alpha2[0];
+        o[nt][1] *= alpha2[0];
+        o[nt][2] *= alpha2[1];
+        o[nt][3] *= alpha2[1];
+      }
     }
 
     // O += P V (V fragments through ldmatrix.trans)

@@ -23,12 +23,17 @@ struct GqaLaunch {
   float* ws_o;    // [b*hq*s, nsplit, d] (nsplit > 1)
   float* ws_lse;  // [b*hq*s, nsplit]
   unsigned* err;
+  unsigned long long wait_ns;  // limit of the tensor-core kernel's bounded waits
 };
 
 // rows of one grouped-head CTA (multiple of 16) for head dim d
 int gqa_rows_per_cta(int d);
 int gqa_ctas_per_sm(int d);
 cudaError_t launch_gqa(const GqaLaunch& p, cudaStream_t stream);
+// tensor-core variant (keys in the MMA M dimension) for KV heads shared by 17-32+ query rows
+bool gqa_tc_eligible(int rows, int d);
+int gqa_tc_rows_per_cta();
+cudaError_t launch_gqa_tc(const GqaLaunch& p, cudaStream_t stream);
 
 // log-sum-exp merge of split partials: rows x nsplit partials of width d
 cudaError_t launch_combine(const float* ws_o, const float* ws_lse, const int32_t* seqlens, int rows, int rows_per_seq,

@@ -176,6 +176,11 @@ int gqa_decode_no_alloc(const decattn_bf16* q, const decattn_bf16* k, const deca
  * context chunks; n > 0 forces n (for split-invariance tests); it also
  * changes the workspace sizes returned afterwards.
  * decattn_last_num_splits: number of chunks the last attention call used.
+ * decattn_set_gqa_kernel: which grouped-head kernel gqa_decode runs. 0 (default)
+ * and 1 run the mma.sync kernel; 2 runs the tensor-core kernel (keys in the MMA M
+ * dimension) wherever it applies (G*s > 16, d in {128, 256}).
+ * Both compute the same attention; the switch exists for tests and measurements.
+ * It also changes the workspace sizes returned afterwards.
  * decattn_test_force_timeout: when nonzero, the next mla_decode kernels wait
  * once on a barrier that nothing signals, with a 1 ms limit, so that the
  * timeout path runs; the kernels then wind down and report
@@ -186,6 +191,7 @@ void decattn_set_wait_limit_ns(unsigned long long ns);
 void decattn_set_forced_splits(int nsplit);
 int decattn_last_num_splits(void);
 void decattn_test_force_timeout(int on);
+void decattn_set_gqa_kernel(int mode);
 
 #ifdef __cplusplus
 }

@@ -162,3 +162,69 @@ def test_full_size_paged_ragged_sampled(hkv):
     seqlens = wl.seqlens()
     q, cache, out, lse = run(wl.b, wl.heads, wl.hkv, wl.d, wl.s, seqlens, paged=True, seed=wl.seed)
     check_sampled(q, cache, out, lse, seqlens, wl.d, seqs=[0, 7], kv_heads=sorted({0, hkv - 1}))
+
+
+# ---------------------------------------------------------------------------
+# Tensor-core path (keys in the MMA M dimension): KV heads shared by more than 16 query
+# rows (G * s > 16) with d in {128, 256}, forced on for these tests; the same cases run
+# through the mma.sync kernel too.
+
+@pytest.fixture(params=[2, 1], ids=["tensor_core", "mma_sync"])
+def gqa_kernel(request):
+    import decode_attention_18_b300 as da
+
+    da.set_gqa_kernel(request.param)
+    yield request.param
+    da.set_gqa_kernel(0)
+
+@pytest.mark.parametrize("b,hq,hkv,d,s,seqlens", [
+    (2, 32, 1, 128, 1, [700, 129]),         # MQA, 32 rows, d = 128
+    (2, 24, 1, 256, 1, [64, 65]),           # MQA 24 rows, tile boundary
+    (2, 8, 1, 256, 3, [300, 40]),           # 24 rows from s = 3 (causal among the new tokens)
+    (1, 24, 1, 128, 4, [333]),              # 96 rows: three row blocks
+    (6, 24, 2, 256, 1, [0, 1, 63, 64, 65, 1000]),  # empty and page-boundary lengths, 2 KV heads
+])
+def test_tensor_core_path_vs_oracle(b, hq, hkv, d, s, seqlens, gqa_kernel):
+    q, cache, out, lse = run(b, hq, hkv, d, s, seqlens, capacity=max(seqlens) + 3, seed=17)
+    check_all(q, cache, out, lse, seqlens, d, f"tc b{b} hq{hq} hkv{hkv} d{d} s{s}")
+    if 0 in seqlens:
+        i = seqlens.index(0)
+        assert torch.all(out[i] == 0) and torch.all(torch.isneginf(lse[i]))
+
+
+def test_tensor_core_path_sharp_and_paged_bitwise(gqa_kernel):
+    import decode_attention_18_b300 as da
+
+    seqlens = [517, 64, 1000]
+    q, cache, out, lse = run(3, 24, 1, 256, 1, seqlens, paged=True, seed=19, q_std=8.0)
+    check_all(q, cache, out, lse, seqlens, 256, "tc paged sharp")
+    cap = max(seqlens)
+    kc = torch.zeros((3, cap, 1, 256), dtype=torch.bfloat16, device=DEV)
+    vc = torch.zeros_like(kc)
+    for i, L in enumerate(seqlens):
+        kc[i, :L] = cache.seq_rows(i, "k")
+        vc[i, :L] = cache.seq_rows(i, "v")
+    sl = torch.tensor(seqlens, dtype=torch.int32, device=DEV)
+    out2, lse2 = da.gqa_decode(q, kc, vc, sl, max_seqlen=cap)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2)
+    assert torch.equal(lse, lse2)
+
+
+@pytest.mark.parametrize("nsplit", [1, 3, 8])
+def test_tensor_core_path_split_invariance(nsplit, gqa_kernel):
+    import decode_attention_18_b300 as da
+
+    seqlens = [2000, 900]
+    q, cache, out, lse = run(2, 24, 1, 256, 1, seqlens, seed=23)
+    da.set_forced_splits(nsplit)
+    try:
+        sl = torch.tensor(seqlens, dtype=torch.int32, device=DEV)
+        out2, lse2 = da.gqa_decode(q, cache.k, cache.v, sl, max_seqlen=max(seqlens))
+        torch.cuda.synchronize()
+    finally:
+        da.set_forced_splits(0)
+    a, b2 = f64(out), f64(out2)
+    assert np.sqrt(np.mean((a - b2) ** 2)) / np.sqrt(np.mean(a ** 2)) <= 1e-2
+    assert np.abs(f64(lse) - f64(lse2)).max() <= 1e-4
+    check_all(q, cache, out2, lse2, seqlens, 256, f"tc nsplit {nsplit}")

@@ -18,7 +18,6 @@
 //     chunks [128 rows x 64] (plus the RoPE chunk), each loaded by TMA as two
 //     64-row boxes (a box never crosses a 64-token page), and the O slab
 //     pairs: the CTA's own output columns of 32 latent rows, re-read from L2.
-//     Tiles two ahead are pulled into L2 first, so the ring waits on L2.
 //   * tcgen05.mma (kind::f16, bf16 in, fp32 accumulate in Tensor Memory):
 //       S  = Q' K'^T    M=128, N=128 keys, K=k+p   (both operands in smem)
 //       O += P Z_half   M=128, N=256 cols, K=16 keys per slab, with P read
@@ -36,9 +35,13 @@
 //     they exchange row maxima through shared memory and keep one reference
 //     maximum per row that moves only when the row maximum grows by more than
 //     2^8 (O is then rescaled in TMEM). Exponentials use ex2.approx.
-//   * Warp roles: warp 0 issues TMA loads and L2 prefetches, warp 1 issues
-//     MMAs (lane 0; the warp zeroes tails and owns the TMEM allocation),
-//     warps 2-9 run the softmax and the epilogue.
+//   * Warp roles: warp 0 issues the TMA loads, warp 1 the MMAs (the warp
+//     zeroes tails and owns the TMEM allocation), warps 2-9 run the softmax
+//     and the epilogue. The producer and the MMA issuer handle every ring item
+//     one after another, so their per-item cost sets the pace: each whole warp
+//     computes the item's operands (warp-uniform values), one elected lane
+//     issues, an already completed barrier costs one test, and the TMEM base
+//     is a constant (the CTA owns all 512 columns).
 //   * Latent rows past the sequence end may hold anything: slabs wholly past
 //     it are not multiplied; a slab that straddles it has its rows past the
 //     end zeroed before the O MMA, so P Z stays finite.
@@ -61,7 +64,6 @@ constexpr int NR = 5;           // ring slots (16 KB each)
 constexpr int SLAB = 16;        // keys per O slab (= MMA K)
 constexpr int PAIR = 2 * SLAB;  // keys per O ring item
 constexpr int BMROWS = 128;     // query rows per CTA (MMA M)
-constexpr int PF = 2;           // tiles pulled into L2 ahead of the ring
 constexpr int NSMW = 8;         // softmax warps
 constexpr int NTHREADS = 32 * (2 + NSMW);
 constexpr float kLog2e = 1.4426950408889634f;
@@ -137,6 +139,25 @@ __device__ __forceinline__ int cache_row(const MlaParams& p, int bi, int key) {
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns, volatile int* abort_flag) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, limit_ns, abort_flag));
 }
+
+// same, with a cheap first test for the common case of a phase that already completed
+__device__ __forceinline__ bool warp_wait_fast(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                               volatile int* abort_flag) {
+  if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
+  return warp_wait(bar, parity, limit_ns, abort_flag);
+}
+
+// position in the ring: next slot and the phase parity of its current use
+struct RingPos {
+  int slot = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void advance() {
+    if (++slot == NR) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
 
 // The ring's item sequence, shared by the producer and the MMA issuer:
 // iteration u (0..ntiles) carries the NCH chunks of tile u (u < ntiles) with
@@ -244,84 +265,80 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  // The CTA allocates all 512 columns, so its allocation can only start at lane 0,
+  // column 0. The kernel uses that address as a constant (operands known to be
+  // warp-uniform keep tcgen05 issue cheap) and checks it here.
+  static_assert(C::TM_COLS == 512, "whole-TMEM allocation");
+  constexpr uint32_t tmem = 0;
+  const bool tmem_ok = *tmem_slot == tmem;
+  if (!tmem_ok && threadIdx.x == 0) raise_error(p.err, kErrLaunch);
 
   auto fail = [&]() {
     raise_error(p.err, kErrWaitTimeout);
     *abort_flag = 1;
   };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer: TMA into the ring + L2 prefetch
-    // One thread's bulk copies are served one after another (~16-19 B/clk per issuing
-    // thread on this part), so the boxes of each ring item are issued by different
-    // lanes, rotating over the warp; the whole warp walks the item sequence together.
+  if (!tmem_ok) {
+    // nothing was issued; fall through to the deallocation
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ producer: TMA into the ring
+    // The whole warp walks the item sequence and computes every coordinate (warp-uniform
+    // values, block-table entries read by all lanes); one elected lane issues the copies.
     const uint64_t pol_last = policy_evict_first();  // O items are the last reads of those rows
+    const bool leader = elect_one();
     int last[NR];
     for (int i = 0; i < NR; ++i) last[i] = -1;
-    int rot = 0;  // lane that issues the next box
-    auto my_box = [&](int nbox) -> int {  // box index this lane issues (or -1); advances the rotation
-      const int k = (lane - rot + 32) & 31;
-      rot = (rot + nbox) & 31;
-      return k < nbox ? k : -1;
-    };
-    auto prefetch_tile = [&](int t) {
-      const int key0 = kstart + t * TK;
-      const bool two = tile_keys(t) > 64;
-      const int k = my_box(2 * C::NCH);
-      if (k >= 0 && (k < C::NCH || two)) {
-        const int row = cache_row(p, bi, key0 + (k >= C::NCH ? 64 : 0));
-        const int j = k % C::NCH;
-        if (j < C::NBL) tma_prefetch_l2_2d(&tm_z64, j * 64, row);
-        else tma_prefetch_l2_2d(&tm_kpe64, 0, row);
-      }
-    };
-    for (int t = 0; t < PF && t < ntiles; ++t) prefetch_tile(t);
-    if (lane == 0) mbar_expect_tx(q_full, C::Q_LAT + C::Q_PE);
-    __syncwarp();
-    {
-      const int k = my_box(C::NBL + 1);
-      if (k >= 0 && k < C::NBL) tma_load_2d(sb + k * C::Q_BOX, &tm_qz, k * 64, qrow0, q_full);
-      if (k == C::NBL) tma_load_2d(sb + C::OFF_QPE, &tm_qpe, 0, qrow0, q_full);
+    if (leader) {
+      mbar_expect_tx(q_full, C::Q_LAT + C::Q_PE);
+      for (int k = 0; k < C::NBL; ++k) tma_load_2d(sb + k * C::Q_BOX, &tm_qz, k * 64, qrow0, q_full);
+      tma_load_2d(sb + C::OFF_QPE, &tm_qpe, 0, qrow0, q_full);
     }
+    __syncwarp();
     int ic = 0;  // ring items issued
+    RingPos rp;
     auto acquire = [&](int& slot) -> bool {
-      slot = ic % NR;
-      if (ic >= NR && !warp_wait(&r_empty[slot], ((ic / NR) - 1) & 1, p.wait_ns, abort_flag)) return false;
+      slot = rp.slot;
+      const uint32_t prev = rp.phase ^ 1u;  // phase of the slot's previous use
+      rp.advance();
+      if (ic >= NR && !warp_wait_fast(&r_empty[slot], prev, p.wait_ns, abort_flag)) return false;
       last[slot] = ic;
       ++ic;
       return true;
     };
     auto chunk = [&](int u, int j) -> bool {
-      if (j == 0 && u + PF < ntiles) prefetch_tile(u + PF);
       int slot;
       if (!acquire(slot)) return false;
       const int key0 = kstart + u * TK;
-      const int nhalf = tile_keys(u) > 64 ? 2 : 1;
+      const bool two = tile_keys(u) > 64;
+      const int row0 = cache_row(p, bi, key0);
+      const int row1 = two ? cache_row(p, bi, key0 + 64) : 0;
       const uint32_t dst = sb + C::OFF_RING + slot * C::SLOT;
-      const bool pe = j == C::NBL;
-      const uint32_t half = pe ? C::HALF_PE : C::HALF_LAT;
-      if (lane == 0) mbar_expect_tx(&r_full[slot], half * nhalf);
-      __syncwarp();
-      const int k = my_box(nhalf);
-      if (k >= 0) {
-        const int row = cache_row(p, bi, key0 + k * 64);
-        if (pe) tma_load_2d(dst + k * half, &tm_kpe64, 0, row, &r_full[slot]);
-        else tma_load_2d(dst + k * half, &tm_z64, j * 64, row, &r_full[slot]);
+      if (leader) {
+        if (j == C::NBL) {
+          mbar_expect_tx(&r_full[slot], C::HALF_PE * (two ? 2 : 1));
+          tma_load_2d(dst, &tm_kpe64, 0, row0, &r_full[slot]);
+          if (two) tma_load_2d(dst + C::HALF_PE, &tm_kpe64, 0, row1, &r_full[slot]);
+        } else {
+          mbar_expect_tx(&r_full[slot], C::HALF_LAT * (two ? 2 : 1));
+          tma_load_2d(dst, &tm_z64, j * 64, row0, &r_full[slot]);
+          if (two) tma_load_2d(dst + C::HALF_LAT, &tm_z64, j * 64, row1, &r_full[slot]);
+        }
       }
+      __syncwarp();
       return true;
     };
     auto pair = [&](int v, int q) -> bool {
       int slot;
       if (!acquire(slot)) return false;
       const uint32_t dst = sb + C::OFF_RING + slot * C::SLOT;
-      if (lane == 0) mbar_expect_tx(&r_full[slot], C::PAIR_BYTES);
-      __syncwarp();
-      const int k = my_box(C::KLH / 64);
-      if (k >= 0) {
-        const int row = cache_row(p, bi, kstart + v * TK + q * PAIR);
-        tma_load_2d_hint(dst + k * C::PBOX, &tm_z32, lh * C::KLH + k * 64, row, &r_full[slot], pol_last);
+      const int row = cache_row(p, bi, kstart + v * TK + q * PAIR);
+      if (leader) {
+        mbar_expect_tx(&r_full[slot], C::PAIR_BYTES);
+#pragma unroll
+        for (int k = 0; k < C::KLH / 64; ++k)
+          tma_load_2d_hint(dst + k * C::PBOX, &tm_z32, lh * C::KLH + k * 64, row, &r_full[slot], pol_last);
       }
+      __syncwarp();
       return true;
     };
     bool ok = true;
@@ -336,11 +353,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (lane 0; the warp zeroes tails)
+    // ------------------------------------------------------------ MMA issuer (one elected lane issues; the warp zeroes tails)
     bool ok = true;
     if (p.test_timeout) ok = warp_wait(test_bar, 0, kTestWaitNs, abort_flag);
     if (ok) ok = warp_wait(q_full, 0, p.wait_ns, abort_flag);
     tc_fence_after();
+    const bool leader = elect_one();
     constexpr uint32_t idS = idesc_bf16_f32(BMROWS, TK, false, false);
     constexpr uint32_t idO = idesc_bf16_f32(BMROWS, C::KLH, false, true);
     // descriptors of the resident Q' chunks and of ring slot 0 (start-address field advanced per slot / k step)
@@ -349,37 +367,48 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint64_t dring = smem_desc(sb + C::OFF_RING, 16, 1024, kSw128);
     const uint64_t dring_pe = smem_desc(sb + C::OFF_RING, 16, 8 * C::PE_ROW, C::PE_SWZ);
     const uint64_t dpair = smem_desc(sb + C::OFF_RING, C::PBOX, 1024, kSw128);  // Z slab read MN-major
-    int ic = 0;        // ring items consumed
+    RingPos rp;
     bool first_o = true;
+    // A ring item written by TMA is ordered before the MMAs that read it by its mbarrier
+    // alone; tcgen05 fences are needed only where other threads touched Tensor Memory (P).
     auto take = [&](int& slot) -> bool {
-      slot = ic % NR;
-      if (!warp_wait(&r_full[slot], (ic / NR) & 1, p.wait_ns, abort_flag)) return false;
-      ++ic;
-      return true;
+      slot = rp.slot;
+      const uint32_t ph = rp.phase;
+      rp.advance();
+      return warp_wait_fast(&r_full[slot], ph, p.wait_ns, abort_flag);
     };
     auto chunk = [&](int u, int j) -> bool {
       int slot;
       if (!take(slot)) return false;
-      if (lane == 0) {
-        tc_fence_after();
-        const uint32_t d_s = tmem + C::TM_S + (u & 1) * TK;
-        const uint64_t so = (uint64_t)((slot * C::SLOT) >> 4);
-        if (j < C::NBL) {
-          const uint64_t qa = dq0 + (uint64_t)((j * C::Q_BOX) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc_mma_ss(d_s, qa + 2 * kk, dring + so + 2 * kk, idS, (j > 0 || kk > 0) ? 1u : 0u);
-        } else {
-#pragma unroll
-          for (int kk = 0; kk < P / 16; ++kk) tc_mma_ss(d_s, dqpe + 2 * kk, dring_pe + so + 2 * kk, idS, 1u);
+      const uint32_t d_s = tmem + C::TM_S + (u & 1) * TK;
+      const uint64_t so = (uint64_t)((slot * C::SLOT) >> 4);
+      if (j < C::NBL) {
+        const uint64_t qa = dq0 + (uint64_t)((j * C::Q_BOX) >> 4);
+        const uint64_t kb = dring + so;
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
+        if (leader) {
+          tc_mma_ss(d_s, qa, kb, idS, acc0);
+          tc_mma_ss(d_s, qa + 2, kb + 2, idS, 1u);
+          tc_mma_ss(d_s, qa + 4, kb + 4, idS, 1u);
+          tc_mma_ss(d_s, qa + 6, kb + 6, idS, 1u);
+          tc_commit(&r_empty[slot]);
         }
-        tc_commit(&r_empty[slot]);
+      } else {
+        const uint64_t kb = dring_pe + so;
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < P / 16; ++kk) tc_mma_ss(d_s, dqpe + 2 * kk, kb + 2 * kk, idS, 1u);
+          tc_commit(&r_empty[slot]);
+        }
       }
       __syncwarp();
       return true;
     };
     auto pair = [&](int v, int q) -> bool {
-      if (q == 0 && !warp_wait(p_full, v & 1, p.wait_ns, abort_flag)) return false;
+      if (q == 0) {
+        if (!warp_wait(p_full, v & 1, p.wait_ns, abort_flag)) return false;
+        tc_fence_after();  // P was written to Tensor Memory by the softmax warps
+      }
       int slot;
       if (!take(slot)) return false;
       const int nsl = tile_slabs(v);
@@ -397,18 +426,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
       }
-      if (lane == 0) {
-        tc_fence_after();
-        const uint64_t so = (uint64_t)((slot * C::SLOT) >> 4);
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int sl = 2 * q + e;
-          if (sl < nsl) {
-            const uint32_t a = tmem + C::TM_S + (v & 1) * TK + sl * (SLAB / 2);
-            tc_mma_ts(tmem, a, dpair + so + (uint64_t)((e * SLAB * 128) >> 4), idO, first_o ? 0u : 1u);
-            first_o = false;
-          }
-        }
+      const uint64_t zb = dpair + (uint64_t)((slot * C::SLOT) >> 4);
+      const uint32_t a0 = tmem + C::TM_S + (v & 1) * TK + 2 * q * (SLAB / 2);
+      const uint32_t acc0 = first_o ? 0u : 1u;
+      if (leader) {
+        tc_mma_ts(tmem, a0, zb, idO, acc0);
+        if (2 * q + 1 < nsl) tc_mma_ts(tmem, a0 + SLAB / 2, zb + (uint64_t)((SLAB * 128) >> 4), idO, 1u);
         tc_commit(&r_empty[slot]);
       }
       first_o = false;
@@ -417,12 +440,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     };
     for (int u = 0; ok && u <= ntiles; ++u) {
       ok = walk_iteration<C::NCH, C::J0>(u, ntiles, tile_pairs(u - 1), chunk, pair);
-      if (ok && lane == 0) tc_commit(u < ntiles ? &s_ready[u & 1] : o_final);
+      if (ok && leader) tc_commit(u < ntiles ? &s_ready[u & 1] : o_final);
       __syncwarp();
     }
-    if (lane == 0) {
-      if (!ok && !*abort_flag) fail();
-      // every issued tcgen05 operation has finished before TMEM is released
+    if (lane == 0 && !ok && !*abort_flag) fail();
+    // every issued tcgen05 operation has finished before TMEM is released
+    if (leader) {
       tc_commit(fin_bar);
       mbar_wait(fin_bar, 0, kTeardownNs, nullptr);
     }
@@ -568,7 +591,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::TM_COLS);
+    tmem_dealloc(*tmem_slot, C::TM_COLS);
   }
 }
 

@@ -143,6 +143,34 @@ Plan gqa_plan(int b, int s, int hq, int hkv, int d, int max_seqlen, int sms) {
   return plan_splits(base, max_seqlen, slots, 256, 512, kPage);
 }
 
+// Balanced grouped-head schedule (gqa_balanced_kernel): used when the planner splits
+// the context, no split count is forced and a CTA holds one 16-row m-tile (the
+// tensor-core variant keeps the fixed chunks). Its grid is one wave of CTAs; the
+// per-CTA share of the key tiles is computed on the device from the actual lengths.
+// With two m-tiles (more than 16 query rows per KV head) the register-bound main loop
+// measured ~12 % slower per tile inside the balanced kernel on B300 (24-head MQA,
+// d = 256: 2.01 vs 1.79 us per 64-key tile, clocks at maximum in both), more than the
+// balance wins back, so those shapes keep the fixed chunks.
+struct GqaBalanced {
+  int grid = 0;          // 0: fixed chunks
+  long long items = 0;   // work items (sequence, KV head, row block)
+  int rpb = 0;           // rows per CTA
+};
+GqaBalanced gqa_balanced(const Plan& pl, int b, int s, int hq, int hkv, int d, int sms) {
+  GqaBalanced gb;
+  const int rows = (hq / hkv) * s;
+  if (pl.nsplit <= 1 || g_forced_splits.load() > 0 || use_gqa_tc(rows, d) || gqa_rows_per_cta(rows) > 16) return gb;
+  gb.rpb = gqa_rows_per_cta(rows);
+  gb.items = (long long)b * hkv * ceil_div(rows, gb.rpb);
+  gb.grid = sms * gqa_balanced_ctas_per_sm(d, rows);
+  return gb;
+}
+size_t balanced_bytes(const GqaBalanced& gb, int d) {
+  const long long records = gb.items + gb.grid;
+  return align256((size_t)records * gb.rpb * d * sizeof(float)) + align256((size_t)records * gb.rpb * sizeof(float)) +
+         align256((size_t)gb.items * 2 * sizeof(int));
+}
+
 // --- latent MLA plan (one CTA per SM: its shared memory holds the 128-row query tile)
 Plan mla_plan(int b, int s, int h, int k, int max_seqlen, int sms) {
   const long long base = (long long)b * mla_latent_parts(k) * ceil_div((long long)h * s, 128);
@@ -196,6 +224,8 @@ size_t gqa_decode_workspace_size(int b, int s, int hq, int hkv, int d, int max_s
   DeviceState* st = nullptr;
   if (device_state(&st)) return 0;
   const Plan pl = gqa_plan(b, s, hq, hkv, d, max_seqlen, st->sms);
+  const GqaBalanced gb = gqa_balanced(pl, b, s, hq, hkv, d, st->sms);
+  if (gb.grid > 0) return balanced_bytes(gb, d);
   return partial_bytes((long long)b * hq * s, pl.nsplit, d);
 }
 
@@ -212,8 +242,9 @@ int gqa_decode(const decattn_bf16* q, const decattn_bf16* k, const decattn_bf16*
   DeviceState* st = nullptr;
   if (int rc = device_state(&st)) return rc;
   const Plan pl = gqa_plan(b, s, hq, hkv, d, max_seqlen, st->sms);
+  const GqaBalanced gb = gqa_balanced(pl, b, s, hq, hkv, d, st->sms);
   const long long rows = (long long)b * hq * s;
-  const size_t need = partial_bytes(rows, pl.nsplit, d);
+  const size_t need = gb.grid > 0 ? balanced_bytes(gb, d) : partial_bytes(rows, pl.nsplit, d);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return DECATTN_ERR_WORKSPACE;
   GqaLaunch a;
   a.q = q;
@@ -239,12 +270,25 @@ int gqa_decode(const decattn_bf16* q, const decattn_bf16* k, const decattn_bf16*
   a.ws_lse = pl.nsplit > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                                        align256((size_t)rows * pl.nsplit * d * sizeof(float)))
                            : nullptr;
+  a.meta = nullptr;
+  a.balanced_grid = gb.grid;
+  if (gb.grid > 0) {
+    const long long records = gb.items + gb.grid;
+    char* w = static_cast<char*>(workspace);
+    const size_t o_bytes = align256((size_t)records * gb.rpb * d * sizeof(float));
+    a.ws_o = reinterpret_cast<float*>(w);
+    a.ws_lse = reinterpret_cast<float*>(w + o_bytes);
+    a.meta = reinterpret_cast<int*>(w + o_bytes + align256((size_t)records * gb.rpb * sizeof(float)));
+  }
   a.err = st->err;
   a.wait_ns = wait_limit();
   g_last_splits.store(pl.nsplit);
   const cudaError_t le = use_gqa_tc((hq / hkv) * s, d) ? launch_gqa_tc(a, stream) : launch_gqa(a, stream);
   if (le != cudaSuccess) return DECATTN_ERR_CUDA;
-  if (pl.nsplit > 1) {
+  if (gb.grid > 0) {
+    if (launch_combine_balanced(a.ws_o, a.ws_lse, a.meta, seqlens, b, hq, s, hkv, d, out, lse, stream) != cudaSuccess)
+      return DECATTN_ERR_CUDA;
+  } else if (pl.nsplit > 1) {
     if (launch_combine(a.ws_o, a.ws_lse, seqlens, (int)rows, hq * s, pl.nsplit, pl.chunk, d, out, lse, stream) !=
         cudaSuccess)
       return DECATTN_ERR_CUDA;

@@ -40,6 +40,7 @@ struct GqaParams {
   float* lse;
   float* ws_o;
   float* ws_lse;
+  int* meta;  // balanced mode: per work item {first partial record, record count}
   unsigned* err;
 };
 
@@ -68,40 +69,27 @@ struct GqaCfg {
 
 __device__ __forceinline__ uint32_t swz(int row, int chunk) { return (uint32_t)(chunk ^ (row & 7)); }
 
+// Where a segment's result goes.
+enum SegOut { kSegFinal = 0, kSegSplit = 1, kSegRecord = 2 };
+
+// Attention of the query rows of block rb of KV head g of sequence bi over keys
+// [kstart, kend) (kstart < kend <= L). out_mode kSegFinal writes bf16 rows and the
+// LSE; kSegSplit writes fp32 partials at chunk index `slot` of the [row][nsplit]
+// layout; kSegRecord writes partial record `slot` ([record][16*MT rows][D]) of the
+// balanced schedule. The caller's threads all enter; shared memory is free again
+// when it returns.
 template <int D, int MT>
-__global__ void __launch_bounds__(128 * MT) gqa_split_kernel(GqaParams p) {
+__device__ __forceinline__ void gqa_segment(const GqaParams& p, uint8_t* smem, float (*s_m)[kSlices][16],
+                                            float (*s_l)[kSlices][16], int bi, int g, int rb, int L, int kstart,
+                                            int kend, int out_mode, int slot) {
   using C = GqaCfg<D, MT>;
   constexpr int NT = D / 8;   // n-tiles of the output
   constexpr int KS = D / 16;  // k-steps of QK^T
-  extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ float s_m[MT][kSlices][16];
-  __shared__ float s_l[MT][kSlices][16];
-
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int mt = warp / kSlices;     // m-tile of this warp
   const int slice = warp % kSlices;  // 16-key slice of each tile
-  const int rb = blockIdx.x % p.nrb;
-  const int split = blockIdx.x / p.nrb;
-  const int g = blockIdx.y;
-  const int bi = blockIdx.z;
-
-  const int L = p.seqlens[bi];
-  const int kstart = split * p.chunk;
-  if (kstart >= L) {  // chunk past the end: the combine skips it
-    if (L <= 0 && p.nsplit == 1) {  // empty sequence without a combine pass: zero rows, LSE = -inf
-      for (int idx = tid; idx < 16 * MT * (D / 8); idx += C::THREADS) {
-        const int rg = rb * MT * 16 + idx / (D / 8);
-        if (rg >= p.R) continue;
-        const size_t rowflat = (size_t)(bi * p.hq + g * p.G + rg / p.s) * p.s + (rg % p.s);
-        *reinterpret_cast<uint4*>(p.out + rowflat * D + (idx % (D / 8)) * 8) = make_uint4(0, 0, 0, 0);
-        if (p.lse && idx % (D / 8) == 0) p.lse[rowflat] = -INFINITY;
-      }
-    }
-    return;
-  }
-  const int kend = min(L, kstart + p.chunk);
   const int ntiles = (kend - kstart + kTileKeys - 1) / kTileKeys;
   const int mrow0 = (rb * MT + mt) * 16;  // first row (within the KV head's rows) of this warp's m-tile
 
@@ -356,31 +344,191 @@ __global__ void __launch_bounds__(128 * MT) gqa_split_kernel(GqaParams p) {
     const float lse = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
     const int j = g * p.G + rg / p.s;
     const size_t rowflat = (size_t)(bi * p.hq + j) * p.s + (rg % p.s);
-    if (p.nsplit == 1) {
+    if (out_mode == kSegFinal) {
       uint2 pk;
       pk.x = pack_bf16(acc.x, acc.y);
       pk.y = pack_bf16(acc.z, acc.w);
       *reinterpret_cast<uint2*>(p.out + rowflat * D + c4) = pk;
       if (p.lse && c4 == 0) p.lse[rowflat] = lse;
+    } else if (out_mode == kSegSplit) {
+      *reinterpret_cast<float4*>(p.ws_o + (rowflat * p.nsplit + slot) * D + c4) = acc;
+      if (c4 == 0) p.ws_lse[rowflat * p.nsplit + slot] = lse;
     } else {
-      *reinterpret_cast<float4*>(p.ws_o + (rowflat * p.nsplit + split) * D + c4) = acc;
-      if (c4 == 0) p.ws_lse[rowflat * p.nsplit + split] = lse;
+      const size_t rec_row = (size_t)slot * (16 * MT) + rr;
+      *reinterpret_cast<float4*>(p.ws_o + rec_row * D + c4) = acc;
+      if (c4 == 0) p.ws_lse[rec_row] = lse;
     }
+  }
+  __syncthreads();  // the merge buffer aliases the pipeline of the next segment
+}
+
+// One CTA per (sequence, KV head, context chunk, block of query rows).
+template <int D, int MT>
+__global__ void __launch_bounds__(128 * MT) gqa_split_kernel(GqaParams p) {
+  using C = GqaCfg<D, MT>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ float s_m[MT][kSlices][16];
+  __shared__ float s_l[MT][kSlices][16];
+  const int tid = threadIdx.x;
+  const int rb = blockIdx.x % p.nrb;
+  const int split = blockIdx.x / p.nrb;
+  const int g = blockIdx.y;
+  const int bi = blockIdx.z;
+  const int L = p.seqlens[bi];
+  const int kstart = split * p.chunk;
+  if (kstart >= L) {  // chunk past the end: the combine skips it
+    if (L <= 0 && p.nsplit == 1) {  // empty sequence without a combine pass: zero rows, LSE = -inf
+      for (int idx = tid; idx < 16 * MT * (D / 8); idx += C::THREADS) {
+        const int rg = rb * MT * 16 + idx / (D / 8);
+        if (rg >= p.R) continue;
+        const size_t rowflat = (size_t)(bi * p.hq + g * p.G + rg / p.s) * p.s + (rg % p.s);
+        *reinterpret_cast<uint4*>(p.out + rowflat * D + (idx % (D / 8)) * 8) = make_uint4(0, 0, 0, 0);
+        if (p.lse && idx % (D / 8) == 0) p.lse[rowflat] = -INFINITY;
+      }
+    }
+    return;
+  }
+  const int kend = min(L, kstart + p.chunk);
+  gqa_segment<D, MT>(p, smem, s_m, s_l, bi, g, rb, L, kstart, kend, p.nsplit == 1 ? kSegFinal : kSegSplit, split);
+}
+
+__device__ __forceinline__ long long tiles_of(int L) { return L > 0 ? (L + kTileKeys - 1) / kTileKeys : 0; }
+
+// Balanced schedule. The work items (sequence, KV head, row block) are laid end to
+// end in sequence-major order, each as its ceil(L/64) key tiles, and CTA c takes the
+// tiles [c*W, (c+1)*W) with W = ceil(total / gridDim.x): every CTA gets the same
+// number of tiles whatever the length mix, and a range may cut items anywhere. A
+// piece that is a whole item is written as final rows; the pieces of a cut item go
+// to partial records (record id = item index + CTA index, unique and increasing along
+// the order) and the CTA holding the item's first tile stores {first record, count}
+// in meta for the combine kernel. Computed from seqlens on the device, so the launch
+// needs only an upper bound of the lengths.
+template <int D, int MT>
+__global__ void __launch_bounds__(128 * MT) gqa_balanced_kernel(GqaParams p) {
+  using C = GqaCfg<D, MT>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ float s_m[MT][kSlices][16];
+  __shared__ float s_l[MT][kSlices][16];
+  constexpr int NW = C::THREADS / 32;
+  __shared__ long long s_wsum[NW];  // inclusive prefix of the warps' tile counts
+  // walk state, kept in shared memory so that nothing but constants stays live in
+  // registers across the (register-bound) segment body
+  __shared__ long long s_base, s_pos, s_end, s_w;
+  __shared__ int s_seq;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int ips = p.hkv * p.nrb;  // work items per sequence
+  // tiles of each thread's block of sequences, and their exclusive prefix (block scan)
+  const int per = (p.b + C::THREADS - 1) / C::THREADS;
+  const int i0 = min(p.b, tid * per), i1 = min(p.b, i0 + per);
+  long long mine = 0;
+  for (int i = i0; i < i1; ++i) mine += tiles_of(p.seqlens[i]);
+  long long incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  if (tid == 0) {
+    s_seq = p.b;
+    s_base = 0;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    long long w = lane < NW ? s_wsum[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < NW; o <<= 1) {
+      const long long n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    if (lane < NW) s_wsum[lane] = w;
+  }
+  __syncthreads();
+  const long long excl = incl - mine + (warp > 0 ? s_wsum[warp - 1] : 0);
+  const long long total = s_wsum[NW - 1] * ips;
+  const long long W = (total + gridDim.x - 1) / gridDim.x;
+  long long pos = (long long)blockIdx.x * W;
+  const long long end = min(total, pos + W);
+  if (pos >= end) return;
+  {  // the sequence holding tile `pos`: found by the one thread whose block contains it
+    long long b0 = excl * ips;
+    if (pos >= b0 && pos < b0 + mine * ips) {
+      for (int i = i0; i < i1; ++i) {
+        const long long st = tiles_of(p.seqlens[i]) * ips;
+        if (pos < b0 + st) {
+          s_seq = i;
+          s_base = b0;
+          break;
+        }
+        b0 += st;
+      }
+    }
+  }
+  if (tid == 0) {
+    s_pos = pos;
+    s_end = end;
+    s_w = W;
+  }
+  __syncthreads();
+#pragma unroll 1
+  while (true) {
+    const long long pos = s_pos, end = s_end, W = s_w;
+    int i = s_seq;
+    long long base = s_base;  // first flattened tile of sequence i
+    long long nt = 0;
+    int L = 0;
+    for (; i < p.b; ++i) {  // skip to the sequence holding tile pos (past ones, empty ones)
+      L = p.seqlens[i];
+      nt = tiles_of(L);
+      if (pos < base + nt * ips) break;
+      base += nt * ips;
+    }
+    if (pos >= end || i >= p.b) break;
+    const long long off = pos - base;
+    const int item_local = (int)(off / nt);
+    const int t0 = (int)(off % nt);
+    const int t1 = (int)min(nt, (long long)t0 + (end - pos));
+    const int g = item_local / p.nrb;
+    const int rb = item_local % p.nrb;
+    const long long item = (long long)i * ips + item_local;
+    const long long first = base + (long long)item_local * nt;  // flattened first tile of the item
+    const int c0 = (int)(first / W);
+    const int c1 = (int)((first + nt - 1) / W);
+    if (t0 == 0 && tid == 0) {
+      p.meta[2 * item] = (int)(item + c0);
+      p.meta[2 * item + 1] = c1 - c0 + 1;
+    }
+    gqa_segment<D, MT>(p, smem, s_m, s_l, i, g, rb, L, t0 * kTileKeys, min(L, t1 * kTileKeys),
+                       c0 == c1 ? kSegFinal : kSegRecord, (int)(item + blockIdx.x));
+    // (gqa_segment ends with a barrier: every thread has read the state above)
+    if (tid == 0) {
+      s_pos = pos + (t1 - t0);
+      s_seq = i;
+      s_base = base;
+    }
+    __syncthreads();
   }
 }
 
 template <int D, int MT>
-cudaError_t launch_gqa_dm(const GqaParams& p, int nsplit, int hkv, int b, cudaStream_t stream) {
+cudaError_t launch_gqa_dm(const GqaParams& p, int nsplit, int hkv, int b, int balanced_grid, cudaStream_t stream) {
   using C = GqaCfg<D, MT>;
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e =
         cudaFuncSetAttribute(gqa_split_kernel<D, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gqa_balanced_kernel<D, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  dim3 grid(p.nrb * nsplit, hkv, b);
-  gqa_split_kernel<D, MT><<<grid, C::THREADS, C::SMEM, stream>>>(p);
+  if (balanced_grid > 0) {
+    gqa_balanced_kernel<D, MT><<<balanced_grid, C::THREADS, C::SMEM, stream>>>(p);
+  } else {
+    dim3 grid(p.nrb * nsplit, hkv, b);
+    gqa_split_kernel<D, MT><<<grid, C::THREADS, C::SMEM, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 
@@ -390,6 +538,35 @@ cudaError_t launch_gqa_dm(const GqaParams& p, int nsplit, int hkv, int b, cudaSt
 static int gqa_mt(int rows) { return rows <= 16 ? 1 : 2; }
 
 int gqa_rows_per_cta(int rows) { return 16 * gqa_mt(rows); }
+
+// Resident CTAs per SM of the balanced kernel (its grid is one wave of them).
+template <int D, int MT>
+static int balanced_occupancy() {
+  using C = GqaCfg<D, MT>;
+  static int cached = 0;
+  if (cached == 0) {
+    int n = 0;
+    if (cudaFuncSetAttribute(gqa_balanced_kernel<D, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) ==
+            cudaSuccess &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_balanced_kernel<D, MT>, C::THREADS, C::SMEM) ==
+            cudaSuccess &&
+        n > 0)
+      cached = n;
+    else
+      return 1;
+  }
+  return cached;
+}
+
+int gqa_balanced_ctas_per_sm(int d, int rows) {
+  const bool two = gqa_mt(rows) == 2;
+  switch (d) {
+    case 64: return two ? balanced_occupancy<64, 2>() : balanced_occupancy<64, 1>();
+    case 128: return two ? balanced_occupancy<128, 2>() : balanced_occupancy<128, 1>();
+    case 256: return two ? balanced_occupancy<256, 2>() : balanced_occupancy<256, 1>();
+    default: return 1;
+  }
+}
 int gqa_ctas_per_sm(int d) { return d <= 64 ? 3 : (d <= 128 ? 2 : 1); }
 
 cudaError_t launch_gqa(const GqaLaunch& a, cudaStream_t stream) {
@@ -418,11 +595,12 @@ cudaError_t launch_gqa(const GqaLaunch& a, cudaStream_t stream) {
   p.lse = a.lse;
   p.ws_o = a.ws_o;
   p.ws_lse = a.ws_lse;
+  p.meta = a.meta;
   p.err = a.err;
-#define DECATTN_GQA_CASE(D)                                                        \
-  case D:                                                                          \
-    return mt == 1 ? launch_gqa_dm<D, 1>(p, a.nsplit, a.hkv, a.b, stream)          \
-                   : launch_gqa_dm<D, 2>(p, a.nsplit, a.hkv, a.b, stream);
+#define DECATTN_GQA_CASE(D)                                                                  \
+  case D:                                                                                    \
+    return mt == 1 ? launch_gqa_dm<D, 1>(p, a.nsplit, a.hkv, a.b, a.balanced_grid, stream)   \
+                   : launch_gqa_dm<D, 2>(p, a.nsplit, a.hkv, a.b, a.balanced_grid, stream);
   switch (a.d) {
     DECATTN_GQA_CASE(64)
     DECATTN_GQA_CASE(128)
@@ -440,80 +618,140 @@ cudaError_t launch_gqa(const GqaLaunch& a, cudaStream_t stream) {
 // Partials whose rows saw no key carry lse_c = -inf and weigh nothing; a row
 // with no partial (empty sequence) gets o = 0, lse = -inf. One warp per row.
 
+// Combine geometry: D/8 threads per row (thread t owns columns 8t .. 8t+7), 256-thread
+// blocks holding 256 / (D/8) rows, so that a launch is about one wave of small blocks.
+template <int D>
+struct MergeCfg {
+  static constexpr int TPR = D / 8;
+  static constexpr int ROWS = 256 / TPR;
+};
+
+// The threads of one row merge its n partials: partial c has its D floats at
+// o0 + c * o_stride and its LSE at l0[c * l_stride]. The loop has no data-dependent
+// branch, so the loads of several partials are in flight together (a partial with
+// LSE = -inf holds zeros and weighs 0).
+template <int D>
+__device__ __forceinline__ void merge_row(const float* __restrict__ o0, size_t o_stride, const float* __restrict__ l0,
+                                          size_t l_stride, int n, __nv_bfloat16* __restrict__ out_row,
+                                          float* __restrict__ lse_out, int t) {
+  float M = -INFINITY;
+  for (int c = 0; c < n; ++c) M = fmaxf(M, l0[c * l_stride]);
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  if (M != -INFINITY) {
+#pragma unroll 8
+    for (int c = 0; c < n; ++c) {
+      const float w = expf(l0[c * l_stride] - M);
+      wsum += w;
+      const float4* src = reinterpret_cast<const float4*>(o0 + c * o_stride + 8 * t);
+      const float4 x0 = src[0], x1 = src[1];
+      acc[0] += w * x0.x;
+      acc[1] += w * x0.y;
+      acc[2] += w * x0.z;
+      acc[3] += w * x0.w;
+      acc[4] += w * x1.x;
+      acc[5] += w * x1.y;
+      acc[6] += w * x1.z;
+      acc[7] += w * x1.w;
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  uint4 pk;
+  pk.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+  pk.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+  pk.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+  pk.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+  *reinterpret_cast<uint4*>(out_row + 8 * t) = pk;
+  if (lse_out && t == 0) *lse_out = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+}
+
+// Fixed chunks: row r merges partials c < ceil(L / chunk) of its sequence.
 template <int D>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ ws_o,
                                                       const float* __restrict__ ws_lse,
                                                       const int32_t* __restrict__ seqlens, int rows,
                                                       int rows_per_seq, int nsplit, int chunk,
                                                       __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
-  constexpr int V = D / 32;  // floats per lane
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (warp >= rows) return;
-  const int bi = warp / rows_per_seq;
-  const int L = seqlens[bi];
-  const int nv = min(nsplit, (L + chunk - 1) / chunk);
-  const float* lrow = ws_lse + (size_t)warp * nsplit;
-  float M = -INFINITY;
-  for (int c = lane; c < nv; c += 32) M = fmaxf(M, lrow[c]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  constexpr int VEC = D >= 128 ? 4 : 2;  // floats per vector access
-  float acc[V];
-#pragma unroll
-  for (int e = 0; e < V; ++e) acc[e] = 0.f;
-  float wsum = 0.f;
-  if (M != -INFINITY) {
-    for (int c = 0; c < nv; ++c) {
-      const float w = expf(lrow[c] - M);
-      wsum += w;
-      if (w == 0.f) continue;
-      const float* src = ws_o + ((size_t)warp * nsplit + c) * D + lane * VEC;
-#pragma unroll
-      for (int e = 0; e < V; e += VEC) {
-        if constexpr (VEC == 4) {
-          const float4 x = *reinterpret_cast<const float4*>(src + e * 32);
-          acc[e + 0] += w * x.x;
-          acc[e + 1] += w * x.y;
-          acc[e + 2] += w * x.z;
-          acc[e + 3] += w * x.w;
-        } else {
-          const float2 x = *reinterpret_cast<const float2*>(src + e * 32);
-          acc[e + 0] += w * x.x;
-          acc[e + 1] += w * x.y;
-        }
-      }
-    }
+  using M = MergeCfg<D>;
+  const int row = blockIdx.x * M::ROWS + threadIdx.x / M::TPR;
+  if (row >= rows) return;
+  const int L = seqlens[row / rows_per_seq];
+  const int nv = L > 0 ? min(nsplit, (L + chunk - 1) / chunk) : 0;
+  merge_row<D>(ws_o + (size_t)row * nsplit * D, D, ws_lse + (size_t)row * nsplit, 1, nv, out + (size_t)row * D,
+               lse_out ? lse_out + row : nullptr, threadIdx.x % M::TPR);
+}
+
+// Combine for the balanced grouped-head schedule: row (bi, head j, token) belongs to
+// work item (bi, KV head j / G, row block) whose meta entry gives its partial records;
+// a whole item (one record) was written as final rows by its CTA, an empty sequence
+// has no item and gets o = 0, LSE = -inf here.
+template <int D>
+__global__ void __launch_bounds__(256) combine_balanced_kernel(const float* __restrict__ ws_o,
+                                                               const float* __restrict__ ws_lse,
+                                                               const int* __restrict__ meta,
+                                                               const int32_t* __restrict__ seqlens, int rows, int hq,
+                                                               int s, int hkv, int G, int rpb, int nrb,
+                                                               __nv_bfloat16* __restrict__ out,
+                                                               float* __restrict__ lse_out) {
+  using M = MergeCfg<D>;
+  const int row = blockIdx.x * M::ROWS + threadIdx.x / M::TPR;
+  if (row >= rows) return;
+  const int bi = row / (hq * s);
+  const int j = (row / s) % hq;
+  const int r = (j % G) * s + row % s;  // row within the KV head's rows
+  const long long item = ((long long)bi * hkv + j / G) * nrb + r / rpb;
+  int first = 0, n = 0;
+  if (seqlens[bi] > 0) {
+    first = meta[2 * item];
+    n = meta[2 * item + 1];
+    if (n <= 1) return;  // written directly by its CTA
   }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  __nv_bfloat16* dst = out + (size_t)warp * D + lane * VEC;
-#pragma unroll
-  for (int e = 0; e < V; e += VEC) {
-    if constexpr (VEC == 4) {
-      uint2 pk;
-      pk.x = pack_bf16(acc[e + 0] * inv, acc[e + 1] * inv);
-      pk.y = pack_bf16(acc[e + 2] * inv, acc[e + 3] * inv);
-      *reinterpret_cast<uint2*>(dst + e * 32) = pk;
-    } else {
-      *reinterpret_cast<uint32_t*>(dst + e * 32) = pack_bf16(acc[e + 0] * inv, acc[e + 1] * inv);
-    }
-  }
-  if (lse_out && lane == 0) lse_out[warp] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+  const size_t rec_row = (size_t)first * rpb + r % rpb;
+  merge_row<D>(ws_o + rec_row * D, (size_t)rpb * D, ws_lse + rec_row, (size_t)rpb, n, out + (size_t)row * D,
+               lse_out ? lse_out + row : nullptr, threadIdx.x % M::TPR);
+}
+
+template <int D>
+static int merge_blocks(int rows) {
+  return (rows + MergeCfg<D>::ROWS - 1) / MergeCfg<D>::ROWS;
 }
 
 cudaError_t launch_combine(const float* ws_o, const float* ws_lse, const int32_t* seqlens, int rows,
                            int rows_per_seq, int nsplit, int chunk, int d, void* out, float* lse,
                            cudaStream_t stream) {
-  const int threads = 256;
-  const int blocks = (rows * 32 + threads - 1) / threads;
   auto* o = static_cast<__nv_bfloat16*>(out);
+#define DECATTN_COMBINE_CASE(D) \
+  case D: combine_kernel<D><<<merge_blocks<D>(rows), 256, 0, stream>>>(ws_o, ws_lse, seqlens, rows, rows_per_seq, nsplit, chunk, o, lse); break;
   switch (d) {
-    case 64: combine_kernel<64><<<blocks, threads, 0, stream>>>(ws_o, ws_lse, seqlens, rows, rows_per_seq, nsplit, chunk, o, lse); break;
-    case 128: combine_kernel<128><<<blocks, threads, 0, stream>>>(ws_o, ws_lse, seqlens, rows, rows_per_seq, nsplit, chunk, o, lse); break;
-    case 256: combine_kernel<256><<<blocks, threads, 0, stream>>>(ws_o, ws_lse, seqlens, rows, rows_per_seq, nsplit, chunk, o, lse); break;
-    case 512: combine_kernel<512><<<blocks, threads, 0, stream>>>(ws_o, ws_lse, seqlens, rows, rows_per_seq, nsplit, chunk, o, lse); break;
+    DECATTN_COMBINE_CASE(64)
+    DECATTN_COMBINE_CASE(128)
+    DECATTN_COMBINE_CASE(256)
+    DECATTN_COMBINE_CASE(512)
     default: return cudaErrorInvalidValue;
   }
+#undef DECATTN_COMBINE_CASE
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_balanced(const float* ws_o, const float* ws_lse, const int* meta, const int32_t* seqlens,
+                                    int b, int hq, int s, int hkv, int d, void* out, float* lse, cudaStream_t stream) {
+  const int rows_kv = (hq / hkv) * s;
+  const int rpb = gqa_rows_per_cta(rows_kv);
+  const int nrb = (rows_kv + rpb - 1) / rpb;
+  const int rows = b * hq * s;
+  auto* o = static_cast<__nv_bfloat16*>(out);
+  const int G = hq / hkv;
+#define DECATTN_COMBINE_CASE(D) \
+  case D: combine_balanced_kernel<D><<<merge_blocks<D>(rows), 256, 0, stream>>>(ws_o, ws_lse, meta, seqlens, rows, hq, s, hkv, G, rpb, nrb, o, lse); break;
+  switch (d) {
+    DECATTN_COMBINE_CASE(64)
+    DECATTN_COMBINE_CASE(128)
+    DECATTN_COMBINE_CASE(256)
+    default: return cudaErrorInvalidValue;
+  }
+#undef DECATTN_COMBINE_CASE
   return cudaGetLastError();
 }
 

@@ -20,8 +20,10 @@ struct GqaLaunch {
   float scale;
   void* out;
   float* lse;
-  float* ws_o;    // [b*hq*s, nsplit, d] (nsplit > 1)
-  float* ws_lse;  // [b*hq*s, nsplit]
+  float* ws_o;    // [b*hq*s, nsplit, d] (nsplit > 1), or balanced: [records, rows per CTA, d]
+  float* ws_lse;  // [b*hq*s, nsplit], or balanced: [records, rows per CTA]
+  int* meta;      // balanced: [work items][2] {first record, count}
+  int balanced_grid;  // > 0: balanced schedule over this many CTAs (mma.sync kernel)
   unsigned* err;
   unsigned long long wait_ns;  // limit of the tensor-core kernel's bounded waits
 };
@@ -29,6 +31,7 @@ struct GqaLaunch {
 // rows of one grouped-head CTA (multiple of 16) for head dim d
 int gqa_rows_per_cta(int d);
 int gqa_ctas_per_sm(int d);
+int gqa_balanced_ctas_per_sm(int d, int rows);  // measured occupancy of the balanced kernel
 cudaError_t launch_gqa(const GqaLaunch& p, cudaStream_t stream);
 // tensor-core variant (keys in the MMA M dimension) for KV heads shared by 17-32+ query rows
 bool gqa_tc_eligible(int rows, int d);
@@ -38,6 +41,9 @@ cudaError_t launch_gqa_tc(const GqaLaunch& p, cudaStream_t stream);
 // log-sum-exp merge of split partials: rows x nsplit partials of width d
 cudaError_t launch_combine(const float* ws_o, const float* ws_lse, const int32_t* seqlens, int rows, int rows_per_seq,
                            int nsplit, int chunk, int d, void* out, float* lse, cudaStream_t stream);
+// combine of the balanced grouped-head schedule (see gqa_balanced_kernel)
+cudaError_t launch_combine_balanced(const float* ws_o, const float* ws_lse, const int* meta, const int32_t* seqlens,
+                                    int b, int hq, int s, int hkv, int d, void* out, float* lse, cudaStream_t stream);
 
 struct ProjLaunch {
   const void* a;     // [b, h, s, kin]

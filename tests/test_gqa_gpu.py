@@ -143,6 +143,49 @@ def test_split_invariance(nsplit):
     check_all(q, cache, out2, lse2, seqlens, 128, f"nsplit {nsplit}")
 
 
+# ---------------------------------------------------------------------------
+# Balanced schedule: whenever the planner splits the context (and no split count is
+# forced) every CTA takes an equal run of key tiles over all (sequence, KV head, row
+# block) items laid end to end, cutting items anywhere; cut items are merged by the
+# combine kernel, whole ones are written directly.
+
+
+@pytest.mark.parametrize("b,hq,hkv,d,s,seqlens", [
+    # many items of mixed length, empty sequences, more items than CTAs take whole
+    (40, 8, 2, 64, 1, [(i * 977) % 3001 if i % 7 else 0 for i in range(40)]),
+    # MQA with 16 query rows per KV head (8 heads x MTP s=2), ragged
+    (5, 8, 1, 256, 2, [5000, 0, 2, 777, 4097]),
+    # one long sequence among short ones
+    (6, 16, 4, 128, 1, [20000, 64, 65, 3, 0, 129]),
+])
+def test_balanced_schedule_vs_oracle(b, hq, hkv, d, s, seqlens):
+    import decode_attention_18_b300 as da
+
+    q, cache, out, lse = run(b, hq, hkv, d, s, seqlens, paged=True, seed=17)
+    assert da.last_num_splits() > 1  # the planner split the context: balanced schedule
+    check_all(q, cache, out, lse, seqlens, d, f"balanced b{b} hq{hq} hkv{hkv} d{d} s{s}")
+    # deterministic: the schedule depends on the lengths only
+    sl = torch.tensor(seqlens, dtype=torch.int32, device=DEV)
+    out2, lse2 = da.gqa_decode(q, cache.k, cache.v, sl, max_seqlen=max(seqlens), block_table=cache.block_table)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
+def test_balanced_schedule_loose_bound():
+    # max_seqlen far above the actual lengths: the grid and workspace follow the bound,
+    # the split of the work follows the lengths
+    import decode_attention_18_b300 as da
+    from decode_attention_18_b300 import workloads as W
+
+    seqlens = [300, 5, 1200]
+    q, cache = W.make_gqa(3, 8, 2, 128, 1, seqlens, capacity=40000, seed=19, device=DEV)
+    sl = torch.tensor(seqlens, dtype=torch.int32, device=DEV)
+    out, lse = da.gqa_decode(q, cache.k, cache.v, sl, max_seqlen=40000)
+    torch.cuda.synchronize()
+    assert da.check_errors() == 0
+    check_all(q, cache, out, lse, seqlens, 128, "loose bound")
+
+
 def test_full_size_gqa_64_8_sampled():
     # b=32, Hq=64, Hkv=8, d=128, t=4096: the grouped-head workload at full size
     from decode_attention_18_b300 import workloads as W

@@ -93,10 +93,10 @@ def test_matches_gqa_decode_on_two_calls_in_a_row(lib):
 
 
 def test_refuses_shapes_beyond_the_fixed_array(lib):
-    # b=64, Hq=128, Hkv=8, d=256 at 64k context: the split partials need far
-    # more than 16 MiB, so the call returns DECATTN_ERR_WORKSPACE and launches
-    # nothing (the small tensors below are never touched).
-    b, hq, hkv, d, s, L = 64, 128, 8, 256, 1, 65536
+    # b=64, Hq=256, Hkv=8 (32 query rows per KV head), d=256 at 64k context: the
+    # split partials need more than 16 MiB, so the call returns DECATTN_ERR_WORKSPACE
+    # and launches nothing (the small tensors below are never touched).
+    b, hq, hkv, d, s, L = 64, 256, 8, 256, 1, 65536
     assert lib.gqa_decode_workspace_size(b, s, hq, hkv, d, L) > SCRATCH_BYTES
     q = torch.zeros((1, hq, s, d), dtype=torch.bfloat16, device=DEV)
     kv_t = torch.zeros((1, 1, hkv, d), dtype=torch.bfloat16, device=DEV)

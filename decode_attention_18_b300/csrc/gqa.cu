@@ -616,7 +616,7 @@ cudaError_t launch_gqa(const GqaLaunch& a, cudaStream_t stream) {
 // Row r of the output merges partials c < ceil(L / chunk) of its sequence:
 //   lse = log sum_c exp(lse_c),  o = sum_c exp(lse_c - lse) o_c
 // Partials whose rows saw no key carry lse_c = -inf and weigh nothing; a row
-// with no partial (empty sequence) gets o = 0, lse = -inf. One warp per row.
+// with no partial (empty sequence) gets o = 0, lse = -inf.
 
 // Combine geometry: D/8 threads per row (thread t owns columns 8t .. 8t+7), 256-thread
 // blocks holding 256 / (D/8) rows, so that a launch is about one wave of small blocks.
@@ -627,35 +627,56 @@ struct MergeCfg {
 };
 
 // The threads of one row merge its n partials: partial c has its D floats at
-// o0 + c * o_stride and its LSE at l0[c * l_stride]. The loop has no data-dependent
-// branch, so the loads of several partials are in flight together (a partial with
-// LSE = -inf holds zeros and weighs 0).
+// o0 + c * o_stride and its LSE at l0[c * l_stride]. Partials are taken four at a
+// time with all their loads issued before any use (one memory round trip per
+// group), merged with a running maximum; a partial with LSE = -inf saw no key and
+// is skipped.
 template <int D>
 __device__ __forceinline__ void merge_row(const float* __restrict__ o0, size_t o_stride, const float* __restrict__ l0,
                                           size_t l_stride, int n, __nv_bfloat16* __restrict__ out_row,
                                           float* __restrict__ lse_out, int t) {
-  float M = -INFINITY;
-  for (int c = 0; c < n; ++c) M = fmaxf(M, l0[c * l_stride]);
+  constexpr int U = 4;
+  float M = -INFINITY, wsum = 0.f;
   float acc[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-  float wsum = 0.f;
-  if (M != -INFINITY) {
-#pragma unroll 8
-    for (int c = 0; c < n; ++c) {
-      const float w = expf(l0[c * l_stride] - M);
-      wsum += w;
-      const float4* src = reinterpret_cast<const float4*>(o0 + c * o_stride + 8 * t);
-      const float4 x0 = src[0], x1 = src[1];
-      acc[0] += w * x0.x;
-      acc[1] += w * x0.y;
-      acc[2] += w * x0.z;
-      acc[3] += w * x0.w;
-      acc[4] += w * x1.x;
-      acc[5] += w * x1.y;
-      acc[6] += w * x1.z;
-      acc[7] += w * x1.w;
+  for (int c0 = 0; c0 < n; c0 += U) {
+    float lv[U];
+    float4 x0[U], x1[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      lv[u] = -INFINITY;
+      x0[u] = x1[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c0 + u < n) {
+        lv[u] = l0[(size_t)(c0 + u) * l_stride];
+        const float4* src = reinterpret_cast<const float4*>(o0 + (size_t)(c0 + u) * o_stride + 8 * t);
+        x0[u] = src[0];
+        x1[u] = src[1];
+      }
     }
+    float mn = M;
+#pragma unroll
+    for (int u = 0; u < U; ++u) mn = fmaxf(mn, lv[u]);
+    if (mn == -INFINITY) continue;
+    const float f = expf(M - mn);  // 0 while nothing was merged yet
+    wsum *= f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] *= f;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (lv[u] == -INFINITY) continue;
+      const float w = expf(lv[u] - mn);
+      wsum += w;
+      acc[0] += w * x0[u].x;
+      acc[1] += w * x0[u].y;
+      acc[2] += w * x0[u].z;
+      acc[3] += w * x0[u].w;
+      acc[4] += w * x1[u].x;
+      acc[5] += w * x1[u].y;
+      acc[6] += w * x1[u].z;
+      acc[7] += w * x1[u].w;
+    }
+    M = mn;
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   uint4 pk;

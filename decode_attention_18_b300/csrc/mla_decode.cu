@@ -554,28 +554,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
       const float lse = l_tot > 0.f ? (m_ref + log2f(l_tot)) * kLn2 : -INFINITY;
       const size_t grow = (size_t)qrow0 + r;
+      // O / l of this warp's 32 rows x OCW columns is staged in shared memory (the query tile's
+      // and ring space: every MMA and copy has completed once o_final fired) and stored as
+      // whole row segments. Straight from the TMEM layout (thread = row) every store
+      // instruction would touch 32 rows with 16 bytes each. Staged rows are 16-byte units
+      // XOR-swizzled by (row & 7), so the column-wise writes and the row-wise reads are
+      // free of bank conflicts.
+      constexpr int F4 = OCW / 4;     // 16-byte units per staged row
+      constexpr int ROWB = OCW * 4;   // bytes per staged row
+      constexpr int RPI = 32 / F4;    // rows per store instruction
+      static_assert(F4 >= 8 && F4 <= 32 && NSMW * 32 * ROWB <= C::OFF_RED, "epilogue staging");
+      uint8_t* stg = smem + (warp - 2) * 32 * ROWB;
 #pragma unroll 1
       for (int c0 = 0; c0 < OCW; c0 += 32) {
         uint32_t v[32];
         tmem_ld32(t_lane + ch * OCW + c0, v);
         tmem_ld_wait();
-        if (!row_ok) continue;
-        const int col = lh * C::KLH + ch * OCW + c0;
-        if (p.nsplit == 1) {
-          uint4* dst = reinterpret_cast<uint4*>(p.o_lat + grow * KL + col);
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            dst[e] = make_uint4(pack_bf16(__uint_as_float(v[8 * e + 0]) * inv, __uint_as_float(v[8 * e + 1]) * inv),
-                                pack_bf16(__uint_as_float(v[8 * e + 2]) * inv, __uint_as_float(v[8 * e + 3]) * inv),
-                                pack_bf16(__uint_as_float(v[8 * e + 4]) * inv, __uint_as_float(v[8 * e + 5]) * inv),
-                                pack_bf16(__uint_as_float(v[8 * e + 6]) * inv, __uint_as_float(v[8 * e + 7]) * inv));
-        } else {
-          float4* dst = reinterpret_cast<float4*>(p.ws_o + (grow * p.nsplit + split) * KL + col);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            dst[e] = make_float4(__uint_as_float(v[4 * e + 0]) * inv, __uint_as_float(v[4 * e + 1]) * inv,
-                                 __uint_as_float(v[4 * e + 2]) * inv, __uint_as_float(v[4 * e + 3]) * inv);
-        }
+        for (int e = 0; e < 8; ++e)
+          *reinterpret_cast<float4*>(stg + lane * ROWB + (((c0 / 4 + e) ^ (lane & 7)) * 16)) =
+              make_float4(__uint_as_float(v[4 * e + 0]) * inv, __uint_as_float(v[4 * e + 1]) * inv,
+                          __uint_as_float(v[4 * e + 2]) * inv, __uint_as_float(v[4 * e + 3]) * inv);
+      }
+      __syncwarp();
+      const int jl = lane % F4;
+#pragma unroll 4
+      for (int rr = lane / F4; rr < 32; rr += RPI) {
+        const int rs = q * 32 + rr;  // row within the tile
+        if (mt * BMROWS + rs >= p.rows) continue;
+        const float4 x = *reinterpret_cast<const float4*>(stg + rr * ROWB + ((jl ^ (rr & 7)) * 16));
+        const size_t g = (size_t)qrow0 + rs;
+        const int col = lh * C::KLH + ch * OCW + jl * 4;
+        if (p.nsplit == 1)
+          *reinterpret_cast<uint2*>(p.o_lat + g * KL + col) = make_uint2(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w));
+        else
+          *reinterpret_cast<float4*>(p.ws_o + (g * p.nsplit + split) * KL + col) = x;
       }
       if (row_ok && lh == 0 && ch == 0) {
         if (p.nsplit == 1) {

@@ -31,6 +31,15 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start while the previous kernel in the stream is still running:
+// pdl_wait() blocks the calling thread until that kernel has completed and its memory
+// operations are visible (no-op when there is none), so everything before it may touch
+// only shared memory, Tensor Memory and kernel parameters. pdl_trigger() lets the next
+// such kernel start once every CTA of this grid has triggered or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -369,6 +369,8 @@ __global__ void __launch_bounds__(128 * MT) gqa_split_kernel(GqaParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ float s_m[MT][kSlices][16];
   __shared__ float s_l[MT][kSlices][16];
+  pdl_wait();  // queries, cache and lengths may come from the previous kernel in the stream
+  pdl_trigger();
   const int tid = threadIdx.x;
   const int rb = blockIdx.x % p.nrb;
   const int split = blockIdx.x / p.nrb;
@@ -415,6 +417,8 @@ __global__ void __launch_bounds__(128 * MT) gqa_balanced_kernel(GqaParams p) {
   // registers across the (register-bound) segment body
   __shared__ long long s_base, s_pos, s_end, s_w;
   __shared__ int s_seq;
+  pdl_wait();  // queries, cache and lengths may come from the previous kernel in the stream
+  pdl_trigger();
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const int ips = p.hkv * p.nrb;  // work items per sequence
@@ -523,13 +527,21 @@ cudaError_t launch_gqa_dm(const GqaParams& p, int nsplit, int hkv, int b, int ba
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  if (balanced_grid > 0) {
-    gqa_balanced_kernel<D, MT><<<balanced_grid, C::THREADS, C::SMEM, stream>>>(p);
-  } else {
-    dim3 grid(p.nrb * nsplit, hkv, b);
-    gqa_split_kernel<D, MT><<<grid, C::THREADS, C::SMEM, stream>>>(p);
-  }
-  return cudaGetLastError();
+  // programmatic dependent launch: the CTAs may be scheduled while the previous kernel
+  // finishes; they wait for it (pdl_wait) before reading anything
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = balanced_grid > 0 ? dim3(balanced_grid) : dim3(p.nrb * nsplit, hkv, b);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = balanced_grid > 0 ? cudaLaunchKernelEx(&cfg, gqa_balanced_kernel<D, MT>, p)
+                                          : cudaLaunchKernelEx(&cfg, gqa_split_kernel<D, MT>, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
@@ -696,6 +708,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       int rows_per_seq, int nsplit, int chunk,
                                                       __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
   using M = MergeCfg<D>;
+  pdl_wait();  // the partials come from the attention kernel just before
+  pdl_trigger();
   const int row = blockIdx.x * M::ROWS + threadIdx.x / M::TPR;
   if (row >= rows) return;
   const int L = seqlens[row / rows_per_seq];
@@ -717,6 +731,8 @@ __global__ void __launch_bounds__(256) combine_balanced_kernel(const float* __re
                                                                __nv_bfloat16* __restrict__ out,
                                                                float* __restrict__ lse_out) {
   using M = MergeCfg<D>;
+  pdl_wait();  // the partials come from the attention kernel just before
+  pdl_trigger();
   const int row = blockIdx.x * M::ROWS + threadIdx.x / M::TPR;
   if (row >= rows) return;
   const int bi = row / (hq * s);
@@ -739,12 +755,34 @@ static int merge_blocks(int rows) {
   return (rows + MergeCfg<D>::ROWS - 1) / MergeCfg<D>::ROWS;
 }
 
+// The combine kernels are launched as programmatic dependents of the attention kernel
+// before them: their blocks may be scheduled while its last CTAs run and wait in
+// pdl_wait() for its results.
+template <class K, class... A>
+static cudaError_t launch_dependent(K kernel, int blocks, cudaStream_t stream, A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 cudaError_t launch_combine(const float* ws_o, const float* ws_lse, const int32_t* seqlens, int rows,
                            int rows_per_seq, int nsplit, int chunk, int d, void* out, float* lse,
                            cudaStream_t stream) {
   auto* o = static_cast<__nv_bfloat16*>(out);
-#define DECATTN_COMBINE_CASE(D) \
-  case D: combine_kernel<D><<<merge_blocks<D>(rows), 256, 0, stream>>>(ws_o, ws_lse, seqlens, rows, rows_per_seq, nsplit, chunk, o, lse); break;
+#define DECATTN_COMBINE_CASE(D)                                                                              \
+  case D:                                                                                                    \
+    if (cudaError_t e = launch_dependent(combine_kernel<D>, merge_blocks<D>(rows), stream, ws_o, ws_lse, seqlens, \
+                                         rows, rows_per_seq, nsplit, chunk, o, lse))                          \
+      return e;                                                                                              \
+    break;
   switch (d) {
     DECATTN_COMBINE_CASE(64)
     DECATTN_COMBINE_CASE(128)
@@ -764,8 +802,12 @@ cudaError_t launch_combine_balanced(const float* ws_o, const float* ws_lse, cons
   const int rows = b * hq * s;
   auto* o = static_cast<__nv_bfloat16*>(out);
   const int G = hq / hkv;
-#define DECATTN_COMBINE_CASE(D) \
-  case D: combine_balanced_kernel<D><<<merge_blocks<D>(rows), 256, 0, stream>>>(ws_o, ws_lse, meta, seqlens, rows, hq, s, hkv, G, rpb, nrb, o, lse); break;
+#define DECATTN_COMBINE_CASE(D)                                                                              \
+  case D:                                                                                                    \
+    if (cudaError_t e = launch_dependent(combine_balanced_kernel<D>, merge_blocks<D>(rows), stream, ws_o,      \
+                                         ws_lse, meta, seqlens, rows, hq, s, hkv, G, rpb, nrb, o, lse))        \
+      return e;                                                                                              \
+    break;
   switch (d) {
     DECATTN_COMBINE_CASE(64)
     DECATTN_COMBINE_CASE(128)

@@ -200,27 +200,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int mt = blockIdx.x / C::NH;
   const int split = blockIdx.y;
   const int bi = blockIdx.z;
-  const int L = p.seqlens[bi];
   const int kstart = split * p.chunk;
-  if (kstart >= L) {  // chunk past the end: the combine skips it
-    if (L <= 0 && p.nsplit == 1) {  // empty sequence without a combine pass: zero rows, LSE = -inf
-      for (int idx = threadIdx.x; idx < BMROWS * (C::KLH / 8); idx += blockDim.x) {
-        const int r = idx / (C::KLH / 8);
-        if (mt * BMROWS + r >= p.rows) continue;
-        const size_t grow = (size_t)bi * p.rows + mt * BMROWS + r;
-        *reinterpret_cast<uint4*>(p.o_lat + grow * KL + lh * C::KLH + (idx % (C::KLH / 8)) * 8) =
-            make_uint4(0, 0, 0, 0);
-        if (p.lse && lh == 0 && idx % (C::KLH / 8) == 0) p.lse[grow] = -INFINITY;
-      }
-    }
-    return;
-  }
-  const int kend = min(L, kstart + p.chunk);
-  const int ntiles = (kend - kstart + TK - 1) / TK;
   const int qrow0 = bi * p.rows + mt * BMROWS;  // first flattened [b*h*s] query row
-  auto tile_keys = [&](int t) { return min(TK, kend - (kstart + t * TK)); };
-  auto tile_slabs = [&](int t) { return (tile_keys(t) + SLAB - 1) / SLAB; };
-  auto tile_pairs = [&](int t) { return t >= 0 ? (tile_keys(t) + PAIR - 1) / PAIR : 0; };
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars + 0;
@@ -236,6 +217,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   float* red = reinterpret_cast<float*>(smem + C::OFF_RED);  // [parity][column half][row]
   volatile int* okf = reinterpret_cast<volatile int*>(bars + 20);  // [parity][column half][quadrant]
 
+  // Set-up that touches no global memory (it overlaps the end of the previous kernel
+  // when the launch allows it).
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < NR; ++i) {
@@ -273,13 +256,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const bool tmem_ok = *tmem_slot == tmem;
   if (!tmem_ok && threadIdx.x == 0) raise_error(p.err, kErrLaunch);
 
+  // inputs written by earlier kernels (queries, cache, lengths) are read from here on
+  pdl_wait();
+  pdl_trigger();
+  const int L = p.seqlens[bi];
+  const bool active = kstart < L;  // a chunk past the end does nothing (the combine skips it)
+  if (!active && L <= 0 && p.nsplit == 1) {  // empty sequence without a combine pass: zero rows, LSE = -inf
+    for (int idx = threadIdx.x; idx < BMROWS * (C::KLH / 8); idx += blockDim.x) {
+      const int r = idx / (C::KLH / 8);
+      if (mt * BMROWS + r >= p.rows) continue;
+      const size_t grow = (size_t)bi * p.rows + mt * BMROWS + r;
+      *reinterpret_cast<uint4*>(p.o_lat + grow * KL + lh * C::KLH + (idx % (C::KLH / 8)) * 8) =
+          make_uint4(0, 0, 0, 0);
+      if (p.lse && lh == 0 && idx % (C::KLH / 8) == 0) p.lse[grow] = -INFINITY;
+    }
+  }
+  const int kend = min(L, kstart + p.chunk);
+  const int ntiles = active ? (kend - kstart + TK - 1) / TK : 0;
+  auto tile_keys = [&](int t) { return min(TK, kend - (kstart + t * TK)); };
+  auto tile_slabs = [&](int t) { return (tile_keys(t) + SLAB - 1) / SLAB; };
+  auto tile_pairs = [&](int t) { return t >= 0 ? (tile_keys(t) + PAIR - 1) / PAIR : 0; };
+
   auto fail = [&]() {
     raise_error(p.err, kErrWaitTimeout);
     *abort_flag = 1;
   };
 
-  if (!tmem_ok) {
-    // nothing was issued; fall through to the deallocation
+  if (!tmem_ok || !active) {
+    // nothing to issue; fall through to the deallocation
   } else if (warp == 0) {
     // ------------------------------------------------------------ producer: TMA into the ring
     // The whole warp walks the item sequence and computes every coordinate (warp-uniform
@@ -685,9 +689,19 @@ cudaError_t launch_kl(const MlaLaunch& a, cudaStream_t stream) {
   p.wait_ns = a.wait_ns;
   p.test_timeout = a.test_timeout;
   const int mtiles = (p.rows + BMROWS - 1) / BMROWS;
-  dim3 grid(C::NH * mtiles, a.nsplit, a.b);
-  mla_latent_kernel<KL, P><<<grid, NTHREADS, C::SMEM, stream>>>(tqz, tqpe, tz64, tkpe64, tz32, p);
-  return cudaGetLastError();
+  // programmatic dependent launch: the set-up overlaps the previous kernel (see pdl_wait)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C::NH * mtiles, a.nsplit, a.b);
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, mla_latent_kernel<KL, P>, tqz, tqpe, tz64, tkpe64, tz32, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -57,9 +57,8 @@ __global__ void __launch_bounds__(128) proj_kernel(ProjParams p) {
     return p.a + ((size_t)(bi * p.h + j) * p.s + i) * p.kin;
   };
 
-  auto load = [&](int kt, int stage) {
+  auto load_a = [&](int kt, int stage) {
     const uint32_t adst = sbase + stage * STAGE;
-    const uint32_t bdst = adst + A_BYTES;
 #pragma unroll
     for (int n = 0; n < (BM * 8) / 128; ++n) {
       const int idx = tid + n * 128;
@@ -69,6 +68,9 @@ __global__ void __launch_bounds__(128) proj_kernel(ProjParams p) {
       const __nv_bfloat16* src = ok ? a_row_ptr(m) + kt * BK + c * 8 : p.a;
       cp_async_16(adst + r * 128 + swz(r, c) * 16, src, ok ? 16u : 0u);
     }
+  };
+  auto load_w = [&](int kt, int stage) {
+    const uint32_t bdst = sbase + stage * STAGE + A_BYTES;
     const __nv_bfloat16* wbase = p.w + (size_t)j * p.kin * p.nout;
 #pragma unroll
     for (int n = 0; n < (BK * (BN / 8)) / 128; ++n) {
@@ -87,15 +89,26 @@ __global__ void __launch_bounds__(128) proj_kernel(ProjParams p) {
 #pragma unroll
     for (int ni = 0; ni < NTW; ++ni) acc[mi][ni][0] = acc[mi][ni][1] = acc[mi][ni][2] = acc[mi][ni][3] = 0.f;
 
+  // The weight does not come from the previous kernel in the stream: its first stages
+  // are requested before pdl_wait, so they load while that kernel finishes. (They join
+  // the first commit group, whose completion is awaited before stage 0 is used.)
+#pragma unroll
+  for (int t = 0; t < NST - 1; ++t)
+    if (t < kiters) load_w(t, t);
+  pdl_wait();  // the activations (and lengths) are the previous kernel's results
+  pdl_trigger();
 #pragma unroll
   for (int t = 0; t < NST - 1; ++t) {
-    if (t < kiters) load(t, t);
+    if (t < kiters) load_a(t, t);
     cp_async_commit();
   }
   for (int kt = 0; kt < kiters; ++kt) {
     cp_async_wait<NST - 2>();
     __syncthreads();
-    if (kt + NST - 1 < kiters) load(kt + NST - 1, (kt + NST - 1) % NST);
+    if (kt + NST - 1 < kiters) {
+      load_a(kt + NST - 1, (kt + NST - 1) % NST);
+      load_w(kt + NST - 1, (kt + NST - 1) % NST);
+    }
     cp_async_commit();
     const uint32_t abase = sbase + (kt % NST) * STAGE;
     const uint32_t bbase = abase + A_BYTES;
@@ -150,9 +163,19 @@ cudaError_t launch_tile(const ProjParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  dim3 grid((p.nout + BN - 1) / BN, (p.M + BM - 1) / BM, p.h);
-  proj_kernel<BM, BN, NST><<<grid, 128, SMEM, stream>>>(p);
-  return cudaGetLastError();
+  // programmatic dependent launch: the weight prefetch overlaps the previous kernel
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((p.nout + BN - 1) / BN, (p.M + BM - 1) / BM, p.h);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, proj_kernel<BM, BN, NST>, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
@@ -178,6 +201,7 @@ cudaError_t launch_proj(const ProjLaunch& a, int num_sms, cudaStream_t stream) {
   const int kiters = (a.kin + BK - 1) / BK;
   if (p.M <= 32) {
     if (a.nout >= 256 && kiters <= 2) return launch_tile<32, 256, 2>(p, stream);
+    if (kiters <= 8) return launch_tile<32, 64, 8>(p, stream);  // every k-stage in flight (96 KB)
     return launch_tile<32, 64, 4>(p, stream);
   }
   if (a.nout >= 128) return launch_tile<64, 128, 3>(p, stream);

@@ -37,6 +37,14 @@
  *   launched. Device-side faults detected by the kernels (a bounded wait that
  *   ran out, a page index outside the pool) are recorded in a device error
  *   word and reported by decattn_check_errors().
+ *   Launch: every kernel is launched as a programmatic dependent of the
+ *   kernel before it on the stream (CUDA programmatic dependent launch): its
+ *   CTAs may start while that kernel finishes, and wait for its completion
+ *   and memory before reading any argument tensor. The one exception is the
+ *   weight of mla_absorb_q / mla_out_proj (w_uk / w_uv), whose first tiles
+ *   are requested before that wait: the weight must not be written by the
+ *   kernel launched immediately before on the same stream (writes by earlier
+ *   kernels, copies or other streams ordered by events are fine).
  */
 #ifndef DECATTN_H
 #define DECATTN_H
@@ -121,7 +129,8 @@ int mla_absorb_q(const decattn_bf16* q_nope, const decattn_bf16* w_uk, decattn_b
  *   o_lat [b, h, s, k] bf16; lse [b, h, s] float or NULL.
  *   Compiled instances (k, p): (512, 64) and (64, 16). Pointers 16-byte
  *   aligned. Tensor-core (tcgen05) kernel with TMA tile loads, split over
- *   the context and merged by a second kernel.
+ *   the context (a chunk count planned from b, s, h and max_seqlen) and
+ *   merged by a second kernel.
  */
 size_t mla_decode_workspace_size(int b, int s, int h, int k, int max_seqlen);
 int mla_decode(const decattn_bf16* qz, const decattn_bf16* q_pe, const decattn_bf16* z, const decattn_bf16* k_pe,

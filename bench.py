@@ -14,8 +14,9 @@ Printed: one JSON line (rank 0). `value` is microseconds per pipeline call of
 the whole job (the timed time divided by the calls all ranks made), so lower
 is better. `roofline` is for the latent-attention call (kernel + combine),
 timed in its own loop of graph replays with CUDA events on its stream.
-`e2e` times the public Python API with the step's queries copied in from
-pinned host memory and the outputs copied back. `cpu_baseline` times the
+`e2e` times the public Python API with every step's queries and lengths copied
+in from pinned host memory and its outputs copied back, the copies on their own
+streams overlapping the neighbouring steps' compute. `cpu_baseline` times the
 fp64 oracle on a bounded sample on the host cores.
 
 --impl reference runs that oracle as the reference arm (rank 0 only).
@@ -293,15 +294,16 @@ def main():
 
     stream = torch.cuda.Stream(device=dev)
 
-    def step(r, parts=("absorb", "decode", "proj")):
+    def step(r, parts=("absorb", "decode", "proj"), seq=None):
         s_, o = sets[r], outs[r]
+        sl_ = sl if seq is None else seq
         if "absorb" in parts:
-            da.mla_absorb_q(s_.q_nope, s_.w_uk, sl, out=o["qz"], stream=stream)
+            da.mla_absorb_q(s_.q_nope, s_.w_uk, sl_, out=o["qz"], stream=stream)
         if "decode" in parts:
-            da.mla_decode(o["qz"], s_.q_pe, s_.z, s_.k_pe, sl, scale=scale, max_seqlen=L, out=o["o_lat"],
+            da.mla_decode(o["qz"], s_.q_pe, s_.z, s_.k_pe, sl_, scale=scale, max_seqlen=L, out=o["o_lat"],
                           lse=o["lse"], workspace=ws, stream=stream)
         if "proj" in parts:
-            da.mla_out_proj(o["o_lat"], s_.w_uv, sl, out=o["out"], stream=stream)
+            da.mla_out_proj(o["o_lat"], s_.w_uv, sl_, out=o["out"], stream=stream)
 
     # warm (first-call set-up happens outside capture), then capture one graph per input set
     with torch.cuda.stream(stream):
@@ -356,35 +358,69 @@ def main():
     ms_per_step = total_ms / args.steps
     value = total_ms * 1e3 / (args.steps * world)  # us per call over the whole job
 
-    # end to end through the public API: queries in from pinned host memory, outputs back
+    # end to end through the public API: every step copies its queries and lengths in from
+    # pinned host memory and its outputs (out, LSE) back. The copies run on their own streams,
+    # ordered by events, so step k+1's inputs upload while step k computes and step k's
+    # outputs download while step k+1 computes, as a serving loop overlaps them; each
+    # input set's buffers are reused only after the step that last used them is done.
     e2e_steps = min(args.steps, 300)
+    h2d_stream = torch.cuda.Stream(device=dev)  # uploads and downloads on their own streams:
+    d2h_stream = torch.cuda.Stream(device=dev)  # the two directions use separate copy engines
     hq_nope = [s_.q_nope.cpu().pin_memory() for s_ in sets]
     hq_pe = [s_.q_pe.cpu().pin_memory() for s_ in sets]
     hsl = torch.tensor(seqlens, dtype=torch.int32).pin_memory()
-    hout = torch.empty((wl.b, wl.heads, wl.s, wl.d), dtype=torch.bfloat16).pin_memory()
-    hlse = torch.empty((wl.b, wl.heads, wl.s), dtype=torch.float32).pin_memory()
+    sls = [torch.empty_like(sl) for _ in range(NBUF)]
+    hout = [torch.empty((wl.b, wl.heads, wl.s, wl.d), dtype=torch.bfloat16).pin_memory() for _ in range(NBUF)]
+    hlse = [torch.empty((wl.b, wl.heads, wl.s), dtype=torch.float32).pin_memory() for _ in range(NBUF)]
+    ev_in = [torch.cuda.Event() for _ in range(NBUF)]
+    ev_done = [torch.cuda.Event() for _ in range(NBUF)]
+    ev_out = [torch.cuda.Event() for _ in range(NBUF)]
+    used = [False] * NBUF
 
-    def e2e_step(r):
-        s_, o = sets[r], outs[r]
-        s_.q_nope.copy_(hq_nope[r], non_blocking=True)
-        s_.q_pe.copy_(hq_pe[r], non_blocking=True)
-        sl.copy_(hsl, non_blocking=True)
-        step(r)
-        hout.copy_(o["out"], non_blocking=True)
-        hlse.copy_(o["lse"], non_blocking=True)
+    def upload(k):
+        r = k % NBUF
+        if used[r]:
+            h2d_stream.wait_event(ev_done[r])  # the step that last read set r has finished
+        with torch.cuda.stream(h2d_stream):
+            sets[r].q_nope.copy_(hq_nope[r], non_blocking=True)
+            sets[r].q_pe.copy_(hq_pe[r], non_blocking=True)
+            sls[r].copy_(hsl, non_blocking=True)
+        ev_in[r].record(h2d_stream)
 
-    with torch.cuda.stream(stream):
-        for k in range(5):
-            e2e_step(k % NBUF)
+    def compute(k):
+        r = k % NBUF
+        stream.wait_event(ev_in[r])
+        if used[r]:
+            stream.wait_event(ev_out[r])  # set r's outputs of the earlier step are downloaded
+        with torch.cuda.stream(stream):
+            step(r, seq=sls[r])
+        ev_done[r].record(stream)
+        used[r] = True
+
+    def download(k):
+        r = k % NBUF
+        d2h_stream.wait_event(ev_done[r])
+        with torch.cuda.stream(d2h_stream):
+            hout[r].copy_(outs[r]["out"], non_blocking=True)
+            hlse[r].copy_(outs[r]["lse"], non_blocking=True)
+        ev_out[r].record(d2h_stream)
+
+    def e2e_run(n):
+        upload(0)
+        for k in range(n):
+            compute(k)
+            if k + 1 < n:
+                upload(k + 1)
+            download(k)
+
+    e2e_run(5)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for k in range(e2e_steps):
-            e2e_step(k % NBUF)
-        e1.record(stream)
+    e0.record(h2d_stream)  # the first upload is the first timed operation
+    e2e_run(e2e_steps)
+    e1.record(d2h_stream)  # after the last download
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     if world > 1:
@@ -392,7 +428,7 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
     h2d = sum(t.numel() * t.element_size() for t in (hq_nope[0], hq_pe[0], hsl))
-    d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
+    d2h = hout[0].numel() * hout[0].element_size() + hlse[0].numel() * hlse[0].element_size()
 
     f_core, b_core, f_proj, b_proj = cost_numbers(wl)
     hbm, tfl, tfl_sus, peak_src = peaks()
@@ -428,7 +464,9 @@ def main():
                      "peak_source": peak_src,
                      "note": "frac of measured peak; the call's roofline time is max(FLOPs/tensor peak, bytes/HBM peak)"},
         "e2e": {"value": e2e_ms * 1e3 / (e2e_steps * world), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "copies": "every step's inputs in and outputs out, on upload / download streams overlapping "
+                          "the neighbouring steps' compute (event-ordered, three input/output sets)"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }

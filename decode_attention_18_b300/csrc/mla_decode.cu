@@ -48,8 +48,13 @@
 //   * Every mbarrier wait is bounded; on time-out the CTA records the error,
 //     stops issuing work, waits for its own copies and MMAs, frees TMEM and
 //     returns.
+//   * Launched as a programmatic dependent of the previous kernel on the
+//     stream: barrier set-up, TMEM allocation and tensor-map prefetch run
+//     before griddepcontrol.wait, every global read after it.
 // Output: with a single chunk, bf16 O_lat and the LSE directly; otherwise fp32
-// partials (O / l, LSE) merged by the combine kernel.
+// partials (O / l, LSE) merged by the combine kernel. Either way O / l is
+// staged in shared memory (free once the last MMA has completed) and stored as
+// whole row segments.
 #include <cuda.h>
 
 #include "common.cuh"

@@ -524,16 +524,28 @@ def extras(dev, stream, hbm, tfl):
 
     res = {}
 
-    def time_calls(fn, n=30, w=5):
+    def time_calls(fns, n=100, w=6):
+        """Seconds per call: one CUDA graph per input set (captured after an eager
+        warm-up call), replayed round-robin, CUDA events on the stream."""
         with torch.cuda.stream(stream):
-            for _ in range(w):
-                fn()
+            for f in fns:
+                f()
+        torch.cuda.synchronize()
+        graphs = []
+        for f in fns:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                f()
+            graphs.append(g)
+        with torch.cuda.stream(stream):
+            for i in range(w):
+                graphs[i % len(graphs)].replay()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             e0.record(stream)
-            for _ in range(n):
-                fn()
+            for i in range(n):
+                graphs[i % len(graphs)].replay()
             e1.record(stream)
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / n * 1e-3
@@ -551,21 +563,20 @@ def extras(dev, stream, hbm, tfl):
         lses = [torch.empty(q.shape[:3], dtype=torch.float32, device=dev) for q, _ in qs]
         wsb = da.ops.load().gqa_decode_workspace_size(wl.b, wl.s, wl.heads, wl.hkv, wl.d, max(seqlens))
         ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
-        it = [0]
+        def call(r):
+            def f():
+                q, c = qs[r]
+                da.gqa_decode(q, c.k, c.v, sl, max_seqlen=max(seqlens),
+                              block_table=c.block_table if wl.paged else None, out=outs[r], lse=lses[r],
+                              workspace=ws, stream=stream)
+            return f
 
-        def fn():
-            r = it[0] % nb
-            it[0] += 1
-            q, c = qs[r]
-            da.gqa_decode(q, c.k, c.v, sl, max_seqlen=max(seqlens), block_table=c.block_table if wl.paged else None,
-                          out=outs[r], lse=lses[r], workspace=ws, stream=stream)
-
-        t = time_calls(fn)
+        t = time_calls([call(r) for r in range(nb)])
         by = cost.gqa_bytes_exact(wl.heads, wl.hkv, wl.d, seqlens, wl.s)
         fl = cost.gqa_flops_exact(wl.heads, wl.d, seqlens, wl.s)
         res[name] = {"us": t * 1e6, "hbm_gbs": by / t / 1e9, "frac_hbm": by / t / 1e9 / hbm,
                      "tflops": fl / t / 1e12, "bytes": by, "num_splits": da.last_num_splits(),
-                     "l2": f"{nb} rotating caches of {by / 1e6:.0f} MB"}
+                     "l2": f"{nb} rotating caches of {by / 1e6:.0f} MB", "timing": "CUDA graph replays"}
         del qs, outs, lses, ws
         torch.cuda.empty_cache()
 
@@ -580,15 +591,13 @@ def extras(dev, stream, hbm, tfl):
         lse = [torch.empty(q.shape[:3], dtype=torch.float32, device=dev) for q in qzs]
         wsb = da.ops.load().mla_decode_workspace_size(wl.b, wl.s, wl.heads, wl.k, max(seqlens))
         ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
-        it = [0]
+        def call(r):
+            def f():
+                da.mla_decode(qzs[r], inp[r].q_pe, inp[r].z, inp[r].k_pe, sl, scale=inp[r].scale,
+                              max_seqlen=max(seqlens), out=o[r], lse=lse[r], workspace=ws, stream=stream)
+            return f
 
-        def fn():
-            r = it[0] % 2
-            it[0] += 1
-            da.mla_decode(qzs[r], inp[r].q_pe, inp[r].z, inp[r].k_pe, sl, scale=inp[r].scale,
-                          max_seqlen=max(seqlens), out=o[r], lse=lse[r], workspace=ws, stream=stream)
-
-        t = time_calls(fn, n=20)
+        t = time_calls([call(r) for r in range(2)], n=60 if s <= 4 else 20)
         fl = cost.mla_flops_exact(wl.heads, wl.k, wl.p, seqlens, wl.s)
         by = cost.mla_bytes_exact(wl.heads, wl.k, wl.p, seqlens, wl.s)
         troof = max(fl / (tfl * 1e12), by / (hbm * 1e9))

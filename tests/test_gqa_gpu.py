@@ -271,3 +271,23 @@ def test_tensor_core_path_split_invariance(nsplit, gqa_kernel):
     assert np.sqrt(np.mean((a - b2) ** 2)) / np.sqrt(np.mean(a ** 2)) <= 1e-2
     assert np.abs(f64(lse) - f64(lse2)).max() <= 1e-4
     check_all(q, cache, out2, lse2, seqlens, 256, f"tc nsplit {nsplit}")
+
+
+def test_multi_wave_split_grid_then_combine():
+    # 24 sequences x 8 KV heads x 7 chunks = 1344 CTAs (several waves), each launched as
+    # a programmatic dependent, then the combine over all their partials
+    import decode_attention_18_b300 as da
+    from decode_attention_18_b300 import workloads as W
+
+    seqlens = [3000 - 97 * i for i in range(24)]
+    q, cache = W.make_gqa(24, 64, 8, 128, 1, seqlens, paged=True, seed=12, device=DEV)
+    sl = torch.tensor(seqlens, dtype=torch.int32, device=DEV)
+    da.set_forced_splits(7)
+    try:
+        out, lse = da.gqa_decode(q, cache.k, cache.v, sl, max_seqlen=max(seqlens), block_table=cache.block_table)
+        torch.cuda.synchronize()
+        assert da.last_num_splits() == 7
+    finally:
+        da.set_forced_splits(0)
+    assert da.check_errors() == 0
+    check_sampled(q, cache, out, lse, seqlens, 128, seqs=[0, 11, 23], kv_heads=[0, 5, 7])

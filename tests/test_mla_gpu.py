@@ -204,3 +204,28 @@ def test_full_size_mtp_s8_sampled():
     wl = W.WORKLOADS["mla_mtp_s8"]
     inp = make(wl.b, wl.heads, wl.d, wl.k, wl.p, wl.s, wl.seqlens(), seed=wl.seed)
     check(inp, forward(inp), seqs=[0, 31], what="mtp s8")
+
+
+def test_multi_wave_split_grid_then_combine():
+    # 64 sequences x 2 column halves x 3 chunks = 384 latent CTAs (more than two waves of
+    # one CTA per SM), each launched as a programmatic dependent, then the combine: the
+    # combine may only start once every latent CTA has started, and must see all partials
+    import decode_attention_18_b300 as da
+
+    seqlens = [1500 - 7 * i for i in range(64)]
+    inp = make(64, 128, 128, 512, 64, 1, seqlens, seed=11)
+    sl = torch.tensor(seqlens, dtype=torch.int32, device=DEV)
+    qz = da.mla_absorb_q(inp.q_nope, inp.w_uk, sl)
+    da.set_forced_splits(3)
+    try:
+        o, lse = da.mla_decode(qz, inp.q_pe, inp.z, inp.k_pe, sl, scale=inp.scale, max_seqlen=max(seqlens))
+        torch.cuda.synchronize()
+        assert da.last_num_splits() == 3
+    finally:
+        da.set_forced_splits(0)
+    assert da.check_errors() == 0
+    seqs = [0, 21, 42, 63]
+    zs, kp = seq_inputs(inp, seqs)
+    ro, rl = A.mla_latent_ref(f64(qz[seqs]), f64(inp.q_pe[seqs]), zs, kp, [seqlens[i] for i in seqs], inp.scale)
+    assert_out_close(f64(o[seqs]), ro, "multi-wave latent")
+    assert_lse_close(f64(lse[seqs]), rl, "multi-wave lse")

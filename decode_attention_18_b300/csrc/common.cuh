@@ -7,6 +7,7 @@
 // allocation, MMA, commit, loads and stores) for the latent MLA kernel.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -29,6 +30,22 @@ __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+// Raises a kernel's dynamic shared-memory limit on the current device, once per device:
+// the attribute belongs to the device's context, so a process that uses the library on
+// several GPUs sets it on each. `done` holds one bit per device (devices 64 and up set
+// it on every call; the call is idempotent, so a race between threads only repeats it).
+template <class Kernel>
+inline cudaError_t ensure_smem_limit(Kernel kernel, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
 }
 
 // Programmatic dependent launch. A kernel launched with programmatic stream

@@ -518,15 +518,9 @@ __global__ void __launch_bounds__(128 * MT) gqa_balanced_kernel(GqaParams p) {
 template <int D, int MT>
 cudaError_t launch_gqa_dm(const GqaParams& p, int nsplit, int hkv, int b, int balanced_grid, cudaStream_t stream) {
   using C = GqaCfg<D, MT>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e =
-        cudaFuncSetAttribute(gqa_split_kernel<D, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gqa_balanced_kernel<D, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> split_attr{0}, balanced_attr{0};
+  if (cudaError_t e = ensure_smem_limit(gqa_split_kernel<D, MT>, C::SMEM, split_attr)) return e;
+  if (cudaError_t e = ensure_smem_limit(gqa_balanced_kernel<D, MT>, C::SMEM, balanced_attr)) return e;
   // programmatic dependent launch: the CTAs may be scheduled while the previous kernel
   // finishes; they wait for it (pdl_wait) before reading anything
   cudaLaunchConfig_t cfg = {};
@@ -555,19 +549,19 @@ int gqa_rows_per_cta(int rows) { return 16 * gqa_mt(rows); }
 template <int D, int MT>
 static int balanced_occupancy() {
   using C = GqaCfg<D, MT>;
-  static int cached = 0;
-  if (cached == 0) {
-    int n = 0;
-    if (cudaFuncSetAttribute(gqa_balanced_kernel<D, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) ==
-            cudaSuccess &&
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_balanced_kernel<D, MT>, C::THREADS, C::SMEM) ==
-            cudaSuccess &&
-        n > 0)
-      cached = n;
-    else
+  // (the same GPU model on every device of a process is assumed for the cached value)
+  static std::atomic<int> cached{0};
+  static std::atomic<unsigned long long> attr{0};
+  int n = cached.load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (ensure_smem_limit(gqa_balanced_kernel<D, MT>, C::SMEM, attr) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_balanced_kernel<D, MT>, C::THREADS, C::SMEM) !=
+            cudaSuccess ||
+        n <= 0)
       return 1;
+    cached.store(n, std::memory_order_relaxed);
   }
-  return cached;
+  return n;
 }
 
 int gqa_balanced_ctas_per_sm(int d, int rows) {

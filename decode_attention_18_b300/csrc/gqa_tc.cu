@@ -526,12 +526,8 @@ bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, 
 template <int D>
 cudaError_t launch_tc(const GqaLaunch& a, cudaStream_t stream) {
   using C = TcCfg<D>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(gqa_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> smem_limit_set{0};
+  if (cudaError_t e = ensure_smem_limit(gqa_tc_kernel<D>, C::SMEM, smem_limit_set)) return e;
   const uint64_t tokens = a.paged ? (uint64_t)a.num_pages * TKY : (uint64_t)a.b * a.capacity;
   CUtensorMap tq, tk, tv;
   {

@@ -659,12 +659,8 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 template <int KL, int P>
 cudaError_t launch_kl(const MlaLaunch& a, cudaStream_t stream) {
   using C = MlaCfg<KL, P>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(mla_latent_kernel<KL, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> smem_limit_set{0};
+  if (cudaError_t e = ensure_smem_limit(mla_latent_kernel<KL, P>, C::SMEM, smem_limit_set)) return e;
   const uint64_t qrows = (uint64_t)a.b * a.h * a.s;
   const uint64_t krows = a.paged ? (uint64_t)a.num_pages * 64 : (uint64_t)a.b * a.capacity;
   CUtensorMap tqz, tqpe, tz64, tkpe64, tz32;

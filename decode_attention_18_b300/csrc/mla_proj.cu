@@ -157,12 +157,8 @@ __global__ void __launch_bounds__(128) proj_kernel(ProjParams p) {
 template <int BM, int BN, int NST>
 cudaError_t launch_tile(const ProjParams& p, cudaStream_t stream) {
   constexpr int SMEM = NST * (BM * BK * 2 + BK * BN * 2);
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(proj_kernel<BM, BN, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> smem_limit_set{0};
+  if (cudaError_t e = ensure_smem_limit(proj_kernel<BM, BN, NST>, SMEM, smem_limit_set)) return e;
   // programmatic dependent launch: the weight prefetch overlaps the previous kernel
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((p.nout + BN - 1) / BN, (p.M + BM - 1) / BM, p.h);

@@ -118,7 +118,7 @@ struct MlaCfg {
   static constexpr int OFF_BAR = align1024(OFF_RED + 2 * 2 * BMROWS * 4);
   // + barriers. No alignment slack: the dynamic window follows the CTA's 1 KB reserved
   // shared memory and is 1024-byte aligned; the kernel checks this and refuses otherwise.
-  static constexpr int SMEM = OFF_BAR + 256;
+  static constexpr int SMEM = OFF_BAR + 512;
   static constexpr int TM_S = KLH;                   // two S buffers after the O accumulator
   static constexpr int TM_COLS = pow2_cols(KLH + 2 * TK);
   static_assert(KL % 64 == 0 && KLH % 64 == 0 && KLH <= 256, "latent width");
@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int qrow0 = bi * p.rows + mt * BMROWS;  // first flattened [b*h*s] query row
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* q_full = bars + 0;
+  uint64_t* q_box = bars + 32;     // [NCH] box j of the query tile Q' landed
   uint64_t* r_full = bars + 1;     // [NR] ring item landed
   uint64_t* r_empty = bars + 6;    // [NR] ring item consumed by its MMAs
   uint64_t* s_ready = bars + 11;   // [2]  S tile in TMEM (and the previous tile's O MMAs complete)
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // Set-up that touches no global memory (it overlaps the end of the previous kernel
   // when the launch allows it).
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    for (int j = 0; j < C::NCH; ++j) mbar_init(&q_box[j], 1);
     for (int i = 0; i < NR; ++i) {
       mbar_init(&r_full[i], 1);
       mbar_init(&r_empty[i], 1);
@@ -297,12 +297,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const bool leader = elect_one();
     int last[NR];
     for (int i = 0; i < NR; ++i) last[i] = -1;
-    if (leader) {
-      mbar_expect_tx(q_full, C::Q_LAT + C::Q_PE);
-      for (int k = 0; k < C::NBL; ++k) tma_load_2d(sb + k * C::Q_BOX, &tm_qz, k * 64, qrow0, q_full);
-      tma_load_2d(sb + C::OFF_QPE, &tm_qpe, 0, qrow0, q_full);
-    }
-    __syncwarp();
+    // Q' box j is requested just before the first tile's chunk j (each on its own barrier),
+    // so the first S MMAs start as soon as their two boxes have landed instead of after the
+    // whole 144 KB query tile.
+    int qb_issued = 0;
     int ic = 0;  // ring items issued
     RingPos rp;
     auto acquire = [&](int& slot) -> bool {
@@ -315,6 +313,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       return true;
     };
     auto chunk = [&](int u, int j) -> bool {
+      if (u == 0) {
+        if (leader) {
+          if (j == C::NBL) {
+            mbar_expect_tx(&q_box[j], C::Q_PE);
+            tma_load_2d(sb + C::OFF_QPE, &tm_qpe, 0, qrow0, &q_box[j]);
+          } else {
+            mbar_expect_tx(&q_box[j], C::Q_BOX);
+            tma_load_2d(sb + j * C::Q_BOX, &tm_qz, j * 64, qrow0, &q_box[j]);
+          }
+        }
+        __syncwarp();
+        qb_issued = j + 1;
+      }
       int slot;
       if (!acquire(slot)) return false;
       const int key0 = kstart + u * TK;
@@ -356,7 +367,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (lane == 0) {
       if (!ok && !*abort_flag) fail();
       // no copy may still be landing in shared memory when the CTA exits
-      mbar_wait(q_full, 0, kTeardownNs, nullptr);
+      for (int j = 0; j < qb_issued; ++j) mbar_wait(&q_box[j], 0, kTeardownNs, nullptr);
       for (int i = 0; i < NR; ++i)
         if (last[i] >= 0) mbar_wait(&r_full[i], (last[i] / NR) & 1, kTeardownNs, nullptr);
     }
@@ -365,8 +376,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ------------------------------------------------------------ MMA issuer (one elected lane issues; the warp zeroes tails)
     bool ok = true;
     if (p.test_timeout) ok = warp_wait(test_bar, 0, kTestWaitNs, abort_flag);
-    if (ok) ok = warp_wait(q_full, 0, p.wait_ns, abort_flag);
-    tc_fence_after();
     const bool leader = elect_one();
     constexpr uint32_t idS = idesc_bf16_f32(BMROWS, TK, false, false);
     constexpr uint32_t idO = idesc_bf16_f32(BMROWS, C::KLH, false, true);
@@ -387,6 +396,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       return warp_wait_fast(&r_full[slot], ph, p.wait_ns, abort_flag);
     };
     auto chunk = [&](int u, int j) -> bool {
+      if (u == 0 && !warp_wait(&q_box[j], 0, p.wait_ns, abort_flag)) return false;  // Q' box j (TMA)
       int slot;
       if (!take(slot)) return false;
       const uint32_t d_s = tmem + C::TM_S + (u & 1) * TK;

@@ -20,6 +20,9 @@
 //    slices of an m-tile are merged through shared memory at the end.
 //  * Output: with one chunk, bf16 rows and the LSE directly; otherwise fp32
 //    (O, LSE) partials for the combine kernel.
+//  * Every kernel here is launched as a programmatic dependent of the kernel
+//    before it on the stream and waits for it (griddepcontrol.wait) before its
+//    first global read, so launch and block scheduling overlap that kernel's end.
 #include "common.cuh"
 #include "internal.h"
 

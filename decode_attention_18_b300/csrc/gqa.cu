@@ -10,8 +10,10 @@
 // tokens (row = head_in_group * s + token), so every K/V byte fetched from HBM
 // serves all G*s rows: the kernel is bound by the cache read (AI ~ G).
 //
-//  * K/V tiles of 64 keys stream through a 3-4 stage cp.async pipeline with
-//    16-byte (128-bit) coalesced loads into XOR-swizzled shared memory.
+//  * K/V tiles of 64 keys stream through a 3-4 stage pipeline of TMA copies:
+//    one thread requests each tile of K and of V as [64 tokens x 64 dims] boxes
+//    of a 3-D tensor map (tokens, KV heads, d), landing 128-byte swizzled in
+//    shared memory and completing on the stage's mbarrier.
 //  * 4 warps per 16-row m-tile (MT m-tiles, 128*MT threads); each warp owns 16
 //    keys of a tile: S = Q K^T and O += P V run on mma.sync m16n8k16 (bf16 in,
 //    fp32 accumulate); the score fragment is reused in registers as the A
@@ -45,6 +47,7 @@ struct GqaParams {
   float* ws_lse;
   int* meta;  // balanced mode: per work item {first partial record, record count}
   unsigned* err;
+  unsigned long long wait_ns;  // limit of the tile waits
 };
 
 constexpr int kTileKeys = 64;
@@ -65,12 +68,16 @@ struct GqaCfg {
   static constexpr int OSTR = D + 2;  // padded fp32 row stride of the merge buffer
   static constexpr int RED_BYTES = kSlices * 16 * MT * OSTR * 4;
   static constexpr int SMEM = PIPE_BYTES > RED_BYTES ? PIPE_BYTES : RED_BYTES;
-  static constexpr int CHUNKS = D / 8;  // 16-byte chunks per row
-  static constexpr int LOADS = kTileKeys * CHUNKS / THREADS;
-  static_assert(kTileKeys * CHUNKS % THREADS == 0, "tile load split");
+  static constexpr int BLK = kTileKeys * 128;  // one [64 keys x 64 dims] block of a tile
+  static_assert(D % 64 == 0, "tiles are 64-dim blocks");
 };
 
-__device__ __forceinline__ uint32_t swz(int row, int chunk) { return (uint32_t)(chunk ^ (row & 7)); }
+// Shared-memory offset of 16-byte chunk c (8 dims) of key row r in a K or V tile: the
+// tile is D/64 blocks of [64 keys x 128 bytes], each with the 128-byte swizzle (chunk
+// index XOR row mod 8) that TMA writes and that keeps ldmatrix free of bank conflicts.
+__device__ __forceinline__ uint32_t tile_off(int r, int c) {
+  return (uint32_t)((c >> 3) * (kTileKeys * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
 
 // Where a segment's result goes.
 enum SegOut { kSegFinal = 0, kSegSplit = 1, kSegRecord = 2 };
@@ -82,9 +89,10 @@ enum SegOut { kSegFinal = 0, kSegSplit = 1, kSegRecord = 2 };
 // balanced schedule. The caller's threads all enter; shared memory is free again
 // when it returns.
 template <int D, int MT>
-__device__ __forceinline__ void gqa_segment(const GqaParams& p, uint8_t* smem, float (*s_m)[kSlices][16],
-                                            float (*s_l)[kSlices][16], int bi, int g, int rb, int L, int kstart,
-                                            int kend, int out_mode, int slot) {
+__device__ __forceinline__ void gqa_segment(const GqaParams& p, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                            uint64_t* full, uint32_t& phase, uint8_t* smem,
+                                            float (*s_m)[kSlices][16], float (*s_l)[kSlices][16], int bi, int g,
+                                            int rb, int L, int kstart, int kend, int out_mode, int slot) {
   using C = GqaCfg<D, MT>;
   constexpr int NT = D / 8;   // n-tiles of the output
   constexpr int KS = D / 16;  // k-steps of QK^T
@@ -120,52 +128,36 @@ __device__ __forceinline__ void gqa_segment(const GqaParams& p, uint8_t* smem, f
     }
   }
 
-  // ---- K/V tile loader (all threads; zero-fill past the chunk end). For a paged cache
-  // the tile's page index comes from page_of(); it is fetched one iteration ahead so that
-  // the block-table read never sits in front of the copies.
+  // ---- K/V tiles by TMA. Thread 0 requests tile t of this KV head's K and V as D/64
+  // boxes of [64 tokens x 64 dims] each (3-D tensor maps over [tokens, KV heads, d]),
+  // completing on the stage's mbarrier; every thread waits on it (bounded). For a paged
+  // cache the tile is one page. Rows past the segment's end are read as they are (or as
+  // zeros past the tensor) and made harmless below.
   const uint32_t sbase = smem_u32(smem);
+  // block-table entry of tile t (read one tile ahead of its copy by thread 0)
   auto page_of = [&](int t) -> int {
-    const int key0 = kstart + t * kTileKeys;
     if (!p.paged || t >= ntiles) return 0;
-    return __ldg(p.block_table + (size_t)bi * p.max_pages + key0 / kTileKeys);
+    return __ldg(p.block_table + (size_t)bi * p.max_pages + (kstart + t * kTileKeys) / kTileKeys);
   };
-  // this thread's 16-byte chunks of a tile: row, shared-memory offset, element offset in the cache
-  // (the element offset fits 32 bits: row < 64, hkv <= 65535, d <= 256)
-  uint32_t ld_soff[C::LOADS];
-  uint32_t ld_goff[C::LOADS];
-#pragma unroll
-  for (int n = 0; n < C::LOADS; ++n) {
-    const int idx = tid + n * C::THREADS;
-    const int kr = idx / C::CHUNKS;
-    const int c = idx % C::CHUNKS;
-    ld_soff[n] = kr * C::ROW_BYTES + swz(kr, c) * 16;
-    ld_goff[n] = (uint32_t)(kr * p.hkv * D + c * 8);
-  }
-  auto load_tile = [&](int t, int stage, int page) {
+  auto issue = [&](int t, int stage, int page) {
     const int key0 = kstart + t * kTileKeys;
-    long long rowbase;  // cache-tensor row of the tile's first token
-    bool page_ok = true;
+    int row0;  // token row of the tile's first key in the cache tensor
     if (p.paged) {
       if (page < 0 || page >= p.num_pages) {
-        page_ok = false;
-        if (tid == 0) raise_error(p.err, kErrBadPage);
+        raise_error(p.err, kErrBadPage);
+        page = 0;  // stay inside the pool; the result is flagged invalid
       }
-      rowbase = (long long)page * kTileKeys;
+      row0 = page * kTileKeys;
     } else {
-      rowbase = (long long)bi * p.capacity + key0;
+      row0 = bi * p.capacity + key0;
     }
     const uint32_t kdst = sbase + stage * C::STAGE_BYTES;
-    const uint32_t vdst = kdst + C::TILE_BYTES;
-    const __nv_bfloat16* kt = p.k + ((size_t)rowbase * p.hkv + g) * D;
-    const __nv_bfloat16* vt = p.v + ((size_t)rowbase * p.hkv + g) * D;
-    const int nvalid = page_ok ? kend - key0 : 0;  // keys of the tile inside the chunk
+    fence_proxy_async_smem();  // this thread's view: earlier generic writes to the stage come first
+    mbar_expect_tx(&full[stage], C::STAGE_BYTES);
 #pragma unroll
-    for (int n = 0; n < C::LOADS; ++n) {
-      const int kr = (tid + n * C::THREADS) / C::CHUNKS;
-      const bool valid = kr < nvalid;
-      const uint32_t goff = valid ? ld_goff[n] : 0u;
-      cp_async_16(kdst + ld_soff[n], kt + goff, valid ? 16u : 0u);
-      cp_async_16(vdst + ld_soff[n], vt + goff, valid ? 16u : 0u);
+    for (int kb = 0; kb < D / 64; ++kb) {
+      tma_load_3d(kdst + kb * C::BLK, tm_k, kb * 64, g, row0, &full[stage]);
+      tma_load_3d(kdst + C::TILE_BYTES + kb * C::BLK, tm_v, kb * 64, g, row0, &full[stage]);
     }
   };
 
@@ -176,26 +168,42 @@ __device__ __forceinline__ void gqa_segment(const GqaParams& p, uint8_t* smem, f
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
 
+  // every thread has finished with the shared memory the first copies overwrite (the
+  // caller's barrier), so thread 0 can start the pipeline
+  int page_next = 0;  // thread 0: block-table entry of the next tile to request
+  if (tid == 0) {
 #pragma unroll
-  for (int t = 0; t < C::NST - 1; ++t) {
-    if (t < ntiles) load_tile(t, t, page_of(t));
-    cp_async_commit();
+    for (int t = 0; t < C::NST - 1; ++t)
+      if (t < ntiles) issue(t, t, page_of(t));
+    page_next = page_of(C::NST - 1);
   }
-  int page_next = page_of(C::NST - 1);  // page of the next tile to load
 
   for (int t = 0; t < ntiles; ++t) {
-    cp_async_wait<C::NST - 2>();
-    __syncthreads();
-    {
-      const int tn = t + C::NST - 1;
-      const int page = page_next;
-      page_next = page_of(tn + 1);
-      if (tn < ntiles) load_tile(tn, tn % C::NST, page);
-      cp_async_commit();
-    }
     const int stage = t % C::NST;
     const uint32_t kbase = sbase + stage * C::STAGE_BYTES;
     const uint32_t vbase = kbase + C::TILE_BYTES;
+    {
+      const uint32_t par = (phase >> stage) & 1u;
+      if (!mbar_wait(&full[stage], par, p.wait_ns, nullptr)) {
+        if ((tid & 31) == 0) raise_error(p.err, kErrWaitTimeout);
+        mbar_wait(&full[stage], par, 1000000000ull, nullptr);  // never leave a copy landing behind
+      }
+      phase ^= 1u << stage;
+    }
+    // V rows past the end of the segment may hold anything (NaN included): their P is 0,
+    // but 0 * NaN is NaN in P V, so they are zeroed (K rows there only feed masked scores)
+    const int nvalid = kend - (kstart + t * kTileKeys);
+    if (nvalid < kTileKeys) {
+      for (int idx = tid; idx < (kTileKeys - nvalid) * (D / 8); idx += C::THREADS) {
+        const int r = nvalid + idx / (D / 8);
+        *reinterpret_cast<uint4*>(smem + (vbase - sbase) + tile_off(r, idx % (D / 8))) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    __syncthreads();  // tile t complete for everyone; every warp is done with tile t-1's stage
+    if (tid == 0 && t + C::NST - 1 < ntiles) {
+      issue(t + C::NST - 1, (t + C::NST - 1) % C::NST, page_next);
+      page_next = page_of(t + C::NST);
+    }
     const int key_w = kstart + t * kTileKeys + slice * 16;  // first key of this warp's slice
 
     // S = Q K^T over the 16 keys of the slice (two n-tiles of 8 keys); for d >= 128 the
@@ -213,7 +221,7 @@ __device__ __forceinline__ void gqa_segment(const GqaParams& p, uint8_t* smem, f
       for (int ks = 0; ks < KS; ++ks) {
         const int c = ks * 2 + ((lane >> 3) & 1);
         uint32_t b0, b1, b2, b3;
-        ldmatrix_x4(kbase + kr * C::ROW_BYTES + swz(kr, c) * 16, b0, b1, b2, b3);
+        ldmatrix_x4(kbase + tile_off(kr, c), b0, b1, b2, b3);
         mma_bf16_16816(sacc[ks % NACC][0], qa[ks], b0, b1);
         mma_bf16_16816(sacc[ks % NACC][1], qa[ks], b2, b3);
       }
@@ -279,14 +287,13 @@ __device__ __forceinline__ void gqa_segment(const GqaParams& p, uint8_t* smem, f
       for (int dp = 0; dp < D / 16; ++dp) {
         const int c = dp * 2 + ((lane >> 4) & 1);
         uint32_t b0, b1, b2, b3;
-        ldmatrix_x4_trans(vbase + kr * C::ROW_BYTES + swz(kr, c) * 16, b0, b1, b2, b3);
+        ldmatrix_x4_trans(vbase + tile_off(kr, c), b0, b1, b2, b3);
         mma_bf16_16816(o[2 * dp], pa, b0, b1);
         mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
       }
     }
   }
-  cp_async_wait<0>();
-  __syncthreads();
+  __syncthreads();  // every copy has been consumed; the merge buffer below reuses the stages
 
   // ---- merge the four key slices of each m-tile through shared memory
   float* red_o = reinterpret_cast<float*>(smem);  // [MT][kSlices][16][OSTR]
@@ -365,13 +372,38 @@ __device__ __forceinline__ void gqa_segment(const GqaParams& p, uint8_t* smem, f
   __syncthreads();  // the merge buffer aliases the pipeline of the next segment
 }
 
+// CTA set-up shared by both kernels (touches only shared memory and kernel parameters):
+// the stage barriers and the tensor-map prefetch. False (for every thread) when the
+// dynamic shared memory is not 1024-byte aligned, which the 128-byte swizzle needs.
+template <int NST>
+__device__ __forceinline__ bool cta_setup(const GqaParams& p, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                          uint64_t* full, uint8_t* smem) {
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) raise_error(p.err, kErrLaunch);
+    return false;
+  }
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int i = 0; i < NST; ++i) mbar_init(&full[i], 1);
+    fence_mbar_init();
+    prefetch_tmap(tm_k);
+    prefetch_tmap(tm_v);
+  }
+  __syncthreads();
+  return true;
+}
+
 // One CTA per (sequence, KV head, context chunk, block of query rows).
 template <int D, int MT>
-__global__ void __launch_bounds__(128 * MT) gqa_split_kernel(GqaParams p) {
+__global__ void __launch_bounds__(128 * MT)
+    gqa_split_kernel(GqaParams p, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   using C = GqaCfg<D, MT>;
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ float s_m[MT][kSlices][16];
   __shared__ float s_l[MT][kSlices][16];
+  __shared__ uint64_t full[C::NST];  // stage landed (TMA transaction count)
+  if (!cta_setup<C::NST>(p, &tm_k, &tm_v, full, smem)) return;
+  uint32_t phase = 0;  // parity of each stage's next completion
   pdl_wait();  // queries, cache and lengths may come from the previous kernel in the stream
   pdl_trigger();
   const int tid = threadIdx.x;
@@ -394,7 +426,8 @@ __global__ void __launch_bounds__(128 * MT) gqa_split_kernel(GqaParams p) {
     return;
   }
   const int kend = min(L, kstart + p.chunk);
-  gqa_segment<D, MT>(p, smem, s_m, s_l, bi, g, rb, L, kstart, kend, p.nsplit == 1 ? kSegFinal : kSegSplit, split);
+  gqa_segment<D, MT>(p, &tm_k, &tm_v, full, phase, smem, s_m, s_l, bi, g, rb, L, kstart, kend,
+                     p.nsplit == 1 ? kSegFinal : kSegSplit, split);
 }
 
 __device__ __forceinline__ long long tiles_of(int L) { return L > 0 ? (L + kTileKeys - 1) / kTileKeys : 0; }
@@ -409,17 +442,22 @@ __device__ __forceinline__ long long tiles_of(int L) { return L > 0 ? (L + kTile
 // in meta for the combine kernel. Computed from seqlens on the device, so the launch
 // needs only an upper bound of the lengths.
 template <int D, int MT>
-__global__ void __launch_bounds__(128 * MT) gqa_balanced_kernel(GqaParams p) {
+__global__ void __launch_bounds__(128 * MT)
+    gqa_balanced_kernel(GqaParams p, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v) {
   using C = GqaCfg<D, MT>;
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ float s_m[MT][kSlices][16];
   __shared__ float s_l[MT][kSlices][16];
+  __shared__ uint64_t full[C::NST];  // stage landed (TMA transaction count)
   constexpr int NW = C::THREADS / 32;
   __shared__ long long s_wsum[NW];  // inclusive prefix of the warps' tile counts
   // walk state, kept in shared memory so that nothing but constants stays live in
   // registers across the (register-bound) segment body
   __shared__ long long s_base, s_pos, s_end, s_w;
   __shared__ int s_seq;
+  if (!cta_setup<C::NST>(p, &tm_k, &tm_v, full, smem)) return;
+  uint32_t phase = 0;  // parity of each stage's next completion (runs on across segments)
   pdl_wait();  // queries, cache and lengths may come from the previous kernel in the stream
   pdl_trigger();
   const int tid = threadIdx.x;
@@ -506,7 +544,8 @@ __global__ void __launch_bounds__(128 * MT) gqa_balanced_kernel(GqaParams p) {
       p.meta[2 * item] = (int)(item + c0);
       p.meta[2 * item + 1] = c1 - c0 + 1;
     }
-    gqa_segment<D, MT>(p, smem, s_m, s_l, i, g, rb, L, t0 * kTileKeys, min(L, t1 * kTileKeys),
+    gqa_segment<D, MT>(p, &tm_k, &tm_v, full, phase, smem, s_m, s_l, i, g, rb, L, t0 * kTileKeys,
+                       min(L, t1 * kTileKeys),
                        c0 == c1 ? kSegFinal : kSegRecord, (int)(item + blockIdx.x));
     // (gqa_segment ends with a barrier: every thread has read the state above)
     if (tid == 0) {
@@ -524,6 +563,18 @@ cudaError_t launch_gqa_dm(const GqaParams& p, int nsplit, int hkv, int b, int ba
   static std::atomic<unsigned long long> split_attr{0}, balanced_attr{0};
   if (cudaError_t e = ensure_smem_limit(gqa_split_kernel<D, MT>, C::SMEM, split_attr)) return e;
   if (cudaError_t e = ensure_smem_limit(gqa_balanced_kernel<D, MT>, C::SMEM, balanced_attr)) return e;
+  // K and V as [tokens, KV heads, d] (contiguous: tokens = b x capacity; paged: pages x 64),
+  // read in boxes of [64 tokens, 1 head, 64 dims]
+  CUtensorMap tk, tv;
+  {
+    const uint64_t tokens = p.paged ? (uint64_t)p.num_pages * kTileKeys : (uint64_t)p.b * p.capacity;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.hkv, (cuuint64_t)tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.hkv * D * 2};
+    const cuuint32_t box[3] = {64, 1, kTileKeys};
+    if (!encode_tmap_bf16_sw128(&tk, p.k, 3, dims, strides, box) ||
+        !encode_tmap_bf16_sw128(&tv, p.v, 3, dims, strides, box))
+      return cudaErrorInvalidValue;
+  }
   // programmatic dependent launch: the CTAs may be scheduled while the previous kernel
   // finishes; they wait for it (pdl_wait) before reading anything
   cudaLaunchConfig_t cfg = {};
@@ -536,8 +587,8 @@ cudaError_t launch_gqa_dm(const GqaParams& p, int nsplit, int hkv, int b, int ba
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = balanced_grid > 0 ? cudaLaunchKernelEx(&cfg, gqa_balanced_kernel<D, MT>, p)
-                                          : cudaLaunchKernelEx(&cfg, gqa_split_kernel<D, MT>, p);
+  const cudaError_t e = balanced_grid > 0 ? cudaLaunchKernelEx(&cfg, gqa_balanced_kernel<D, MT>, p, tk, tv)
+                                          : cudaLaunchKernelEx(&cfg, gqa_split_kernel<D, MT>, p, tk, tv);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -606,6 +657,7 @@ cudaError_t launch_gqa(const GqaLaunch& a, cudaStream_t stream) {
   p.ws_lse = a.ws_lse;
   p.meta = a.meta;
   p.err = a.err;
+  p.wait_ns = a.wait_ns;
 #define DECATTN_GQA_CASE(D)                                                                  \
   case D:                                                                                    \
     return mt == 1 ? launch_gqa_dm<D, 1>(p, a.nsplit, a.hkv, a.b, a.balanced_grid, stream)   \

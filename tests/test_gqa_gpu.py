@@ -291,3 +291,37 @@ def test_multi_wave_split_grid_then_combine():
         da.set_forced_splits(0)
     assert da.check_errors() == 0
     check_sampled(q, cache, out, lse, seqlens, 128, seqs=[0, 11, 23], kv_heads=[0, 5, 7])
+
+
+def _poison_past_end(tensors, seqlens, paged, block_table):
+    """Write NaN into every cache row past each sequence's end (rows a kernel may load
+    with a tile but must never let into a result)."""
+    for t in tensors:
+        for i, L in enumerate(seqlens):
+            if not paged:
+                t[i, L:] = float("nan")
+            elif L % 64:
+                t[int(block_table[i, (L - 1) // 64])][L % 64:] = float("nan")
+
+
+@pytest.mark.parametrize("paged", [False, True])
+@pytest.mark.parametrize("nsplit", [0, 3])
+def test_nan_past_the_end_is_never_read(paged, nsplit):
+    import decode_attention_18_b300 as da
+    from decode_attention_18_b300 import workloads as W
+
+    seqlens = [130, 1, 64, 97, 200]
+    q, cache = W.make_gqa(5, 16, 4, 128, 1, seqlens, paged=paged, capacity=None if paged else 260, seed=13,
+                          device=DEV)
+    _poison_past_end((cache.k, cache.v), seqlens, paged, cache.block_table)
+    sl = torch.tensor(seqlens, dtype=torch.int32, device=DEV)
+    da.set_forced_splits(nsplit)
+    try:
+        out, lse = da.gqa_decode(q, cache.k, cache.v, sl, max_seqlen=max(seqlens),
+                                 block_table=cache.block_table if paged else None)
+        torch.cuda.synchronize()
+    finally:
+        da.set_forced_splits(0)
+    assert da.check_errors() == 0
+    assert torch.isfinite(out.float()).all()
+    check_all(q, cache, out, lse, seqlens, 128, f"nan past end paged={paged} splits={nsplit}")

@@ -229,3 +229,18 @@ def test_multi_wave_split_grid_then_combine():
     ro, rl = A.mla_latent_ref(f64(qz[seqs]), f64(inp.q_pe[seqs]), zs, kp, [seqlens[i] for i in seqs], inp.scale)
     assert_out_close(f64(o[seqs]), ro, "multi-wave latent")
     assert_lse_close(f64(lse[seqs]), rl, "multi-wave lse")
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_nan_past_the_end_is_never_read(paged):
+    seqlens = [300, 45, 129]
+    inp = make(3, 128, 128, 512, 64, 1, seqlens, paged=paged, capacity=None if paged else 400, seed=14)
+    for t in (inp.z, inp.k_pe):
+        for i, L in enumerate(seqlens):
+            if not paged:
+                t[i, L:] = float("nan")
+            elif L % 64:
+                t[int(inp.block_table[i, (L - 1) // 64])][L % 64:] = float("nan")
+    res = forward(inp)
+    assert torch.isfinite(res[3].float()).all() and torch.isfinite(res[0].float()).all()
+    check(inp, res, what=f"nan past end paged={paged}")

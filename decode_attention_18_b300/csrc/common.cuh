@@ -1,10 +1,12 @@
 // Shared device helpers for the decode-attention kernels (sm_103a).
 //
 // Inline-PTX wrappers for the pieces the kernels are built from: cp.async
-// (128-bit global->shared copies), ldmatrix + mma.sync (bf16 tensor-core
+// (128-bit global->shared copies, used by the projection GEMM), TMA tile loads
+// (the grouped-head and latent kernels), ldmatrix + mma.sync (bf16 tensor-core
 // fragments for the grouped-head kernel and the projection GEMMs), mbarrier
-// waits with a time limit, TMA tile loads, and tcgen05 (Tensor Memory
-// allocation, MMA, commit, loads and stores) for the latent MLA kernel.
+// waits with a time limit, programmatic-dependent-launch controls, and tcgen05
+// (Tensor Memory allocation, MMA, commit, loads and stores) for the latent MLA
+// kernel; on the host, the per-device shared-memory limit and tensor-map encoding.
 #pragma once
 
 #include <atomic>

@@ -306,12 +306,13 @@ def _poison_past_end(tensors, seqlens, paged, block_table):
 
 @pytest.mark.parametrize("paged", [False, True])
 @pytest.mark.parametrize("nsplit", [0, 3])
-def test_nan_past_the_end_is_never_read(paged, nsplit):
+@pytest.mark.parametrize("hq,d", [(16, 128), (16, 256), (96, 256)])  # d = 256 with one and two m-tiles
+def test_nan_past_the_end_is_never_read(paged, nsplit, hq, d):
     import decode_attention_18_b300 as da
     from decode_attention_18_b300 import workloads as W
 
     seqlens = [130, 1, 64, 97, 200]
-    q, cache = W.make_gqa(5, 16, 4, 128, 1, seqlens, paged=paged, capacity=None if paged else 260, seed=13,
+    q, cache = W.make_gqa(5, hq, 4, d, 1, seqlens, paged=paged, capacity=None if paged else 260, seed=13,
                           device=DEV)
     _poison_past_end((cache.k, cache.v), seqlens, paged, cache.block_table)
     sl = torch.tensor(seqlens, dtype=torch.int32, device=DEV)
@@ -324,4 +325,4 @@ def test_nan_past_the_end_is_never_read(paged, nsplit):
         da.set_forced_splits(0)
     assert da.check_errors() == 0
     assert torch.isfinite(out.float()).all()
-    check_all(q, cache, out, lse, seqlens, 128, f"nan past end paged={paged} splits={nsplit}")
+    check_all(q, cache, out, lse, seqlens, d, f"nan past end paged={paged} splits={nsplit} d={d}")

@@ -688,15 +688,15 @@ struct MergeCfg {
 };
 
 // The threads of one row merge its n partials: partial c has its D floats at
-// o0 + c * o_stride and its LSE at l0[c * l_stride]. Partials are taken four at a
+// o0 + c * o_stride and its LSE at l0[c * l_stride]. Partials are taken U at a
 // time with all their loads issued before any use (one memory round trip per
 // group), merged with a running maximum; a partial with LSE = -inf saw no key and
-// is skipped.
-template <int D>
+// is skipped. (U = 2 where there are at most two partials: fewer registers, more
+// blocks resident.)
+template <int D, int U = 4>
 __device__ __forceinline__ void merge_row(const float* __restrict__ o0, size_t o_stride, const float* __restrict__ l0,
                                           size_t l_stride, int n, __nv_bfloat16* __restrict__ out_row,
                                           float* __restrict__ lse_out, int t) {
-  constexpr int U = 4;
   float M = -INFINITY, wsum = 0.f;
   float acc[8];
 #pragma unroll
@@ -750,7 +750,7 @@ __device__ __forceinline__ void merge_row(const float* __restrict__ o0, size_t o
 }
 
 // Fixed chunks: row r merges partials c < ceil(L / chunk) of its sequence.
-template <int D>
+template <int D, int U>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ ws_o,
                                                       const float* __restrict__ ws_lse,
                                                       const int32_t* __restrict__ seqlens, int rows,
@@ -763,8 +763,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   if (row >= rows) return;
   const int L = seqlens[row / rows_per_seq];
   const int nv = L > 0 ? min(nsplit, (L + chunk - 1) / chunk) : 0;
-  merge_row<D>(ws_o + (size_t)row * nsplit * D, D, ws_lse + (size_t)row * nsplit, 1, nv, out + (size_t)row * D,
-               lse_out ? lse_out + row : nullptr, threadIdx.x % M::TPR);
+  merge_row<D, U>(ws_o + (size_t)row * nsplit * D, D, ws_lse + (size_t)row * nsplit, 1, nv, out + (size_t)row * D,
+                  lse_out ? lse_out + row : nullptr, threadIdx.x % M::TPR);
 }
 
 // Combine for the balanced grouped-head schedule: row (bi, head j, token) belongs to
@@ -828,8 +828,10 @@ cudaError_t launch_combine(const float* ws_o, const float* ws_lse, const int32_t
   auto* o = static_cast<__nv_bfloat16*>(out);
 #define DECATTN_COMBINE_CASE(D)                                                                              \
   case D:                                                                                                    \
-    if (cudaError_t e = launch_dependent(combine_kernel<D>, merge_blocks<D>(rows), stream, ws_o, ws_lse, seqlens, \
-                                         rows, rows_per_seq, nsplit, chunk, o, lse))                          \
+    if (cudaError_t e = nsplit <= 2 ? launch_dependent(combine_kernel<D, 2>, merge_blocks<D>(rows), stream, ws_o,  \
+                                                       ws_lse, seqlens, rows, rows_per_seq, nsplit, chunk, o, lse) \
+                                    : launch_dependent(combine_kernel<D, 4>, merge_blocks<D>(rows), stream, ws_o,  \
+                                                       ws_lse, seqlens, rows, rows_per_seq, nsplit, chunk, o, lse)) \
       return e;                                                                                              \
     break;
   switch (d) {

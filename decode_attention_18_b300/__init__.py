@@ -11,12 +11,11 @@ from .ops import (  # noqa: F401
     mla_forward,
     mla_out_proj,
     set_forced_splits,
-    set_gqa_kernel,
     set_wait_limit_ns,
     test_force_timeout,
 )
 
 __all__ = [
     "gqa_decode", "mla_absorb_q", "mla_decode", "mla_out_proj", "mla_forward", "check_errors",
-    "set_forced_splits", "set_gqa_kernel", "last_num_splits", "set_wait_limit_ns", "test_force_timeout", "DecAttnError",
+    "set_forced_splits", "last_num_splits", "set_wait_limit_ns", "test_force_timeout", "DecAttnError",
 ]

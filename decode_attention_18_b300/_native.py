@@ -25,7 +25,6 @@ SYMBOLS = (
     "decattn_last_num_splits",
     "decattn_test_force_timeout",
     "gqa_decode_no_alloc",
-    "decattn_set_gqa_kernel",
 )
 
 
@@ -86,8 +85,6 @@ def load():
     lib.decattn_last_num_splits.argtypes = []
     lib.decattn_test_force_timeout.restype = None
     lib.decattn_test_force_timeout.argtypes = [I]
-    lib.decattn_set_gqa_kernel.restype = None
-    lib.decattn_set_gqa_kernel.argtypes = [I]
     lib.gqa_decode_no_alloc.restype = I
     lib.gqa_decode_no_alloc.argtypes = [P, P, P, KV, P, I, I, I, I, I, I, F, P, P, P]
     _lib = lib

@@ -30,16 +30,6 @@ std::atomic<unsigned long long> g_wait_ns{0};
 std::atomic<int> g_forced_splits{0};
 std::atomic<int> g_last_splits{0};
 std::atomic<int> g_test_timeout{0};
-std::atomic<int> g_gqa_kernel{0};  // 0 auto, 1 mma.sync kernel, 2 tensor-core kernel (where eligible)
-
-// Which grouped-head kernel runs. By default the mma.sync kernel: on B300 it measured as
-// fast as or faster than the tensor-core kernel (keys in the MMA M dimension) on every
-// shape tried (MQA with 24 / 32 / 48 / 64 / 96 query rows per KV head, d = 128 and 256),
-// both being bound there by the latency of their shared-memory rings rather than by math.
-// Callers (and the tests) can force the tensor-core kernel where it applies.
-bool use_gqa_tc(int rows, int d) {
-  return gqa_tc_eligible(rows, d) && g_gqa_kernel.load() == 2;
-}
 
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
 constexpr int kPage = 64;  // chunks are whole 64-key pages (and whole kernel tiles)
@@ -136,10 +126,8 @@ int check_kv(const decattn_kv& kv, int b, int max_seqlen) {
 // --- grouped-head plan
 Plan gqa_plan(int b, int s, int hq, int hkv, int d, int max_seqlen, int sms) {
   const int rows = (hq / hkv) * s;
-  const bool tc = use_gqa_tc(rows, d);
-  const int rpc = tc ? gqa_tc_rows_per_cta() : gqa_rows_per_cta(rows);
-  const long long base = (long long)b * hkv * ceil_div(rows, rpc);
-  const long long slots = (long long)sms * (tc ? 1 : gqa_ctas_per_sm(d));
+  const long long base = (long long)b * hkv * ceil_div(rows, gqa_rows_per_cta(rows));
+  const long long slots = (long long)sms * gqa_ctas_per_sm(d);
   return plan_splits(base, max_seqlen, slots, 256, 512, kPage);
 }
 
@@ -159,7 +147,7 @@ struct GqaBalanced {
 GqaBalanced gqa_balanced(const Plan& pl, int b, int s, int hq, int hkv, int d, int sms) {
   GqaBalanced gb;
   const int rows = (hq / hkv) * s;
-  if (pl.nsplit <= 1 || g_forced_splits.load() > 0 || use_gqa_tc(rows, d) || gqa_rows_per_cta(rows) > 16) return gb;
+  if (pl.nsplit <= 1 || g_forced_splits.load() > 0 || gqa_rows_per_cta(rows) > 16) return gb;
   gb.rpb = gqa_rows_per_cta(rows);
   gb.items = (long long)b * hkv * ceil_div(rows, gb.rpb);
   gb.grid = sms * gqa_balanced_ctas_per_sm(d, rows);
@@ -200,7 +188,6 @@ void decattn_set_wait_limit_ns(unsigned long long ns) { g_wait_ns.store(ns); }
 void decattn_set_forced_splits(int nsplit) { g_forced_splits.store(nsplit > 0 ? nsplit : 0); }
 int decattn_last_num_splits(void) { return g_last_splits.load(); }
 void decattn_test_force_timeout(int on) { g_test_timeout.store(on ? 1 : 0); }
-void decattn_set_gqa_kernel(int mode) { g_gqa_kernel.store(mode == 1 || mode == 2 ? mode : 0); }
 
 int decattn_check_errors(cudaStream_t stream) {
   DeviceState* st = nullptr;
@@ -282,11 +269,12 @@ int gqa_decode(const decattn_bf16* q, const decattn_bf16* k, const decattn_bf16*
   }
   a.err = st->err;
   a.wait_ns = wait_limit();
+  a.test_timeout = g_test_timeout.load();
   g_last_splits.store(pl.nsplit);
-  const cudaError_t le = use_gqa_tc((hq / hkv) * s, d) ? launch_gqa_tc(a, stream) : launch_gqa(a, stream);
-  if (le != cudaSuccess) return DECATTN_ERR_CUDA;
+  if (launch_gqa(a, stream) != cudaSuccess) return DECATTN_ERR_CUDA;
   if (gb.grid > 0) {
-    if (launch_combine_balanced(a.ws_o, a.ws_lse, a.meta, seqlens, b, hq, s, hkv, d, out, lse, stream) != cudaSuccess)
+    if (launch_combine_balanced(a.ws_o, a.ws_lse, a.meta, seqlens, b, hq, s, hkv, d, gb.items + gb.grid, out, lse,
+                                stream) != cudaSuccess)
       return DECATTN_ERR_CUDA;
   } else if (pl.nsplit > 1) {
     if (launch_combine(a.ws_o, a.ws_lse, seqlens, (int)rows, hq * s, pl.nsplit, pl.chunk, d, out, lse, stream) !=

@@ -48,6 +48,7 @@ struct GqaParams {
   int* meta;  // balanced mode: per work item {first partial record, record count}
   unsigned* err;
   unsigned long long wait_ns;  // limit of the tile waits
+  int test_timeout;            // nonzero: the first tile wait also waits on a barrier nothing signals
 };
 
 constexpr int kTileKeys = 64;
@@ -55,6 +56,8 @@ constexpr int kSlices = 4;  // warps (key slices of 16) per m-tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.f;  // move a row's reference maximum only past 2^8
+constexpr unsigned long long kTeardownNs = 1000000000ull;  // 1 s for own copies after a time-out
+constexpr unsigned long long kTestWaitNs = 1000000ull;     // 1 ms forced-timeout wait
 
 template <int D, int MT_>
 struct GqaCfg {
@@ -87,10 +90,12 @@ enum SegOut { kSegFinal = 0, kSegSplit = 1, kSegRecord = 2 };
 // LSE; kSegSplit writes fp32 partials at chunk index `slot` of the [row][nsplit]
 // layout; kSegRecord writes partial record `slot` ([record][16*MT rows][D]) of the
 // balanced schedule. The caller's threads all enter; shared memory is free again
-// when it returns.
+// when it returns. Returns false (in every thread) when a tile wait ran out: the
+// error is recorded, the copies already requested have been waited for (bounded) and
+// nothing was written.
 template <int D, int MT>
-__device__ __forceinline__ void gqa_segment(const GqaParams& p, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
-                                            uint64_t* full, uint32_t& phase, uint8_t* smem,
+__device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                            uint64_t* full, uint64_t* never, uint32_t& phase, uint8_t* smem,
                                             float (*s_m)[kSlices][16], float (*s_l)[kSlices][16], int bi, int g,
                                             int rb, int L, int kstart, int kend, int out_mode, int slot) {
   using C = GqaCfg<D, MT>;
@@ -182,24 +187,33 @@ __device__ __forceinline__ void gqa_segment(const GqaParams& p, const CUtensorMa
     const int stage = t % C::NST;
     const uint32_t kbase = sbase + stage * C::STAGE_BYTES;
     const uint32_t vbase = kbase + C::TILE_BYTES;
-    {
-      const uint32_t par = (phase >> stage) & 1u;
-      if (!mbar_wait(&full[stage], par, p.wait_ns, nullptr)) {
-        if ((tid & 31) == 0) raise_error(p.err, kErrWaitTimeout);
-        mbar_wait(&full[stage], par, 1000000000ull, nullptr);  // never leave a copy landing behind
-      }
-      phase ^= 1u << stage;
-    }
+    bool landed = mbar_wait(&full[stage], (phase >> stage) & 1u, p.wait_ns, nullptr);
+    if (t == 0 && p.test_timeout) landed = mbar_wait(never, 0, kTestWaitNs, nullptr) && landed;
+    phase ^= 1u << stage;
     // V rows past the end of the segment may hold anything (NaN included): their P is 0,
     // but 0 * NaN is NaN in P V, so they are zeroed (K rows there only feed masked scores)
     const int nvalid = kend - (kstart + t * kTileKeys);
-    if (nvalid < kTileKeys) {
+    if (landed && nvalid < kTileKeys) {
       for (int idx = tid; idx < (kTileKeys - nvalid) * (D / 8); idx += C::THREADS) {
         const int r = nvalid + idx / (D / 8);
         *reinterpret_cast<uint4*>(smem + (vbase - sbase) + tile_off(r, idx % (D / 8))) = make_uint4(0, 0, 0, 0);
       }
     }
-    __syncthreads();  // tile t complete for everyone; every warp is done with tile t-1's stage
+    // tile t complete for everyone; every warp is done with tile t-1's stage
+    if (__syncthreads_or(!landed)) {
+      // A wait ran out (in some thread): record it, let the copies already requested
+      // (tiles t .. t+NST-2) land before the CTA leaves their shared memory, and stop.
+      if (tid == 0) {
+        raise_error(p.err, kErrWaitTimeout);
+        for (int j = 0; j < C::NST - 1 && t + j < ntiles; ++j) {
+          const int st = (t + j) % C::NST;
+          const uint32_t par = ((phase >> st) & 1u) ^ (j == 0 ? 1u : 0u);  // tile t's bit already moved on
+          mbar_wait(&full[st], par, kTeardownNs, nullptr);
+        }
+      }
+      __syncthreads();
+      return false;
+    }
     if (tid == 0 && t + C::NST - 1 < ntiles) {
       issue(t + C::NST - 1, (t + C::NST - 1) % C::NST, page_next);
       page_next = page_of(t + C::NST);
@@ -370,10 +384,12 @@ __device__ __forceinline__ void gqa_segment(const GqaParams& p, const CUtensorMa
     }
   }
   __syncthreads();  // the merge buffer aliases the pipeline of the next segment
+  return true;
 }
 
 // CTA set-up shared by both kernels (touches only shared memory and kernel parameters):
-// the stage barriers and the tensor-map prefetch. False (for every thread) when the
+// the stage barriers (full[0 .. NST-1]), one barrier that nothing ever signals
+// (full[NST], waited on by the forced-timeout test) and the tensor-map prefetch. False (for every thread) when the
 // dynamic shared memory is not 1024-byte aligned, which the 128-byte swizzle needs.
 template <int NST>
 __device__ __forceinline__ bool cta_setup(const GqaParams& p, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
@@ -384,7 +400,7 @@ __device__ __forceinline__ bool cta_setup(const GqaParams& p, const CUtensorMap*
   }
   if (threadIdx.x == 0) {
 #pragma unroll
-    for (int i = 0; i < NST; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i <= NST; ++i) mbar_init(&full[i], 1);
     fence_mbar_init();
     prefetch_tmap(tm_k);
     prefetch_tmap(tm_v);
@@ -401,7 +417,7 @@ __global__ void __launch_bounds__(128 * MT)
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ float s_m[MT][kSlices][16];
   __shared__ float s_l[MT][kSlices][16];
-  __shared__ uint64_t full[C::NST];  // stage landed (TMA transaction count)
+  __shared__ uint64_t full[C::NST + 1];  // stage landed (TMA transaction count); + the never-signalled one
   if (!cta_setup<C::NST>(p, &tm_k, &tm_v, full, smem)) return;
   uint32_t phase = 0;  // parity of each stage's next completion
   pdl_wait();  // queries, cache and lengths may come from the previous kernel in the stream
@@ -426,7 +442,7 @@ __global__ void __launch_bounds__(128 * MT)
     return;
   }
   const int kend = min(L, kstart + p.chunk);
-  gqa_segment<D, MT>(p, &tm_k, &tm_v, full, phase, smem, s_m, s_l, bi, g, rb, L, kstart, kend,
+  gqa_segment<D, MT>(p, &tm_k, &tm_v, full, full + C::NST, phase, smem, s_m, s_l, bi, g, rb, L, kstart, kend,
                      p.nsplit == 1 ? kSegFinal : kSegSplit, split);
 }
 
@@ -449,7 +465,7 @@ __global__ void __launch_bounds__(128 * MT)
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ float s_m[MT][kSlices][16];
   __shared__ float s_l[MT][kSlices][16];
-  __shared__ uint64_t full[C::NST];  // stage landed (TMA transaction count)
+  __shared__ uint64_t full[C::NST + 1];  // stage landed (TMA transaction count); + the never-signalled one
   constexpr int NW = C::THREADS / 32;
   __shared__ long long s_wsum[NW];  // inclusive prefix of the warps' tile counts
   // walk state, kept in shared memory so that nothing but constants stays live in
@@ -458,6 +474,7 @@ __global__ void __launch_bounds__(128 * MT)
   __shared__ int s_seq;
   if (!cta_setup<C::NST>(p, &tm_k, &tm_v, full, smem)) return;
   uint32_t phase = 0;  // parity of each stage's next completion (runs on across segments)
+  bool aborted = false;  // a tile wait ran out: the walk goes on, writing meta only
   pdl_wait();  // queries, cache and lengths may come from the previous kernel in the stream
   pdl_trigger();
   const int tid = threadIdx.x;
@@ -544,10 +561,16 @@ __global__ void __launch_bounds__(128 * MT)
       p.meta[2 * item] = (int)(item + c0);
       p.meta[2 * item + 1] = c1 - c0 + 1;
     }
-    gqa_segment<D, MT>(p, &tm_k, &tm_v, full, phase, smem, s_m, s_l, i, g, rb, L, t0 * kTileKeys,
-                       min(L, t1 * kTileKeys),
-                       c0 == c1 ? kSegFinal : kSegRecord, (int)(item + blockIdx.x));
-    // (gqa_segment ends with a barrier: every thread has read the state above)
+    // After a time-out the remaining pieces are not computed, but every item whose first
+    // tile lies in this CTA's range still gets its meta entry, so the combine reads only
+    // records inside the workspace.
+    if (!aborted)
+      aborted = !gqa_segment<D, MT>(p, &tm_k, &tm_v, full, full + C::NST, phase, smem, s_m, s_l, i, g, rb, L,
+                                    t0 * kTileKeys, min(L, t1 * kTileKeys), c0 == c1 ? kSegFinal : kSegRecord,
+                                    (int)(item + blockIdx.x));
+    else
+      __syncthreads();
+    // (both branches end with a barrier: every thread has read the state above)
     if (tid == 0) {
       s_pos = pos + (t1 - t0);
       s_seq = i;
@@ -658,6 +681,7 @@ cudaError_t launch_gqa(const GqaLaunch& a, cudaStream_t stream) {
   p.meta = a.meta;
   p.err = a.err;
   p.wait_ns = a.wait_ns;
+  p.test_timeout = a.test_timeout;
 #define DECATTN_GQA_CASE(D)                                                                  \
   case D:                                                                                    \
     return mt == 1 ? launch_gqa_dm<D, 1>(p, a.nsplit, a.hkv, a.b, a.balanced_grid, stream)   \
@@ -776,7 +800,7 @@ __global__ void __launch_bounds__(256) combine_balanced_kernel(const float* __re
                                                                const float* __restrict__ ws_lse,
                                                                const int* __restrict__ meta,
                                                                const int32_t* __restrict__ seqlens, int rows, int hq,
-                                                               int s, int hkv, int G, int rpb, int nrb,
+                                                               int s, int hkv, int G, int rpb, int nrb, long long records,
                                                                __nv_bfloat16* __restrict__ out,
                                                                float* __restrict__ lse_out) {
   using M = MergeCfg<D>;
@@ -793,6 +817,10 @@ __global__ void __launch_bounds__(256) combine_balanced_kernel(const float* __re
     first = meta[2 * item];
     n = meta[2 * item + 1];
     if (n <= 1) return;  // written directly by its CTA
+    // meta is written by the attention kernel for every item; the clamp only keeps a
+    // corrupted entry from sending the loads outside the workspace
+    if (first < 0 || first >= records) return;
+    n = (int)min((long long)n, records - first);
   }
   const size_t rec_row = (size_t)first * rpb + r % rpb;
   merge_row<D>(ws_o + rec_row * D, (size_t)rpb * D, ws_lse + rec_row, (size_t)rpb, n, out + (size_t)row * D,
@@ -846,7 +874,8 @@ cudaError_t launch_combine(const float* ws_o, const float* ws_lse, const int32_t
 }
 
 cudaError_t launch_combine_balanced(const float* ws_o, const float* ws_lse, const int* meta, const int32_t* seqlens,
-                                    int b, int hq, int s, int hkv, int d, void* out, float* lse, cudaStream_t stream) {
+                                    int b, int hq, int s, int hkv, int d, long long records, void* out, float* lse,
+                                    cudaStream_t stream) {
   const int rows_kv = (hq / hkv) * s;
   const int rpb = gqa_rows_per_cta(rows_kv);
   const int nrb = (rows_kv + rpb - 1) / rpb;
@@ -856,7 +885,7 @@ cudaError_t launch_combine_balanced(const float* ws_o, const float* ws_lse, cons
 #define DECATTN_COMBINE_CASE(D)                                                                              \
   case D:                                                                                                    \
     if (cudaError_t e = launch_dependent(combine_balanced_kernel<D>, merge_blocks<D>(rows), stream, ws_o,      \
-                                         ws_lse, meta, seqlens, rows, hq, s, hkv, G, rpb, nrb, o, lse))        \
+                                         ws_lse, meta, seqlens, rows, hq, s, hkv, G, rpb, nrb, records, o, lse)) \
       return e;                                                                                              \
     break;
   switch (d) {

@@ -25,7 +25,8 @@ struct GqaLaunch {
   int* meta;      // balanced: [work items][2] {first record, count}
   int balanced_grid;  // > 0: balanced schedule over this many CTAs (mma.sync kernel)
   unsigned* err;
-  unsigned long long wait_ns;  // limit of the tensor-core kernel's bounded waits
+  unsigned long long wait_ns;  // limit of the bounded tile waits
+  int test_timeout;            // forced-timeout test: one wait on a barrier nothing signals
 };
 
 // rows of one grouped-head CTA (multiple of 16) for head dim d
@@ -33,17 +34,14 @@ int gqa_rows_per_cta(int d);
 int gqa_ctas_per_sm(int d);
 int gqa_balanced_ctas_per_sm(int d, int rows);  // measured occupancy of the balanced kernel
 cudaError_t launch_gqa(const GqaLaunch& p, cudaStream_t stream);
-// tensor-core variant (keys in the MMA M dimension) for KV heads shared by 17-32+ query rows
-bool gqa_tc_eligible(int rows, int d);
-int gqa_tc_rows_per_cta();
-cudaError_t launch_gqa_tc(const GqaLaunch& p, cudaStream_t stream);
 
 // log-sum-exp merge of split partials: rows x nsplit partials of width d
 cudaError_t launch_combine(const float* ws_o, const float* ws_lse, const int32_t* seqlens, int rows, int rows_per_seq,
                            int nsplit, int chunk, int d, void* out, float* lse, cudaStream_t stream);
 // combine of the balanced grouped-head schedule (see gqa_balanced_kernel)
 cudaError_t launch_combine_balanced(const float* ws_o, const float* ws_lse, const int* meta, const int32_t* seqlens,
-                                    int b, int hq, int s, int hkv, int d, void* out, float* lse, cudaStream_t stream);
+                                    int b, int hq, int s, int hkv, int d, long long records, void* out, float* lse,
+                                    cudaStream_t stream);
 
 struct ProjLaunch {
   const void* a;     // [b, h, s, kin]

@@ -154,12 +154,6 @@ def set_forced_splits(n: int):
     load().decattn_set_forced_splits(int(n))
 
 
-def set_gqa_kernel(mode: int):
-    """0 (default) or 1: the mma.sync grouped-head kernel; 2: the tensor-core one (keys
-    in the MMA M dimension) wherever it applies (G*s > 16, d in {128, 256})."""
-    load().decattn_set_gqa_kernel(int(mode))
-
-
 def last_num_splits() -> int:
     return int(load().decattn_last_num_splits())
 

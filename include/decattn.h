@@ -179,28 +179,30 @@ int gqa_decode_no_alloc(const decattn_bf16* q, const decattn_bf16* k, const deca
  * decattn_check_errors: synchronises `stream`, reads and clears the device
  * error word of the current device; returns DECATTN_ERR_TIMEOUT if a bounded
  * wait ran out, DECATTN_ERR_INVALID_ARG if a page index was outside the pool,
- * DECATTN_ERR_CUDA on a CUDA error, else DECATTN_OK.
+ * DECATTN_ERR_CUDA on a CUDA error, else DECATTN_OK. There is ONE error word
+ * per device, shared by every stream and host thread: it collects the faults
+ * of all calls on that device since it was last cleared, whichever stream they
+ * ran on, and the first decattn_check_errors to read it (on any stream) reports
+ * and clears them. Only work ordered before the synchronised stream's point is
+ * sure to have landed in it; to attribute a fault to one call, run that call
+ * alone (or synchronise the other streams first) before checking.
  * decattn_set_wait_limit_ns: limit of every device-side wait (0 = default,
  * 2 s). decattn_set_forced_splits: 0 = let the planner choose the number of
  * context chunks; n > 0 forces n (for split-invariance tests); it also
  * changes the workspace sizes returned afterwards.
  * decattn_last_num_splits: number of chunks the last attention call used.
- * decattn_set_gqa_kernel: which grouped-head kernel gqa_decode runs. 0 (default)
- * and 1 run the mma.sync kernel; 2 runs the tensor-core kernel (keys in the MMA M
- * dimension) wherever it applies (G*s > 16, d in {128, 256}).
- * Both compute the same attention; the switch exists for tests and measurements.
- * It also changes the workspace sizes returned afterwards.
- * decattn_test_force_timeout: when nonzero, the next mla_decode kernels wait
- * once on a barrier that nothing signals, with a 1 ms limit, so that the
- * timeout path runs; the kernels then wind down and report
- * DECATTN_ERR_TIMEOUT through decattn_check_errors. Test use only.
+ * decattn_test_force_timeout: when nonzero, the next mla_decode and gqa_decode
+ * kernels wait once on a barrier that nothing signals, with a 1 ms limit, so that
+ * the timeout path runs; the kernels then wind down (no new copies, their own
+ * copies in flight waited for, Tensor Memory freed) and report
+ * DECATTN_ERR_TIMEOUT through decattn_check_errors. Their outputs are not
+ * valid then. Test use only.
  */
 int decattn_check_errors(cudaStream_t stream);
 void decattn_set_wait_limit_ns(unsigned long long ns);
 void decattn_set_forced_splits(int nsplit);
 int decattn_last_num_splits(void);
 void decattn_test_force_timeout(int on);
-void decattn_set_gqa_kernel(int mode);
 
 #ifdef __cplusplus
 }

@@ -10,7 +10,7 @@ Citations name the page and its section:
            between MHA and GQA?".
   [LESSON] "MQA, GQA & MLA" lesson, "01 Concept".
 
-Readings taken where the pages leave a step open (all listed in the design doc):
+Readings taken where the pages leave a step open:
   * query head j reads KV head j // G with G = Hq / Hkv: contiguous groups,
     as in [LESSON] "24 query heads in 4 groups of 6";
   * seqlens[b] counts every key of sequence b including the s new tokens;

@@ -60,3 +60,60 @@ def qz_rounding_lse_bound(qz_exact, o_lat_exact, scale):
     (bf16 round-to-nearest), so |dLSE| <= scale * 2^-9 * sum_i |Qz_i| |O_lat_i|.
     Returned with the 1e-3 allowance added."""
     return LSE_ABS + scale * 2.0 ** -9 * np.sum(np.abs(qz_exact) * np.abs(o_lat_exact), axis=-1)
+
+
+# ---------------------------------------------------------------------------
+# the checker's view of a cache: sequence rows in logical order, gathered from a
+# paged pool by the oracle's own gather_paged (the package's helpers are not used
+# on the checker side)
+
+
+class _LazyPool:
+    """Indexable like a [num_pages, 64, ...] array: pool[page] is that page in
+    float64, fetched from the device on demand (optionally one KV head only)."""
+
+    def __init__(self, t, kv_head=None):
+        self.t, self.kv_head = t, kv_head
+
+    def _page(self, x):
+        if self.kv_head is not None:
+            x = x[:, self.kv_head:self.kv_head + 1]
+        return f64(x)
+
+    def __getitem__(self, idx):
+        if isinstance(idx, tuple):  # pool[:0, 0]: the empty case
+            return np.zeros((0,) + self._page(self.t[0]).shape[1:])
+        return self._page(self.t[int(idx)])
+
+
+def cache_rows(t, i, L, block_table=None, kv_head=None, page_size=64):
+    """Rows [L, ...] of sequence i in logical order as float64: a contiguous
+    cache [b, capacity, ...] is sliced, a paged pool [num_pages, 64, ...] is
+    gathered with oracle.attention.gather_paged through block_table [b, max_pages]."""
+    from oracle import attention as A
+
+    if block_table is None:
+        x = t[i, :L]
+        if kv_head is not None:
+            x = x[:, kv_head:kv_head + 1]
+        return f64(x)
+    return A.gather_paged(_LazyPool(t, kv_head), block_table[i].cpu().numpy(), L, page_size)
+
+
+def gqa_rows(cache, i, which, kv_head=None):
+    """K or V rows of sequence i of a workloads.KVCache (checker side)."""
+    t = cache.k if which == "k" else cache.v
+    return cache_rows(t, i, cache.seqlens[i], cache.block_table if cache.paged else None, kv_head)
+
+
+def mla_rows(inp, i, which):
+    """Z or K_pe rows of sequence i of workloads.MLAInputs (checker side)."""
+    t = inp.z if which == "z" else inp.k_pe
+    return cache_rows(t, i, inp.seqlens[i], inp.block_table if inp.paged else None)
+
+
+def as_device_bf16(rows, like):
+    """fp64 rows (exact bf16 values) back to a bf16 tensor on `like`'s device."""
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(rows)).to(device=like.device, dtype=torch.bfloat16)

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 from oracle import attention as A
-from tests.helpers import assert_lse_close, assert_out_close, f64
+from tests.helpers import gqa_rows, as_device_bf16, assert_lse_close, assert_out_close, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -42,8 +42,8 @@ def run(b, hq, hkv, d, s, seqlens, paged=False, capacity=None, q_std=1.0, seed=0
 
 def check_all(q, cache, out, lse, seqlens, d, what):
     b = q.shape[0]
-    ks = [f64(cache.seq_rows(i, "k")) for i in range(b)]
-    vs = [f64(cache.seq_rows(i, "v")) for i in range(b)]
+    ks = [gqa_rows(cache, i, "k") for i in range(b)]
+    vs = [gqa_rows(cache, i, "v") for i in range(b)]
     ro, rl = A.gqa_ref(f64(q), ks, vs, seqlens, 1 / math.sqrt(d))
     assert_out_close(f64(out), ro, what)
     assert_lse_close(f64(lse), rl, what)
@@ -56,12 +56,11 @@ def check_sampled(q, cache, out, lse, seqlens, d, seqs, kv_heads):
     hkv = cache.k.shape[2]
     G = hq // hkv
     for i in seqs:
-        K = cache.seq_rows(i, "k")
-        V = cache.seq_rows(i, "v")
         for g in kv_heads:
             heads = slice(g * G, (g + 1) * G)
-            ro, rl = A.gqa_ref(f64(q[i:i + 1, heads]), [f64(K[:, g:g + 1])], [f64(V[:, g:g + 1])], [seqlens[i]],
-                               1 / math.sqrt(d))
+            K = gqa_rows(cache, i, "k", kv_head=g)
+            V = gqa_rows(cache, i, "v", kv_head=g)
+            ro, rl = A.gqa_ref(f64(q[i:i + 1, heads]), [K], [V], [seqlens[i]], 1 / math.sqrt(d))
             assert_out_close(f64(out[i:i + 1, heads]), ro, f"seq {i} kv head {g}")
             assert_lse_close(f64(lse[i:i + 1, heads]), rl, f"seq {i} kv head {g}")
 
@@ -111,8 +110,8 @@ def test_paged_equals_contiguous_bitwise():
     kc = torch.zeros((3, cap, 4, 128), dtype=torch.bfloat16, device=DEV)
     vc = torch.zeros_like(kc)
     for i, L in enumerate(seqlens):
-        kc[i, :L] = cache.seq_rows(i, "k")
-        vc[i, :L] = cache.seq_rows(i, "v")
+        kc[i, :L] = as_device_bf16(gqa_rows(cache, i, "k"), kc)
+        vc[i, :L] = as_device_bf16(gqa_rows(cache, i, "v"), vc)
     sl = torch.tensor(seqlens, dtype=torch.int32, device=DEV)
     out2, lse2 = da.gqa_decode(q, kc, vc, sl, max_seqlen=cap)
     torch.cuda.synchronize()
@@ -208,17 +207,7 @@ def test_full_size_paged_ragged_sampled(hkv):
 
 
 # ---------------------------------------------------------------------------
-# Tensor-core path (keys in the MMA M dimension): KV heads shared by more than 16 query
-# rows (G * s > 16) with d in {128, 256}, forced on for these tests; the same cases run
-# through the mma.sync kernel too.
-
-@pytest.fixture(params=[2, 1], ids=["tensor_core", "mma_sync"])
-def gqa_kernel(request):
-    import decode_attention_18_b300 as da
-
-    da.set_gqa_kernel(request.param)
-    yield request.param
-    da.set_gqa_kernel(0)
+# KV heads shared by more than 16 query rows (two m-tiles per CTA, several row blocks)
 
 @pytest.mark.parametrize("b,hq,hkv,d,s,seqlens", [
     (2, 32, 1, 128, 1, [700, 129]),         # MQA, 32 rows, d = 128
@@ -227,26 +216,26 @@ def gqa_kernel(request):
     (1, 24, 1, 128, 4, [333]),              # 96 rows: three row blocks
     (6, 24, 2, 256, 1, [0, 1, 63, 64, 65, 1000]),  # empty and page-boundary lengths, 2 KV heads
 ])
-def test_tensor_core_path_vs_oracle(b, hq, hkv, d, s, seqlens, gqa_kernel):
+def test_many_rows_per_kv_head_vs_oracle(b, hq, hkv, d, s, seqlens):
     q, cache, out, lse = run(b, hq, hkv, d, s, seqlens, capacity=max(seqlens) + 3, seed=17)
-    check_all(q, cache, out, lse, seqlens, d, f"tc b{b} hq{hq} hkv{hkv} d{d} s{s}")
+    check_all(q, cache, out, lse, seqlens, d, f"rows b{b} hq{hq} hkv{hkv} d{d} s{s}")
     if 0 in seqlens:
         i = seqlens.index(0)
         assert torch.all(out[i] == 0) and torch.all(torch.isneginf(lse[i]))
 
 
-def test_tensor_core_path_sharp_and_paged_bitwise(gqa_kernel):
+def test_many_rows_sharp_and_paged_bitwise():
     import decode_attention_18_b300 as da
 
     seqlens = [517, 64, 1000]
     q, cache, out, lse = run(3, 24, 1, 256, 1, seqlens, paged=True, seed=19, q_std=8.0)
-    check_all(q, cache, out, lse, seqlens, 256, "tc paged sharp")
+    check_all(q, cache, out, lse, seqlens, 256, "24-row MQA paged sharp")
     cap = max(seqlens)
     kc = torch.zeros((3, cap, 1, 256), dtype=torch.bfloat16, device=DEV)
     vc = torch.zeros_like(kc)
     for i, L in enumerate(seqlens):
-        kc[i, :L] = cache.seq_rows(i, "k")
-        vc[i, :L] = cache.seq_rows(i, "v")
+        kc[i, :L] = as_device_bf16(gqa_rows(cache, i, "k"), kc)
+        vc[i, :L] = as_device_bf16(gqa_rows(cache, i, "v"), vc)
     sl = torch.tensor(seqlens, dtype=torch.int32, device=DEV)
     out2, lse2 = da.gqa_decode(q, kc, vc, sl, max_seqlen=cap)
     torch.cuda.synchronize()
@@ -255,7 +244,7 @@ def test_tensor_core_path_sharp_and_paged_bitwise(gqa_kernel):
 
 
 @pytest.mark.parametrize("nsplit", [1, 3, 8])
-def test_tensor_core_path_split_invariance(nsplit, gqa_kernel):
+def test_many_rows_split_invariance(nsplit):
     import decode_attention_18_b300 as da
 
     seqlens = [2000, 900]
@@ -270,7 +259,7 @@ def test_tensor_core_path_split_invariance(nsplit, gqa_kernel):
     a, b2 = f64(out), f64(out2)
     assert np.sqrt(np.mean((a - b2) ** 2)) / np.sqrt(np.mean(a ** 2)) <= 1e-2
     assert np.abs(f64(lse) - f64(lse2)).max() <= 1e-4
-    check_all(q, cache, out2, lse2, seqlens, 256, f"tc nsplit {nsplit}")
+    check_all(q, cache, out2, lse2, seqlens, 256, f"24-row MQA nsplit {nsplit}")
 
 
 def test_multi_wave_split_grid_then_combine():

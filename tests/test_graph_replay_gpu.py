@@ -9,7 +9,7 @@ import pytest
 import torch
 
 from oracle import attention as A
-from tests.helpers import assert_lse_close, assert_out_close, f64
+from tests.helpers import gqa_rows, mla_rows, assert_lse_close, assert_out_close, f64
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -78,8 +78,8 @@ def test_mla_pipeline_graph_replays():
     # the last replay against the oracle (latent stage fed the replay's own Qz)
     x = sets[-1]
     gqz, go, gl, _ = results[-1]
-    zs = [f64(x.seq_rows(i, "z")) for i in range(b)]
-    kp = [f64(x.seq_rows(i, "kpe")) for i in range(b)]
+    zs = [mla_rows(x, i, "z") for i in range(b)]
+    kp = [mla_rows(x, i, "kpe") for i in range(b)]
     ro, rl = A.mla_latent_ref(f64(gqz), f64(x.q_pe), zs, kp, seqlens, x.scale)
     assert_out_close(f64(go), ro, "graph replay latent")
     assert_lse_close(f64(gl), rl, "graph replay lse")
@@ -124,8 +124,8 @@ def test_gqa_graph_replays(hkv, d, paged):
         torch.cuda.synchronize()
         assert torch.equal(go, eo) and torch.equal(gl, el)
     q, c = sets[-1]
-    ks = [f64(c.seq_rows(i, "k")) for i in range(b)]
-    vs = [f64(c.seq_rows(i, "v")) for i in range(b)]
+    ks = [gqa_rows(c, i, "k") for i in range(b)]
+    vs = [gqa_rows(c, i, "v") for i in range(b)]
     ro, rl = A.gqa_ref(f64(q), ks, vs, seqlens, 1 / math.sqrt(d))
     assert_out_close(f64(results[-1][0]), ro, "graph replay gqa")
     assert_lse_close(f64(results[-1][1]), rl, "graph replay gqa lse")

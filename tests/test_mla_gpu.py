@@ -11,7 +11,7 @@ import pytest
 import torch
 
 from oracle import attention as A
-from tests.helpers import assert_lse_close, assert_out_close, f64, qz_rounding_lse_bound
+from tests.helpers import mla_rows, as_device_bf16, assert_lse_close, assert_out_close, f64, qz_rounding_lse_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -50,8 +50,8 @@ def forward(inp):
 
 
 def seq_inputs(inp, seqs):
-    zs = [f64(inp.seq_rows(i, "z")) for i in seqs]
-    kp = [f64(inp.seq_rows(i, "kpe")) for i in seqs]
+    zs = [mla_rows(inp, i, "z") for i in seqs]
+    kp = [mla_rows(inp, i, "kpe") for i in seqs]
     return zs, kp
 
 
@@ -101,6 +101,8 @@ def test_tiny_workload():
     (2, 128, 2, [300, 40]),      # MTP s=2: two row tiles, causal
     (1, 64, 4, [97]),            # s=4
     (2, 8, 32, [64, 200]),       # s=32
+    (2, 16, 16, [300, 40]),      # s=16: two row tiles
+    (1, 128, 16, [200]),         # s=16 at h=128: 2048 rows, 16 row tiles, short context
 ])
 def test_dsv3_shapes_small(b, h, s, seqlens):
     inp = make(b, h, 128, 512, 64, s, seqlens, capacity=max(seqlens) + 5, seed=1)
@@ -128,8 +130,8 @@ def test_paged_vs_oracle_and_bitwise_contiguous():
     z = torch.zeros((3, cap, 512), dtype=torch.bfloat16, device=DEV)
     kpe = torch.zeros((3, cap, 64), dtype=torch.bfloat16, device=DEV)
     for i, L in enumerate(seqlens):
-        z[i, :L] = inp.seq_rows(i, "z")
-        kpe[i, :L] = inp.seq_rows(i, "kpe")
+        z[i, :L] = as_device_bf16(mla_rows(inp, i, "z"), z)
+        kpe[i, :L] = as_device_bf16(mla_rows(inp, i, "kpe"), kpe)
     sl = torch.tensor(seqlens, dtype=torch.int32, device=DEV)
     o2, l2 = da.mla_decode(res[2], inp.q_pe, z, kpe, sl, scale=inp.scale, max_seqlen=cap)
     torch.cuda.synchronize()
@@ -204,6 +206,17 @@ def test_full_size_mtp_s8_sampled():
     wl = W.WORKLOADS["mla_mtp_s8"]
     inp = make(wl.b, wl.heads, wl.d, wl.k, wl.p, wl.s, wl.seqlens(), seed=wl.seed)
     check(inp, forward(inp), seqs=[0, 31], what="mtp s8")
+
+
+@pytest.mark.parametrize("s", [16, 32])
+def test_full_size_mtp_sampled(s):
+    # b=32, h=128, t=4096 prior + s new tokens: 2048 / 4096 query rows per sequence
+    # (16 / 32 row tiles), the s-sweep's largest shapes
+    from decode_attention_18_b300 import workloads as W
+
+    wl = W.WORKLOADS[f"mla_mtp_s{s}"]
+    inp = make(wl.b, wl.heads, wl.d, wl.k, wl.p, wl.s, wl.seqlens(), seed=wl.seed)
+    check(inp, forward(inp), seqs=[0, 31], what=f"mtp s{s}")
 
 
 def test_multi_wave_split_grid_then_combine():

@@ -9,7 +9,7 @@ import pytest
 import torch
 
 from oracle import attention as A
-from tests.helpers import assert_lse_close, assert_out_close, f64
+from tests.helpers import mla_rows, assert_lse_close, assert_out_close, f64
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -41,8 +41,8 @@ def test_forced_timeout_reports_status_and_context_survives():
     # the same call afterwards runs normally and is correct
     qz, o, lse = _run(inp)
     assert da.check_errors() == 0
-    zs = [f64(inp.seq_rows(i, "z")) for i in range(2)]
-    kp = [f64(inp.seq_rows(i, "kpe")) for i in range(2)]
+    zs = [mla_rows(inp, i, "z") for i in range(2)]
+    kp = [mla_rows(inp, i, "kpe") for i in range(2)]
     ro, rl = A.mla_latent_ref(f64(qz), f64(inp.q_pe), zs, kp, inp.seqlens, inp.scale)
     assert_out_close(f64(o), ro, "after timeout")
     assert_lse_close(f64(lse), rl, "after timeout")

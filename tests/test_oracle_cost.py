@@ -125,3 +125,118 @@ def test_mtp_crosses_ridge_between_s1_and_s2():
     ai1 = cost.mla_flops(1, 128, 1, 4096, 512, 64) / cost.mla_bytes(1, 128, 1, 4096, 512, 64)
     ai2 = cost.mla_flops(1, 128, 2, 4096, 512, 64) / cost.mla_bytes(1, 128, 2, 4096, 512, 64)
     assert ai1 < r < ai2
+
+
+# ---------------------------------------------------------------------------
+# counts pinned against the tensors they describe: bytes are the nbytes of
+# arrays of a 2-byte type shaped as the method reads and writes them, FLOPs
+# are numpy's own count of the contraction (einsum_path) or a loop count.
+
+W2 = "float16"  # any 2-byte element type stands in for bf16
+
+
+def _nbytes(*shapes):
+    import numpy as np
+
+    return sum(np.zeros(sh, dtype=W2).nbytes for sh in shapes)
+
+
+def _einsum_flops(spec, *shapes):
+    """numpy's naive FLOP count of the contraction. The report prints four
+    significant digits, so the shapes are kept small enough to be exact."""
+    import numpy as np
+
+    ops = [np.zeros(sh) for sh in shapes]
+    report = np.einsum_path(spec, *ops, optimize="optimal")[1]
+    for line in report.splitlines():
+        if "Naive FLOP count" in line:
+            n = float(line.split(":")[1])
+            assert n < 1e4, "count too large to be printed exactly"
+            return int(round(n))
+    raise AssertionError(report)
+
+
+@pytest.mark.parametrize("b,h,s,din,dout", [(2, 3, 5, 4, 7), (32, 128, 1, 128, 512), (1, 1, 3, 512, 128)])
+def test_proj_flops_and_bytes_from_tensors(b, h, s, din, dout):
+    # absorb-style GEMM: activations [b,h,s,din] x weights [h,din,dout] -> [b,h,s,dout]
+    if 2 * b * h * s * din * dout < 10**4:
+        assert cost.proj_flops(b, h, s, din, dout) == _einsum_flops("bhsd,hdk->bhsk", (b, h, s, din), (h, din, dout))
+    n_madd = 0
+    for _ in range(b * h * s):          # one output row per (sequence, head, token)
+        for _ in range(dout):           # each output column
+            n_madd += din               # one multiply-add per reduction element
+    assert cost.proj_flops(b, h, s, din, dout) == 2 * n_madd
+    assert cost.proj_bytes(b, h, s, din, dout) == _nbytes((b, h, s, din), (h, din, dout), (b, h, s, dout))
+
+
+def test_split_latent_bytes_term_by_term():
+    # "Mla Analysis", Cost Models, MLAvar6+: the nine byte terms are, in order, the
+    # tensors the split method moves: q_pe [b,h,s,p], q_nope [b,h,s,d], Qz [b,h,s,k],
+    # old latents Z [b,o,k], RoPE keys of all t tokens [b,t,p], decompressed K and V
+    # of the n new tokens [b,h,n,d] each, the output [b,h,s,d] and the latent output
+    # [b,h,s,k]. Distinct primes make every term identifiable.
+    b, h, s, o, n, d, p, k = 2, 3, 5, 7, 11, 13, 17, 19
+    t = o + n
+    shapes = [(b, h, s, p), (b, h, s, d), (b, h, s, k), (b, o, k), (b, t, p), (b, h, n, d), (b, h, n, d),
+              (b, h, s, d), (b, h, s, k)]
+    assert cost.split_latent_bytes(b, h, s, o, n, d, p, k) == _nbytes(*shapes)
+    b, h, s, o, n, d, p, k = 1, 2, 3, 2, 3, 5, 7, 11  # small enough for exact FLOP reports
+    t = o + n
+    # FLOPs: RoPE scores over all t keys, scores + values over the n decompressed keys
+    # (d each), scores + values over the o latent keys (k each)
+    f = (_einsum_flops("bhsp,btp->bhst", (b, h, s, p), (b, t, p))
+         + 2 * _einsum_flops("bhsd,bhnd->bhsn", (b, h, s, d), (b, h, n, d))
+         + 2 * _einsum_flops("bhsk,bok->bhso", (b, h, s, k), (b, o, k)))
+    assert cost.split_latent_flops(b, h, s, o, n, d, p, k) == f
+
+
+def test_mla_and_fa_counts_from_tensors():
+    # FlashMLA bytes: Qz, q_pe in, O_lat out per row; Z and K_pe per cached token
+    b, h, s, t, k, p, d = 2, 3, 5, 7, 11, 13, 17
+    assert cost.mla_bytes(b, h, s, t, k, p) == _nbytes((b, h, s, k), (b, h, s, p), (b, h, s, k), (b, t, k), (b, t, p))
+    b, h, s, t, k, p = 1, 2, 3, 5, 7, 11
+    f = (_einsum_flops("bhsk,btk->bhst", (b, h, s, k), (b, t, k)) + _einsum_flops("bhsp,btp->bhst", (b, h, s, p), (b, t, p))
+         + _einsum_flops("bhst,btk->bhsk", (b, h, s, t), (b, t, k)))
+    assert cost.mla_flops(b, h, s, t, k, p) == f
+    b, h, s, t, k, p, d = 1, 2, 3, 5, 7, 11, 13
+    # FlashAttention over expanded keys [d + p] and values [d], per head
+    assert cost.fa_bytes(b, h, s, t, d, p) == _nbytes((b, h, s, d + p), (b, h, s, d), (b, h, t, d + p), (b, h, t, d))
+    d, p = 3, 2
+    f = (_einsum_flops("bhsc,bhtc->bhst", (b, h, s, d + p), (b, h, t, d + p))
+         + _einsum_flops("bhst,bhtd->bhsd", (b, h, s, t), (b, h, t, d)))
+    assert cost.fa_flops(b, h, s, t, d, p) == f
+
+
+def test_gqa_counts_from_tensors():
+    b, hq, hkv, s, t, d = 2, 6, 3, 5, 7, 8
+    assert cost.gqa_bytes(b, hq, hkv, s, t, d) == _nbytes((b, hq, s, d), (b, hq, s, d), (b, t, hkv, d), (b, t, hkv, d))
+    f = (_einsum_flops("bhsd,bhtd->bhst", (b, hq, s, d), (b, hq, t, d))
+         + _einsum_flops("bhst,bhtd->bhsd", (b, hq, s, t), (b, hq, t, d)))
+    assert cost.gqa_flops(b, hq, s, t, d) == f
+
+
+def test_mla_cache_bytes_per_token_layer():
+    # "MQA, GQA & MLA" lesson: the MLA cache holds one latent vector plus the decoupled
+    # RoPE key per token and layer; DeepSeek-V3 shapes (k = 512, p = 64) -> 1152 bytes
+    assert cost.mla_cache_bytes_per_token_layer(512, 64) == _nbytes((512,), (64,)) == 1152
+    assert cost.mla_cache_bytes_per_token_layer(64, 16) == _nbytes((1, 64), (1, 16))
+    # a grouped-head cache of the same token: K and V of every KV head
+    assert cost.kv_bytes_per_token_layer(8, 128) == _nbytes((8, 128), (8, 128))
+
+
+def test_roofline_time_and_attainable_by_hand():
+    # compute-bound: 2e12 FLOP at 1e15 FLOP/s = 2 ms beats 1e9 B at 1e12 B/s = 1 ms
+    assert cost.roofline_time(2e12, 1e9, 1e15, 1e12) == pytest.approx(2e-3)
+    # memory-bound: 1e12 FLOP (1 ms) vs 3e9 B (3 ms)
+    assert cost.roofline_time(1e12, 3e9, 1e15, 1e12) == pytest.approx(3e-3)
+    # attainable throughput, H100 row of the ridge table (989.5 TFLOP/s, 3.35 TB/s):
+    # AI 1 (FlashAttention decode) -> 3.35 TFLOP/s; AI 819 (s = 1024) -> the 989.5 peak
+    assert cost.attainable_flops(1.0, 989.5e12, 3.35e12) == pytest.approx(3.35e12)
+    assert cost.attainable_flops(819.0, 989.5e12, 3.35e12) == pytest.approx(989.5e12)
+    # at the ridge both limits meet
+    r = cost.ridge_point(989.5e12, 3.35e12)
+    assert cost.attainable_flops(r, 989.5e12, 3.35e12) == pytest.approx(989.5e12)
+    # time and throughput agree: flops / roofline_time == attainable(flops / bytes)
+    for fl, by in ((2e12, 1e9), (1e12, 3e9), (5e11, 5e8)):
+        assert fl / cost.roofline_time(fl, by, 989.5e12, 3.35e12) == pytest.approx(
+            cost.attainable_flops(fl / by, 989.5e12, 3.35e12))

@@ -159,10 +159,13 @@ size_t balanced_bytes(const GqaBalanced& gb, int d) {
          align256((size_t)gb.items * 2 * sizeof(int));
 }
 
-// --- latent MLA plan (one CTA per SM: its shared memory holds the 128-row query tile)
+// --- latent MLA plan: one cluster of two CTAs (each alone on its SM) per (sequence,
+// 128-row tile, chunk), so sms / 2 clusters run at once
 Plan mla_plan(int b, int s, int h, int k, int max_seqlen, int sms) {
-  const long long base = (long long)b * mla_latent_parts(k) * ceil_div((long long)h * s, 128);
-  return plan_splits(base, max_seqlen, sms, 384, 512, mla_tile_keys());
+  (void)k;
+  const long long base = (long long)b * ceil_div((long long)h * s, 128);
+  const int per = mla_ctas_per_row_tile();
+  return plan_splits(base, max_seqlen, sms / per > 0 ? sms / per : 1, 384, 512, mla_tile_keys());
 }
 
 }  // namespace

@@ -72,8 +72,8 @@ struct MlaLaunch {
   unsigned long long wait_ns;
   int test_timeout;
 };
-// latent-dimension partitions (CTAs) per 128-row tile for latent width k
-int mla_latent_parts(int k);
+// CTAs per 128-row tile of the latent kernel (a cluster: scores CTA + output CTA)
+int mla_ctas_per_row_tile();
 // keys per latent tile (context chunks are multiples of it)
 int mla_tile_keys();
 bool mla_supported(int k, int p);

@@ -106,10 +106,12 @@ Plan plan_splits(long long base, int max_seqlen, long long slots, int overhead_k
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-size_t partial_bytes(long long rows, int nsplit, int width) {
+// split partials: O [rows, nsplit, width] of elem_bytes each, then LSE [rows, nsplit] fp32
+size_t partial_bytes(long long rows, int nsplit, int width, size_t elem_bytes = sizeof(float)) {
   if (nsplit <= 1) return 0;
-  return align256((size_t)rows * nsplit * width * sizeof(float)) + align256((size_t)rows * nsplit * sizeof(float));
+  return align256((size_t)rows * nsplit * width * elem_bytes) + align256((size_t)rows * nsplit * sizeof(float));
 }
+constexpr size_t kMlaPartialBytes = 2;  // the latent kernel's O / l partials are bf16
 
 int check_kv(const decattn_kv& kv, int b, int max_seqlen) {
   if (kv.paged) {
@@ -280,7 +282,7 @@ int gqa_decode(const decattn_bf16* q, const decattn_bf16* k, const decattn_bf16*
                                 stream) != cudaSuccess)
       return DECATTN_ERR_CUDA;
   } else if (pl.nsplit > 1) {
-    if (launch_combine(a.ws_o, a.ws_lse, seqlens, (int)rows, hq * s, pl.nsplit, pl.chunk, d, out, lse, stream) !=
+    if (launch_combine(a.ws_o, false, a.ws_lse, seqlens, (int)rows, hq * s, pl.nsplit, pl.chunk, d, out, lse, stream) !=
         cudaSuccess)
       return DECATTN_ERR_CUDA;
   }
@@ -323,7 +325,7 @@ size_t mla_decode_workspace_size(int b, int s, int h, int k, int max_seqlen) {
   DeviceState* st = nullptr;
   if (device_state(&st)) return 0;
   const Plan pl = mla_plan(b, s, h, k, max_seqlen, st->sms);
-  return partial_bytes((long long)b * h * s, pl.nsplit, k);
+  return partial_bytes((long long)b * h * s, pl.nsplit, k, kMlaPartialBytes);
 }
 
 int mla_decode(const decattn_bf16* qz, const decattn_bf16* q_pe, const decattn_bf16* z, const decattn_bf16* k_pe,
@@ -342,7 +344,7 @@ int mla_decode(const decattn_bf16* qz, const decattn_bf16* q_pe, const decattn_b
   if (int rc = device_state(&st)) return rc;
   const Plan pl = mla_plan(b, s, h, k, max_seqlen, st->sms);
   const long long rows = (long long)b * h * s;
-  const size_t need = partial_bytes(rows, pl.nsplit, k);
+  const size_t need = partial_bytes(rows, pl.nsplit, k, kMlaPartialBytes);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return DECATTN_ERR_WORKSPACE;
   MlaLaunch a;
   a.qz = qz;
@@ -365,9 +367,9 @@ int mla_decode(const decattn_bf16* qz, const decattn_bf16* q_pe, const decattn_b
   a.scale = scale;
   a.o_lat = o_lat;
   a.lse = lse;
-  a.ws_o = pl.nsplit > 1 ? static_cast<float*>(workspace) : nullptr;
+  a.ws_o = pl.nsplit > 1 ? workspace : nullptr;
   a.ws_lse = pl.nsplit > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                                       align256((size_t)rows * pl.nsplit * k * sizeof(float)))
+                                                       align256((size_t)rows * pl.nsplit * k * kMlaPartialBytes))
                            : nullptr;
   a.err = st->err;
   a.wait_ns = wait_limit();
@@ -375,7 +377,7 @@ int mla_decode(const decattn_bf16* qz, const decattn_bf16* q_pe, const decattn_b
   g_last_splits.store(pl.nsplit);
   if (launch_mla_latent(a, stream) != cudaSuccess) return DECATTN_ERR_CUDA;
   if (pl.nsplit > 1) {
-    if (launch_combine(a.ws_o, a.ws_lse, seqlens, (int)rows, h * s, pl.nsplit, pl.chunk, k, o_lat, lse, stream) !=
+    if (launch_combine(a.ws_o, true, a.ws_lse, seqlens, (int)rows, h * s, pl.nsplit, pl.chunk, k, o_lat, lse, stream) !=
         cudaSuccess)
       return DECATTN_ERR_CUDA;
   }

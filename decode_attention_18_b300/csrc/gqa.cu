@@ -711,14 +711,26 @@ struct MergeCfg {
   static constexpr int ROWS = 256 / TPR;
 };
 
-// The threads of one row merge its n partials: partial c has its D floats at
+// Partial element loads: 8 consecutive values (fp32 or bf16 partials).
+__device__ __forceinline__ void load8(const float* p, float* v) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float* v) {
+  const uint4 a = *reinterpret_cast<const uint4*>(p);
+  v[0] = bf16_lo(a.x); v[1] = bf16_hi(a.x); v[2] = bf16_lo(a.y); v[3] = bf16_hi(a.y);
+  v[4] = bf16_lo(a.z); v[5] = bf16_hi(a.z); v[6] = bf16_lo(a.w); v[7] = bf16_hi(a.w);
+}
+
+// The threads of one row merge its n partials: partial c has its D values at
 // o0 + c * o_stride and its LSE at l0[c * l_stride]. Partials are taken U at a
 // time with all their loads issued before any use (one memory round trip per
 // group), merged with a running maximum; a partial with LSE = -inf saw no key and
 // is skipped. (U = 2 where there are at most two partials: fewer registers, more
-// blocks resident.)
-template <int D, int U = 4>
-__device__ __forceinline__ void merge_row(const float* __restrict__ o0, size_t o_stride, const float* __restrict__ l0,
+// blocks resident.) T is the partials' element type (fp32, or bf16 for the latent
+// kernel's O / l partials).
+template <int D, int U = 4, class T = float>
+__device__ __forceinline__ void merge_row(const T* __restrict__ o0, size_t o_stride, const float* __restrict__ l0,
                                           size_t l_stride, int n, __nv_bfloat16* __restrict__ out_row,
                                           float* __restrict__ lse_out, int t) {
   float M = -INFINITY, wsum = 0.f;
@@ -727,16 +739,15 @@ __device__ __forceinline__ void merge_row(const float* __restrict__ o0, size_t o
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
   for (int c0 = 0; c0 < n; c0 += U) {
     float lv[U];
-    float4 x0[U], x1[U];
+    float x[U][8];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       lv[u] = -INFINITY;
-      x0[u] = x1[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[u][e] = 0.f;
       if (c0 + u < n) {
         lv[u] = l0[(size_t)(c0 + u) * l_stride];
-        const float4* src = reinterpret_cast<const float4*>(o0 + (size_t)(c0 + u) * o_stride + 8 * t);
-        x0[u] = src[0];
-        x1[u] = src[1];
+        load8(o0 + (size_t)(c0 + u) * o_stride + 8 * t, x[u]);
       }
     }
     float mn = M;
@@ -752,14 +763,8 @@ __device__ __forceinline__ void merge_row(const float* __restrict__ o0, size_t o
       if (lv[u] == -INFINITY) continue;
       const float w = expf(lv[u] - mn);
       wsum += w;
-      acc[0] += w * x0[u].x;
-      acc[1] += w * x0[u].y;
-      acc[2] += w * x0[u].z;
-      acc[3] += w * x0[u].w;
-      acc[4] += w * x1[u].x;
-      acc[5] += w * x1[u].y;
-      acc[6] += w * x1[u].z;
-      acc[7] += w * x1[u].w;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += w * x[u][e];
     }
     M = mn;
   }
@@ -774,9 +779,8 @@ __device__ __forceinline__ void merge_row(const float* __restrict__ o0, size_t o
 }
 
 // Fixed chunks: row r merges partials c < ceil(L / chunk) of its sequence.
-template <int D, int U>
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ ws_o,
-                                                      const float* __restrict__ ws_lse,
+template <int D, int U, class T>
+__global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ ws_o, const float* __restrict__ ws_lse,
                                                       const int32_t* __restrict__ seqlens, int rows,
                                                       int rows_per_seq, int nsplit, int chunk,
                                                       __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
@@ -787,8 +791,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   if (row >= rows) return;
   const int L = seqlens[row / rows_per_seq];
   const int nv = L > 0 ? min(nsplit, (L + chunk - 1) / chunk) : 0;
-  merge_row<D, U>(ws_o + (size_t)row * nsplit * D, D, ws_lse + (size_t)row * nsplit, 1, nv, out + (size_t)row * D,
-                  lse_out ? lse_out + row : nullptr, threadIdx.x % M::TPR);
+  merge_row<D, U, T>(ws_o + (size_t)row * nsplit * D, D, ws_lse + (size_t)row * nsplit, 1, nv, out + (size_t)row * D,
+                     lse_out ? lse_out + row : nullptr, threadIdx.x % M::TPR);
 }
 
 // Combine for the balanced grouped-head schedule: row (bi, head j, token) belongs to
@@ -850,18 +854,16 @@ static cudaError_t launch_dependent(K kernel, int blocks, cudaStream_t stream, A
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-cudaError_t launch_combine(const float* ws_o, const float* ws_lse, const int32_t* seqlens, int rows,
-                           int rows_per_seq, int nsplit, int chunk, int d, void* out, float* lse,
-                           cudaStream_t stream) {
-  auto* o = static_cast<__nv_bfloat16*>(out);
-#define DECATTN_COMBINE_CASE(D)                                                                              \
-  case D:                                                                                                    \
-    if (cudaError_t e = nsplit <= 2 ? launch_dependent(combine_kernel<D, 2>, merge_blocks<D>(rows), stream, ws_o,  \
-                                                       ws_lse, seqlens, rows, rows_per_seq, nsplit, chunk, o, lse) \
-                                    : launch_dependent(combine_kernel<D, 4>, merge_blocks<D>(rows), stream, ws_o,  \
-                                                       ws_lse, seqlens, rows, rows_per_seq, nsplit, chunk, o, lse)) \
-      return e;                                                                                              \
-    break;
+template <class T>
+static cudaError_t launch_combine_t(const T* ws_o, const float* ws_lse, const int32_t* seqlens, int rows,
+                                   int rows_per_seq, int nsplit, int chunk, int d, __nv_bfloat16* o, float* lse,
+                                   cudaStream_t stream) {
+#define DECATTN_COMBINE_CASE(D)                                                                                 \
+  case D:                                                                                                       \
+    return nsplit <= 2 ? launch_dependent(combine_kernel<D, 2, T>, merge_blocks<D>(rows), stream, ws_o, ws_lse,  \
+                                          seqlens, rows, rows_per_seq, nsplit, chunk, o, lse)                    \
+                       : launch_dependent(combine_kernel<D, 4, T>, merge_blocks<D>(rows), stream, ws_o, ws_lse,  \
+                                          seqlens, rows, rows_per_seq, nsplit, chunk, o, lse);
   switch (d) {
     DECATTN_COMBINE_CASE(64)
     DECATTN_COMBINE_CASE(128)
@@ -870,7 +872,18 @@ cudaError_t launch_combine(const float* ws_o, const float* ws_lse, const int32_t
     default: return cudaErrorInvalidValue;
   }
 #undef DECATTN_COMBINE_CASE
-  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* ws_o, bool bf16_partials, const float* ws_lse, const int32_t* seqlens, int rows,
+                           int rows_per_seq, int nsplit, int chunk, int d, void* out, float* lse,
+                           cudaStream_t stream) {
+  auto* o = static_cast<__nv_bfloat16*>(out);
+  const cudaError_t e =
+      bf16_partials ? launch_combine_t(static_cast<const __nv_bfloat16*>(ws_o), ws_lse, seqlens, rows, rows_per_seq,
+                                       nsplit, chunk, d, o, lse, stream)
+                    : launch_combine_t(static_cast<const float*>(ws_o), ws_lse, seqlens, rows, rows_per_seq, nsplit,
+                                       chunk, d, o, lse, stream);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_combine_balanced(const float* ws_o, const float* ws_lse, const int* meta, const int32_t* seqlens,

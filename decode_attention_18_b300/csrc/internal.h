@@ -35,9 +35,10 @@ int gqa_ctas_per_sm(int d);
 int gqa_balanced_ctas_per_sm(int d, int rows);  // measured occupancy of the balanced kernel
 cudaError_t launch_gqa(const GqaLaunch& p, cudaStream_t stream);
 
-// log-sum-exp merge of split partials: rows x nsplit partials of width d
-cudaError_t launch_combine(const float* ws_o, const float* ws_lse, const int32_t* seqlens, int rows, int rows_per_seq,
-                           int nsplit, int chunk, int d, void* out, float* lse, cudaStream_t stream);
+// log-sum-exp merge of split partials: rows x nsplit partials of width d (fp32, or bf16
+// when bf16_partials) and their fp32 LSEs
+cudaError_t launch_combine(const void* ws_o, bool bf16_partials, const float* ws_lse, const int32_t* seqlens, int rows,
+                           int rows_per_seq, int nsplit, int chunk, int d, void* out, float* lse, cudaStream_t stream);
 // combine of the balanced grouped-head schedule (see gqa_balanced_kernel)
 cudaError_t launch_combine_balanced(const float* ws_o, const float* ws_lse, const int* meta, const int32_t* seqlens,
                                     int b, int hq, int s, int hkv, int d, long long records, void* out, float* lse,
@@ -66,7 +67,7 @@ struct MlaLaunch {
   float scale;
   void* o_lat;
   float* lse;
-  float* ws_o;    // [b*h*s, nsplit, k]
+  void* ws_o;     // [b*h*s, nsplit, k] bf16 O / l partials
   float* ws_lse;  // [b*h*s, nsplit]
   unsigned* err;
   unsigned long long wait_ns;

@@ -13,30 +13,34 @@
 //   * Tensor Memory (128 lanes x 512 fp32 columns per SM) holds exactly the
 //     fp32 O_lat of 128 rows x k = 512, so the work is split by role instead of
 //     by output columns (which would make both CTAs compute the same scores):
-//       - the S CTA (cluster rank 0) keeps Q' = [Qz | q_pe] of its 128 rows in
-//         Tensor Memory (288 columns) as the A operand and computes
-//         S = Q' K'^T one 64-key tile (one page) at a time into three 64-column
-//         S buffers (tcgen05.mma kind::f16, M=128 N=64, B = the K' chunks in
-//         shared memory); four softmax warps (thread = row) turn S into P (bf16)
-//         and ship it, with the row rescale factors, to the O CTA's shared memory
-//         in one bulk copy per tile (cp.async.bulk shared::cta -> shared::cluster,
-//         completing on the O CTA's mbarrier);
+//       - the S CTA (cluster rank 0) keeps Qz of its 128 rows in Tensor Memory
+//         (256 columns, the A operand) and q_pe in shared memory, and computes
+//         S = Qz Z^T + q_pe K_pe^T one 128-key tile (two pages) at a time into
+//         two 128-column S buffers (tcgen05.mma kind::f16, M=128 N=128, B = the
+//         cache chunks in shared memory); eight softmax warps (thread = row, each
+//         warp half of a tile's keys, row maxima exchanged through shared memory)
+//         turn S into P (bf16) and ship it with the row rescale factors to the O
+//         CTA's shared memory in one bulk copy per tile (cp.async.bulk
+//         shared::cta -> shared::cluster, completing on the O CTA's mbarrier);
 //       - the O CTA (rank 1) keeps the whole fp32 O_lat [128 x 512] in Tensor
 //         Memory and accumulates O += P Z (M=128 N=256 K=16, A = P and B = the
 //         Z slab, both in shared memory), streaming Z itself; its MMA commits
 //         free the P buffers of the S CTA (a commit multicast to its mbarrier).
 //     Every cache byte enters each SM's shared memory once per tile, and the
 //     scores are computed once ("Cost Models", FlashMLA FLOP count).
-//   * Cache tiles are 64 keys, one page of a paged pool: TMA boxes of
-//     [64 keys x 64 dims] (128-byte swizzle) feed an S-ring (3 chunks per item)
-//     and an O-ring ([64 keys x 256 columns] per item).
+//   * The query tile reaches Tensor Memory through the S ring's first lap: TMA
+//     boxes of [128 rows x 64] land in the ring slots and the softmax warps move
+//     them (shared -> registers -> tcgen05.st) before the slots carry cache.
+//   * Cache chunks are [128 keys x 64 dims], two TMA boxes of one 64-token
+//     page each (128-byte swizzle); the O ring carries [64 keys x 256 columns].
 //   * Online softmax with a lazily moved reference maximum: a row's reference
 //     moves only when its maximum grows past it by 2^8 (P stays below 256); the
 //     O CTA then rescales those rows of O in Tensor Memory before the tile's
 //     MMAs (rare after the first tile). Exponentials use ex2.approx.
 //   * Keys past a row's causal limit (token i of s sees keys 0 .. L - s + i)
 //     are masked in the softmax; Z rows past the sequence end are zeroed in
-//     shared memory before the O MMAs (a cache may hold anything there).
+//     shared memory before the O MMAs (a cache may hold anything there), and
+//     the second page of a last tile that lies wholly past the end is skipped.
 //   * Output: with one chunk, bf16 O_lat and the LSE directly; otherwise fp32
 //     partials (O / l, LSE) merged by the combine kernel. The S CTA writes the
 //     LSE, the O CTA the rows (staged through shared memory, whole row segments).
@@ -56,86 +60,103 @@ namespace decattn {
 
 namespace {
 
-constexpr int TK = 64;                     // keys per tile (one 64-token page)
+constexpr int TK = 128;                    // keys per tile (two 64-token pages)
+constexpr int HK = 64;                     // keys per page / per TMA box / per softmax warp
 constexpr int BM = 128;                    // query rows per row tile (MMA M)
-constexpr int NSB = 3;                     // S buffers in Tensor Memory (S CTA)
+constexpr int NSB = 2;                     // S buffers in Tensor Memory (S CTA)
 constexpr int NMSG = 2;                    // P message buffers (staging in S, landing in O)
-constexpr int NSMW = 4;                    // softmax warps (S) / rescale + epilogue warps (O)
+constexpr int NSMW = 8;                    // softmax warps (S) / rescale + epilogue warps (O)
 constexpr int NTHREADS = 32 * (2 + NSMW);  // producer, MMA issuer, NSMW row warps
-constexpr int CHUNK = TK * 128;            // one [64 keys x 64 dims] box, 128-byte rows
-constexpr int P_TILE = BM * TK * 2;        // P [128 rows x 64 keys] bf16, K-major, 128-byte swizzle
-constexpr int MSG_ALPHA = P_TILE;          // [128] float row rescale factors
-constexpr int MSG_FLAGS = MSG_ALPHA + BM * 4;  // [NSMW] per-warp "a row was rescaled" words
+constexpr int HALF_BOX = HK * 128;         // one [64 keys x 64 dims] box, 128-byte rows
+constexpr int CHUNK = TK * 128;            // one [128 keys x 64 dims] chunk (two boxes)
+constexpr int P_BLK = BM * HK * 2;         // P [128 rows x 64 keys] bf16, K-major, 128-byte swizzle
+constexpr int MSG_ALPHA = 2 * P_BLK;       // [128] float row rescale factors
+constexpr int MSG_FLAGS = MSG_ALPHA + BM * 4;  // [4] per-quadrant "a row was rescaled" words
 constexpr int MSG_BYTES = MSG_FLAGS + 16;
-constexpr int MSG_STRIDE = 17 * 1024;      // 1024-byte aligned message slots
+constexpr int MSG_STRIDE = 34 * 1024;      // 1024-byte aligned message slots
 constexpr int FIN_BYTES = BM * 4;          // [128] float 1/l, sent once at the end
-constexpr int S_NR = 7;                    // S-ring slots
-constexpr int O_NR = 5;                    // O-ring slots
+constexpr int S_NR = 3;                    // S-ring slots (CPI chunks each)
+constexpr int O_NR = 4;                    // O-ring slots
+constexpr int PF = 2;                      // S CTA: L2 prefetch distance in tiles
+constexpr int SB0 = 256;                   // first S buffer column (Qz holds columns 0 .. k/2-1)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.f;                        // move the reference max only past 2^8
 constexpr unsigned long long kTeardownNs = 1000000000ull;  // 1 s for own copies / MMAs at exit
 constexpr unsigned long long kTestWaitNs = 1000000ull;     // 1 ms forced-timeout wait
 constexpr uint32_t kRankS = 0, kRankO = 1;
-constexpr int kBarA = 1, kBarB = 2;        // named barriers of the softmax warps
+constexpr int kBarA = 1, kBarB = 2;        // named barriers of the row warps
 
 static_assert(MSG_BYTES % 16 == 0 && MSG_BYTES <= MSG_STRIDE, "message");
+static_assert(SB0 + NSB * TK <= 512, "tensor memory");
 
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
 template <int KL, int P>
 struct MlaCfg {
-  static constexpr int NBL = KL / 64;                   // latent chunks per tile
+  static constexpr int NBL = KL / 64;                   // latent chunks per tile (= query boxes)
   static constexpr int NCH = NBL + 1;                   // + the RoPE chunk
-  static constexpr int CPI = NCH % 3 == 0 ? 3 : NCH;    // chunks per S-ring item
+  // chunks per S-ring item: each wait / commit of the ring costs ~250 cycles of the issuing
+  // warp, so an item carries 12 MMAs (3 chunks x 4 k-steps) where the tile allows
+  static constexpr int CPI = NCH % 3 == 0 ? 3 : NCH;
   static constexpr int NITEM = NCH / CPI;               // S-ring items per tile
   static constexpr int S_ITEM = CPI * CHUNK;
+  static constexpr int QS = (NBL + CPI - 1) / CPI;      // ring slots of the query lap
+  static constexpr int LAT0 = NBL < CPI ? NBL : CPI;    // latent chunks of a full S-ring item
+  static constexpr int LATL = NBL - (NITEM - 1) * CPI;  // latent chunks of a tile's last item (+ RoPE)
   static constexpr int PE_ROW = P * 2;                  // bytes per RoPE row
   static constexpr uint32_t PE_SWZ = PE_ROW == 128 ? kSw128 : (PE_ROW == 64 ? kSw64 : kSw32);
-  static constexpr int PE_BOX = TK * PE_ROW;
+  static constexpr int PE_HALF = HK * PE_ROW;           // one RoPE box (64 keys)
   static constexpr int ON = KL < 256 ? KL : 256;        // O MMA N (columns per O-ring item)
   static constexpr int NH = KL / ON;                    // O column blocks
-  static constexpr int O_ITEM = TK * ON * 2;            // [64 keys x ON columns]
-  static constexpr int QC = (KL + P) / 2;               // Tensor Memory columns of Q'
-  static constexpr int SB0 = (QC + 31) & ~31;           // first S buffer column
-  static constexpr int OFF_MSG = 0;                     // same offset in both CTAs (peer-addressed)
-  static constexpr int OFF_RING = NMSG * MSG_STRIDE;
-  static constexpr int RING_END = cmax(OFF_RING + S_NR * S_ITEM, OFF_RING + O_NR * O_ITEM);
-  static constexpr int OFF_FIN = RING_END;              // same offset in both CTAs
-  static constexpr int OFF_BAR = OFF_FIN + FIN_BYTES;   // same offset in both CTAs
+  static constexpr int O_ITEM = HK * ON * 2;            // [64 keys x ON columns]
+  static constexpr int OCOLS = KL / 2;                  // O columns per row warp (rescale, epilogue)
+  static constexpr int PASS = OCOLS < 128 ? OCOLS : 128;  // epilogue staging pass (columns)
+  // S CTA: one P staging slot, q_pe, the S-ring
+  static constexpr int OFF_STG = 0;
+  static constexpr int OFF_QPE = MSG_STRIDE;
+  static constexpr int OFF_SRING = OFF_QPE + ((BM * PE_ROW + 1023) & ~1023);
+  // O CTA: NMSG message slots (written by the S CTA's copies), the O-ring
+  static constexpr int OFF_MSG = 0;
+  static constexpr int OFF_ORING = NMSG * MSG_STRIDE;
+  // both: 1/l, the row-statistics exchange and the barriers at the same offsets (peer-addressed)
+  static constexpr int OFF_FIN = cmax(OFF_SRING + S_NR * S_ITEM, OFF_ORING + O_NR * O_ITEM);
+  static constexpr int OFF_RED = OFF_FIN + FIN_BYTES;   // row maxima [2][2][128], row sums [2][128]
+  static constexpr int OFF_BAR = OFF_RED + 6 * BM * 4;  // same offset in both CTAs
   static constexpr int SMEM = OFF_BAR + 512;
-  static_assert(KL % 64 == 0 && KL % ON == 0 && ON % 16 == 0 && ON <= 256, "latent width");
+  static_assert(KL % 64 == 0 && KL / 2 <= SB0 && KL % ON == 0 && ON % 16 == 0 && ON <= 256, "latent width");
+  static_assert(NCH % CPI == 0 && 2 * CPI <= 8 && QS <= S_NR && LATL >= 1, "S-ring items");
   static_assert(P % 16 == 0 && PE_ROW <= 128, "rope width");
-  static_assert(NCH % CPI == 0 && CPI <= 32, "S-ring items");
-  static_assert(SB0 + NSB * TK <= 512 && KL <= 512, "tensor memory");
-  static_assert(S_ITEM % 1024 == 0 && O_ITEM % 1024 == 0 && OFF_RING % 1024 == 0, "swizzle alignment");
-  static_assert(4 * 32 * 512 <= O_NR * O_ITEM || KL < 128, "epilogue staging");
+  static_assert(OCOLS % 32 == 0 && OCOLS % PASS == 0, "row-warp columns");
+  static_assert(NSMW * 32 * PASS * 4 <= O_NR * O_ITEM, "epilogue staging");
+  static_assert(OFF_SRING % 1024 == 0 && OFF_ORING % 1024 == 0 && O_ITEM % 1024 == 0 && OFF_QPE % 1024 == 0,
+                "swizzle alignment");
   static_assert(SMEM <= 232448, "shared memory");
 };
 
 // barrier slots (8 bytes each) at OFF_BAR, the same in both CTAs
 enum : int {
-  B_FULL = 0,       // [S_NR] ring item landed
-  B_EMPTY = 7,      // [S_NR] ring item consumed
-  B_SFULL = 14,     // [NSB] S tile in Tensor Memory (S CTA)
-  B_SEMPTY = 17,    // [NSB] S tile read by the softmax warps (S CTA)
+  B_FULL = 0,       // [8] ring item landed
+  B_EMPTY = 8,      // [8] ring item consumed
+  B_SFULL = 16,     // [NSB] S tile in Tensor Memory (S CTA)
+  B_SEMPTY = 18,    // [NSB] S tile read by the softmax warps (S CTA)
   B_PFULL = 20,     // [NMSG] P message landed (O CTA; the S CTA's copy completes on it)
   B_PFREE = 22,     // [NMSG] O CTA's MMAs done with message buffer (S CTA; O's commit arrives)
-  B_QREADY = 24,    // Q' in Tensor Memory (S CTA)
-  B_FINFULL = 25,   // 1/l landed (O CTA)
-  B_ODONE = 26,     // every O MMA issued before a rescale complete (O CTA)
-  B_OFINAL = 27,    // every O MMA complete (O CTA)
-  B_CREQ = 28,      // rescale request (or end marker) for the row warps (O CTA)
-  B_CDONE = 29,     // rescale done (O CTA)
-  B_TEST = 30,      // never signalled: the forced-timeout test waits on it
-  B_FIN = 31,       // teardown: every tcgen05 op of the MMA issuer complete
-  B_COUNT = 32
+  B_QREADY = 24,    // Qz in Tensor Memory (S CTA)
+  B_QPE = 25,       // q_pe landed (S CTA)
+  B_FINFULL = 26,   // 1/l landed (O CTA)
+  B_ODONE = 27,     // every O MMA issued before a rescale complete (O CTA)
+  B_OFINAL = 28,    // every O MMA complete (O CTA)
+  B_CREQ = 29,      // rescale request (or end marker) for the row warps (O CTA)
+  B_CDONE = 30,     // rescale done (O CTA)
+  B_TEST = 31,      // never signalled: the forced-timeout test waits on it
+  B_FIN = 32,       // teardown: every tcgen05 op of the MMA issuer complete
+  B_COUNT = 33
 };
-static_assert(S_NR <= 7 && O_NR <= 7, "ring barrier slots");
+static_assert(S_NR <= 8 && O_NR <= 8, "ring barrier slots");
 
 struct MlaParams {
-  const __nv_bfloat16* qz;
-  const __nv_bfloat16* q_pe;
+  __nv_bfloat16* ws_ob;  // bf16 O / l partials [b*h*s, nsplit, k]
   const int32_t* seqlens;
   const int32_t* block_table;
   int max_pages, paged, capacity, num_pages;
@@ -143,15 +164,14 @@ struct MlaParams {
   float scale_log2;
   __nv_bfloat16* o_lat;
   float* lse;
-  float* ws_o;
   float* ws_lse;
   unsigned* err;
   unsigned long long wait_ns;
   int test_timeout;
 };
 
-// cache row of `key` of sequence bi (paged: through the block table; a tile never
-// crosses a page because tiles and pages are both 64 keys and chunks are whole tiles)
+// cache row of `key` of sequence bi (paged: through the block table; a 64-key box never
+// crosses a page because boxes and pages are both 64 keys and chunks are whole tiles)
 __device__ __forceinline__ int cache_row(const MlaParams& p, int bi, int key) {
   if (p.paged) {
     int page = p.block_table[(size_t)bi * p.max_pages + key / 64];
@@ -183,9 +203,23 @@ struct RingPos {
   }
 };
 
-template <int KL, int P>
+// Tensor maps (all bf16, 128-byte swizzle):
+//   tm_q3   Qz viewed as {64 columns, rows, k/64 chunks} (strides: row k*2 B, chunk 128 B),
+//           box {64, 128, LAT0}: one box per query-lap slot, chunk-major as the MMAs read it
+//   tm_qpe  q_pe [rows, p], box [128 rows, p]
+//   tm_za / tm_zb   contiguous cache: Z viewed like Qz, boxes {64, 128, LAT0} / {64, 128, LATL}
+//           (one box per S-ring item); paged pool: Z [rows, k] with boxes [64 rows, 64] (one
+//           box per chunk and page), tm_zb unused
+//   tm_kpe  K_pe [rows, p], box [128 rows, p] (contiguous) or [64 rows, p] (paged)
+//   tm_zo   Z viewed like Qz, box {64, 64, ON/64}: one [64 keys x ON columns] O-ring item
+// TMA serves about one box per few hundred cycles per SM (a single issuing thread half that),
+// whatever its size up to tens of KB, so the cache streams use the largest boxes the layout
+// allows.
+template <int KL, int P, bool PAGED>
 __global__ void __launch_bounds__(NTHREADS, 1)
-    mla_pair_kernel(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_kpe,
+    mla_pair_kernel(const __grid_constant__ CUtensorMap tm_q3, const __grid_constant__ CUtensorMap tm_qpe,
+                    const __grid_constant__ CUtensorMap tm_za, const __grid_constant__ CUtensorMap tm_zb,
+                    const __grid_constant__ CUtensorMap tm_kpe, const __grid_constant__ CUtensorMap tm_zo,
                     MlaParams p) {
   using C = MlaCfg<KL, P>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -207,7 +241,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   // ---- set-up that touches no global memory (overlaps the previous kernel's end)
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 7; ++i) {
+    for (int i = 0; i < 8; ++i) {
       mbar_init(&bars[B_FULL + i], 1);
       mbar_init(&bars[B_EMPTY + i], 1);
     }
@@ -219,7 +253,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&bars[B_PFULL + i], 1);
       mbar_init(&bars[B_PFREE + i], 1);
     }
-    mbar_init(&bars[B_QREADY], NSMW);
+    mbar_init(&bars[B_QREADY], 1);
+    mbar_init(&bars[B_QPE], 1);
     mbar_init(&bars[B_FINFULL], 1);
     mbar_init(&bars[B_ODONE], 1);
     mbar_init(&bars[B_OFINAL], 1);
@@ -234,8 +269,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tm_z);
+    prefetch_tmap(&tm_q3);
+    prefetch_tmap(&tm_qpe);
+    prefetch_tmap(&tm_za);
+    prefetch_tmap(&tm_zb);
     prefetch_tmap(&tm_kpe);
+    prefetch_tmap(&tm_zo);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -286,16 +325,65 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // =====================================================================================
     // S CTA
     if (warp == 0) {
-      // ------------------------------------------------ producer: K' chunks into the S-ring
-      // The whole warp walks the items (warp-uniform values); lane 0 arms the item's
-      // barrier and lanes 0..CPI-1 each request one chunk box.
+      // ------------------------------------------------ producer: query tile, then cache chunks
+      // The whole warp walks the items (warp-uniform values, block-table entries read by
+      // every lane); one lane arms an item's barrier and one lane per box requests it. The
+      // issuing lanes rotate (independent request streams), and tiles PF ahead are
+      // prefetched into L2, which keeps more of the cache stream in flight than the ring
+      // itself can hold.
       RingPos<S_NR> rp;
       int ic = 0;
       int last[S_NR];
       for (int i = 0; i < S_NR; ++i) last[i] = -1;
       bool ok = true;
+      auto prefetch_tile = [&](int t) {
+        const int key0 = kstart + t * TK;
+        if (t >= ntiles || key0 >= kend) return;
+        if constexpr (PAGED) {
+          const bool two = kend - key0 > HK;
+          const int k = lane;  // box k: chunk k / 2, page k % 2
+          if (k < 2 * C::NCH && (two || (k & 1) == 0)) {
+            const int row = cache_row(p, bi, key0 + (k & 1) * HK);
+            if (k / 2 == C::NBL)
+              tma_prefetch_l2_2d(&tm_kpe, 0, row);
+            else
+              tma_prefetch_l2_2d(&tm_za, (k / 2) * 64, row);
+          }
+        } else {
+          const int row = cache_row(p, bi, key0);
+          if (lane < C::NITEM - 1)
+            tma_prefetch_l2_3d(&tm_za, 0, row, lane * C::CPI);
+          else if (lane == C::NITEM - 1)
+            tma_prefetch_l2_3d(&tm_zb, 0, row, lane * C::CPI);
+          else if (lane == C::NITEM)
+            tma_prefetch_l2_2d(&tm_kpe, 0, row);
+        }
+      };
+      if (ntiles > 0) {
+        // first lap: the query tile (chunk-major boxes of CPI chunks, moved into Tensor
+        // Memory by the softmax warps, which then free the slots) and q_pe in its own region
+        if (lane == 0) {
+          mbar_expect_tx(&bars[B_QPE], BM * C::PE_ROW);
+          tma_load_2d(sb + C::OFF_QPE, &tm_qpe, 0, qrow0, &bars[B_QPE]);
+        }
+        for (int qs = 0; qs < C::QS; ++qs) {
+          const int slot = rp.slot;
+          rp.advance();
+          last[slot] = ic++;
+          if (lane == 1 + qs) {  // a box's chunks past the last one read as zeros (and count in full)
+            mbar_expect_tx(&bars[B_FULL + slot], C::LAT0 * CHUNK);
+            tma_load_3d(sb + C::OFF_SRING + slot * C::S_ITEM, &tm_q3, 0, qrow0, qs * C::CPI, &bars[B_FULL + slot]);
+          }
+          __syncwarp();
+        }
+        for (int t = 0; t < PF; ++t) prefetch_tile(t);
+      }
       for (int t = 0; ok && t < ntiles; ++t) {
-        const int row0 = cache_row(p, bi, kstart + t * TK);
+        const int key0 = kstart + t * TK;
+        const bool two = kend - key0 > HK;  // the tile's second page holds keys of the chunk
+        const int row0 = cache_row(p, bi, key0);
+        const int row1 = (PAGED && two) ? cache_row(p, bi, key0 + HK) : 0;
+        prefetch_tile(t + PF);
         for (int it = 0; it < C::NITEM; ++it) {
           const int slot = rp.slot;
           const uint32_t prev = rp.phase ^ 1u;
@@ -304,18 +392,38 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ok = false;
             break;
           }
-          last[slot] = ic++;
-          const bool has_pe = it == C::NITEM - 1;
-          const uint32_t bytes = has_pe ? (C::CPI - 1) * CHUNK + C::PE_BOX : C::CPI * CHUNK;
-          if (lane == 0) mbar_expect_tx(&bars[B_FULL + slot], bytes);
-          __syncwarp();
-          if (lane < C::CPI) {
-            const int j = it * C::CPI + lane;
-            const uint32_t dst = sb + C::OFF_RING + slot * C::S_ITEM + lane * CHUNK;
-            if (j < C::NBL)
-              tma_load_2d(dst, &tm_z, j * 64, row0, &bars[B_FULL + slot]);
-            else
-              tma_load_2d(dst, &tm_kpe, 0, row0, &bars[B_FULL + slot]);
+          const bool has_pe = it == C::NITEM - 1;  // the RoPE chunk is the tile's last
+          const uint32_t base = sb + C::OFF_SRING + slot * C::S_ITEM;
+          if constexpr (PAGED) {
+            const int lb = (ic & 3) * 8;  // first issuing lane of this item
+            last[slot] = ic++;
+            const uint32_t bytes =
+                ((has_pe ? (C::CPI - 1) * HALF_BOX + C::PE_HALF : C::CPI * HALF_BOX)) * (two ? 2 : 1);
+            if (lane == lb) mbar_expect_tx(&bars[B_FULL + slot], bytes);
+            __syncwarp();
+            const int k = lane - lb;  // box k: chunk it*CPI + k/2 of the tile, page k % 2
+            if (k >= 0 && k < 2 * C::CPI && (two || (k & 1) == 0)) {
+              const int c = it * C::CPI + k / 2;
+              const bool pe = c == C::NBL;
+              const uint32_t dst = base + (k / 2) * CHUNK + (k & 1) * (pe ? C::PE_HALF : HALF_BOX);
+              const int row = (k & 1) ? row1 : row0;
+              if (pe)
+                tma_load_2d(dst, &tm_kpe, 0, row, &bars[B_FULL + slot]);
+              else
+                tma_load_2d(dst, &tm_za, c * 64, row, &bars[B_FULL + slot]);
+            }
+          } else {
+            // one box of the item's latent chunks [128 keys x 64] x LAT (rows past the
+            // sequence are read as they are and masked), plus the RoPE box on the last item
+            const int lb = (ic & 1) * 2;
+            last[slot] = ic++;
+            const int lat = has_pe ? C::LATL : C::LAT0;
+            if (lane == lb) {
+              mbar_expect_tx(&bars[B_FULL + slot], lat * CHUNK + (has_pe ? BM * C::PE_ROW : 0));
+              tma_load_3d(base, has_pe ? &tm_zb : &tm_za, 0, row0, it * C::CPI, &bars[B_FULL + slot]);
+            }
+            __syncwarp();
+            if (has_pe && lane == lb + 1) tma_load_2d(base + lat * CHUNK, &tm_kpe, 0, row0, &bars[B_FULL + slot]);
           }
           __syncwarp();
         }
@@ -324,26 +432,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!ok && !*abort_flag) fail();
         for (int i = 0; i < S_NR; ++i)  // no copy may still be landing when the CTA exits
           if (last[i] >= 0) mbar_wait(&bars[B_FULL + i], (last[i] / S_NR) & 1, kTeardownNs, nullptr);
+        if (ntiles > 0) mbar_wait(&bars[B_QPE], 0, kTeardownNs, nullptr);
       }
       __syncwarp();
     } else if (warp == 1) {
-      // ------------------------------------------------ MMA issuer: S = Q' K'^T
-      bool ok = ntiles == 0 || warp_wait(&bars[B_QREADY], 0, p.wait_ns, abort_flag);
+      // ------------------------------------------------ MMA issuer: S = Qz Z^T + q_pe K_pe^T
+      bool ok = ntiles == 0 || (warp_wait(&bars[B_QREADY], 0, p.wait_ns, abort_flag) &&
+                                warp_wait(&bars[B_QPE], 0, p.wait_ns, abort_flag));
       if (ok && ntiles > 0 && p.test_timeout) ok = warp_wait(&bars[B_TEST], 0, kTestWaitNs, abort_flag);
-      tc_fence_after();  // Q' was written to Tensor Memory by the softmax warps
+      tc_fence_after();  // Qz was written to Tensor Memory by the softmax warps
       const bool leader = elect_one();
       constexpr uint32_t idS = idesc_bf16_f32(BM, TK, false, false);
-      const uint64_t dring = smem_desc(sb + C::OFF_RING, 16, 1024, kSw128);
-      const uint64_t dring_pe = smem_desc(sb + C::OFF_RING, 16, 8 * C::PE_ROW, C::PE_SWZ);
+      const uint64_t dring = smem_desc(sb + C::OFF_SRING, 16, 1024, kSw128);
+      const uint64_t dring_pe = smem_desc(sb + C::OFF_SRING, 16, 8 * C::PE_ROW, C::PE_SWZ);
+      const uint64_t dqpe = smem_desc(sb + C::OFF_QPE, 16, 8 * C::PE_ROW, C::PE_SWZ);
       RingPos<S_NR> rp;
+      for (int j = 0; j < C::QS; ++j) rp.advance();  // the first lap carried the query tile
       for (int t = 0; ok && t < ntiles; ++t) {
-        const int buf = t % NSB;
-        if (t >= NSB && !warp_wait(&bars[B_SEMPTY + buf], ((t / NSB) - 1) & 1, p.wait_ns, abort_flag)) {
+        const int buf = t & 1;
+        if (t >= NSB && !warp_wait(&bars[B_SEMPTY + buf], ((t >> 1) - 1) & 1, p.wait_ns, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();  // the softmax warps' loads of this buffer come first
-        const uint32_t d_s = tmem + C::SB0 + buf * TK;
+        const uint32_t d_s = tmem + SB0 + buf * TK;
         for (int it = 0; it < C::NITEM; ++it) {
           const int slot = rp.slot;
           const uint32_t ph = rp.phase;
@@ -354,17 +466,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           if (leader) {
 #pragma unroll
-            for (int c = 0; c < C::CPI; ++c) {
-              const int j = it * C::CPI + c;
-              const uint64_t so = (uint64_t)((slot * C::S_ITEM + c * CHUNK) >> 4);
+            for (int cc = 0; cc < C::CPI; ++cc) {
+              const int j = it * C::CPI + cc;
+              const uint64_t so = (uint64_t)((slot * C::S_ITEM + cc * CHUNK) >> 4);
               if (j < C::NBL) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                   tc_mma_ts(d_s, tmem + j * 32 + kk * 8, dring + so + 2 * kk, idS, (j | kk) ? 1u : 0u);
               } else {
 #pragma unroll
-                for (int kk = 0; kk < P / 16; ++kk)
-                  tc_mma_ts(d_s, tmem + KL / 2 + kk * 8, dring_pe + so + 2 * kk, idS, 1u);
+                for (int kk = 0; kk < P / 16; ++kk) tc_mma_ss(d_s, dqpe + 2 * kk, dring_pe + so + 2 * kk, idS, 1u);
               }
             }
             tc_commit(&bars[B_EMPTY + slot]);
@@ -382,8 +493,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       __syncwarp();
     } else {
-      // ------------------------------------------------ Q' load, softmax, P messages (warps 2-5)
-      const int q = warp & 3;  // Tensor Memory lane quadrant this warp may access
+      // ------------------------------------------------ query move, softmax, P messages (warps 2-9)
+      const int q = warp & 3;            // Tensor Memory lane quadrant this warp may access
+      const int hh = (warp - 2) >> 2;    // half of each tile's keys (and of the query boxes) of this warp
       const int r = q * 32 + lane;
       const int row_in_seq = mt * BM + r;
       const bool row_ok = row_in_seq < p.rows;
@@ -391,58 +503,55 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint32_t t_lane = tmem + ((uint32_t)(q * 32) << 16);
       const size_t grow = (size_t)qrow0 + r;
       const bool issuer = warp == 2 && lane == 0;
+      float* red = reinterpret_cast<float*>(smem + C::OFF_RED);  // maxima [parity][half][row], then sums [half][row]
+      bool ok = ntiles > 0;
       if (ntiles > 0) {
-        // Q' row r into Tensor Memory (A operand: lane = row, two bf16 per column, even k low)
-#pragma unroll 1
-        for (int c0 = 0; c0 < C::NBL; ++c0) {
-          uint32_t v[32];
-          const uint4* src = reinterpret_cast<const uint4*>(p.qz + grow * KL + c0 * 64);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const uint4 x = row_ok ? __ldg(src + e) : make_uint4(0, 0, 0, 0);
-            v[4 * e] = x.x;
-            v[4 * e + 1] = x.y;
-            v[4 * e + 2] = x.z;
-            v[4 * e + 3] = x.w;
+        // Qz row r into Tensor Memory (A operand: lane = row, two bf16 per column, even k
+        // low): box j is [128 rows x 64] with 128-byte swizzled rows in ring slot j
+        constexpr int JPER = (C::NBL + 1) / 2;
+        bool okq = true;
+        for (int j = hh * JPER; j < C::NBL && j < (hh + 1) * JPER; ++j) {
+          if (!warp_wait(&bars[B_FULL + j / C::CPI], 0, p.wait_ns, abort_flag)) {
+            okq = false;
+            break;
           }
-          tmem_st32(t_lane + c0 * 32, v);
-        }
-        {
-          const uint4* src = reinterpret_cast<const uint4*>(p.q_pe + grow * P);
+          const uint8_t* bx = smem + C::OFF_SRING + (j / C::CPI) * C::S_ITEM + (j % C::CPI) * CHUNK + r * 128;
           uint32_t v[32];
 #pragma unroll
-          for (int e = 0; e < P / 8; ++e) {
-            const uint4 x = row_ok ? __ldg(src + e) : make_uint4(0, 0, 0, 0);
-            v[4 * e] = x.x;
-            v[4 * e + 1] = x.y;
-            v[4 * e + 2] = x.z;
-            v[4 * e + 3] = x.w;
+          for (int u = 0; u < 8; ++u) {
+            const uint4 x = *reinterpret_cast<const uint4*>(bx + ((u ^ (r & 7)) << 4));
+            v[4 * u] = x.x;
+            v[4 * u + 1] = x.y;
+            v[4 * u + 2] = x.z;
+            v[4 * u + 3] = x.w;
           }
-          if constexpr (P == 64)
-            tmem_st32(t_lane + KL / 2, v);
-          else
-            tmem_st8(t_lane + KL / 2, v);
+          tmem_st32(t_lane + j * 32, v);
         }
         tmem_st_wait();
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[B_QREADY]);
+        ok = named_bar_and(kBarA, 32 * NSMW, okq && !*abort_flag);
+        if (issuer) {
+          if (ok) {
+            for (int j = 0; j < C::QS; ++j) mbar_arrive(&bars[B_EMPTY + j]);  // the slots may carry cache
+            mbar_arrive(&bars[B_QREADY]);
+          } else if (!*abort_flag) {
+            fail();
+          }
+        }
       }
-      const uint32_t peer_msg0 = mapa_shared(sb + C::OFF_MSG, peer);
+      const uint32_t peer_msg0 = mapa_shared(sb + C::OFF_MSG, peer);  // the O CTA's message slots
       const uint32_t peer_pfull0 = mapa_shared(smem_u32(&bars[B_PFULL]), peer);
       float m_ref = -INFINITY, l_run = 0.f;
-      bool ok = true;
-      for (int t = 0; t < ntiles; ++t) {
-        const int buf = t % NSB;
-        const int m = t % NMSG;
-        const bool okw = warp_wait(&bars[B_SFULL + buf], (t / NSB) & 1, p.wait_ns, abort_flag);
-        float x[TK];
-        float alpha = 1.f;
-        uint32_t pk[TK / 2];
+      for (int t = 0; ok && t < ntiles; ++t) {
+        const int buf = t & 1;
+        const int m = t & 1;  // message buffer
+        const bool okw = warp_wait(&bars[B_SFULL + buf], (t >> 1) & 1, p.wait_ns, abort_flag);
+        float x[HK];
+        float mx = -INFINITY;
         if (okw) {
           tc_fence_after();
           uint32_t sv[32];
-          const uint32_t sbuf = t_lane + C::SB0 + buf * TK;
+          const uint32_t sbuf = t_lane + SB0 + buf * TK + hh * HK;
           tmem_ld32(sbuf, sv);
           tmem_ld_wait();
 #pragma unroll
@@ -454,84 +563,92 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[B_SEMPTY + buf]);  // the buffer may be overwritten
-          const int kb = kstart + t * TK;
-          if (kb + TK > lim) {
+          const int kb = kstart + t * TK + hh * HK;
+          if (kb + HK > lim) {
 #pragma unroll
-            for (int c = 0; c < TK; ++c)
+            for (int c = 0; c < HK; ++c)
               if (kb + c >= lim) x[c] = -INFINITY;
           }
           float m8[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) m8[e] = x[e];
 #pragma unroll
-          for (int c = 8; c < TK; ++c) m8[c & 7] = fmaxf(m8[c & 7], x[c]);
-          const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-          if (mx > m_ref + kRescaleLog2) {
-            alpha = fast_exp2(m_ref - mx);  // 0 when nothing was seen yet
-            m_ref = mx;
-            l_run *= alpha;
-          }
-          const float mneg = m_ref == -INFINITY ? 0.f : -m_ref;  // all keys masked so far: x = -inf -> 0
-          float ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int e = 0; e < TK / 2; ++e) {
-            const float p0 = fast_exp2(x[2 * e] + mneg);
-            const float p1 = fast_exp2(x[2 * e + 1] + mneg);
-            ps[e & 3] += p0 + p1;
-            pk[e] = pack_bf16(p0, p1);
-          }
-          l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+          for (int c = 8; c < HK; ++c) m8[c & 7] = fmaxf(m8[c & 7], x[c]);
+          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         }
-        // every softmax warp arrives here on every tile, whatever its wait did, so that
-        // all leave the loop together; the issuer has released staging slot m (below)
+        red[((t & 1) * 2 + hh) * BM + r] = mx;
+        if (issuer && t > 0) bulk_wait_read<0>();  // the previous tile's copy has read the staging slot
+        // every row warp arrives here on every tile, whatever its wait did, so that all leave
+        // the loop together; the other half's maxima are written, and the staging slot is free
         if (!named_bar_and(kBarA, 32 * NSMW, okw && !*abort_flag)) {
           ok = false;
           break;
         }
-        // P row r into staging slot m: 128-byte row, 16-byte unit u at (u ^ (r & 7))
-        uint8_t* st = msg(m);
+        mx = fmaxf(mx, red[((t & 1) * 2 + (hh ^ 1)) * BM + r]);
+        float alpha = 1.f;
+        if (mx > m_ref + kRescaleLog2) {  // both halves of a row take the same decision
+          alpha = fast_exp2(m_ref - mx);  // 0 when nothing was seen yet
+          m_ref = mx;
+          l_run *= alpha;
+        }
+        const float mneg = m_ref == -INFINITY ? 0.f : -m_ref;  // all keys masked so far: x = -inf -> 0
+        uint32_t pk[HK / 2];
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int e = 0; e < HK / 2; ++e) {
+          const float p0 = fast_exp2(x[2 * e] + mneg);
+          const float p1 = fast_exp2(x[2 * e + 1] + mneg);
+          ps[e & 3] += p0 + p1;
+          pk[e] = pack_bf16(p0, p1);
+        }
+        l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        // P row r, keys of this half, into staging slot m: K-block hh of [128 rows x 64 keys],
+        // 128-byte rows, 16-byte unit u at (u ^ (r & 7))
+        uint8_t* st = smem + C::OFF_STG;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(st + r * 128 + ((u ^ (r & 7)) << 4)) =
+          *reinterpret_cast<uint4*>(st + hh * P_BLK + r * 128 + ((u ^ (r & 7)) << 4)) =
               make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-        // the first tile fills an empty O (its MMAs do not accumulate): nothing to rescale
-        const float a_out = t == 0 ? 1.f : alpha;
-        reinterpret_cast<float*>(st + MSG_ALPHA)[r] = a_out;
-        const bool any = __any_sync(0xffffffffu, a_out != 1.f);
-        if (lane == 0) reinterpret_cast<int*>(st + MSG_FLAGS)[warp - 2] = any ? 1 : 0;
+        if (hh == 0) {
+          // the first tile fills an empty O (its MMAs do not accumulate): nothing to rescale
+          const float a_out = t == 0 ? 1.f : alpha;
+          reinterpret_cast<float*>(st + MSG_ALPHA)[r] = a_out;
+          const bool any = __any_sync(0xffffffffu, a_out != 1.f);
+          if (lane == 0) reinterpret_cast<int*>(st + MSG_FLAGS)[q] = any ? 1 : 0;
+        }
         fence_proxy_async_smem();  // the bulk copy (async proxy) reads what these stores wrote
         named_bar_sync(kBarB, 32 * NSMW);
         if (issuer) {
           // the O CTA's MMAs are done with its message buffer m (tile t - NMSG)
           const bool free_ok =
-              t < NMSG || mbar_wait(&bars[B_PFREE + m], ((t / NMSG) - 1) & 1, p.wait_ns, abort_flag);
+              t < NMSG || mbar_wait(&bars[B_PFREE + m], ((t >> 1) - 1) & 1, p.wait_ns, abort_flag);
           if (free_ok) {
-            bulk_copy_to_peer(peer_msg0 + m * MSG_STRIDE, sb + C::OFF_MSG + m * MSG_STRIDE, MSG_BYTES,
-                              peer_pfull0 + m * 8);
+            bulk_copy_to_peer(peer_msg0 + m * MSG_STRIDE, sb + C::OFF_STG, MSG_BYTES, peer_pfull0 + m * 8);
             bulk_commit();
-            bulk_wait_read<NMSG - 1>();  // staging slot (t + 1) % NMSG is free for the next tile
           } else if (!*abort_flag) {
             fail();
           }
         }
       }
       ok = named_bar_and(kBarA, 32 * NSMW, ok && !*abort_flag);
-      const float lse = l_run > 0.f ? (m_ref + log2f(l_run)) * kLn2 : -INFINITY;
-      if (ok && ntiles > 0) {
+      red[(4 + hh) * BM + r] = l_run;
+      named_bar_sync(kBarB, 32 * NSMW);
+      const float l_tot = red[4 * BM + r] + red[5 * BM + r];
+      if (ok && hh == 0) {
         if (row_ok) {
+          const float lse = l_tot > 0.f ? (m_ref + log2f(l_tot)) * kLn2 : -INFINITY;
           if (p.nsplit == 1) {
             if (p.lse) p.lse[grow] = lse;
           } else {
             p.ws_lse[grow * p.nsplit + split] = lse;
           }
         }
-        reinterpret_cast<float*>(smem + C::OFF_FIN)[r] = l_run > 0.f ? 1.f / l_run : 0.f;
+        reinterpret_cast<float*>(smem + C::OFF_FIN)[r] = l_tot > 0.f ? 1.f / l_tot : 0.f;
         fence_proxy_async_smem();
       }
-      named_bar_sync(kBarB, 32 * NSMW);
+      named_bar_sync(kBarA, 32 * NSMW);
       if (issuer) {
-        if (ok && ntiles > 0) {
+        if (ok) {
           bulk_copy_to_peer(mapa_shared(sb + C::OFF_FIN, peer), sb + C::OFF_FIN, FIN_BYTES,
                             mapa_shared(smem_u32(&bars[B_FINFULL]), peer));
           bulk_commit();
@@ -540,7 +657,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // the O CTA's last commits into this CTA's barriers have arrived
         if (ok)
           for (int t = ntiles > NMSG ? ntiles - NMSG : 0; t < ntiles; ++t)
-            if (!mbar_wait(&bars[B_PFREE + t % NMSG], (t / NMSG) & 1, p.wait_ns, abort_flag)) {
+            if (!mbar_wait(&bars[B_PFREE + (t & 1)], (t >> 1) & 1, p.wait_ns, abort_flag)) {
               if (!*abort_flag) fail();
               break;
             }
@@ -557,22 +674,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int i = 0; i < O_NR; ++i) last[i] = -1;
       bool ok = true;
       for (int t = 0; ok && t < ntiles; ++t) {
-        const int row0 = cache_row(p, bi, kstart + t * TK);
-        for (int nh = 0; nh < C::NH; ++nh) {
-          const int slot = rp.slot;
-          const uint32_t prev = rp.phase ^ 1u;
-          rp.advance();
-          if (ic >= O_NR && !warp_wait(&bars[B_EMPTY + slot], prev, p.wait_ns, abort_flag)) {
-            ok = false;
-            break;
+        const int key0 = kstart + t * TK;
+        const int nkh = kend - key0 > HK ? 2 : 1;
+        for (int kh = 0; ok && kh < nkh; ++kh) {
+          const int row0 = cache_row(p, bi, key0 + kh * HK);
+          for (int nh = 0; nh < C::NH; ++nh) {
+            const int slot = rp.slot;
+            const uint32_t prev = rp.phase ^ 1u;
+            rp.advance();
+            if (ic >= O_NR && !warp_wait(&bars[B_EMPTY + slot], prev, p.wait_ns, abort_flag)) {
+              ok = false;
+              break;
+            }
+            last[slot] = ic;
+            if (lane == (ic & 1)) {  // one box per item; the issuing lane alternates
+              mbar_expect_tx(&bars[B_FULL + slot], C::O_ITEM);
+              tma_load_3d(sb + C::OFF_ORING + slot * C::O_ITEM, &tm_zo, 0, row0, nh * (C::ON / 64), &bars[B_FULL + slot]);
+            }
+            ++ic;
+            __syncwarp();
           }
-          last[slot] = ic++;
-          if (lane == 0) mbar_expect_tx(&bars[B_FULL + slot], C::O_ITEM);
-          __syncwarp();
-          if (lane < C::ON / 64)
-            tma_load_2d(sb + C::OFF_RING + slot * C::O_ITEM + lane * CHUNK, &tm_z, nh * C::ON + lane * 64, row0,
-                        &bars[B_FULL + slot]);
-          __syncwarp();
         }
       }
       if (lane == 0) {
@@ -585,16 +706,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // ------------------------------------------------ MMA issuer: O += P Z
       const bool leader = elect_one();
       constexpr uint32_t idO = idesc_bf16_f32(BM, C::ON, false, true);
-      const uint64_t dmsg = smem_desc(sb + C::OFF_MSG, 16, 1024, kSw128);      // P, K-major
-      const uint64_t dz = smem_desc(sb + C::OFF_RING, CHUNK, 1024, kSw128);    // Z slab, MN-major
+      const uint64_t dmsg = smem_desc(sb + C::OFF_MSG, 16, 1024, kSw128);       // P, K-major
+      const uint64_t dz = smem_desc(sb + C::OFF_ORING, HALF_BOX, 1024, kSw128);  // Z slab, MN-major
       RingPos<O_NR> rp;
       int ncorr = 0;
       bool ok = true;
       for (int t = 0; ok && t < ntiles; ++t) {
-        const int m = t % NMSG;
+        const int m = t & 1;
         if (leader) mbar_expect_tx(&bars[B_PFULL + m], MSG_BYTES);  // this use's one arrival + bytes
         __syncwarp();
-        if (!warp_wait(&bars[B_PFULL + m], (t / NMSG) & 1, p.wait_ns, abort_flag)) {
+        if (!warp_wait(&bars[B_PFULL + m], (t >> 1) & 1, p.wait_ns, abort_flag)) {
           ok = false;
           break;
         }
@@ -623,37 +744,40 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tc_fence_after();  // the rescaled O (tcgen05.st of the row warps) comes first
         }
         const int key0 = kstart + t * TK;
-        for (int nh = 0; nh < C::NH; ++nh) {
-          const int slot = rp.slot;
-          const uint32_t ph = rp.phase;
-          rp.advance();
-          if (!warp_wait(&bars[B_FULL + slot], ph, p.wait_ns, abort_flag)) {
-            ok = false;
-            break;
-          }
-          const int first_bad = L - key0;  // rows at or past the sequence end may hold anything
-          if (first_bad < TK) {
-            uint8_t* item = smem + C::OFF_RING + slot * C::O_ITEM;
-            const int nrow = TK - first_bad;
-            for (int idx = lane; idx < nrow * (C::ON / 64) * 8; idx += 32) {
-              const int rr = first_bad + idx / ((C::ON / 64) * 8);
-              const int rem = idx % ((C::ON / 64) * 8);
-              *reinterpret_cast<uint4*>(item + (rem / 8) * CHUNK + rr * 128 + (rem % 8) * 16) =
-                  make_uint4(0, 0, 0, 0);
+        const int nkh = kend - key0 > HK ? 2 : 1;
+        for (int kh = 0; ok && kh < nkh; ++kh) {
+          for (int nh = 0; nh < C::NH; ++nh) {
+            const int slot = rp.slot;
+            const uint32_t ph = rp.phase;
+            rp.advance();
+            if (!warp_wait(&bars[B_FULL + slot], ph, p.wait_ns, abort_flag)) {
+              ok = false;
+              break;
             }
-            fence_proxy_async_smem();
+            const int first_bad = L - (key0 + kh * HK);  // rows at or past the sequence end may hold anything
+            if (first_bad < HK) {
+              uint8_t* item = smem + C::OFF_ORING + slot * C::O_ITEM;
+              const int nrow = HK - first_bad;
+              for (int idx = lane; idx < nrow * (C::ON / 64) * 8; idx += 32) {
+                const int rr = first_bad + idx / ((C::ON / 64) * 8);
+                const int rem = idx % ((C::ON / 64) * 8);
+                *reinterpret_cast<uint4*>(item + (rem / 8) * HALF_BOX + rr * 128 + (rem % 8) * 16) =
+                    make_uint4(0, 0, 0, 0);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+            }
+            if (leader) {
+              const uint64_t a0 = dmsg + (uint64_t)((m * MSG_STRIDE + kh * P_BLK) >> 4);
+              const uint64_t b0 = dz + (uint64_t)((slot * C::O_ITEM) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < HK / 16; ++kk)
+                tc_mma_ss(tmem + nh * C::ON, a0 + 2 * kk, b0 + (uint64_t)((kk * 16 * 128) >> 4), idO,
+                          (t > 0 || kh > 0 || kk > 0) ? 1u : 0u);
+              tc_commit(&bars[B_EMPTY + slot]);
+            }
             __syncwarp();
           }
-          if (leader) {
-            const uint64_t a0 = dmsg + (uint64_t)((m * MSG_STRIDE) >> 4);
-            const uint64_t b0 = dz + (uint64_t)((slot * C::O_ITEM) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < TK / 16; ++kk)
-              tc_mma_ss(tmem + nh * C::ON, a0 + 2 * kk, b0 + (uint64_t)((kk * 16 * 128) >> 4), idO,
-                        (t > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(&bars[B_EMPTY + slot]);
-          }
-          __syncwarp();
         }
         if (!ok) break;
         if (leader) tc_commit_multicast(&bars[B_PFREE + m], (uint16_t)(1u << kRankS));  // S may refill buffer m
@@ -673,7 +797,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else {
       // ------------------------------------------------ rescale requests, then the epilogue
       const int q = warp & 3;
+      const int hh = (warp - 2) >> 2;  // half of the output columns of this warp
       const int r = q * 32 + lane;
+      const int c_lo = hh * C::OCOLS;
       const uint32_t t_lane = tmem + ((uint32_t)(q * 32) << 16);
       bool ok = true;
       for (int k = 0;; ++k) {
@@ -683,11 +809,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         const int tile = *req_tile;
         if (tile < 0) break;
-        const float alpha = reinterpret_cast<const volatile float*>(msg(tile % NMSG) + MSG_ALPHA)[r];
+        const float alpha = reinterpret_cast<const volatile float*>(msg(tile & 1) + MSG_ALPHA)[r];
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
           tc_fence_after();
 #pragma unroll 1
-          for (int c0 = 0; c0 < KL; c0 += 32) {
+          for (int c0 = c_lo; c0 < c_lo + C::OCOLS; c0 += 32) {
             uint32_t v[32];
             tmem_ld32(t_lane + c0, v);
             tmem_ld_wait();
@@ -709,18 +835,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         } else {
           tc_fence_after();
           const float inv = reinterpret_cast<const float*>(smem + C::OFF_FIN)[r];
-          // O / l of this warp's 32 rows is staged through shared memory (the O-ring, idle
-          // once every MMA has completed) in passes of 128 columns and stored as whole row
-          // segments; staged rows are 16-byte units XOR-swizzled by (row & 7).
-          constexpr int PASS = KL < 128 ? KL : 128;
-          constexpr int F4 = PASS / 4;  // 16-byte units per staged row
-          constexpr int ROWB = PASS * 4;
-          constexpr int RPI = 32 / F4;  // rows per store instruction
-          uint8_t* stg = smem + C::OFF_RING + (warp - 2) * 32 * ROWB;
+          // O / l of this warp's 32 rows x OCOLS columns is staged through shared memory (the
+          // O-ring, idle once every MMA has completed) in passes of PASS columns and stored as
+          // whole row segments; staged rows are 16-byte units XOR-swizzled by (row & 7).
+          constexpr int F4 = C::PASS / 4;  // 16-byte units per staged row
+          constexpr int ROWB = C::PASS * 4;
+          constexpr int RPI = 32 / F4;     // rows per store instruction
+          uint8_t* stg = smem + C::OFF_ORING + (warp - 2) * 32 * ROWB;
 #pragma unroll 1
-          for (int c0 = 0; c0 < KL; c0 += PASS) {
+          for (int c0 = c_lo; c0 < c_lo + C::OCOLS; c0 += C::PASS) {
 #pragma unroll 1
-            for (int cc = 0; cc < PASS; cc += 32) {
+            for (int cc = 0; cc < C::PASS; cc += 32) {
               uint32_t v[32];
               tmem_ld32(t_lane + c0 + cc, v);
               tmem_ld_wait();
@@ -739,11 +864,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               const float4 xv = *reinterpret_cast<const float4*>(stg + rr * ROWB + ((jl ^ (rr & 7)) * 16));
               const size_t g = (size_t)qrow0 + rs;
               const int col = c0 + jl * 4;
-              if (p.nsplit == 1)
-                *reinterpret_cast<uint2*>(p.o_lat + g * KL + col) =
-                    make_uint2(pack_bf16(xv.x, xv.y), pack_bf16(xv.z, xv.w));
-              else
-                *reinterpret_cast<float4*>(p.ws_o + (g * p.nsplit + split) * KL + col) = xv;
+              __nv_bfloat16* dst = p.nsplit == 1 ? p.o_lat + g * KL : p.ws_ob + (g * p.nsplit + split) * KL;
+              *reinterpret_cast<uint2*>(dst + col) = make_uint2(pack_bf16(xv.x, xv.y), pack_bf16(xv.z, xv.w));
             }
             __syncwarp();
           }
@@ -778,18 +900,37 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
   return encode_tmap_bf16(m, base, 2, dims, strides, box, swizzle_for((int)box_cols * 2));
 }
 
-template <int KL, int P>
-cudaError_t launch_kl(const MlaLaunch& a, cudaStream_t stream) {
+// 3-D view {64 columns, rows, cols/64 chunks} of a [rows, cols] bf16 matrix (row stride cols*2
+// bytes, chunk stride 128 bytes) with boxes {64, box_rows, box_chunks}: a box lands chunk-major,
+// [box_chunks][box_rows][64], each 128-byte row swizzled
+bool make_chunk_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                    uint32_t box_chunks) {
+  const cuuint64_t dims[3] = {64, rows, cols / 64};
+  const cuuint64_t strides[2] = {cols * 2, 128};
+  const cuuint32_t box[3] = {64, box_rows, box_chunks};
+  return encode_tmap_bf16(m, base, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <int KL, int P, bool PAGED>
+cudaError_t launch_klp(const MlaLaunch& a, cudaStream_t stream) {
   using C = MlaCfg<KL, P>;
   static std::atomic<unsigned long long> smem_limit_set{0};
-  if (cudaError_t e = ensure_smem_limit(mla_pair_kernel<KL, P>, C::SMEM, smem_limit_set)) return e;
+  if (cudaError_t e = ensure_smem_limit(mla_pair_kernel<KL, P, PAGED>, C::SMEM, smem_limit_set)) return e;
   const uint64_t krows = a.paged ? (uint64_t)a.num_pages * 64 : (uint64_t)a.b * a.capacity;
-  CUtensorMap tz, tkpe;
-  if (!make_map(&tz, a.z, krows, KL, TK, 64) || !make_map(&tkpe, a.k_pe, krows, P, TK, P))
-    return cudaErrorInvalidValue;
+  const uint64_t qrows = (uint64_t)a.b * a.h * a.s;
+  CUtensorMap tq3, tqpe, tza, tzb, tkpe, tzo;
+  bool ok = make_chunk_map(&tq3, a.qz, qrows, KL, BM, C::LAT0) && make_map(&tqpe, a.q_pe, qrows, P, BM, P) &&
+            make_chunk_map(&tzo, a.z, krows, KL, HK, C::ON / 64);
+  if (PAGED) {
+    ok = ok && make_map(&tza, a.z, krows, KL, HK, 64) && make_map(&tkpe, a.k_pe, krows, P, HK, P);
+    tzb = tza;
+  } else {
+    ok = ok && make_chunk_map(&tza, a.z, krows, KL, TK, C::LAT0) && make_chunk_map(&tzb, a.z, krows, KL, TK, C::LATL) &&
+         make_map(&tkpe, a.k_pe, krows, P, TK, P);
+  }
+  if (!ok) return cudaErrorInvalidValue;
   MlaParams p;
-  p.qz = static_cast<const __nv_bfloat16*>(a.qz);
-  p.q_pe = static_cast<const __nv_bfloat16*>(a.q_pe);
+  p.ws_ob = static_cast<__nv_bfloat16*>(a.ws_o);
   p.seqlens = a.seqlens;
   p.block_table = a.block_table;
   p.max_pages = a.max_pages;
@@ -805,7 +946,6 @@ cudaError_t launch_kl(const MlaLaunch& a, cudaStream_t stream) {
   p.scale_log2 = a.scale * kLog2e;
   p.o_lat = static_cast<__nv_bfloat16*>(a.o_lat);
   p.lse = a.lse;
-  p.ws_o = a.ws_o;
   p.ws_lse = a.ws_lse;
   p.err = a.err;
   p.wait_ns = a.wait_ns;
@@ -826,8 +966,13 @@ cudaError_t launch_kl(const MlaLaunch& a, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, mla_pair_kernel<KL, P>, tz, tkpe, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, mla_pair_kernel<KL, P, PAGED>, tq3, tqpe, tza, tzb, tkpe, tzo, p);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int KL, int P>
+cudaError_t launch_kl(const MlaLaunch& a, cudaStream_t stream) {
+  return a.paged ? launch_klp<KL, P, true>(a, stream) : launch_klp<KL, P, false>(a, stream);
 }
 
 }  // namespace

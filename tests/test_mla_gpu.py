@@ -164,7 +164,7 @@ def test_split_invariance(nsplit):
         sl = torch.tensor(inp.seqlens, dtype=torch.int32, device=DEV)
         o2, l2 = da.mla_decode(base[2], inp.q_pe, inp.z, inp.k_pe, sl, scale=inp.scale, max_seqlen=1500)
         torch.cuda.synchronize()
-        chunk = -(-(-(-1500 // nsplit)) // 64) * 64  # chunks are whole 64-key latent tiles (pages)
+        chunk = -(-(-(-1500 // nsplit)) // 128) * 128  # chunks are whole 128-key latent tiles
         assert da.last_num_splits() == -(-1500 // chunk)
     finally:
         da.set_forced_splits(0)

@@ -587,6 +587,26 @@ def extras(dev, stream, hbm, tfl):
         del qs, outs, lses, ws
         torch.cuda.empty_cache()
 
+    # the two projection GEMMs of the headline pipeline, each alone
+    wl = W.WORKLOADS["mla_dsv3"]
+    seqlens = wl.seqlens()
+    inp = [W.make_mla(wl.b, wl.heads, wl.d, wl.k, wl.p, wl.s, seqlens, seed=wl.seed + r, device=dev) for r in range(3)]
+    sl = torch.tensor(seqlens, dtype=torch.int32, device=dev)
+    qzs = [torch.empty((wl.b, wl.heads, wl.s, wl.k), dtype=torch.bfloat16, device=dev) for _ in inp]
+    outs = [torch.empty((wl.b, wl.heads, wl.s, wl.d), dtype=torch.bfloat16, device=dev) for _ in inp]
+    olats = [torch.randn((wl.b, wl.heads, wl.s, wl.k), device=dev).to(torch.bfloat16) for _ in inp]
+    t_abs = time_calls([(lambda r=r: da.mla_absorb_q(inp[r].q_nope, inp[r].w_uk, sl, out=qzs[r], stream=stream))
+                        for r in range(3)], n=300)
+    t_out = time_calls([(lambda r=r: da.mla_out_proj(olats[r], inp[r].w_uv, sl, out=outs[r], stream=stream))
+                        for r in range(3)], n=300)
+    pb = cost.proj_bytes(wl.b, wl.heads, wl.s, wl.d, wl.k)
+    res["proj_absorb"] = {"us": t_abs * 1e6, "hbm_gbs": pb / t_abs / 1e9, "frac_hbm": pb / t_abs / 1e9 / hbm,
+                          "bytes": pb, "l2": "3 rotating weight sets of 16.8 MB"}
+    res["proj_out"] = {"us": t_out * 1e6, "hbm_gbs": pb / t_out / 1e9, "frac_hbm": pb / t_out / 1e9 / hbm,
+                       "bytes": pb, "l2": "3 rotating weight sets of 16.8 MB"}
+    del inp, qzs, outs, olats
+    torch.cuda.empty_cache()
+
     for s in (1, 2, 4, 8, 16, 32):
         wl = W.WORKLOADS["mla_dsv3"] if s == 1 else W.WORKLOADS[f"mla_mtp_s{s}"]
         seqlens = wl.seqlens()

@@ -306,7 +306,7 @@ int mla_absorb_q(const decattn_bf16* q_nope, const decattn_bf16* w_uk, decattn_b
   if (b == 0) return DECATTN_OK;
   DeviceState* st = nullptr;
   if (int rc = device_state(&st)) return rc;
-  ProjLaunch a{q_nope, w_uk, qz, seqlens, b, s, h, d, k, scale};
+  ProjLaunch a{st->err, wait_limit(), q_nope, w_uk, qz, seqlens, b, s, h, d, k, scale};
   return launch_proj(a, st->sms, stream) == cudaSuccess ? DECATTN_OK : DECATTN_ERR_CUDA;
 }
 
@@ -316,7 +316,7 @@ int mla_out_proj(const decattn_bf16* o_lat, const decattn_bf16* w_uv, decattn_bf
   if (b == 0) return DECATTN_OK;
   DeviceState* st = nullptr;
   if (int rc = device_state(&st)) return rc;
-  ProjLaunch a{o_lat, w_uv, out, seqlens, b, s, h, k, d, scale};
+  ProjLaunch a{st->err, wait_limit(), o_lat, w_uv, out, seqlens, b, s, h, k, d, scale};
   return launch_proj(a, st->sms, stream) == cudaSuccess ? DECATTN_OK : DECATTN_ERR_CUDA;
 }
 

@@ -45,6 +45,8 @@ cudaError_t launch_combine_balanced(const float* ws_o, const float* ws_lse, cons
                                     cudaStream_t stream);
 
 struct ProjLaunch {
+  unsigned* err;     // device error word
+  unsigned long long wait_ns;
   const void* a;     // [b, h, s, kin]
   const void* w;     // [h, kin, nout]
   void* c;           // [b, h, s, nout]

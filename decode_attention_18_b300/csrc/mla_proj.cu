@@ -7,8 +7,16 @@
 //   C[b, j, r, :] = scale * A[b, j, r, :] @ W[j]      (W[j] is kin x nout)
 // with M = b*s rows per head. At decode sizes M is small (32 rows for 32
 // sequences of one token) and the kernel is bound by reading W (h*kin*nout
-// bf16, 16.8 MB for h=128, d=128, k=512), so it streams W once through a
-// cp.async pipeline and runs mma.sync m16n8k16 (bf16, fp32 accumulate).
+// bf16, 16.8 MB for h=128, d=128, k=512), so it streams W once and runs
+// mma.sync m16n8k16 (bf16, fp32 accumulate) on it. W arrives by TMA: one
+// thread requests each k-stage as [64 k x 64 n] boxes (128-byte swizzle) on the
+// stage's mbarrier, every stage of a CTA in flight at once, the first ones
+// before the programmatic-launch wait (W is not an output of the previous
+// kernel). Issuing W as 16-byte cp.async copies instead costs one instruction per
+// 16 bytes (thousands per CTA), which bounds the stream well below HBM speed.
+// The activation rows (a few KB per CTA) still come by cp.async.
+#include <cstring>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -19,6 +27,8 @@ namespace {
 constexpr int BK = 64;
 
 struct ProjParams {
+  unsigned* err;
+  unsigned long long wait_ns;
   const __nv_bfloat16* a;
   const __nv_bfloat16* w;
   __nv_bfloat16* c;
@@ -30,9 +40,11 @@ struct ProjParams {
 __device__ __forceinline__ uint32_t swz(int row, int chunk) { return (uint32_t)(chunk ^ (row & 7)); }
 
 // One CTA: BM rows of one head x BN output columns, 4 warps laid out (BM/32) x (4/(BM/32)),
-// each warp 32 rows x WN columns; NST k-stages of BK in flight (cp.async, 16-byte chunks).
-template <int BM, int BN, int NST>
-__global__ void __launch_bounds__(128) proj_kernel(ProjParams p) {
+// each warp 32 rows x WN columns; NST k-stages of BK in flight. TMA_W: the W tile of a stage
+// is BN/64 TMA boxes of [64 k x 64 n] (box-major, 128-byte swizzle); otherwise (narrow
+// outputs) 16-byte cp.async copies with the same swizzle over BN*2-byte rows.
+template <int BM, int BN, int NST, bool TMA_W>
+__global__ void __launch_bounds__(128) proj_kernel(const __grid_constant__ CUtensorMap tm_w, ProjParams p) {
   constexpr int WMW = BM / 32;               // warps along M
   constexpr int WNW = 4 / WMW;               // warps along N
   constexpr int WN = BN / WNW;               // columns per warp
@@ -42,7 +54,9 @@ __global__ void __launch_bounds__(128) proj_kernel(ProjParams p) {
   constexpr int B_BYTES = BK * B_ROW;        // [64 k][BN n]
   constexpr int STAGE = A_BYTES + B_BYTES;
   static_assert(NTW % 2 == 0 && (BM * 8) % 128 == 0 && (BK * (BN / 8)) % 128 == 0, "tile shape");
+  static_assert(!TMA_W || (BN % 64 == 0 && A_BYTES % 1024 == 0 && STAGE % 1024 == 0), "TMA tile shape");
   extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ uint64_t wbar[NST];  // stage's W landed (TMA)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wm = warp / WNW, wn = warp % WNW;
@@ -69,8 +83,23 @@ __global__ void __launch_bounds__(128) proj_kernel(ProjParams p) {
       cp_async_16(adst + r * 128 + swz(r, c) * 16, src, ok ? 16u : 0u);
     }
   };
+  // shared-memory offset of 16-byte chunk c (8 columns) of k-row r of a stage's W tile
+  auto w_off = [&](int r, int c) -> uint32_t {
+    if constexpr (TMA_W) return (uint32_t)((c >> 3) * (BK * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+    else return (uint32_t)(r * B_ROW + swz(r, c) * 16);
+  };
+  uint32_t wphase = 0;  // parity of each stage's next W completion (TMA_W)
   auto load_w = [&](int kt, int stage) {
     const uint32_t bdst = sbase + stage * STAGE + A_BYTES;
+    if constexpr (TMA_W) {
+      if (tid == 0) {
+        mbar_expect_tx(&wbar[stage], B_BYTES);
+#pragma unroll
+        for (int cb = 0; cb < BN / 64; ++cb)
+          tma_load_2d(bdst + cb * (BK * 128), &tm_w, n0 + cb * 64, j * p.kin + kt * BK, &wbar[stage]);
+      }
+      return;
+    }
     const __nv_bfloat16* wbase = p.w + (size_t)j * p.kin * p.nout;
 #pragma unroll
     for (int n = 0; n < (BK * (BN / 8)) / 128; ++n) {
@@ -89,9 +118,23 @@ __global__ void __launch_bounds__(128) proj_kernel(ProjParams p) {
 #pragma unroll
     for (int ni = 0; ni < NTW; ++ni) acc[mi][ni][0] = acc[mi][ni][1] = acc[mi][ni][2] = acc[mi][ni][3] = 0.f;
 
+  if constexpr (TMA_W) {
+    if (smem_u32(smem) & 1023u) {  // the 128-byte swizzle needs 1024-byte aligned stages
+      if (tid == 0) raise_error(p.err, kErrLaunch);
+      return;
+    }
+    if (tid == 0) {
+#pragma unroll
+      for (int i = 0; i < NST; ++i) mbar_init(&wbar[i], 1);
+      fence_mbar_init();
+      prefetch_tmap(&tm_w);
+    }
+    __syncthreads();
+  }
   // The weight does not come from the previous kernel in the stream: its first stages
-  // are requested before pdl_wait, so they load while that kernel finishes. (They join
-  // the first commit group, whose completion is awaited before stage 0 is used.)
+  // are requested before pdl_wait, so they load while that kernel finishes. (With
+  // cp.async they join the first commit group, whose completion is awaited before stage
+  // 0 is used; with TMA each stage has its barrier.)
 #pragma unroll
   for (int t = 0; t < NST - 1; ++t)
     if (t < kiters) load_w(t, t);
@@ -102,8 +145,17 @@ __global__ void __launch_bounds__(128) proj_kernel(ProjParams p) {
     if (t < kiters) load_a(t, t);
     cp_async_commit();
   }
+  bool w_ok = true;
   for (int kt = 0; kt < kiters; ++kt) {
     cp_async_wait<NST - 2>();
+    if constexpr (TMA_W) {
+      const int stage = kt % NST;
+      if (!mbar_wait(&wbar[stage], (wphase >> stage) & 1u, p.wait_ns, nullptr)) {
+        w_ok = false;  // recorded below; the stage's copy is waited for before the CTA leaves
+        mbar_wait(&wbar[stage], (wphase >> stage) & 1u, 1000000000ull, nullptr);
+      }
+      wphase ^= 1u << stage;
+    }
     __syncthreads();
     if (kt + NST - 1 < kiters) {
       load_a(kt + NST - 1, (kt + NST - 1) % NST);
@@ -126,7 +178,7 @@ __global__ void __launch_bounds__(128) proj_kernel(ProjParams p) {
         const int r = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
         const int c = (wn * WN) / 8 + np * 2 + (lane >> 4);
         uint32_t b0, b1, b2, b3;
-        ldmatrix_x4_trans(bbase + r * B_ROW + swz(r, c) * 16, b0, b1, b2, b3);
+        ldmatrix_x4_trans(bbase + w_off(r, c), b0, b1, b2, b3);
 #pragma unroll
         for (int mi = 0; mi < 2; ++mi) {
           mma_bf16_16816(acc[mi][2 * np], af[mi], b0, b1);
@@ -136,6 +188,7 @@ __global__ void __launch_bounds__(128) proj_kernel(ProjParams p) {
     }
   }
   cp_async_wait<0>();
+  if (!w_ok && tid == 0) raise_error(p.err, kErrWaitTimeout);
 
   // epilogue: scale, bf16 (round to nearest even); rows of empty sequences are zero
 #pragma unroll
@@ -154,11 +207,22 @@ __global__ void __launch_bounds__(128) proj_kernel(ProjParams p) {
     }
 }
 
-template <int BM, int BN, int NST>
+template <int BM, int BN, int NST, bool TMA_W>
 cudaError_t launch_tile(const ProjParams& p, cudaStream_t stream) {
   constexpr int SMEM = NST * (BM * BK * 2 + BK * BN * 2);
   static std::atomic<unsigned long long> smem_limit_set{0};
-  if (cudaError_t e = ensure_smem_limit(proj_kernel<BM, BN, NST>, SMEM, smem_limit_set)) return e;
+  if (cudaError_t e = ensure_smem_limit(proj_kernel<BM, BN, NST, TMA_W>, SMEM, smem_limit_set)) return e;
+  // W viewed as [h * kin rows, nout columns], boxes [64 k x 64 n]; k-rows of a stage past
+  // kin read the next head's rows (their A columns are zero) or zeros past the tensor
+  CUtensorMap tw;
+  if (TMA_W) {
+    const cuuint64_t dims[2] = {(cuuint64_t)p.nout, (cuuint64_t)p.h * p.kin};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.nout * 2};
+    const cuuint32_t box[2] = {64, BK};
+    if (!encode_tmap_bf16_sw128(&tw, p.w, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  } else {
+    memset(&tw, 0, sizeof(tw));
+  }
   // programmatic dependent launch: the weight prefetch overlaps the previous kernel
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((p.nout + BN - 1) / BN, (p.M + BM - 1) / BM, p.h);
@@ -170,7 +234,7 @@ cudaError_t launch_tile(const ProjParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, proj_kernel<BM, BN, NST>, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, proj_kernel<BM, BN, NST, TMA_W>, tw, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -184,6 +248,8 @@ cudaError_t launch_tile(const ProjParams& p, cudaStream_t stream) {
 // d -> k) and narrow ones when it is tall (output projection: k -> d).
 cudaError_t launch_proj(const ProjLaunch& a, int num_sms, cudaStream_t stream) {
   ProjParams p;
+  p.err = a.err;
+  p.wait_ns = a.wait_ns;
   p.a = static_cast<const __nv_bfloat16*>(a.a);
   p.w = static_cast<const __nv_bfloat16*>(a.w);
   p.c = static_cast<__nv_bfloat16*>(a.c);
@@ -197,13 +263,19 @@ cudaError_t launch_proj(const ProjLaunch& a, int num_sms, cudaStream_t stream) {
   p.scale = a.scale;
   (void)num_sms;
   const int kiters = (a.kin + BK - 1) / BK;
+  // W by TMA where the output is a whole number of 64-column boxes (the pointer is
+  // 16-byte aligned and rows are nout*2 bytes, a multiple of 16, as the API checks)
+  const bool tma = a.nout % 64 == 0;
   if (p.M <= 32) {
-    if (a.nout >= 256 && kiters <= 2) return launch_tile<32, 128, 2>(p, stream);  // 4 column tiles per head
-    if (kiters <= 8) return launch_tile<32, 64, 8>(p, stream);  // every k-stage in flight (96 KB)
-    return launch_tile<32, 64, 4>(p, stream);
+    if (a.nout >= 256 && kiters <= 2)  // 4 column tiles per head
+      return tma ? launch_tile<32, 128, 2, true>(p, stream) : launch_tile<32, 128, 2, false>(p, stream);
+    if (kiters <= 8)  // every k-stage in flight (96 KB)
+      return tma ? launch_tile<32, 64, 8, true>(p, stream) : launch_tile<32, 64, 8, false>(p, stream);
+    return tma ? launch_tile<32, 64, 4, true>(p, stream) : launch_tile<32, 64, 4, false>(p, stream);
   }
-  if (a.nout >= 128) return launch_tile<64, 128, 3>(p, stream);
-  return launch_tile<64, 64, 3>(p, stream);
+  if (a.nout >= 128)
+    return tma ? launch_tile<64, 128, 3, true>(p, stream) : launch_tile<64, 128, 3, false>(p, stream);
+  return tma ? launch_tile<64, 64, 3, true>(p, stream) : launch_tile<64, 64, 3, false>(p, stream);
 }
 
 }  // namespace decattn

@@ -9,10 +9,12 @@
 // sequences of one token) and the kernel is bound by reading W (h*kin*nout
 // bf16, 16.8 MB for h=128, d=128, k=512), so it streams W once and runs
 // mma.sync m16n8k16 (bf16, fp32 accumulate) on it. W arrives by TMA: one
-// thread requests each k-stage as [64 k x 64 n] boxes (128-byte swizzle) on the
-// stage's mbarrier, every stage of a CTA in flight at once, the first ones
-// before the programmatic-launch wait (W is not an output of the previous
-// kernel). Issuing W as 16-byte cp.async copies instead costs one instruction per
+// thread requests each k-stage as a single box of [64 k x BN n] (a 3-D view of W
+// in 64-column chunks, 128-byte swizzle) on the stage's mbarrier. At decode sizes
+// the CTA's whole weight slab fits in its stages, so every stage is requested at
+// once, before the programmatic-launch wait (W is not an output of the previous
+// kernel): one DRAM round trip per CTA, in as few and as large boxes as the
+// swizzle allows. Issuing W as 16-byte cp.async copies instead costs one instruction per
 // 16 bytes (thousands per CTA), which bounds the stream well below HBM speed.
 // The activation rows (a few KB per CTA) still come by cp.async.
 #include <cstring>
@@ -43,6 +45,8 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) { return (uint32_t)(
 // each warp 32 rows x WN columns; NST k-stages of BK in flight. TMA_W: the W tile of a stage
 // is BN/64 TMA boxes of [64 k x 64 n] (box-major, 128-byte swizzle); otherwise (narrow
 // outputs) 16-byte cp.async copies with the same swizzle over BN*2-byte rows.
+// Stage t holds k-tile t (t < NST) and then every NST-th one after it; all NST stages
+// are requested before the first is consumed.
 template <int BM, int BN, int NST, bool TMA_W>
 __global__ void __launch_bounds__(128) proj_kernel(const __grid_constant__ CUtensorMap tm_w, ProjParams p) {
   constexpr int WMW = BM / 32;               // warps along M
@@ -94,9 +98,7 @@ __global__ void __launch_bounds__(128) proj_kernel(const __grid_constant__ CUten
     if constexpr (TMA_W) {
       if (tid == 0) {
         mbar_expect_tx(&wbar[stage], B_BYTES);
-#pragma unroll
-        for (int cb = 0; cb < BN / 64; ++cb)
-          tma_load_2d(bdst + cb * (BK * 128), &tm_w, n0 + cb * 64, j * p.kin + kt * BK, &wbar[stage]);
+        tma_load_3d(bdst, &tm_w, 0, j * p.kin + kt * BK, n0 / 64, &wbar[stage]);
       }
       return;
     }
@@ -131,22 +133,24 @@ __global__ void __launch_bounds__(128) proj_kernel(const __grid_constant__ CUten
     }
     __syncthreads();
   }
-  // The weight does not come from the previous kernel in the stream: its first stages
-  // are requested before pdl_wait, so they load while that kernel finishes. (With
-  // cp.async they join the first commit group, whose completion is awaited before stage
-  // 0 is used; with TMA each stage has its barrier.)
+  // The weight does not come from the previous kernel in the stream: its stages are
+  // requested before pdl_wait, so they load while that kernel finishes. (With cp.async
+  // they join the first commit group, whose completion is awaited before stage 0 is
+  // used; with TMA each stage has its barrier.) Commit group t carries k-tile t.
 #pragma unroll
-  for (int t = 0; t < NST - 1; ++t)
+  for (int t = 0; t < NST; ++t)
     if (t < kiters) load_w(t, t);
   pdl_wait();  // the activations (and lengths) are the previous kernel's results
   pdl_trigger();
 #pragma unroll
-  for (int t = 0; t < NST - 1; ++t) {
+  for (int t = 0; t < NST; ++t) {
     if (t < kiters) load_a(t, t);
     cp_async_commit();
   }
   bool w_ok = true;
   for (int kt = 0; kt < kiters; ++kt) {
+    // groups 0 .. kt+1 complete: k-tile t < NST is group t, a later one is group t + 1
+    // (the iteration that refills it commits after the empty commit of iteration 0)
     cp_async_wait<NST - 2>();
     if constexpr (TMA_W) {
       const int stage = kt % NST;
@@ -156,12 +160,12 @@ __global__ void __launch_bounds__(128) proj_kernel(const __grid_constant__ CUten
       }
       wphase ^= 1u << stage;
     }
-    __syncthreads();
-    if (kt + NST - 1 < kiters) {
-      load_a(kt + NST - 1, (kt + NST - 1) % NST);
-      load_w(kt + NST - 1, (kt + NST - 1) % NST);
+    __syncthreads();  // every warp is done with stage (kt - 1) % NST
+    if (kt >= 1 && kt - 1 + NST < kiters) {
+      load_a(kt - 1 + NST, (kt - 1) % NST);
+      load_w(kt - 1 + NST, (kt - 1) % NST);
     }
-    cp_async_commit();
+    cp_async_commit();  // group NST + kt (k-tile kt - 1 + NST when kt >= 1, else empty)
     const uint32_t abase = sbase + (kt % NST) * STAGE;
     const uint32_t bbase = abase + A_BYTES;
 #pragma unroll
@@ -212,14 +216,16 @@ cudaError_t launch_tile(const ProjParams& p, cudaStream_t stream) {
   constexpr int SMEM = NST * (BM * BK * 2 + BK * BN * 2);
   static std::atomic<unsigned long long> smem_limit_set{0};
   if (cudaError_t e = ensure_smem_limit(proj_kernel<BM, BN, NST, TMA_W>, SMEM, smem_limit_set)) return e;
-  // W viewed as [h * kin rows, nout columns], boxes [64 k x 64 n]; k-rows of a stage past
-  // kin read the next head's rows (their A columns are zero) or zeros past the tensor
+  // W viewed as [h * kin rows, nout columns] in 64-column chunks: dims {64 columns, rows,
+  // nout/64 chunks}, so one box {64, BK, BN/64} lands chunk-major, [chunk][k row][128 B]
+  // swizzled. k-rows of a stage past kin read the next head's rows (their A columns are
+  // zero) or zeros past the tensor.
   CUtensorMap tw;
   if (TMA_W) {
-    const cuuint64_t dims[2] = {(cuuint64_t)p.nout, (cuuint64_t)p.h * p.kin};
-    const cuuint64_t strides[1] = {(cuuint64_t)p.nout * 2};
-    const cuuint32_t box[2] = {64, BK};
-    if (!encode_tmap_bf16_sw128(&tw, p.w, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    const cuuint64_t dims[3] = {64, (cuuint64_t)p.h * p.kin, (cuuint64_t)p.nout / 64};
+    const cuuint64_t strides[2] = {(cuuint64_t)p.nout * 2, 128};
+    const cuuint32_t box[3] = {64, BK, BN / 64};
+    if (!encode_tmap_bf16_sw128(&tw, p.w, 3, dims, strides, box)) return cudaErrorInvalidValue;
   } else {
     memset(&tw, 0, sizeof(tw));
   }

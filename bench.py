@@ -355,6 +355,20 @@ def main():
         total_ms = timed(graphs, args.steps, args.warmup)
     dec_steps = max(args.steps, 500)
     dec_ms = timed(dgraphs, dec_steps, max(3, args.warmup // 4))
+
+    def per_call(gs, n):
+        """Per-replay durations (an event pair around each replay): median, p10, p90."""
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        with torch.cuda.stream(stream):
+            ev[0].record(stream)
+            for k in range(n):
+                gs[k % NBUF].replay()
+                ev[k + 1].record(stream)
+        torch.cuda.synchronize()
+        return distribution_us([ev[k].elapsed_time(ev[k + 1]) * 1e-3 for k in range(n)])
+
+    step_dist = per_call(graphs, 300)
+    dec_dist = per_call(dgraphs, 300)
     assert da.check_errors(stream) == 0
 
     ms_per_step = total_ms / args.steps
@@ -457,6 +471,8 @@ def main():
         "step_breakdown": {
             "pipeline_us": ms_per_step * 1e3,
             "latent_call_us": dec_s * 1e6,
+            "pipeline_per_call": step_dist,
+            "latent_per_call": dec_dist,
             "pipeline_tflops": (f_core + 2 * f_proj) / step_s / 1e12,
             "pipeline_hbm_gbs": (b_core + 2 * b_proj) / step_s / 1e9,
             "latent_tflops": f_core / dec_s / 1e12,
@@ -533,7 +549,9 @@ def extras(dev, stream, hbm, tfl):
 
     def time_calls(fns, n=100, w=6):
         """Seconds per call: one CUDA graph per input set (captured after an eager
-        warm-up call), replayed round-robin, CUDA events on the stream."""
+        warm-up call), replayed round-robin, an event pair around every replay on
+        the stream. Returns the mean; the per-call median, p10 and p90 are kept in
+        `dist` for the caller's record."""
         with torch.cuda.stream(stream):
             for f in fns:
                 f()
@@ -548,15 +566,19 @@ def extras(dev, stream, hbm, tfl):
             for i in range(w):
                 graphs[i % len(graphs)].replay()
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
         with torch.cuda.stream(stream):
-            e0.record(stream)
+            ev[0].record(stream)
             for i in range(n):
                 graphs[i % len(graphs)].replay()
-            e1.record(stream)
+                ev[i + 1].record(stream)
         torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / n * 1e-3
+        per = [ev[i].elapsed_time(ev[i + 1]) * 1e-3 for i in range(n)]
+        dist.clear()
+        dist.update(distribution_us(per))
+        return ev[0].elapsed_time(ev[n]) / n * 1e-3
 
+    dist = {}
     for name in ("gqa_64_8", "gqa_paged_hkv24", "gqa_paged_hkv4", "gqa_paged_hkv1"):
         wl = W.WORKLOADS[name]
         seqlens = wl.seqlens()
@@ -581,7 +603,7 @@ def extras(dev, stream, hbm, tfl):
         t = time_calls([call(r) for r in range(nb)])
         by = cost.gqa_bytes_exact(wl.heads, wl.hkv, wl.d, seqlens, wl.s)
         fl = cost.gqa_flops_exact(wl.heads, wl.d, seqlens, wl.s)
-        res[name] = {"us": t * 1e6, "hbm_gbs": by / t / 1e9, "frac_hbm": by / t / 1e9 / hbm,
+        res[name] = {"us": t * 1e6, **dist, "hbm_gbs": by / t / 1e9, "frac_hbm": by / t / 1e9 / hbm,
                      "tflops": fl / t / 1e12, "bytes": by, "num_splits": da.last_num_splits(),
                      "l2": f"{nb} rotating caches of {by / 1e6:.0f} MB", "timing": "CUDA graph replays"}
         del qs, outs, lses, ws
@@ -595,14 +617,14 @@ def extras(dev, stream, hbm, tfl):
     qzs = [torch.empty((wl.b, wl.heads, wl.s, wl.k), dtype=torch.bfloat16, device=dev) for _ in inp]
     outs = [torch.empty((wl.b, wl.heads, wl.s, wl.d), dtype=torch.bfloat16, device=dev) for _ in inp]
     olats = [torch.randn((wl.b, wl.heads, wl.s, wl.k), device=dev).to(torch.bfloat16) for _ in inp]
+    pb = cost.proj_bytes(wl.b, wl.heads, wl.s, wl.d, wl.k)
     t_abs = time_calls([(lambda r=r: da.mla_absorb_q(inp[r].q_nope, inp[r].w_uk, sl, out=qzs[r], stream=stream))
                         for r in range(3)], n=300)
+    res["proj_absorb"] = {"us": t_abs * 1e6, **dist, "hbm_gbs": pb / t_abs / 1e9, "frac_hbm": pb / t_abs / 1e9 / hbm,
+                          "bytes": pb, "l2": "3 rotating weight sets of 16.8 MB"}
     t_out = time_calls([(lambda r=r: da.mla_out_proj(olats[r], inp[r].w_uv, sl, out=outs[r], stream=stream))
                         for r in range(3)], n=300)
-    pb = cost.proj_bytes(wl.b, wl.heads, wl.s, wl.d, wl.k)
-    res["proj_absorb"] = {"us": t_abs * 1e6, "hbm_gbs": pb / t_abs / 1e9, "frac_hbm": pb / t_abs / 1e9 / hbm,
-                          "bytes": pb, "l2": "3 rotating weight sets of 16.8 MB"}
-    res["proj_out"] = {"us": t_out * 1e6, "hbm_gbs": pb / t_out / 1e9, "frac_hbm": pb / t_out / 1e9 / hbm,
+    res["proj_out"] = {"us": t_out * 1e6, **dist, "hbm_gbs": pb / t_out / 1e9, "frac_hbm": pb / t_out / 1e9 / hbm,
                        "bytes": pb, "l2": "3 rotating weight sets of 16.8 MB"}
     del inp, qzs, outs, olats
     torch.cuda.empty_cache()
@@ -628,13 +650,66 @@ def extras(dev, stream, hbm, tfl):
         fl = cost.mla_flops_exact(wl.heads, wl.k, wl.p, seqlens, wl.s)
         by = cost.mla_bytes_exact(wl.heads, wl.k, wl.p, seqlens, wl.s)
         troof = max(fl / (tfl * 1e12), by / (hbm * 1e9))
-        res[f"mla_s{s}"] = {"us": t * 1e6, "tflops": fl / t / 1e12, "hbm_gbs": by / t / 1e9, "ai": fl / by,
+        res[f"mla_s{s}"] = {"us": t * 1e6, **dist, "tflops": fl / t / 1e12, "hbm_gbs": by / t / 1e9, "ai": fl / by,
                             "roofline_us": troof * 1e6, "frac_roofline": troof / t,
                             "bound": "tensor" if fl / (tfl * 1e12) > by / (hbm * 1e9) else "hbm",
                             "num_splits": da.last_num_splits()}
         del inp, qzs, o, lse, ws
         torch.cuda.empty_cache()
+
+    # expanded form ("Mla Analysis", Cost Models - FlashAttention; Regime Selection):
+    # the latent cache of 32 sequences of 4096 + 32 keys decompressed once into per-head
+    # keys [nope || rope] (192 values) and values (128) for all 128 heads (10.8 GB), then
+    # grouped-head decode with Hkv = Hq = 128 at each s, beside the absorbed call above
+    b, h, d, k, p, smax, t0 = 32, 128, 128, 512, 64, 32, 4096
+    cap = t0 + smax
+    x = W.make_mla(b, h, d, k, p, smax, [cap] * b, capacity=cap, seed=5, device=dev)
+    kf = torch.empty((b, cap, h, d + p), dtype=torch.bfloat16, device=dev)
+    vf = torch.empty((b, cap, h, d), dtype=torch.bfloat16, device=dev)
+    t_dec = time_calls([lambda: da.mla_decompress_kv(x.z, x.k_pe, x.w_uk, x.w_uv, k_out=kf, v_out=vf, stream=stream)],
+                       n=5, w=1)
+    rows = b * cap
+    dfl, dby = cost.decompress_flops(rows, h, d, k), cost.decompress_bytes(rows, h, d, k, p)
+    res["mla_decompress"] = {"us": t_dec * 1e6, **dist, "rows": rows, "tflops": dfl / t_dec / 1e12,
+                             "frac_tensor": dfl / t_dec / 1e12 / tfl, "hbm_gbs": dby / t_dec / 1e9,
+                             "bound": "tensor" if dfl / (tfl * 1e12) > dby / (hbm * 1e9) else "hbm",
+                             "note": "once per cached token, not per decode step"}
+    q_all = torch.cat([x.q_nope, x.q_pe], dim=-1).contiguous()  # the expanded query [q_nope || q_pe]
+    crossover = {}
+    for s in (1, 2, 4, 8, 16, 32):
+        L = t0 + (s if s > 1 else 0)  # the latent sweep's lengths
+        seqlens = [L] * b
+        sl = torch.tensor(seqlens, dtype=torch.int32, device=dev)
+        q = q_all[:, :, :s].contiguous()
+        o = torch.empty((b, h, s, d), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((b, h, s), dtype=torch.float32, device=dev)
+        wsb = da.ops.load().gqa_decode_dv_workspace_size(b, s, h, h, d + p, d, L)
+        ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+        t = time_calls([lambda: da.gqa_decode_dv(q, kf, vf, sl, scale=x.scale, max_seqlen=L, out=o, lse=lse,
+                                                 workspace=ws, stream=stream)], n=10 if s <= 8 else 5, w=2)
+        fl = cost.fa_flops_exact(h, d, p, seqlens, s)
+        by = cost.fa_bytes_exact(h, d, p, seqlens, s)
+        troof = max(fl / (tfl * 1e12), by / (hbm * 1e9))
+        res[f"mla_expanded_s{s}"] = {"us": t * 1e6, **dist, "tflops": fl / t / 1e12, "hbm_gbs": by / t / 1e9,
+                                     "ai": fl / by, "roofline_us": troof * 1e6, "frac_roofline": troof / t,
+                                     "bound": "tensor" if fl / (tfl * 1e12) > by / (hbm * 1e9) else "hbm",
+                                     "num_splits": da.last_num_splits(), "bytes": by}
+        crossover[f"s{s}"] = {"absorbed_us": res[f"mla_s{s}"]["us"], "expanded_us": t * 1e6,
+                              "expanded_over_absorbed": t * 1e6 / res[f"mla_s{s}"]["us"]}
+        del o, lse, ws
+    res["expanded_vs_absorbed"] = crossover
+    del x, kf, vf, q_all
+    torch.cuda.empty_cache()
     return res
+
+
+def distribution_us(per_call_s):
+    """Median, p10 and p90 of per-call times (seconds in, microseconds out)."""
+    import numpy as np
+
+    a = np.asarray(per_call_s, dtype=np.float64) * 1e6
+    return {"p10_us": float(np.percentile(a, 10)), "p50_us": float(np.percentile(a, 50)),
+            "p90_us": float(np.percentile(a, 90)), "calls": int(a.size)}
 
 
 if __name__ == "__main__":

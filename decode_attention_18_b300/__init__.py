@@ -1,13 +1,16 @@
 """B300-native (sm_103a) decode attention: grouped-head (MHA / GQA / MQA)
-split-KV decode and absorbed latent MLA, behind the C ABI of
-include/decattn.h. The native library is loaded on first use."""
+split-KV decode, absorbed latent MLA and the expanded (decompressed) MLA form,
+behind the C ABI of include/decattn.h. The native library is loaded on first
+use."""
 from ._native import DecAttnError, LIB_PATH, SYMBOLS  # noqa: F401
 from .ops import (  # noqa: F401
     check_errors,
     gqa_decode,
+    gqa_decode_dv,
     last_num_splits,
     mla_absorb_q,
     mla_decode,
+    mla_decompress_kv,
     mla_forward,
     mla_out_proj,
     set_forced_splits,
@@ -16,6 +19,6 @@ from .ops import (  # noqa: F401
 )
 
 __all__ = [
-    "gqa_decode", "mla_absorb_q", "mla_decode", "mla_out_proj", "mla_forward", "check_errors",
-    "set_forced_splits", "last_num_splits", "set_wait_limit_ns", "test_force_timeout", "DecAttnError",
+    "gqa_decode", "gqa_decode_dv", "mla_decompress_kv", "mla_absorb_q", "mla_decode", "mla_out_proj", "mla_forward",
+    "check_errors", "set_forced_splits", "last_num_splits", "set_wait_limit_ns", "test_force_timeout", "DecAttnError",
 ]

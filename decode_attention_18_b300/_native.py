@@ -25,6 +25,9 @@ SYMBOLS = (
     "decattn_last_num_splits",
     "decattn_test_force_timeout",
     "gqa_decode_no_alloc",
+    "gqa_decode_dv_workspace_size",
+    "gqa_decode_dv",
+    "mla_decompress_kv",
 )
 
 
@@ -87,6 +90,12 @@ def load():
     lib.decattn_test_force_timeout.argtypes = [I]
     lib.gqa_decode_no_alloc.restype = I
     lib.gqa_decode_no_alloc.argtypes = [P, P, P, KV, P, I, I, I, I, I, I, F, P, P, P]
+    lib.gqa_decode_dv_workspace_size.restype = SZ
+    lib.gqa_decode_dv_workspace_size.argtypes = [I, I, I, I, I, I, I]
+    lib.gqa_decode_dv.restype = I
+    lib.gqa_decode_dv.argtypes = [P, P, P, KV, P, I, I, I, I, I, I, I, F, P, P, P, SZ, P]
+    lib.mla_decompress_kv.restype = I
+    lib.mla_decompress_kv.argtypes = [P, P, P, P, I, I, I, I, I, P, P, P]
     _lib = lib
     return lib
 

@@ -63,6 +63,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
+constexpr int kMaxS = 32;  // new tokens per sequence in one call
+
 struct Plan {
   int nsplit;
   int chunk;
@@ -126,10 +128,10 @@ int check_kv(const decattn_kv& kv, int b, int max_seqlen) {
 }
 
 // --- grouped-head plan
-Plan gqa_plan(int b, int s, int hq, int hkv, int d, int max_seqlen, int sms) {
+Plan gqa_plan(int b, int s, int hq, int hkv, int dk, int dv, int max_seqlen, int sms) {
   const int rows = (hq / hkv) * s;
   const long long base = (long long)b * hkv * ceil_div(rows, gqa_rows_per_cta(rows));
-  const long long slots = (long long)sms * gqa_ctas_per_sm(d);
+  const long long slots = (long long)sms * gqa_ctas_per_sm(dk, dv);
   return plan_splits(base, max_seqlen, slots, 256, 512, kPage);
 }
 
@@ -146,18 +148,18 @@ struct GqaBalanced {
   long long items = 0;   // work items (sequence, KV head, row block)
   int rpb = 0;           // rows per CTA
 };
-GqaBalanced gqa_balanced(const Plan& pl, int b, int s, int hq, int hkv, int d, int sms) {
+GqaBalanced gqa_balanced(const Plan& pl, int b, int s, int hq, int hkv, int dk, int dv, int sms) {
   GqaBalanced gb;
   const int rows = (hq / hkv) * s;
   if (pl.nsplit <= 1 || g_forced_splits.load() > 0 || gqa_rows_per_cta(rows) > 16) return gb;
   gb.rpb = gqa_rows_per_cta(rows);
   gb.items = (long long)b * hkv * ceil_div(rows, gb.rpb);
-  gb.grid = sms * gqa_balanced_ctas_per_sm(d, rows);
+  gb.grid = sms * gqa_balanced_ctas_per_sm(dk, dv, rows);
   return gb;
 }
-size_t balanced_bytes(const GqaBalanced& gb, int d) {
+size_t balanced_bytes(const GqaBalanced& gb, int dv) {
   const long long records = gb.items + gb.grid;
-  return align256((size_t)records * gb.rpb * d * sizeof(float)) + align256((size_t)records * gb.rpb * sizeof(float)) +
+  return align256((size_t)records * gb.rpb * dv * sizeof(float)) + align256((size_t)records * gb.rpb * sizeof(float)) +
          align256((size_t)gb.items * 2 * sizeof(int));
 }
 
@@ -211,32 +213,36 @@ int decattn_check_errors(cudaStream_t stream) {
 
 // ------------------------------------------------------------------ grouped-head
 
-size_t gqa_decode_workspace_size(int b, int s, int hq, int hkv, int d, int max_seqlen) {
-  if (b < 1 || s < 1 || hq < 1 || hkv < 1 || hq % hkv || d < 1) return 0;
+size_t gqa_decode_dv_workspace_size(int b, int s, int hq, int hkv, int dk, int dv, int max_seqlen) {
+  if (b < 1 || s < 1 || hq < 1 || hkv < 1 || hq % hkv || dk < 1 || dv < 1) return 0;
   DeviceState* st = nullptr;
   if (device_state(&st)) return 0;
-  const Plan pl = gqa_plan(b, s, hq, hkv, d, max_seqlen, st->sms);
-  const GqaBalanced gb = gqa_balanced(pl, b, s, hq, hkv, d, st->sms);
-  if (gb.grid > 0) return balanced_bytes(gb, d);
-  return partial_bytes((long long)b * hq * s, pl.nsplit, d);
+  const Plan pl = gqa_plan(b, s, hq, hkv, dk, dv, max_seqlen, st->sms);
+  const GqaBalanced gb = gqa_balanced(pl, b, s, hq, hkv, dk, dv, st->sms);
+  if (gb.grid > 0) return balanced_bytes(gb, dv);
+  return partial_bytes((long long)b * hq * s, pl.nsplit, dv);
 }
 
-int gqa_decode(const decattn_bf16* q, const decattn_bf16* k, const decattn_bf16* v, decattn_kv kv,
-               const int32_t* seqlens, int max_seqlen, int b, int s, int hq, int hkv, int d, float scale,
-               decattn_bf16* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  if (b < 0 || s < 1 || s > 32 || hq < 1 || hkv < 1 || hq % hkv || max_seqlen < 0) return DECATTN_ERR_INVALID_ARG;
+size_t gqa_decode_workspace_size(int b, int s, int hq, int hkv, int d, int max_seqlen) {
+  return gqa_decode_dv_workspace_size(b, s, hq, hkv, d, d, max_seqlen);
+}
+
+int gqa_decode_dv(const decattn_bf16* q, const decattn_bf16* k, const decattn_bf16* v, decattn_kv kv,
+                  const int32_t* seqlens, int max_seqlen, int b, int s, int hq, int hkv, int dk, int dv, float scale,
+                  decattn_bf16* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (b < 0 || s < 1 || s > kMaxS || hq < 1 || hkv < 1 || hq % hkv || max_seqlen < 0) return DECATTN_ERR_INVALID_ARG;
   if (b == 0) return DECATTN_OK;
   if (!q || !k || !v || !seqlens || !out) return DECATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 128 && d != 256) return DECATTN_ERR_UNSUPPORTED;
+  if (!gqa_supported(dk, dv)) return DECATTN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return DECATTN_ERR_INVALID_ARG;
   if (hkv > 65535 || b > 65535) return DECATTN_ERR_INVALID_ARG;
   if (int rc = check_kv(kv, b, max_seqlen)) return rc;
   DeviceState* st = nullptr;
   if (int rc = device_state(&st)) return rc;
-  const Plan pl = gqa_plan(b, s, hq, hkv, d, max_seqlen, st->sms);
-  const GqaBalanced gb = gqa_balanced(pl, b, s, hq, hkv, d, st->sms);
+  const Plan pl = gqa_plan(b, s, hq, hkv, dk, dv, max_seqlen, st->sms);
+  const GqaBalanced gb = gqa_balanced(pl, b, s, hq, hkv, dk, dv, st->sms);
   const long long rows = (long long)b * hq * s;
-  const size_t need = gb.grid > 0 ? balanced_bytes(gb, d) : partial_bytes(rows, pl.nsplit, d);
+  const size_t need = gb.grid > 0 ? balanced_bytes(gb, dv) : partial_bytes(rows, pl.nsplit, dv);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return DECATTN_ERR_WORKSPACE;
   GqaLaunch a;
   a.q = q;
@@ -252,7 +258,8 @@ int gqa_decode(const decattn_bf16* q, const decattn_bf16* k, const decattn_bf16*
   a.s = s;
   a.hq = hq;
   a.hkv = hkv;
-  a.d = d;
+  a.dk = dk;
+  a.dv = dv;
   a.nsplit = pl.nsplit;
   a.chunk = pl.chunk;
   a.scale = scale;
@@ -260,14 +267,14 @@ int gqa_decode(const decattn_bf16* q, const decattn_bf16* k, const decattn_bf16*
   a.lse = lse;
   a.ws_o = pl.nsplit > 1 ? static_cast<float*>(workspace) : nullptr;
   a.ws_lse = pl.nsplit > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                                       align256((size_t)rows * pl.nsplit * d * sizeof(float)))
+                                                       align256((size_t)rows * pl.nsplit * dv * sizeof(float)))
                            : nullptr;
   a.meta = nullptr;
   a.balanced_grid = gb.grid;
   if (gb.grid > 0) {
     const long long records = gb.items + gb.grid;
     char* w = static_cast<char*>(workspace);
-    const size_t o_bytes = align256((size_t)records * gb.rpb * d * sizeof(float));
+    const size_t o_bytes = align256((size_t)records * gb.rpb * dv * sizeof(float));
     a.ws_o = reinterpret_cast<float*>(w);
     a.ws_lse = reinterpret_cast<float*>(w + o_bytes);
     a.meta = reinterpret_cast<int*>(w + o_bytes + align256((size_t)records * gb.rpb * sizeof(float)));
@@ -278,21 +285,28 @@ int gqa_decode(const decattn_bf16* q, const decattn_bf16* k, const decattn_bf16*
   g_last_splits.store(pl.nsplit);
   if (launch_gqa(a, stream) != cudaSuccess) return DECATTN_ERR_CUDA;
   if (gb.grid > 0) {
-    if (launch_combine_balanced(a.ws_o, a.ws_lse, a.meta, seqlens, b, hq, s, hkv, d, gb.items + gb.grid, out, lse,
+    if (launch_combine_balanced(a.ws_o, a.ws_lse, a.meta, seqlens, b, hq, s, hkv, dv, gb.items + gb.grid, out, lse,
                                 stream) != cudaSuccess)
       return DECATTN_ERR_CUDA;
   } else if (pl.nsplit > 1) {
-    if (launch_combine(a.ws_o, false, a.ws_lse, seqlens, (int)rows, hq * s, pl.nsplit, pl.chunk, d, out, lse, stream) !=
-        cudaSuccess)
+    if (launch_combine(a.ws_o, false, a.ws_lse, seqlens, (int)rows, hq * s, pl.nsplit, pl.chunk, dv, out, lse,
+                       stream) != cudaSuccess)
       return DECATTN_ERR_CUDA;
   }
   return DECATTN_OK;
 }
 
+int gqa_decode(const decattn_bf16* q, const decattn_bf16* k, const decattn_bf16* v, decattn_kv kv,
+               const int32_t* seqlens, int max_seqlen, int b, int s, int hq, int hkv, int d, float scale,
+               decattn_bf16* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return gqa_decode_dv(q, k, v, kv, seqlens, max_seqlen, b, s, hq, hkv, d, d, scale, out, lse, workspace,
+                       workspace_bytes, stream);
+}
+
 // ------------------------------------------------------------------ MLA
 
 static int check_proj(const void* a, const void* w, const void* c, int b, int s, int h, int kin, int nout) {
-  if (b < 0 || s < 1 || s > 32 || h < 1 || kin < 8 || nout < 8) return DECATTN_ERR_INVALID_ARG;
+  if (b < 0 || s < 1 || s > kMaxS || h < 1 || kin < 8 || nout < 8) return DECATTN_ERR_INVALID_ARG;
   if (!a || !w || !c) return DECATTN_ERR_INVALID_ARG;
   if (kin % 8 || nout % 8) return DECATTN_ERR_UNSUPPORTED;
   if (!aligned16(a) || !aligned16(w) || !aligned16(c)) return DECATTN_ERR_INVALID_ARG;
@@ -320,6 +334,23 @@ int mla_out_proj(const decattn_bf16* o_lat, const decattn_bf16* w_uv, decattn_bf
   return launch_proj(a, st->sms, stream) == cudaSuccess ? DECATTN_OK : DECATTN_ERR_CUDA;
 }
 
+int mla_decompress_kv(const decattn_bf16* z, const decattn_bf16* k_pe, const decattn_bf16* w_uk,
+                      const decattn_bf16* w_uv, int rows, int h, int d, int k, int p, decattn_bf16* k_out,
+                      decattn_bf16* v_out, cudaStream_t stream) {
+  if (rows < 0 || h < 1 || d < 1 || k < 1 || p < 0) return DECATTN_ERR_INVALID_ARG;
+  if (rows == 0) return DECATTN_OK;
+  if (!z || !k_pe || !w_uk || !w_uv || !k_out || !v_out) return DECATTN_ERR_INVALID_ARG;
+  if (!mla_expand_supported(d, k, p)) return DECATTN_ERR_UNSUPPORTED;
+  if (!aligned16(z) || !aligned16(k_pe) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(k_out) ||
+      !aligned16(v_out))
+    return DECATTN_ERR_INVALID_ARG;
+  if (h > 65535 * 8 || (long long)h * k > INT_MAX) return DECATTN_ERR_INVALID_ARG;
+  DeviceState* st = nullptr;
+  if (int rc = device_state(&st)) return rc;
+  ExpandLaunch a{z, k_pe, w_uk, w_uv, k_out, v_out, rows, h, k, st->err, wait_limit()};
+  return launch_mla_expand(a, stream) == cudaSuccess ? DECATTN_OK : DECATTN_ERR_CUDA;
+}
+
 size_t mla_decode_workspace_size(int b, int s, int h, int k, int max_seqlen) {
   if (b < 1 || s < 1 || h < 1 || k < 1) return 0;
   DeviceState* st = nullptr;
@@ -332,7 +363,7 @@ int mla_decode(const decattn_bf16* qz, const decattn_bf16* q_pe, const decattn_b
                decattn_kv kv, const int32_t* seqlens, int max_seqlen, int b, int s, int h, int k, int p,
                float scale, decattn_bf16* o_lat, float* lse, void* workspace, size_t workspace_bytes,
                cudaStream_t stream) {
-  if (b < 0 || s < 1 || s > 32 || h < 1 || max_seqlen < 0) return DECATTN_ERR_INVALID_ARG;
+  if (b < 0 || s < 1 || s > kMaxS || h < 1 || max_seqlen < 0) return DECATTN_ERR_INVALID_ARG;
   if (b == 0) return DECATTN_OK;
   if (!qz || !q_pe || !z || !k_pe || !seqlens || !o_lat) return DECATTN_ERR_INVALID_ARG;
   if (!mla_supported(k, p)) return DECATTN_ERR_UNSUPPORTED;

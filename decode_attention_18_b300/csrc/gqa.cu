@@ -59,24 +59,29 @@ constexpr float kRescaleLog2 = 8.f;  // move a row's reference maximum only past
 constexpr unsigned long long kTeardownNs = 1000000000ull;  // 1 s for own copies after a time-out
 constexpr unsigned long long kTestWaitNs = 1000000ull;     // 1 ms forced-timeout wait
 
-template <int D, int MT_>
+// DK: width of a query / key row; DV: width of a value / output row (equal for plain
+// grouped-head attention; 192 and 128 for the expanded MLA form, whose keys carry the
+// 64 RoPE dimensions that its values lack).
+template <int DK, int DV, int MT_>
 struct GqaCfg {
   static constexpr int MT = MT_;  // 16-row m-tiles per CTA
   static constexpr int THREADS = 128 * MT;
-  static constexpr int NST = D <= 64 ? 4 : 3;  // pipeline stages
-  static constexpr int ROW_BYTES = D * 2;
-  static constexpr int TILE_BYTES = kTileKeys * ROW_BYTES;  // one K (or V) tile
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int K_TILE = kTileKeys * DK * 2;  // one K tile
+  static constexpr int V_TILE = kTileKeys * DV * 2;  // one V tile
+  static constexpr int STAGE_BYTES = K_TILE + V_TILE;
+  // pipeline stages: 4 for small rows, 3 for 128 or 256 dims (two resp. one CTA per SM);
+  // the 192/128 form takes 4 (160 KB, one CTA per SM, three tiles in flight)
+  static constexpr int NST = (DK <= 64 || DK != DV) ? 4 : 3;
   static constexpr int PIPE_BYTES = NST * STAGE_BYTES;
-  static constexpr int OSTR = D + 2;  // padded fp32 row stride of the merge buffer
+  static constexpr int OSTR = DV + 2;  // padded fp32 row stride of the merge buffer
   static constexpr int RED_BYTES = kSlices * 16 * MT * OSTR * 4;
   static constexpr int SMEM = PIPE_BYTES > RED_BYTES ? PIPE_BYTES : RED_BYTES;
   static constexpr int BLK = kTileKeys * 128;  // one [64 keys x 64 dims] block of a tile
-  static_assert(D % 64 == 0, "tiles are 64-dim blocks");
+  static_assert(DK % 64 == 0 && DV % 64 == 0, "tiles are 64-dim blocks");
 };
 
 // Shared-memory offset of 16-byte chunk c (8 dims) of key row r in a K or V tile: the
-// tile is D/64 blocks of [64 keys x 128 bytes], each with the 128-byte swizzle (chunk
+// tile is DK/64 (K) or DV/64 (V) blocks of [64 keys x 128 bytes], each with the 128-byte swizzle (chunk
 // index XOR row mod 8) that TMA writes and that keeps ldmatrix free of bank conflicts.
 __device__ __forceinline__ uint32_t tile_off(int r, int c) {
   return (uint32_t)((c >> 3) * (kTileKeys * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
@@ -86,21 +91,22 @@ __device__ __forceinline__ uint32_t tile_off(int r, int c) {
 enum SegOut { kSegFinal = 0, kSegSplit = 1, kSegRecord = 2 };
 
 // Attention of the query rows of block rb of KV head g of sequence bi over keys
-// [kstart, kend) (kstart < kend <= L). out_mode kSegFinal writes bf16 rows and the
+// [kstart, kend) (kstart < kend <= L). Query and key rows are DK wide, value and
+// output rows DV wide. out_mode kSegFinal writes bf16 rows and the
 // LSE; kSegSplit writes fp32 partials at chunk index `slot` of the [row][nsplit]
-// layout; kSegRecord writes partial record `slot` ([record][16*MT rows][D]) of the
+// layout; kSegRecord writes partial record `slot` ([record][16*MT rows][DV]) of the
 // balanced schedule. The caller's threads all enter; shared memory is free again
 // when it returns. Returns false (in every thread) when a tile wait ran out: the
 // error is recorded, the copies already requested have been waited for (bounded) and
 // nothing was written.
-template <int D, int MT>
+template <int DK, int DV, int MT>
 __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                             uint64_t* full, uint64_t* never, uint32_t& phase, uint8_t* smem,
                                             float (*s_m)[kSlices][16], float (*s_l)[kSlices][16], int bi, int g,
                                             int rb, int L, int kstart, int kend, int out_mode, int slot) {
-  using C = GqaCfg<D, MT>;
-  constexpr int NT = D / 8;   // n-tiles of the output
-  constexpr int KS = D / 16;  // k-steps of QK^T
+  using C = GqaCfg<DK, DV, MT>;
+  constexpr int NT = DV / 8;   // n-tiles of the output
+  constexpr int KS = DK / 16;  // k-steps of QK^T
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -126,15 +132,15 @@ __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMa
       uint32_t val = 0;
       if (r < p.R) {
         const int j = g * p.G + r / p.s;
-        const size_t off = ((size_t)(bi * p.hq + j) * p.s + (r % p.s)) * D + col;
+        const size_t off = ((size_t)(bi * p.hq + j) * p.s + (r % p.s)) * DK + col;
         val = __ldg(reinterpret_cast<const unsigned int*>(p.q + off));
       }
       qa[ks][e] = val;
     }
   }
 
-  // ---- K/V tiles by TMA. Thread 0 requests tile t of this KV head's K and V as D/64
-  // boxes of [64 tokens x 64 dims] each (3-D tensor maps over [tokens, KV heads, d]),
+  // ---- K/V tiles by TMA. Thread 0 requests tile t of this KV head's K and V as DK/64
+  // and DV/64 boxes of [64 tokens x 64 dims] (3-D tensor maps over [tokens, KV heads, d]),
   // completing on the stage's mbarrier; every thread waits on it (bounded). For a paged
   // cache the tile is one page. Rows past the segment's end are read as they are (or as
   // zeros past the tensor) and made harmless below.
@@ -160,10 +166,10 @@ __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMa
     fence_proxy_async_smem();  // this thread's view: earlier generic writes to the stage come first
     mbar_expect_tx(&full[stage], C::STAGE_BYTES);
 #pragma unroll
-    for (int kb = 0; kb < D / 64; ++kb) {
-      tma_load_3d(kdst + kb * C::BLK, tm_k, kb * 64, g, row0, &full[stage]);
-      tma_load_3d(kdst + C::TILE_BYTES + kb * C::BLK, tm_v, kb * 64, g, row0, &full[stage]);
-    }
+    for (int kb = 0; kb < DK / 64; ++kb) tma_load_3d(kdst + kb * C::BLK, tm_k, kb * 64, g, row0, &full[stage]);
+#pragma unroll
+    for (int kb = 0; kb < DV / 64; ++kb)
+      tma_load_3d(kdst + C::K_TILE + kb * C::BLK, tm_v, kb * 64, g, row0, &full[stage]);
   };
 
   // ---- online-softmax state and output accumulator (rows lane/4 and lane/4 + 8)
@@ -186,7 +192,7 @@ __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMa
   for (int t = 0; t < ntiles; ++t) {
     const int stage = t % C::NST;
     const uint32_t kbase = sbase + stage * C::STAGE_BYTES;
-    const uint32_t vbase = kbase + C::TILE_BYTES;
+    const uint32_t vbase = kbase + C::K_TILE;
     bool landed = mbar_wait(&full[stage], (phase >> stage) & 1u, p.wait_ns, nullptr);
     if (t == 0 && p.test_timeout) landed = mbar_wait(never, 0, kTestWaitNs, nullptr) && landed;
     phase ^= 1u << stage;
@@ -194,9 +200,9 @@ __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMa
     // but 0 * NaN is NaN in P V, so they are zeroed (K rows there only feed masked scores)
     const int nvalid = kend - (kstart + t * kTileKeys);
     if (landed && nvalid < kTileKeys) {
-      for (int idx = tid; idx < (kTileKeys - nvalid) * (D / 8); idx += C::THREADS) {
-        const int r = nvalid + idx / (D / 8);
-        *reinterpret_cast<uint4*>(smem + (vbase - sbase) + tile_off(r, idx % (D / 8))) = make_uint4(0, 0, 0, 0);
+      for (int idx = tid; idx < (kTileKeys - nvalid) * (DV / 8); idx += C::THREADS) {
+        const int r = nvalid + idx / (DV / 8);
+        *reinterpret_cast<uint4*>(smem + (vbase - sbase) + tile_off(r, idx % (DV / 8))) = make_uint4(0, 0, 0, 0);
       }
     }
     // tile t complete for everyone; every warp is done with tile t-1's stage
@@ -298,7 +304,7 @@ __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMa
     {
       const int kr = slice * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
-      for (int dp = 0; dp < D / 16; ++dp) {
+      for (int dp = 0; dp < DV / 16; ++dp) {
         const int c = dp * 2 + ((lane >> 4) & 1);
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4_trans(vbase + tile_off(kr, c), b0, b1, b2, b3);
@@ -338,9 +344,9 @@ __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMa
   __syncthreads();
 
   // ---- final rows (one chunk) or fp32 partials
-  for (int idx = tid; idx < 16 * MT * (D / 4); idx += C::THREADS) {
-    const int rr = idx / (D / 4);  // row within the CTA
-    const int c4 = (idx % (D / 4)) * 4;
+  for (int idx = tid; idx < 16 * MT * (DV / 4); idx += C::THREADS) {
+    const int rr = idx / (DV / 4);  // row within the CTA
+    const int c4 = (idx % (DV / 4)) * 4;
     const int m2 = rr / 16, r = rr % 16;
     const int rg = rb * MT * 16 + rr;
     if (rg >= p.R) continue;
@@ -372,14 +378,14 @@ __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMa
       uint2 pk;
       pk.x = pack_bf16(acc.x, acc.y);
       pk.y = pack_bf16(acc.z, acc.w);
-      *reinterpret_cast<uint2*>(p.out + rowflat * D + c4) = pk;
+      *reinterpret_cast<uint2*>(p.out + rowflat * DV + c4) = pk;
       if (p.lse && c4 == 0) p.lse[rowflat] = lse;
     } else if (out_mode == kSegSplit) {
-      *reinterpret_cast<float4*>(p.ws_o + (rowflat * p.nsplit + slot) * D + c4) = acc;
+      *reinterpret_cast<float4*>(p.ws_o + (rowflat * p.nsplit + slot) * DV + c4) = acc;
       if (c4 == 0) p.ws_lse[rowflat * p.nsplit + slot] = lse;
     } else {
       const size_t rec_row = (size_t)slot * (16 * MT) + rr;
-      *reinterpret_cast<float4*>(p.ws_o + rec_row * D + c4) = acc;
+      *reinterpret_cast<float4*>(p.ws_o + rec_row * DV + c4) = acc;
       if (c4 == 0) p.ws_lse[rec_row] = lse;
     }
   }
@@ -410,10 +416,10 @@ __device__ __forceinline__ bool cta_setup(const GqaParams& p, const CUtensorMap*
 }
 
 // One CTA per (sequence, KV head, context chunk, block of query rows).
-template <int D, int MT>
+template <int DK, int DV, int MT>
 __global__ void __launch_bounds__(128 * MT)
     gqa_split_kernel(GqaParams p, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
-  using C = GqaCfg<D, MT>;
+  using C = GqaCfg<DK, DV, MT>;
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ float s_m[MT][kSlices][16];
   __shared__ float s_l[MT][kSlices][16];
@@ -431,19 +437,19 @@ __global__ void __launch_bounds__(128 * MT)
   const int kstart = split * p.chunk;
   if (kstart >= L) {  // chunk past the end: the combine skips it
     if (L <= 0 && p.nsplit == 1) {  // empty sequence without a combine pass: zero rows, LSE = -inf
-      for (int idx = tid; idx < 16 * MT * (D / 8); idx += C::THREADS) {
-        const int rg = rb * MT * 16 + idx / (D / 8);
+      for (int idx = tid; idx < 16 * MT * (DV / 8); idx += C::THREADS) {
+        const int rg = rb * MT * 16 + idx / (DV / 8);
         if (rg >= p.R) continue;
         const size_t rowflat = (size_t)(bi * p.hq + g * p.G + rg / p.s) * p.s + (rg % p.s);
-        *reinterpret_cast<uint4*>(p.out + rowflat * D + (idx % (D / 8)) * 8) = make_uint4(0, 0, 0, 0);
-        if (p.lse && idx % (D / 8) == 0) p.lse[rowflat] = -INFINITY;
+        *reinterpret_cast<uint4*>(p.out + rowflat * DV + (idx % (DV / 8)) * 8) = make_uint4(0, 0, 0, 0);
+        if (p.lse && idx % (DV / 8) == 0) p.lse[rowflat] = -INFINITY;
       }
     }
     return;
   }
   const int kend = min(L, kstart + p.chunk);
-  gqa_segment<D, MT>(p, &tm_k, &tm_v, full, full + C::NST, phase, smem, s_m, s_l, bi, g, rb, L, kstart, kend,
-                     p.nsplit == 1 ? kSegFinal : kSegSplit, split);
+  gqa_segment<DK, DV, MT>(p, &tm_k, &tm_v, full, full + C::NST, phase, smem, s_m, s_l, bi, g, rb, L, kstart, kend,
+                          p.nsplit == 1 ? kSegFinal : kSegSplit, split);
 }
 
 __device__ __forceinline__ long long tiles_of(int L) { return L > 0 ? (L + kTileKeys - 1) / kTileKeys : 0; }
@@ -457,11 +463,11 @@ __device__ __forceinline__ long long tiles_of(int L) { return L > 0 ? (L + kTile
 // the order) and the CTA holding the item's first tile stores {first record, count}
 // in meta for the combine kernel. Computed from seqlens on the device, so the launch
 // needs only an upper bound of the lengths.
-template <int D, int MT>
+template <int DK, int DV, int MT>
 __global__ void __launch_bounds__(128 * MT)
     gqa_balanced_kernel(GqaParams p, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v) {
-  using C = GqaCfg<D, MT>;
+  using C = GqaCfg<DK, DV, MT>;
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ float s_m[MT][kSlices][16];
   __shared__ float s_l[MT][kSlices][16];
@@ -565,9 +571,9 @@ __global__ void __launch_bounds__(128 * MT)
     // tile lies in this CTA's range still gets its meta entry, so the combine reads only
     // records inside the workspace.
     if (!aborted)
-      aborted = !gqa_segment<D, MT>(p, &tm_k, &tm_v, full, full + C::NST, phase, smem, s_m, s_l, i, g, rb, L,
-                                    t0 * kTileKeys, min(L, t1 * kTileKeys), c0 == c1 ? kSegFinal : kSegRecord,
-                                    (int)(item + blockIdx.x));
+      aborted = !gqa_segment<DK, DV, MT>(p, &tm_k, &tm_v, full, full + C::NST, phase, smem, s_m, s_l, i, g, rb, L,
+                                         t0 * kTileKeys, min(L, t1 * kTileKeys), c0 == c1 ? kSegFinal : kSegRecord,
+                                         (int)(item + blockIdx.x));
     else
       __syncthreads();
     // (both branches end with a barrier: every thread has read the state above)
@@ -580,22 +586,24 @@ __global__ void __launch_bounds__(128 * MT)
   }
 }
 
-template <int D, int MT>
+template <int DK, int DV, int MT>
 cudaError_t launch_gqa_dm(const GqaParams& p, int nsplit, int hkv, int b, int balanced_grid, cudaStream_t stream) {
-  using C = GqaCfg<D, MT>;
+  using C = GqaCfg<DK, DV, MT>;
   static std::atomic<unsigned long long> split_attr{0}, balanced_attr{0};
-  if (cudaError_t e = ensure_smem_limit(gqa_split_kernel<D, MT>, C::SMEM, split_attr)) return e;
-  if (cudaError_t e = ensure_smem_limit(gqa_balanced_kernel<D, MT>, C::SMEM, balanced_attr)) return e;
-  // K and V as [tokens, KV heads, d] (contiguous: tokens = b x capacity; paged: pages x 64),
-  // read in boxes of [64 tokens, 1 head, 64 dims]
+  if (cudaError_t e = ensure_smem_limit(gqa_split_kernel<DK, DV, MT>, C::SMEM, split_attr)) return e;
+  if (cudaError_t e = ensure_smem_limit(gqa_balanced_kernel<DK, DV, MT>, C::SMEM, balanced_attr)) return e;
+  // K and V as [tokens, KV heads, width] (contiguous: tokens = b x capacity; paged:
+  // pages x 64), read in boxes of [64 tokens, 1 head, 64 dims]
   CUtensorMap tk, tv;
   {
     const uint64_t tokens = p.paged ? (uint64_t)p.num_pages * kTileKeys : (uint64_t)p.b * p.capacity;
-    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.hkv, (cuuint64_t)tokens};
-    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.hkv * D * 2};
     const cuuint32_t box[3] = {64, 1, kTileKeys};
-    if (!encode_tmap_bf16_sw128(&tk, p.k, 3, dims, strides, box) ||
-        !encode_tmap_bf16_sw128(&tv, p.v, 3, dims, strides, box))
+    const cuuint64_t kdims[3] = {(cuuint64_t)DK, (cuuint64_t)p.hkv, (cuuint64_t)tokens};
+    const cuuint64_t kstrides[2] = {(cuuint64_t)DK * 2, (cuuint64_t)p.hkv * DK * 2};
+    const cuuint64_t vdims[3] = {(cuuint64_t)DV, (cuuint64_t)p.hkv, (cuuint64_t)tokens};
+    const cuuint64_t vstrides[2] = {(cuuint64_t)DV * 2, (cuuint64_t)p.hkv * DV * 2};
+    if (!encode_tmap_bf16_sw128(&tk, p.k, 3, kdims, kstrides, box) ||
+        !encode_tmap_bf16_sw128(&tv, p.v, 3, vdims, vstrides, box))
       return cudaErrorInvalidValue;
   }
   // programmatic dependent launch: the CTAs may be scheduled while the previous kernel
@@ -610,8 +618,8 @@ cudaError_t launch_gqa_dm(const GqaParams& p, int nsplit, int hkv, int b, int ba
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = balanced_grid > 0 ? cudaLaunchKernelEx(&cfg, gqa_balanced_kernel<D, MT>, p, tk, tv)
-                                          : cudaLaunchKernelEx(&cfg, gqa_split_kernel<D, MT>, p, tk, tv);
+  const cudaError_t e = balanced_grid > 0 ? cudaLaunchKernelEx(&cfg, gqa_balanced_kernel<DK, DV, MT>, p, tk, tv)
+                                          : cudaLaunchKernelEx(&cfg, gqa_split_kernel<DK, DV, MT>, p, tk, tv);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -623,16 +631,16 @@ static int gqa_mt(int rows) { return rows <= 16 ? 1 : 2; }
 int gqa_rows_per_cta(int rows) { return 16 * gqa_mt(rows); }
 
 // Resident CTAs per SM of the balanced kernel (its grid is one wave of them).
-template <int D, int MT>
+template <int DK, int DV, int MT>
 static int balanced_occupancy() {
-  using C = GqaCfg<D, MT>;
+  using C = GqaCfg<DK, DV, MT>;
   // (the same GPU model on every device of a process is assumed for the cached value)
   static std::atomic<int> cached{0};
   static std::atomic<unsigned long long> attr{0};
   int n = cached.load(std::memory_order_relaxed);
   if (n == 0) {
-    if (ensure_smem_limit(gqa_balanced_kernel<D, MT>, C::SMEM, attr) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_balanced_kernel<D, MT>, C::THREADS, C::SMEM) !=
+    if (ensure_smem_limit(gqa_balanced_kernel<DK, DV, MT>, C::SMEM, attr) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_balanced_kernel<DK, DV, MT>, C::THREADS, C::SMEM) !=
             cudaSuccess ||
         n <= 0)
       return 1;
@@ -641,16 +649,24 @@ static int balanced_occupancy() {
   return n;
 }
 
-int gqa_balanced_ctas_per_sm(int d, int rows) {
+int gqa_balanced_ctas_per_sm(int dk, int dv, int rows) {
   const bool two = gqa_mt(rows) == 2;
-  switch (d) {
-    case 64: return two ? balanced_occupancy<64, 2>() : balanced_occupancy<64, 1>();
-    case 128: return two ? balanced_occupancy<128, 2>() : balanced_occupancy<128, 1>();
-    case 256: return two ? balanced_occupancy<256, 2>() : balanced_occupancy<256, 1>();
+  if (dk == 192 && dv == 128) return two ? balanced_occupancy<192, 128, 2>() : balanced_occupancy<192, 128, 1>();
+  if (dk != dv) return 1;
+  switch (dk) {
+    case 64: return two ? balanced_occupancy<64, 64, 2>() : balanced_occupancy<64, 64, 1>();
+    case 128: return two ? balanced_occupancy<128, 128, 2>() : balanced_occupancy<128, 128, 1>();
+    case 256: return two ? balanced_occupancy<256, 256, 2>() : balanced_occupancy<256, 256, 1>();
     default: return 1;
   }
 }
-int gqa_ctas_per_sm(int d) { return d <= 64 ? 3 : (d <= 128 ? 2 : 1); }
+int gqa_ctas_per_sm(int dk, int dv) {
+  if (dk != dv) return 1;
+  return dk <= 64 ? 3 : (dk <= 128 ? 2 : 1);
+}
+bool gqa_supported(int dk, int dv) {
+  return (dk == dv && (dk == 64 || dk == 128 || dk == 256)) || (dk == 192 && dv == 128);
+}
 
 cudaError_t launch_gqa(const GqaLaunch& a, cudaStream_t stream) {
   GqaParams p;
@@ -682,18 +698,16 @@ cudaError_t launch_gqa(const GqaLaunch& a, cudaStream_t stream) {
   p.err = a.err;
   p.wait_ns = a.wait_ns;
   p.test_timeout = a.test_timeout;
-#define DECATTN_GQA_CASE(D)                                                                  \
-  case D:                                                                                    \
-    return mt == 1 ? launch_gqa_dm<D, 1>(p, a.nsplit, a.hkv, a.b, a.balanced_grid, stream)   \
-                   : launch_gqa_dm<D, 2>(p, a.nsplit, a.hkv, a.b, a.balanced_grid, stream);
-  switch (a.d) {
-    DECATTN_GQA_CASE(64)
-    DECATTN_GQA_CASE(128)
-    DECATTN_GQA_CASE(256)
-    default:
-      return cudaErrorInvalidValue;
-  }
+#define DECATTN_GQA_CASE(DK, DV)                                                                     \
+  if (a.dk == DK && a.dv == DV)                                                                      \
+    return mt == 1 ? launch_gqa_dm<DK, DV, 1>(p, a.nsplit, a.hkv, a.b, a.balanced_grid, stream)      \
+                   : launch_gqa_dm<DK, DV, 2>(p, a.nsplit, a.hkv, a.b, a.balanced_grid, stream);
+  DECATTN_GQA_CASE(64, 64)
+  DECATTN_GQA_CASE(128, 128)
+  DECATTN_GQA_CASE(256, 256)
+  DECATTN_GQA_CASE(192, 128)
 #undef DECATTN_GQA_CASE
+  return cudaErrorInvalidValue;
 }
 
 // ---------------------------------------------------------------------------

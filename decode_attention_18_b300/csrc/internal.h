@@ -15,12 +15,13 @@ struct GqaLaunch {
   const int32_t* seqlens;
   const int32_t* block_table;
   int max_pages, paged, capacity, num_pages;
-  int b, s, hq, hkv, d;
+  int b, s, hq, hkv;
+  int dk, dv;  // query/key width, value/output width
   int nsplit, chunk;
   float scale;
   void* out;
   float* lse;
-  float* ws_o;    // [b*hq*s, nsplit, d] (nsplit > 1), or balanced: [records, rows per CTA, d]
+  float* ws_o;    // [b*hq*s, nsplit, dv] (nsplit > 1), or balanced: [records, rows per CTA, dv]
   float* ws_lse;  // [b*hq*s, nsplit], or balanced: [records, rows per CTA]
   int* meta;      // balanced: [work items][2] {first record, count}
   int balanced_grid;  // > 0: balanced schedule over this many CTAs (mma.sync kernel)
@@ -29,10 +30,11 @@ struct GqaLaunch {
   int test_timeout;            // forced-timeout test: one wait on a barrier nothing signals
 };
 
-// rows of one grouped-head CTA (multiple of 16) for head dim d
-int gqa_rows_per_cta(int d);
-int gqa_ctas_per_sm(int d);
-int gqa_balanced_ctas_per_sm(int d, int rows);  // measured occupancy of the balanced kernel
+// rows of one grouped-head CTA (multiple of 16) for `rows` query rows per KV head
+int gqa_rows_per_cta(int rows);
+int gqa_ctas_per_sm(int dk, int dv);
+int gqa_balanced_ctas_per_sm(int dk, int dv, int rows);  // measured occupancy of the balanced kernel
+bool gqa_supported(int dk, int dv);
 cudaError_t launch_gqa(const GqaLaunch& p, cudaStream_t stream);
 
 // log-sum-exp merge of split partials: rows x nsplit partials of width d (fp32, or bf16
@@ -75,6 +77,21 @@ struct MlaLaunch {
   unsigned long long wait_ns;
   int test_timeout;
 };
+// Expanded-form MLA cache: K = [Z W_uk^T || K_pe], V = Z W_uv for `rows` cache rows
+struct ExpandLaunch {
+  const void* z;     // [rows, k]
+  const void* k_pe;  // [rows, p]
+  const void* w_uk;  // [h, d, k]
+  const void* w_uv;  // [h, k, d]
+  void* k_out;       // [rows, h, d + p]
+  void* v_out;       // [rows, h, d]
+  int rows, h, k;
+  unsigned* err;
+  unsigned long long wait_ns;
+};
+bool mla_expand_supported(int d, int k, int p);
+cudaError_t launch_mla_expand(const ExpandLaunch& p, cudaStream_t stream);
+
 // CTAs per 128-row tile of the latent kernel (a cluster: scores CTA + output CTA)
 int mla_ctas_per_row_tile();
 // keys per latent tile (context chunks are multiples of it)

@@ -82,6 +82,46 @@ def gqa_decode(q, k, v, seqlens, *, max_seqlen=None, scale=None, block_table=Non
     return out, lse
 
 
+def gqa_decode_dv(q, k, v, seqlens, *, scale, max_seqlen=None, block_table=None, out=None, lse=None,
+                  return_lse=True, workspace=None, stream=None):
+    """Grouped-head decode with value rows of their own width: q [b, Hq, s, dk],
+    k [b, capacity, Hkv, dk], v [b, capacity, Hkv, dv] (or paged pools with
+    block_table). Returns (out [b, Hq, s, dv] bf16, lse [b, Hq, s] or None)."""
+    lib = load()
+    _need(q, "q"), _need(k, "k"), _need(v, "v"), _need(seqlens, "seqlens", torch.int32)
+    b, hq, s, dk = (int(x) for x in q.shape)
+    hkv, dv = int(k.shape[2]), int(v.shape[3])
+    L = _max_seqlen(seqlens, max_seqlen)
+    if out is None:
+        out = torch.empty((b, hq, s, dv), dtype=_BF16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((b, hq, s), dtype=torch.float32, device=q.device)
+    ws, wsb = _workspace(lib.gqa_decode_dv_workspace_size(b, s, hq, hkv, dk, dv, L), workspace, q.device)
+    check(lib.gqa_decode_dv(_p(q), _p(k), _p(v), _kv_desc(k, block_table), _p(seqlens), L, b, s, hq, hkv, dk, dv,
+                            float(scale), _p(out), _p(lse), _p(ws), wsb, _stream(stream)), "gqa_decode_dv")
+    return out, lse
+
+
+def mla_decompress_kv(z, k_pe, w_uk, w_uv, *, k_out=None, v_out=None, stream=None):
+    """Expanded-form cache: K = [Z W_uk^T || K_pe], V = Z W_uv for every cache row.
+    z [..., k] and k_pe [..., p] with the same leading (row) shape, w_uk [h, d, k],
+    w_uv [h, k, d]. Returns (k_out [..., h, d + p], v_out [..., h, d])."""
+    lib = load()
+    for t, n in ((z, "z"), (k_pe, "k_pe"), (w_uk, "w_uk"), (w_uv, "w_uv")):
+        _need(t, n)
+    lead = tuple(int(x) for x in z.shape[:-1])
+    rows = int(math.prod(lead))
+    k, p = int(z.shape[-1]), int(k_pe.shape[-1])
+    h, d = int(w_uk.shape[0]), int(w_uk.shape[1])
+    if k_out is None:
+        k_out = torch.empty(lead + (h, d + p), dtype=_BF16, device=z.device)
+    if v_out is None:
+        v_out = torch.empty(lead + (h, d), dtype=_BF16, device=z.device)
+    check(lib.mla_decompress_kv(_p(z), _p(k_pe), _p(w_uk), _p(w_uv), rows, h, d, k, p, _p(k_out), _p(v_out),
+                                _stream(stream)), "mla_decompress_kv")
+    return k_out, v_out
+
+
 def mla_absorb_q(q_nope, w_uk, seqlens=None, *, scale=1.0, out=None, stream=None):
     """Qz = scale * q_nope @ W_uk per head. q_nope [b, h, s, d], w_uk [h, d, k]."""
     lib = load()

@@ -104,6 +104,42 @@ int gqa_decode(const decattn_bf16* q, const decattn_bf16* k, const decattn_bf16*
                decattn_bf16* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Grouped-head decode with value rows narrower than key rows: the same
+ * computation, arguments, layouts, errors and workspace rules as gqa_decode,
+ * with the width split in two.
+ *   q    [b, Hq, s, dk]; k contiguous [b, capacity, Hkv, dk] or paged
+ *        [num_pages, 64, Hkv, dk]; v likewise with dv; out [b, Hq, s, dv].
+ *   Compiled (dk, dv): (64, 64), (128, 128), (256, 256) and (192, 128), the
+ *   last for the expanded MLA form ([SKILL] Cost Models - FlashAttention:
+ *   keys carry d + p = 192 values, values d = 128), run with Hkv = Hq = h.
+ *   Other pairs return DECATTN_ERR_UNSUPPORTED.
+ */
+size_t gqa_decode_dv_workspace_size(int b, int s, int hq, int hkv, int dk, int dv, int max_seqlen);
+int gqa_decode_dv(const decattn_bf16* q, const decattn_bf16* k, const decattn_bf16* v, decattn_kv kv,
+                  const int32_t* seqlens, int max_seqlen, int b, int s, int hq, int hkv, int dk, int dv, float scale,
+                  decattn_bf16* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Expanded MLA, cache decompression ([SKILL] Absorption Trick: the keys and
+ * values the latent cache stands for; Cost Models - FlashAttention; Regime
+ * Selection). For every cache row m < rows and head j < h:
+ *   k_out[m, j, 0:d]   = z[m, :] @ w_uk[j]^T      (w_uk [h, d, k])
+ *   k_out[m, j, d:d+p] = k_pe[m, :]               (shared RoPE part)
+ *   v_out[m, j, :]     = z[m, :] @ w_uv[j]        (w_uv [h, k, d])
+ *   z [rows, k], k_pe [rows, p] (the latent cache, contiguous [b*capacity]
+ *   rows or a paged pool of num_pages*64 rows: the result keeps the row
+ *   order, so the same block table addresses it), k_out [rows, h, d+p],
+ *   v_out [rows, h, d]; all bf16, fp32 accumulation, bf16 output (round to
+ *   nearest even). Compiled for d = 128, p = 64, k a multiple of 64 up to
+ *   512 (else DECATTN_ERR_UNSUPPORTED). Pointers 16-byte aligned. Tensor-core
+ *   (tcgen05) GEMM. gqa_decode_dv with Hkv = Hq = h, dk = d + p, dv = d then
+ *   runs the expanded attention.
+ */
+int mla_decompress_kv(const decattn_bf16* z, const decattn_bf16* k_pe, const decattn_bf16* w_uk,
+                      const decattn_bf16* w_uv, int rows, int h, int d, int k, int p, decattn_bf16* k_out,
+                      decattn_bf16* v_out, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Absorbed MLA, step 1: query absorption ([SKILL] Absorption Trick, score
  * line: Q K^T = (Q Wk^T) Z^T = Qz Z^T).
  *   qz[b, j, r, :] = scale * q_nope[b, j, r, :] @ w_uk[j]

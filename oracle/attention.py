@@ -174,10 +174,32 @@ def mla_absorbed_ref(q_nope, q_pe, z_seqs, kpe_seqs, w_uk, w_uv, seqlens, scale)
     return mla_out_proj_ref(o_lat, w_uv), lse, qz, o_lat
 
 
+def mla_decompress_ref(z, k_pe, w_uk, w_uv):
+    """The per-head keys and values a latent cache stands for ([SKILL]
+    "Absorption Trick": K = Z Wk, V = Z Wv with the up-projections; "Cost
+    Models - FlashAttention": keys of d + p values, values of d).
+
+    z [..., k] and k_pe [..., p] (any leading row shape), W_uk [h, d, k],
+    W_uv [h, k, d]. Returns K [..., h, d + p] with K[..., j, :d] = z W_uk[j]^T
+    and K[..., j, d:] = k_pe (the RoPE part every head shares), and
+    V [..., h, d] with V[..., j, :] = z W_uv[j]."""
+    z = np.asarray(z, np.float64)
+    kpe = np.asarray(k_pe, np.float64)
+    w_uk = np.asarray(w_uk, np.float64)
+    w_uv = np.asarray(w_uv, np.float64)
+    h = w_uk.shape[0]
+    nope = np.einsum("...k,hdk->...hd", z, w_uk)
+    rope = np.broadcast_to(kpe[..., None, :], kpe.shape[:-1] + (h, kpe.shape[-1]))
+    K = np.concatenate([nope, rope], axis=-1)
+    V = np.einsum("...k,hkd->...hd", z, w_uv)
+    return K, V
+
+
 def mla_expanded_ref(q_nope, q_pe, z_seqs, kpe_seqs, w_uk, w_uv, seqlens, scale):
-    """Brute force with decompressed per-head keys and values: K_j = [Z W_uk[j]^T
-    | K_pe] (L x (d + p)), V_j = Z W_uv[j] (L x d), query [q_nope | q_pe], then
-    plain per-head attention. Used only to check the absorbed form."""
+    """Brute force with decompressed per-head keys and values (mla_decompress_ref):
+    K_j = [Z W_uk[j]^T | K_pe] (L x (d + p)), V_j = Z W_uv[j] (L x d), query
+    [q_nope | q_pe], then plain per-head attention. The expanded form of the
+    pages' regime comparison, and the check of the absorbed form."""
     b, h, s, d = q_nope.shape
     out = np.zeros((b, h, s, w_uv.shape[2]), dtype=np.float64)
     lse = np.full((b, h, s), -np.inf, dtype=np.float64)
@@ -186,14 +208,11 @@ def mla_expanded_ref(q_nope, q_pe, z_seqs, kpe_seqs, w_uk, w_uv, seqlens, scale)
         counts = causal_key_counts(L, s)
         if L == 0:
             continue
-        Z = np.asarray(z_seqs[bi][:L], np.float64)
-        KPE = np.asarray(kpe_seqs[bi][:L], np.float64)
+        K, V = mla_decompress_ref(z_seqs[bi][:L], kpe_seqs[bi][:L], w_uk, w_uv)
         for j in range(h):
-            Kj = np.concatenate([Z @ np.asarray(w_uk[j], np.float64).T, KPE], axis=1)
-            Vj = Z @ np.asarray(w_uv[j], np.float64)
             qrow = np.concatenate([np.asarray(q_nope[bi, j], np.float64),
                                    np.asarray(q_pe[bi, j], np.float64)], axis=1)
-            o, l = attend_rows(qrow, Kj, Vj, counts, scale)
+            o, l = attend_rows(qrow, K[:, j, :], V[:, j, :], counts, scale)
             out[bi, j] = o
             lse[bi, j] = l
     return out, lse

@@ -130,6 +130,33 @@ def mla_bytes_exact(h, k, p, seqlens, s, w=BF16_BYTES):
     return w * (rows + cache)
 
 
+def fa_flops_exact(h, d, p, seqlens, s):
+    """Expanded form (FlashAttention over decompressed keys of d + p and values of d,
+    one KV head per query head): 2 (2d + p) per (query token, key) pair and head."""
+    return sum(2 * h * causal_keys(L, s) * (2 * d + p) for L in seqlens if L > 0)
+
+
+def fa_bytes_exact(h, d, p, seqlens, s, w=BF16_BYTES):
+    """Query rows (d + p) in and output rows (d) out per head and new token; K (d + p)
+    and V (d) of every head per cached key."""
+    rows = len(seqlens) * h * s * (2 * d + p)
+    cache = sum(seqlens) * h * (2 * d + p)
+    return w * (rows + cache)
+
+
+# --- decompression of the latent cache into the expanded form: per cache row and
+# head, K_nope = z W_uk^T (d outputs over k) and V = z W_uv (d outputs over k)
+
+def decompress_flops(rows, h, d, k):
+    return 2 * rows * h * d * k * 2
+
+
+def decompress_bytes(rows, h, d, k, p, w=BF16_BYTES):
+    """Read the latent rows (k + p) and both weights (h d k each); write K (d + p) and
+    V (d) of every head per row."""
+    return w * (rows * (k + p) + 2 * h * d * k + rows * h * (2 * d + p))
+
+
 # --- absorption and output-projection GEMMs (per-head, weights [h, d, k] and
 # [h, k, d]); both are weight-times-activation products outside the attention
 # core, like the projections the "Why MLA and MTP Fight Each Other" post leaves

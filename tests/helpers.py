@@ -62,6 +62,26 @@ def qz_rounding_lse_bound(qz_exact, o_lat_exact, scale):
     return LSE_ABS + scale * 2.0 ** -9 * np.sum(np.abs(qz_exact) * np.abs(o_lat_exact), axis=-1)
 
 
+def key_rounding_lse_bound(q_rows, keys_exact, rounded_cols, lse_exact, counts, scale):
+    """Per-row bound on the LSE change caused by storing keys in bf16 (the expanded
+    form's decompressed cache; the oracle keeps them exact): to first order
+    dLSE = sum_m P_m dx_m with dx_m = scale * sum_i q_i dK_mi and |dK_mi| <= 2^-9 |K_mi|
+    on the rounded columns, so |dLSE| <= scale * 2^-9 * sum_m P_m sum_i |q_i| |K_mi|.
+    q_rows [R, dk], keys_exact [L, dk], counts[r] keys seen by row r, P from the exact
+    logits and LSE. Returned with the 1e-3 allowance added."""
+    q_rows = np.asarray(q_rows, np.float64)
+    keys_exact = np.asarray(keys_exact, np.float64)
+    x = scale * (q_rows @ keys_exact.T)
+    mag = np.abs(keys_exact[:, rounded_cols]) @ np.abs(q_rows[:, rounded_cols]).T  # [L, R]
+    out = np.full(q_rows.shape[0], LSE_ABS)
+    for r in range(q_rows.shape[0]):
+        n = int(counts[r])
+        if n > 0 and np.isfinite(lse_exact[r]):
+            P = np.exp(x[r, :n] - lse_exact[r])
+            out[r] += scale * 2.0 ** -9 * float(P @ mag[:n, r])
+    return out
+
+
 # ---------------------------------------------------------------------------
 # the checker's view of a cache: sequence rows in logical order, gathered from a
 # paged pool by the oracle's own gather_paged (the package's helpers are not used

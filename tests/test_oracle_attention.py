@@ -241,6 +241,45 @@ def test_mla_expanded_vs_sdpa():
         np.testing.assert_allclose(l[bi], torch.logsumexp(logits, -1).numpy(), atol=1e-12)
 
 
+def test_mla_decompress_brute_force():
+    # every element of the decompressed cache by explicit loops over the latent dims
+    rows, h, d, k, p = 3, 2, 3, 4, 2
+    z = rand(rows, k)
+    kpe = rand(rows, p)
+    w_uk = rand(h, d, k)
+    w_uv = rand(h, k, d)
+    K, V = A.mla_decompress_ref(z, kpe, w_uk, w_uv)
+    assert K.shape == (rows, h, d + p) and V.shape == (rows, h, d)
+    for m in range(rows):
+        for j in range(h):
+            for c in range(d):
+                kn = sum(z[m, x] * w_uk[j, c, x] for x in range(k))
+                vv = sum(z[m, x] * w_uv[j, x, c] for x in range(k))
+                assert abs(K[m, j, c] - kn) < 1e-12 and abs(V[m, j, c] - vv) < 1e-12
+            for c in range(p):
+                assert K[m, j, d + c] == kpe[m, c]
+    # any leading row shape: [b, capacity] rows give the same rows
+    K2, V2 = A.mla_decompress_ref(z.reshape(1, rows, k), kpe.reshape(1, rows, p), w_uk, w_uv)
+    np.testing.assert_array_equal(K2[0], K)
+    np.testing.assert_array_equal(V2[0], V)
+
+
+def test_mla_expanded_is_mha_over_the_decompressed_cache():
+    # the expanded form is grouped-head attention with Hkv = Hq = h, keys d + p wide
+    # and values d wide, over the decompressed cache: the grouped-head definition
+    # (pinned against SDPA above) gives the same result
+    b, h, d, k, p, s = 2, 3, 8, 12, 4, 2
+    seqlens = [6, 13]
+    q_nope, q_pe, zs, kpes, w_uk, w_uv = mla_case(b, h, d, k, p, s, seqlens)
+    scale = 1 / math.sqrt(d + p)
+    o1, l1 = A.mla_expanded_ref(q_nope, q_pe, zs, kpes, w_uk, w_uv, seqlens, scale)
+    ks, vs = zip(*(A.mla_decompress_ref(zs[i], kpes[i], w_uk, w_uv) for i in range(b)))
+    q = np.concatenate([q_nope, q_pe], axis=-1)
+    o2, l2 = A.gqa_ref(q, ks, vs, seqlens, scale)
+    np.testing.assert_allclose(o1, o2, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(l1, l2, atol=1e-12, rtol=0)
+
+
 def test_mla_rope_part_matters():
     # dropping the q_pe K_pe^T term would change the result: the expanded path
     # carries it in its keys, so the identity above fails without it

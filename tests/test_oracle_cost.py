@@ -207,6 +207,36 @@ def test_mla_and_fa_counts_from_tensors():
     assert cost.fa_flops(b, h, s, t, d, p) == f
 
 
+def test_expanded_exact_counts_from_tensors():
+    # executed counts of the expanded form, ragged lengths and a causal window: the
+    # bytes of the tensors it reads and writes, the FLOPs of its two contractions
+    # token by token (each new token i of sequence b sees L_b - s + i + 1 keys)
+    h, d, p, s = 3, 5, 2, 2
+    seqlens = [4, 7, 0]
+    b = len(seqlens)
+    nb = _nbytes((b, h, s, d + p), (b, h, s, d)) + sum(_nbytes((L, h, d + p), (L, h, d)) for L in seqlens)
+    assert cost.fa_bytes_exact(h, d, p, seqlens, s) == nb
+    f = 0
+    for L in seqlens:
+        for i in range(s):
+            n = L - s + i + 1 if L else 0
+            if n > 0:
+                f += (_einsum_flops("hc,hnc->hn", (h, d + p), (h, n, d + p))
+                      + _einsum_flops("hn,hnd->hd", (h, n), (h, n, d)))
+    assert cost.fa_flops_exact(h, d, p, seqlens, s) == f
+    # equal lengths and s = 1: the pages' formulas
+    assert cost.fa_flops_exact(h, d, p, [7] * 4, 1) == cost.fa_flops(4, h, 1, 7, d, p)
+    assert cost.fa_bytes_exact(h, d, p, [7] * 4, 1) == cost.fa_bytes(4, h, 1, 7, d, p)
+
+
+def test_decompress_counts_from_tensors():
+    rows, h, d, k, p = 5, 3, 4, 6, 2
+    f = (_einsum_flops("mk,hdk->mhd", (rows, k), (h, d, k)) + _einsum_flops("mk,hkd->mhd", (rows, k), (h, k, d)))
+    assert cost.decompress_flops(rows, h, d, k) == f
+    assert cost.decompress_bytes(rows, h, d, k, p) == _nbytes((rows, k), (rows, p), (h, d, k), (h, k, d),
+                                                              (rows, h, d + p), (rows, h, d))
+
+
 def test_gqa_counts_from_tensors():
     b, hq, hkv, s, t, d = 2, 6, 3, 5, 7, 8
     assert cost.gqa_bytes(b, hq, hkv, s, t, d) == _nbytes((b, hq, s, d), (b, hq, s, d), (b, t, hkv, d), (b, t, hkv, d))

@@ -629,7 +629,7 @@ def extras(dev, stream, hbm, tfl):
     del inp, qzs, outs, olats
     torch.cuda.empty_cache()
 
-    for s in (1, 2, 4, 8, 16, 32):
+    for s in SWEEP_S:
         wl = W.WORKLOADS["mla_dsv3"] if s == 1 else W.WORKLOADS[f"mla_mtp_s{s}"]
         seqlens = wl.seqlens()
         inp = [W.make_mla(wl.b, wl.heads, wl.d, wl.k, wl.p, wl.s, seqlens, seed=wl.seed + r, device=dev)
@@ -646,7 +646,7 @@ def extras(dev, stream, hbm, tfl):
                               max_seqlen=max(seqlens), out=o[r], lse=lse[r], workspace=ws, stream=stream)
             return f
 
-        t = time_calls([call(r) for r in range(2)], n=60 if s <= 4 else 20)
+        t = time_calls([call(r) for r in range(2)], n=60 if s <= 4 else (20 if s <= 32 else 6))
         fl = cost.mla_flops_exact(wl.heads, wl.k, wl.p, seqlens, wl.s)
         by = cost.mla_bytes_exact(wl.heads, wl.k, wl.p, seqlens, wl.s)
         troof = max(fl / (tfl * 1e12), by / (hbm * 1e9))
@@ -658,10 +658,10 @@ def extras(dev, stream, hbm, tfl):
         torch.cuda.empty_cache()
 
     # expanded form ("Mla Analysis", Cost Models - FlashAttention; Regime Selection):
-    # the latent cache of 32 sequences of 4096 + 32 keys decompressed once into per-head
-    # keys [nope || rope] (192 values) and values (128) for all 128 heads (10.8 GB), then
+    # the latent cache of 32 sequences of 4096 + 128 keys decompressed once into per-head
+    # keys [nope || rope] (192 values) and values (128) for all 128 heads (11.1 GB), then
     # grouped-head decode with Hkv = Hq = 128 at each s, beside the absorbed call above
-    b, h, d, k, p, smax, t0 = 32, 128, 128, 512, 64, 32, 4096
+    b, h, d, k, p, smax, t0 = 32, 128, 128, 512, 64, max(SWEEP_S), 4096
     cap = t0 + smax
     x = W.make_mla(b, h, d, k, p, smax, [cap] * b, capacity=cap, seed=5, device=dev)
     kf = torch.empty((b, cap, h, d + p), dtype=torch.bfloat16, device=dev)
@@ -676,7 +676,7 @@ def extras(dev, stream, hbm, tfl):
                              "note": "once per cached token, not per decode step"}
     q_all = torch.cat([x.q_nope, x.q_pe], dim=-1).contiguous()  # the expanded query [q_nope || q_pe]
     crossover = {}
-    for s in (1, 2, 4, 8, 16, 32):
+    for s in SWEEP_S:
         L = t0 + (s if s > 1 else 0)  # the latent sweep's lengths
         seqlens = [L] * b
         sl = torch.tensor(seqlens, dtype=torch.int32, device=dev)
@@ -686,7 +686,7 @@ def extras(dev, stream, hbm, tfl):
         wsb = da.ops.load().gqa_decode_dv_workspace_size(b, s, h, h, d + p, d, L)
         ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
         t = time_calls([lambda: da.gqa_decode_dv(q, kf, vf, sl, scale=x.scale, max_seqlen=L, out=o, lse=lse,
-                                                 workspace=ws, stream=stream)], n=10 if s <= 8 else 5, w=2)
+                                                 workspace=ws, stream=stream)], n=10 if s <= 8 else 4, w=1)
         fl = cost.fa_flops_exact(h, d, p, seqlens, s)
         by = cost.fa_bytes_exact(h, d, p, seqlens, s)
         troof = max(fl / (tfl * 1e12), by / (hbm * 1e9))
@@ -701,6 +701,11 @@ def extras(dev, stream, hbm, tfl):
     del x, kf, vf, q_all
     torch.cuda.empty_cache()
     return res
+
+
+# new tokens per sequence of the absorbed / expanded sweep: decode (1), speculative (2 .. 32)
+# and the start of the prefill-sized regime, where the two forms cross
+SWEEP_S = (1, 2, 4, 8, 16, 32, 64, 128)
 
 
 def distribution_us(per_call_s):

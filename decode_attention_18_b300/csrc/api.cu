@@ -63,7 +63,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
-constexpr int kMaxS = 32;  // new tokens per sequence in one call
+constexpr int kMaxS = 1024;  // new tokens per sequence in one call (decode, speculative and prefill-sized)
 
 struct Plan {
   int nsplit;

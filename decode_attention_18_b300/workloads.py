@@ -208,7 +208,7 @@ WORKLOADS = {
     "gqa_64_8": Workload("gqa b32 hq64 hkv8 d128 t4096 s1", "gqa", 32, 64, 128, 1, 4096, hkv=8),
     "mla_dsv3": Workload("mla b32 h128 d128 k512 p64 t4096 s1", "mla", 32, 128, 128, 1, 4096, k=512, p=64),
     **{f"mla_mtp_s{s}": Workload(f"mla b32 h128 d128 k512 p64 t4096+{s} s{s} causal", "mla", 32, 128, 128, s,
-                                 4096, k=512, p=64) for s in (2, 4, 8, 16, 32)},
+                                 4096, k=512, p=64) for s in (2, 4, 8, 16, 32, 64, 128)},
     **{f"gqa_paged_hkv{hk}": Workload(f"gqa paged b8 hq24 hkv{hk} d256 L~U[16384,32768] s1", "gqa", 8, 24, 256,
                                       1, 0, hkv=hk, paged=True, ragged=(16384, 32768))
        for hk in (24, 4, 1)},

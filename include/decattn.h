@@ -21,7 +21,7 @@
  *            a latent plus a decoupled RoPE part).
  *
  * Conventions shared by all calls
- *   b   sequences, s new tokens per sequence (1..32), seqlens[i] = keys of
+ *   b   sequences, s new tokens per sequence (1..1024), seqlens[i] = keys of
  *       sequence i INCLUDING its s new tokens (a device int32[b]); token r of
  *       the s new ones attends to keys 0 .. seqlens[i]-s+r (causal among the
  *       new tokens, aligned to the end); seqlens[i] = 0 gives a zero output
@@ -61,7 +61,7 @@ typedef uint16_t decattn_bf16; /* bfloat16 bit pattern */
 
 enum decattn_status {
   DECATTN_OK = 0,
-  DECATTN_ERR_INVALID_ARG = 1, /* null pointer, Hq % Hkv != 0, s outside 1..32, page_size != 64, ... */
+  DECATTN_ERR_INVALID_ARG = 1, /* null pointer, Hq % Hkv != 0, s outside 1..1024, page_size != 64, ... */
   DECATTN_ERR_UNSUPPORTED = 2, /* head dim / (k, p) without a compiled instance */
   DECATTN_ERR_WORKSPACE = 3,   /* workspace missing or too small */
   DECATTN_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */

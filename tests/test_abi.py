@@ -77,7 +77,7 @@ def test_invalid_arguments_rejected_without_launch(lib):
     # null pointers and bad head counts are refused before any CUDA call
     assert lib.gqa_decode(null, null, null, kv, null, 16, 1, 1, 8, 3, 128, 1.0, null, null, null, 0, null) == 1
     assert lib.gqa_decode(null, null, null, kv, null, 16, 1, 0, 8, 8, 128, 1.0, null, null, null, 0, null) == 1
-    assert lib.gqa_decode(null, null, null, kv, null, 16, 1, 33, 8, 8, 128, 1.0, null, null, null, 0, null) == 1
+    assert lib.gqa_decode(null, null, null, kv, null, 16, 1, 1025, 8, 8, 128, 1.0, null, null, null, 0, null) == 1
     assert lib.mla_decode(null, null, null, null, kv, null, 16, 1, 1, 8, 512, 64, 1.0, null, null, null, 0,
                           null) == 1
     assert lib.mla_absorb_q(null, null, null, null, 1, 1, 8, 128, 512, 1.0, null) == 1

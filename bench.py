@@ -700,6 +700,37 @@ def extras(dev, stream, hbm, tfl):
     res["expanded_vs_absorbed"] = crossover
     del x, kf, vf, q_all
     torch.cuda.empty_cache()
+
+    # hybrid form ("Mla Analysis", MLAvar6+ Design): the n most recent keys decompressed,
+    # the o = L - n older ones latent, merged by LSE; the whole step (absorb, latent part,
+    # W_uv, expanded part, merge) against the absorbed pipeline (absorb, latent, W_uv) at
+    # the same s, and against the pages' cost model of the split
+    for s in (1, 32):
+        L = t0 + (s if s > 1 else 0)
+        seqlens = [L] * b
+        x = W.make_mla(b, h, d, k, p, s, seqlens, capacity=L, seed=7, device=dev)
+        sl = torch.tensor(seqlens, dtype=torch.int32, device=dev)
+        q_full = torch.cat([x.q_nope, x.q_pe], dim=-1).contiguous()
+        absorbed = time_calls([lambda: da.mla_forward(x.q_nope, x.q_pe, x.z, x.k_pe, x.w_uk, x.w_uv, sl,
+                                                      scale=x.scale, max_seqlen=L, stream=stream)], n=20, w=2)
+        res[f"mla_absorbed_pipeline_s{s}"] = {"us": absorbed * 1e6, **dist}
+        for n in (s, 256, 1024):
+            kr, vr = da.mla_decompress_kv(x.z[:, L - n:].contiguous(), x.k_pe[:, L - n:].contiguous(), x.w_uk, x.w_uv)
+            sl_old = torch.full((b,), L - n, dtype=torch.int32, device=dev)
+            sl_rec = torch.full((b,), n, dtype=torch.int32, device=dev)
+            t = time_calls([lambda: da.mla_split_forward(x.q_nope, x.q_pe, q_full, x.z, x.k_pe, kr, vr, x.w_uk, x.w_uv,
+                                                         sl_old, sl_rec, scale=x.scale, max_old=L - n, max_recent=n,
+                                                         stream=stream)], n=20, w=2)
+            fl = cost.split_latent_flops(b, h, s, L - n, n, d, p, k)
+            by = cost.split_latent_bytes(b, h, s, L - n, n, d, p, k)
+            troof = max(fl / (tfl * 1e12), by / (hbm * 1e9))
+            res[f"mla_split_s{s}_n{n}"] = {"us": t * 1e6, **dist, "old": L - n, "recent": n,
+                                           "model_flops": fl, "model_bytes": by, "roofline_us": troof * 1e6,
+                                           "frac_roofline": troof / t, "over_absorbed_pipeline": t / absorbed,
+                                           "note": "cost model counts the attention core only, as the pages do"}
+            del kr, vr
+        del x, q_full
+        torch.cuda.empty_cache()
     return res
 
 

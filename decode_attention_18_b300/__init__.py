@@ -4,6 +4,7 @@ behind the C ABI of include/decattn.h. The native library is loaded on first
 use."""
 from ._native import DecAttnError, LIB_PATH, SYMBOLS  # noqa: F401
 from .ops import (  # noqa: F401
+    attn_merge_lse,
     check_errors,
     gqa_decode,
     gqa_decode_dv,
@@ -13,6 +14,7 @@ from .ops import (  # noqa: F401
     mla_decompress_kv,
     mla_forward,
     mla_out_proj,
+    mla_split_forward,
     set_forced_splits,
     set_wait_limit_ns,
     test_force_timeout,
@@ -20,5 +22,6 @@ from .ops import (  # noqa: F401
 
 __all__ = [
     "gqa_decode", "gqa_decode_dv", "mla_decompress_kv", "mla_absorb_q", "mla_decode", "mla_out_proj", "mla_forward",
+    "attn_merge_lse", "mla_split_forward",
     "check_errors", "set_forced_splits", "last_num_splits", "set_wait_limit_ns", "test_force_timeout", "DecAttnError",
 ]

@@ -28,6 +28,7 @@ SYMBOLS = (
     "gqa_decode_dv_workspace_size",
     "gqa_decode_dv",
     "mla_decompress_kv",
+    "attn_merge_lse",
 )
 
 
@@ -96,6 +97,8 @@ def load():
     lib.gqa_decode_dv.argtypes = [P, P, P, KV, P, I, I, I, I, I, I, I, F, P, P, P, SZ, P]
     lib.mla_decompress_kv.restype = I
     lib.mla_decompress_kv.argtypes = [P, P, P, P, I, I, I, I, I, P, P, P]
+    lib.attn_merge_lse.restype = I
+    lib.attn_merge_lse.argtypes = [P, P, P, P, I, I, P, P, P]
     _lib = lib
     return lib
 

@@ -351,6 +351,19 @@ int mla_decompress_kv(const decattn_bf16* z, const decattn_bf16* k_pe, const dec
   return launch_mla_expand(a, stream) == cudaSuccess ? DECATTN_OK : DECATTN_ERR_CUDA;
 }
 
+int attn_merge_lse(const decattn_bf16* out_a, const float* lse_a, const decattn_bf16* out_b, const float* lse_b,
+                   int rows, int d, decattn_bf16* out, float* lse, cudaStream_t stream) {
+  if (rows < 0 || d < 8 || d % 8) return DECATTN_ERR_INVALID_ARG;
+  if (rows == 0) return DECATTN_OK;
+  if (!out_a || !lse_a || !out_b || !lse_b || !out) return DECATTN_ERR_INVALID_ARG;
+  if (!aligned16(out_a) || !aligned16(out_b) || !aligned16(out)) return DECATTN_ERR_INVALID_ARG;
+  if ((long long)rows * (d / 8) > (long long)INT_MAX * 256) return DECATTN_ERR_INVALID_ARG;
+  DeviceState* st = nullptr;
+  if (int rc = device_state(&st)) return rc;
+  return launch_merge2(out_a, lse_a, out_b, lse_b, rows, d, out, lse, stream) == cudaSuccess ? DECATTN_OK
+                                                                                               : DECATTN_ERR_CUDA;
+}
+
 size_t mla_decode_workspace_size(int b, int s, int h, int k, int max_seqlen) {
   if (b < 1 || s < 1 || h < 1 || k < 1) return 0;
   DeviceState* st = nullptr;

@@ -77,6 +77,10 @@ struct MlaLaunch {
   unsigned long long wait_ns;
   int test_timeout;
 };
+// out = LSE-weighted merge of two results over disjoint key sets (rows x d, bf16; fp32 LSEs)
+cudaError_t launch_merge2(const void* oa, const float* la, const void* ob, const float* lb, int rows, int d, void* out,
+                          float* lse, cudaStream_t stream);
+
 // Expanded-form MLA cache: K = [Z W_uk^T || K_pe], V = Z W_uv for `rows` cache rows
 struct ExpandLaunch {
   const void* z;     // [rows, k]

@@ -185,6 +185,50 @@ def mla_forward(q_nope, q_pe, z, k_pe, w_uk, w_uv, seqlens, *, scale, max_seqlen
     return out, lse, qz, o_lat
 
 
+def attn_merge_lse(out_a, lse_a, out_b, lse_b, *, out=None, lse=None, stream=None):
+    """LSE merge of two results over disjoint key sets of the same rows:
+    out_a, out_b [..., d] bf16 and lse_a, lse_b [...] fp32. Returns (out, lse)."""
+    lib = load()
+    _need(out_a, "out_a"), _need(out_b, "out_b")
+    _need(lse_a, "lse_a", torch.float32), _need(lse_b, "lse_b", torch.float32)
+    d = int(out_a.shape[-1])
+    rows = int(out_a.numel()) // d
+    if out is None:
+        out = torch.empty_like(out_a)
+    if lse is None:
+        lse = torch.empty_like(lse_a)
+    check(lib.attn_merge_lse(_p(out_a), _p(lse_a), _p(out_b), _p(lse_b), rows, d, _p(out), _p(lse),
+                             _stream(stream)), "attn_merge_lse")
+    return out, lse
+
+
+def mla_split_forward(q_nope, q_pe, q_full, z, k_pe, k_recent, v_recent, w_uk, w_uv, seqlens_old, seqlens_recent, *,
+                      scale, max_old, max_recent, block_table=None, recent_block_table=None, workspace=None,
+                      stream=None):
+    """The hybrid form ("Mla Analysis", MLAvar6+ Design): the o_i older keys of
+    sequence i attended in latent form, its n_i most recent keys in decompressed
+    form, the two merged by log-sum-exp.
+
+    z [b, cap, k] / k_pe [b, cap, p] (or paged with block_table): the latent cache,
+    of which keys 0 .. o_i - 1 are read (seqlens_old = o_i). k_recent
+    [b, cap_r, h, d + p] / v_recent [b, cap_r, h, d] (or paged with
+    recent_block_table): the decompressed recent keys, o_i .. o_i + n_i - 1, as
+    mla_decompress_kv writes them (seqlens_recent = n_i >= s: the s new tokens are
+    the last of them, causal among themselves). q_full = [q_nope || q_pe] per head.
+    Every new token sees all o_i older keys. Returns (out [b, h, s, d], lse)."""
+    b, h, s, k = int(q_nope.shape[0]), int(q_nope.shape[1]), int(q_nope.shape[2]), int(w_uk.shape[2])
+    p = int(q_pe.shape[3])
+    qz = mla_absorb_q(q_nope, w_uk, stream=stream)
+    # the older keys precede every new token: the h*s query rows of a sequence attend
+    # to all o_i of them, which is the latent call with one token per row ([b, h*s, 1, .])
+    o_lat, lse_a = mla_decode(qz.view(b, h * s, 1, k), q_pe.view(b, h * s, 1, p), z, k_pe, seqlens_old, scale=scale,
+                              max_seqlen=max_old, block_table=block_table, workspace=workspace, stream=stream)
+    out_a = mla_out_proj(o_lat.view(b, h, s, k), w_uv, stream=stream)
+    out_b, lse_b = gqa_decode_dv(q_full, k_recent, v_recent, seqlens_recent, scale=scale, max_seqlen=max_recent,
+                                 block_table=recent_block_table, stream=stream)
+    return attn_merge_lse(out_a, lse_a.view(b, h, s), out_b, lse_b, out=out_a, stream=stream)
+
+
 def check_errors(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device error status."""
     return int(load().decattn_check_errors(_stream(stream)))

@@ -140,6 +140,21 @@ int mla_decompress_kv(const decattn_bf16* z, const decattn_bf16* k_pe, const dec
                       decattn_bf16* v_out, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Log-sum-exp merge of two attention results over disjoint key sets of the
+ * same query rows ([SKILL] MLAvar6+ Design: older keys in latent form,
+ * recent keys decompressed, joined into one softmax):
+ *   lse = log(exp(lse_a) + exp(lse_b))
+ *   out = exp(lse_a - lse) * out_a + exp(lse_b - lse) * out_b
+ *   out_a, out_b, out [rows, d] bf16 (out may alias out_a or out_b);
+ *   lse_a, lse_b [rows] float (natural log; -inf = that side saw no key);
+ *   lse [rows] float or NULL. Rows where both sides are -inf get out = 0,
+ *   lse = -inf; an empty side's out values are never used. d a multiple of 8,
+ *   bf16 pointers 16-byte aligned.
+ */
+int attn_merge_lse(const decattn_bf16* out_a, const float* lse_a, const decattn_bf16* out_b, const float* lse_b,
+                   int rows, int d, decattn_bf16* out, float* lse, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Absorbed MLA, step 1: query absorption ([SKILL] Absorption Trick, score
  * line: Q K^T = (Q Wk^T) Z^T = Qz Z^T).
  *   qz[b, j, r, :] = scale * q_nope[b, j, r, :] @ w_uk[j]

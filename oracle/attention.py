@@ -218,6 +218,40 @@ def mla_expanded_ref(q_nope, q_pe, z_seqs, kpe_seqs, w_uk, w_uv, seqlens, scale)
     return out, lse
 
 
+def mla_split_latent_ref(q_nope, q_pe, z_seqs, kpe_seqs, w_uk, w_uv, seqlens, scale, n_recent):
+    """The hybrid form ([SKILL] "MLAvar6+ Design"): of the L_b keys of sequence b
+    the o_b = L_b - n_b older ones are attended in latent form (scores Qz Z^T +
+    q_pe K_pe^T, values O_lat, projected by W_uv) and the n_b most recent ones in
+    expanded form (decompressed keys and values); the two softmaxes over disjoint
+    key sets are joined by merge_partials_ref. n_recent[b] >= s (the new tokens
+    are the last keys and see each other causally); every new token sees all o_b
+    older keys. Exactly the full attention up to rounding.
+    Returns (out [b, h, s, d], lse [b, h, s])."""
+    b, h, s, d = q_nope.shape
+    out = np.zeros((b, h, s, w_uv.shape[2]), dtype=np.float64)
+    lse = np.full((b, h, s), -np.inf, dtype=np.float64)
+    qz = mla_absorb_ref(q_nope, w_uk)
+    for bi in range(b):
+        L, n = int(seqlens[bi]), int(n_recent[bi])
+        if L == 0:
+            continue
+        if not s <= n <= L:
+            raise ValueError(f"recent keys {n} must cover the {s} new tokens and fit in {L}")
+        o = L - n
+        # latent part: every one of the h*s rows sees all o older keys (one token per row)
+        qz_rows = qz[bi:bi + 1].reshape(1, h * s, 1, -1)
+        qpe_rows = np.asarray(q_pe[bi:bi + 1], np.float64).reshape(1, h * s, 1, -1)
+        lat, l_a = mla_latent_ref(qz_rows, qpe_rows, [z_seqs[bi][:o]], [kpe_seqs[bi][:o]], [o], scale)
+        o_a = mla_out_proj_ref(lat.reshape(1, h, s, -1), w_uv)[0]
+        # expanded part: the n recent keys, causal among the s new tokens at their end
+        o_b, l_b = mla_expanded_ref(q_nope[bi:bi + 1], q_pe[bi:bi + 1], [z_seqs[bi][o:L]], [kpe_seqs[bi][o:L]],
+                                    w_uk, w_uv, [n], scale)
+        m_o, m_l = merge_partials_ref([o_a, o_b[0]], [l_a.reshape(h, s), l_b[0]])
+        out[bi] = m_o
+        lse[bi] = m_l
+    return out, lse
+
+
 # ---------------------------------------------------------------------------
 # merging split partials (log-sum-exp merge; exact up to rounding)
 

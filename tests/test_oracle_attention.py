@@ -280,6 +280,43 @@ def test_mla_expanded_is_mha_over_the_decompressed_cache():
     np.testing.assert_allclose(l1, l2, atol=1e-12, rtol=0)
 
 
+@pytest.mark.parametrize("s,seqlens,n_recent", [
+    (1, [40, 9], [1, 9]),          # one recent key; all keys recent (no latent part)
+    (3, [30, 12], [3, 7]),         # recent part exactly the new tokens; a mixed split
+    (2, [25, 25], [13, 24]),
+])
+def test_mla_split_latent_equals_absorbed(s, seqlens, n_recent):
+    # "MLAvar6+ Design": splitting the keys into a latent and a decompressed part and
+    # merging the two softmaxes changes nothing but rounding
+    b, h, d, k, p = len(seqlens), 3, 8, 12, 4
+    q_nope, q_pe, zs, kpes, w_uk, w_uv = mla_case(b, h, d, k, p, s, seqlens)
+    scale = 1 / math.sqrt(d + p)
+    o1, l1, _, _ = A.mla_absorbed_ref(q_nope, q_pe, zs, kpes, w_uk, w_uv, seqlens, scale)
+    o2, l2 = A.mla_split_latent_ref(q_nope, q_pe, zs, kpes, w_uk, w_uv, seqlens, scale, n_recent)
+    np.testing.assert_allclose(o2, o1, atol=1e-10, rtol=0)
+    np.testing.assert_allclose(l2, l1, atol=1e-10, rtol=0)
+
+
+def test_mla_split_latent_uses_both_parts():
+    # a wrong split (older keys dropped, or the recent part not causal) is caught:
+    # perturbing one older key's latent changes the result, and so does the last key
+    s, seqlens, n_recent = 2, [20], [5]
+    q_nope, q_pe, zs, kpes, w_uk, w_uv = mla_case(1, 2, 6, 10, 4, s, seqlens)
+    base, _ = A.mla_split_latent_ref(q_nope, q_pe, zs, kpes, w_uk, w_uv, seqlens, 0.4, n_recent)
+    for m in (3, 19):
+        z2 = [zs[0].copy()]
+        z2[0][m] += 1.0
+        o, _ = A.mla_split_latent_ref(q_nope, q_pe, z2, kpes, w_uk, w_uv, seqlens, 0.4, n_recent)
+        assert np.abs(o - base).max() > 1e-4
+    # the last key is seen only by the last new token (causal among the new tokens)
+    z3 = [zs[0].copy()]
+    z3[0][19] += 1.0
+    o, _ = A.mla_split_latent_ref(q_nope, q_pe, z3, kpes, w_uk, w_uv, seqlens, 0.4, n_recent)
+    np.testing.assert_array_equal(o[:, :, 0], base[:, :, 0])
+    with pytest.raises(ValueError):
+        A.mla_split_latent_ref(q_nope, q_pe, zs, kpes, w_uk, w_uv, seqlens, 0.4, [1])  # n < s
+
+
 def test_mla_rope_part_matters():
     # dropping the q_pe K_pe^T term would change the result: the expanded path
     # carries it in its keys, so the identity above fails without it

@@ -606,7 +606,27 @@ def extras(dev, stream, hbm, tfl):
         res[name] = {"us": t * 1e6, **dist, "hbm_gbs": by / t / 1e9, "frac_hbm": by / t / 1e9 / hbm,
                      "tflops": fl / t / 1e12, "bytes": by, "num_splits": da.last_num_splits(),
                      "l2": f"{nb} rotating caches of {by / 1e6:.0f} MB", "timing": "CUDA graph replays"}
-        del qs, outs, lses, ws
+        del qs, ws
+        # the same workload over an FP8 (E4M3) cache: half the cache bytes
+        f8 = [W.make_gqa_fp8(wl.b, wl.heads, wl.hkv, wl.d, wl.s, seqlens, paged=wl.paged, seed=wl.seed + r, device=dev)
+              for r in range(nb)]
+        wsb = da.ops.load().gqa_decode_fp8_workspace_size(wl.b, wl.s, wl.heads, wl.hkv, wl.d, max(seqlens))
+        ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+
+        def call8(r):
+            def f():
+                q, c, ks, vs = f8[r]
+                da.gqa_decode_fp8(q, c.k, c.v, sl, k_scale=ks, v_scale=vs, max_seqlen=max(seqlens),
+                                  block_table=c.block_table if wl.paged else None, out=outs[r], lse=lses[r],
+                                  workspace=ws, stream=stream)
+            return f
+
+        t8 = time_calls([call8(r) for r in range(nb)])
+        by8 = cost.gqa_fp8_bytes_exact(wl.heads, wl.hkv, wl.d, seqlens, wl.s)
+        res[name + "_fp8"] = {"us": t8 * 1e6, **dist, "hbm_gbs": by8 / t8 / 1e9, "frac_hbm": by8 / t8 / 1e9 / hbm,
+                              "bytes": by8, "speedup_over_bf16": t / t8, "num_splits": da.last_num_splits(),
+                              "cache": "E4M3 bytes, per-tensor scales"}
+        del f8, outs, lses, ws
         torch.cuda.empty_cache()
 
     # the two projection GEMMs of the headline pipeline, each alone

@@ -8,6 +8,7 @@ from .ops import (  # noqa: F401
     check_errors,
     gqa_decode,
     gqa_decode_dv,
+    gqa_decode_fp8,
     last_num_splits,
     mla_absorb_q,
     mla_decode,
@@ -21,7 +22,7 @@ from .ops import (  # noqa: F401
 )
 
 __all__ = [
-    "gqa_decode", "gqa_decode_dv", "mla_decompress_kv", "mla_absorb_q", "mla_decode", "mla_out_proj", "mla_forward",
+    "gqa_decode", "gqa_decode_dv", "gqa_decode_fp8", "mla_decompress_kv", "mla_absorb_q", "mla_decode", "mla_out_proj", "mla_forward",
     "attn_merge_lse", "mla_split_forward",
     "check_errors", "set_forced_splits", "last_num_splits", "set_wait_limit_ns", "test_force_timeout", "DecAttnError",
 ]

@@ -29,6 +29,8 @@ SYMBOLS = (
     "gqa_decode_dv",
     "mla_decompress_kv",
     "attn_merge_lse",
+    "gqa_decode_fp8_workspace_size",
+    "gqa_decode_fp8",
 )
 
 
@@ -99,6 +101,10 @@ def load():
     lib.mla_decompress_kv.argtypes = [P, P, P, P, I, I, I, I, I, P, P, P]
     lib.attn_merge_lse.restype = I
     lib.attn_merge_lse.argtypes = [P, P, P, P, I, I, P, P, P]
+    lib.gqa_decode_fp8_workspace_size.restype = SZ
+    lib.gqa_decode_fp8_workspace_size.argtypes = [I, I, I, I, I, I]
+    lib.gqa_decode_fp8.restype = I
+    lib.gqa_decode_fp8.argtypes = [P, P, P, KV, P, I, I, I, I, I, I, F, F, F, P, P, P, SZ, P]
     _lib = lib
     return lib
 

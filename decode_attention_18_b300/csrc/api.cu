@@ -148,13 +148,13 @@ struct GqaBalanced {
   long long items = 0;   // work items (sequence, KV head, row block)
   int rpb = 0;           // rows per CTA
 };
-GqaBalanced gqa_balanced(const Plan& pl, int b, int s, int hq, int hkv, int dk, int dv, int sms) {
+GqaBalanced gqa_balanced(const Plan& pl, int b, int s, int hq, int hkv, int dk, int dv, int sms, bool fp8 = false) {
   GqaBalanced gb;
   const int rows = (hq / hkv) * s;
   if (pl.nsplit <= 1 || g_forced_splits.load() > 0 || gqa_rows_per_cta(rows) > 16) return gb;
   gb.rpb = gqa_rows_per_cta(rows);
   gb.items = (long long)b * hkv * ceil_div(rows, gb.rpb);
-  gb.grid = sms * gqa_balanced_ctas_per_sm(dk, dv, rows);
+  gb.grid = sms * gqa_balanced_ctas_per_sm(dk, dv, rows, fp8);
   return gb;
 }
 size_t balanced_bytes(const GqaBalanced& gb, int dv) {
@@ -170,6 +170,98 @@ Plan mla_plan(int b, int s, int h, int k, int max_seqlen, int sms) {
   const long long base = (long long)b * ceil_div((long long)h * s, 128);
   const int per = mla_ctas_per_row_tile();
   return plan_splits(base, max_seqlen, sms / per > 0 ? sms / per : 1, 384, 512, mla_tile_keys());
+}
+
+}  // namespace
+}  // namespace decattn
+
+namespace decattn {
+namespace {
+
+size_t gqa_workspace(int b, int s, int hq, int hkv, int dk, int dv, int max_seqlen, bool fp8) {
+  if (b < 1 || s < 1 || hq < 1 || hkv < 1 || hq % hkv || dk < 1 || dv < 1) return 0;
+  DeviceState* st = nullptr;
+  if (device_state(&st)) return 0;
+  const Plan pl = gqa_plan(b, s, hq, hkv, dk, dv, max_seqlen, st->sms);
+  const GqaBalanced gb = gqa_balanced(pl, b, s, hq, hkv, dk, dv, st->sms, fp8);
+  if (gb.grid > 0) return balanced_bytes(gb, dv);
+  return partial_bytes((long long)b * hq * s, pl.nsplit, dv);
+}
+
+// grouped-head decode, bf16 or FP8 (e4m3 bytes with per-tensor scales) cache
+int gqa_decode_impl(const void* q, const void* k, const void* v, decattn_kv kv, const int32_t* seqlens, int max_seqlen,
+                    int b, int s, int hq, int hkv, int dk, int dv, float scale, bool fp8, float k_scale,
+                    float v_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                    cudaStream_t stream) {
+  if (b < 0 || s < 1 || s > kMaxS || hq < 1 || hkv < 1 || hq % hkv || max_seqlen < 0) return DECATTN_ERR_INVALID_ARG;
+  if (b == 0) return DECATTN_OK;
+  if (!q || !k || !v || !seqlens || !out) return DECATTN_ERR_INVALID_ARG;
+  if (fp8 && !(k_scale > 0.f && v_scale > 0.f && k_scale < INFINITY && v_scale < INFINITY))
+    return DECATTN_ERR_INVALID_ARG;
+  if (!gqa_supported(dk, dv, fp8)) return DECATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return DECATTN_ERR_INVALID_ARG;
+  if (hkv > 65535 || b > 65535) return DECATTN_ERR_INVALID_ARG;
+  if (int rc = check_kv(kv, b, max_seqlen)) return rc;
+  DeviceState* st = nullptr;
+  if (int rc = device_state(&st)) return rc;
+  const Plan pl = gqa_plan(b, s, hq, hkv, dk, dv, max_seqlen, st->sms);
+  const GqaBalanced gb = gqa_balanced(pl, b, s, hq, hkv, dk, dv, st->sms, fp8);
+  const long long rows = (long long)b * hq * s;
+  const size_t need = gb.grid > 0 ? balanced_bytes(gb, dv) : partial_bytes(rows, pl.nsplit, dv);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return DECATTN_ERR_WORKSPACE;
+  GqaLaunch a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.seqlens = seqlens;
+  a.block_table = kv.block_table;
+  a.max_pages = kv.max_pages;
+  a.paged = kv.paged;
+  a.capacity = kv.capacity;
+  a.num_pages = kv.num_pages;
+  a.b = b;
+  a.s = s;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.dk = dk;
+  a.dv = dv;
+  a.fp8 = fp8 ? 1 : 0;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.nsplit = pl.nsplit;
+  a.chunk = pl.chunk;
+  a.scale = scale;
+  a.out = out;
+  a.lse = lse;
+  a.ws_o = pl.nsplit > 1 ? static_cast<float*>(workspace) : nullptr;
+  a.ws_lse = pl.nsplit > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                       align256((size_t)rows * pl.nsplit * dv * sizeof(float)))
+                           : nullptr;
+  a.meta = nullptr;
+  a.balanced_grid = gb.grid;
+  if (gb.grid > 0) {
+    const long long records = gb.items + gb.grid;
+    char* w = static_cast<char*>(workspace);
+    const size_t o_bytes = align256((size_t)records * gb.rpb * dv * sizeof(float));
+    a.ws_o = reinterpret_cast<float*>(w);
+    a.ws_lse = reinterpret_cast<float*>(w + o_bytes);
+    a.meta = reinterpret_cast<int*>(w + o_bytes + align256((size_t)records * gb.rpb * sizeof(float)));
+  }
+  a.err = st->err;
+  a.wait_ns = wait_limit();
+  a.test_timeout = g_test_timeout.load();
+  g_last_splits.store(pl.nsplit);
+  if (launch_gqa(a, stream) != cudaSuccess) return DECATTN_ERR_CUDA;
+  if (gb.grid > 0) {
+    if (launch_combine_balanced(a.ws_o, a.ws_lse, a.meta, seqlens, b, hq, s, hkv, dv, gb.items + gb.grid, out, lse,
+                                stream) != cudaSuccess)
+      return DECATTN_ERR_CUDA;
+  } else if (pl.nsplit > 1) {
+    if (launch_combine(a.ws_o, false, a.ws_lse, seqlens, (int)rows, hq * s, pl.nsplit, pl.chunk, dv, out, lse,
+                       stream) != cudaSuccess)
+      return DECATTN_ERR_CUDA;
+  }
+  return DECATTN_OK;
 }
 
 }  // namespace
@@ -213,87 +305,31 @@ int decattn_check_errors(cudaStream_t stream) {
 
 // ------------------------------------------------------------------ grouped-head
 
-size_t gqa_decode_dv_workspace_size(int b, int s, int hq, int hkv, int dk, int dv, int max_seqlen) {
-  if (b < 1 || s < 1 || hq < 1 || hkv < 1 || hq % hkv || dk < 1 || dv < 1) return 0;
-  DeviceState* st = nullptr;
-  if (device_state(&st)) return 0;
-  const Plan pl = gqa_plan(b, s, hq, hkv, dk, dv, max_seqlen, st->sms);
-  const GqaBalanced gb = gqa_balanced(pl, b, s, hq, hkv, dk, dv, st->sms);
-  if (gb.grid > 0) return balanced_bytes(gb, dv);
-  return partial_bytes((long long)b * hq * s, pl.nsplit, dv);
-}
 
 size_t gqa_decode_workspace_size(int b, int s, int hq, int hkv, int d, int max_seqlen) {
-  return gqa_decode_dv_workspace_size(b, s, hq, hkv, d, d, max_seqlen);
+  return gqa_workspace(b, s, hq, hkv, d, d, max_seqlen, false);
+}
+
+size_t gqa_decode_dv_workspace_size(int b, int s, int hq, int hkv, int dk, int dv, int max_seqlen) {
+  return gqa_workspace(b, s, hq, hkv, dk, dv, max_seqlen, false);
+}
+
+size_t gqa_decode_fp8_workspace_size(int b, int s, int hq, int hkv, int d, int max_seqlen) {
+  return gqa_workspace(b, s, hq, hkv, d, d, max_seqlen, true);
 }
 
 int gqa_decode_dv(const decattn_bf16* q, const decattn_bf16* k, const decattn_bf16* v, decattn_kv kv,
                   const int32_t* seqlens, int max_seqlen, int b, int s, int hq, int hkv, int dk, int dv, float scale,
                   decattn_bf16* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  if (b < 0 || s < 1 || s > kMaxS || hq < 1 || hkv < 1 || hq % hkv || max_seqlen < 0) return DECATTN_ERR_INVALID_ARG;
-  if (b == 0) return DECATTN_OK;
-  if (!q || !k || !v || !seqlens || !out) return DECATTN_ERR_INVALID_ARG;
-  if (!gqa_supported(dk, dv)) return DECATTN_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return DECATTN_ERR_INVALID_ARG;
-  if (hkv > 65535 || b > 65535) return DECATTN_ERR_INVALID_ARG;
-  if (int rc = check_kv(kv, b, max_seqlen)) return rc;
-  DeviceState* st = nullptr;
-  if (int rc = device_state(&st)) return rc;
-  const Plan pl = gqa_plan(b, s, hq, hkv, dk, dv, max_seqlen, st->sms);
-  const GqaBalanced gb = gqa_balanced(pl, b, s, hq, hkv, dk, dv, st->sms);
-  const long long rows = (long long)b * hq * s;
-  const size_t need = gb.grid > 0 ? balanced_bytes(gb, dv) : partial_bytes(rows, pl.nsplit, dv);
-  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return DECATTN_ERR_WORKSPACE;
-  GqaLaunch a;
-  a.q = q;
-  a.k = k;
-  a.v = v;
-  a.seqlens = seqlens;
-  a.block_table = kv.block_table;
-  a.max_pages = kv.max_pages;
-  a.paged = kv.paged;
-  a.capacity = kv.capacity;
-  a.num_pages = kv.num_pages;
-  a.b = b;
-  a.s = s;
-  a.hq = hq;
-  a.hkv = hkv;
-  a.dk = dk;
-  a.dv = dv;
-  a.nsplit = pl.nsplit;
-  a.chunk = pl.chunk;
-  a.scale = scale;
-  a.out = out;
-  a.lse = lse;
-  a.ws_o = pl.nsplit > 1 ? static_cast<float*>(workspace) : nullptr;
-  a.ws_lse = pl.nsplit > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                                       align256((size_t)rows * pl.nsplit * dv * sizeof(float)))
-                           : nullptr;
-  a.meta = nullptr;
-  a.balanced_grid = gb.grid;
-  if (gb.grid > 0) {
-    const long long records = gb.items + gb.grid;
-    char* w = static_cast<char*>(workspace);
-    const size_t o_bytes = align256((size_t)records * gb.rpb * dv * sizeof(float));
-    a.ws_o = reinterpret_cast<float*>(w);
-    a.ws_lse = reinterpret_cast<float*>(w + o_bytes);
-    a.meta = reinterpret_cast<int*>(w + o_bytes + align256((size_t)records * gb.rpb * sizeof(float)));
-  }
-  a.err = st->err;
-  a.wait_ns = wait_limit();
-  a.test_timeout = g_test_timeout.load();
-  g_last_splits.store(pl.nsplit);
-  if (launch_gqa(a, stream) != cudaSuccess) return DECATTN_ERR_CUDA;
-  if (gb.grid > 0) {
-    if (launch_combine_balanced(a.ws_o, a.ws_lse, a.meta, seqlens, b, hq, s, hkv, dv, gb.items + gb.grid, out, lse,
-                                stream) != cudaSuccess)
-      return DECATTN_ERR_CUDA;
-  } else if (pl.nsplit > 1) {
-    if (launch_combine(a.ws_o, false, a.ws_lse, seqlens, (int)rows, hq * s, pl.nsplit, pl.chunk, dv, out, lse,
-                       stream) != cudaSuccess)
-      return DECATTN_ERR_CUDA;
-  }
-  return DECATTN_OK;
+  return gqa_decode_impl(q, k, v, kv, seqlens, max_seqlen, b, s, hq, hkv, dk, dv, scale, false, 1.f, 1.f, out, lse,
+                         workspace, workspace_bytes, stream);
+}
+
+int gqa_decode_fp8(const decattn_bf16* q, const uint8_t* k, const uint8_t* v, decattn_kv kv, const int32_t* seqlens,
+                   int max_seqlen, int b, int s, int hq, int hkv, int d, float scale, float k_scale, float v_scale,
+                   decattn_bf16* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return gqa_decode_impl(q, k, v, kv, seqlens, max_seqlen, b, s, hq, hkv, d, d, scale, true, k_scale, v_scale, out,
+                         lse, workspace, workspace_bytes, stream);
 }
 
 int gqa_decode(const decattn_bf16* q, const decattn_bf16* k, const decattn_bf16* v, decattn_kv kv,

@@ -397,16 +397,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
 }
 
 // ---------------------------------------------------------------------------
-// host: tiled tensor map over a bf16 tensor with 128-byte swizzle (the driver entry point
-// is looked up once; false if it is unavailable or rejects the description)
+// host: tiled tensor maps (the driver entry point is looked up once; false if it is
+// unavailable or rejects the description)
 
 typedef CUresult (*DecattnEncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                          const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
                                          CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
                                          CUtensorMapFloatOOBfill);
 
-inline bool encode_tmap_bf16(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
-                             const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swizzle) {
+inline bool encode_tmap(CUtensorMap* m, CUtensorMapDataType type, const void* base, int rank, const cuuint64_t* dims,
+                        const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swizzle) {
   static std::atomic<DecattnEncodeTiledFn> fn{nullptr};
   DecattnEncodeTiledFn enc = fn.load(std::memory_order_acquire);
   if (!enc) {
@@ -419,10 +419,21 @@ inline bool encode_tmap_bf16(CUtensorMap* m, const void* base, int rank, const c
     enc = reinterpret_cast<DecattnEncodeTiledFn>(ptr);
     fn.store(enc, std::memory_order_release);
   }
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (rank < 1 || rank > 5) return false;
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return enc(m, type, rank, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline bool encode_tmap_bf16(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+                             const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swizzle) {
+  return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides, box, swizzle);
+}
+
+// bytes (e.g. an FP8 cache), no swizzle
+inline bool encode_tmap_u8(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+                           const cuuint64_t* strides, const cuuint32_t* box) {
+  return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, rank, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 inline bool encode_tmap_bf16_sw128(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,

@@ -25,6 +25,9 @@
 //  * Every kernel here is launched as a programmatic dependent of the kernel
 //    before it on the stream and waits for it (griddepcontrol.wait) before its
 //    first global read, so launch and block scheduling overlap that kernel's end.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -49,6 +52,7 @@ struct GqaParams {
   unsigned* err;
   unsigned long long wait_ns;  // limit of the tile waits
   int test_timeout;            // nonzero: the first tile wait also waits on a barrier nothing signals
+  float v_scale;               // FP8 cache: value dequantisation scale, applied to the output (else 1)
 };
 
 constexpr int kTileKeys = 64;
@@ -62,23 +66,40 @@ constexpr unsigned long long kTestWaitNs = 1000000ull;     // 1 ms forced-timeou
 // DK: width of a query / key row; DV: width of a value / output row (equal for plain
 // grouped-head attention; 192 and 128 for the expanded MLA form, whose keys carry the
 // 64 RoPE dimensions that its values lack).
-template <int DK, int DV, int MT_>
+template <int DK, int DV, int MT_, bool FP8_ = false>
 struct GqaCfg {
+  static constexpr bool FP8 = FP8_;  // cache in e4m3 bytes, widened to bf16 in shared memory per tile
   static constexpr int MT = MT_;  // 16-row m-tiles per CTA
   static constexpr int THREADS = 128 * MT;
-  static constexpr int K_TILE = kTileKeys * DK * 2;  // one K tile
+  static constexpr int K_TILE = kTileKeys * DK * 2;  // one K tile (bf16, as the MMAs read it)
   static constexpr int V_TILE = kTileKeys * DV * 2;  // one V tile
-  static constexpr int STAGE_BYTES = K_TILE + V_TILE;
+  static constexpr int CACHE_ELEM = FP8 ? 1 : 2;     // bytes per cached value
+  static constexpr int K_LOAD = kTileKeys * DK * CACHE_ELEM;  // bytes one K tile copy lands
+  static constexpr int V_LOAD = kTileKeys * DV * CACHE_ELEM;
+  static constexpr int STAGE_BYTES = K_LOAD + V_LOAD;
   // pipeline stages: 4 for small rows, 3 for 128 or 256 dims (two resp. one CTA per SM);
-  // the 192/128 form takes 4 (160 KB, one CTA per SM, three tiles in flight)
-  static constexpr int NST = (DK <= 64 || DK != DV) ? 4 : 3;
-  static constexpr int PIPE_BYTES = NST * STAGE_BYTES;
+  // the 192/128 form takes 4 (160 KB, one CTA per SM, three tiles in flight); an FP8
+  // stage is half as large, so it takes twice as many stages in the same space
+  static constexpr int NST = FP8 ? (DK <= 64 ? 6 : 4) : ((DK <= 64 || DK != DV) ? 4 : 3);
+  // FP8: the bf16 tile pair the MMAs read, written from the landed stage by all threads
+  static constexpr int WORK_OFF = NST * STAGE_BYTES;
+  static constexpr int PIPE_BYTES = NST * STAGE_BYTES + (FP8 ? K_TILE + V_TILE : 0);
   static constexpr int OSTR = DV + 2;  // padded fp32 row stride of the merge buffer
   static constexpr int RED_BYTES = kSlices * 16 * MT * OSTR * 4;
   static constexpr int SMEM = PIPE_BYTES > RED_BYTES ? PIPE_BYTES : RED_BYTES;
   static constexpr int BLK = kTileKeys * 128;  // one [64 keys x 64 dims] block of a tile
   static_assert(DK % 64 == 0 && DV % 64 == 0, "tiles are 64-dim blocks");
 };
+
+// Two e4m3 values (low byte first) to a bf16 pair (low half first). Exact: every e4m3
+// value, subnormals included, is a float16 and a bfloat16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t v) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E4M3);
+  __half_raw lo, hi;
+  lo.x = h.x;
+  hi.x = h.y;
+  return pack_bf16(__half2float(__half(lo)), __half2float(__half(hi)));
+}
 
 // Shared-memory offset of 16-byte chunk c (8 dims) of key row r in a K or V tile: the
 // tile is DK/64 (K) or DV/64 (V) blocks of [64 keys x 128 bytes], each with the 128-byte swizzle (chunk
@@ -98,13 +119,15 @@ enum SegOut { kSegFinal = 0, kSegSplit = 1, kSegRecord = 2 };
 // balanced schedule. The caller's threads all enter; shared memory is free again
 // when it returns. Returns false (in every thread) when a tile wait ran out: the
 // error is recorded, the copies already requested have been waited for (bounded) and
-// nothing was written.
-template <int DK, int DV, int MT>
+// nothing was written. FP8: the cache holds e4m3 bytes; each landed tile is widened
+// to bf16 (exactly) into one work tile pair that the MMAs read; the key scale is part
+// of p.scale_log2 and the value scale p.v_scale multiplies the output.
+template <int DK, int DV, int MT, bool FP8 = false>
 __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                             uint64_t* full, uint64_t* never, uint32_t& phase, uint8_t* smem,
                                             float (*s_m)[kSlices][16], float (*s_l)[kSlices][16], int bi, int g,
                                             int rb, int L, int kstart, int kend, int out_mode, int slot) {
-  using C = GqaCfg<DK, DV, MT>;
+  using C = GqaCfg<DK, DV, MT, FP8>;
   constexpr int NT = DV / 8;   // n-tiles of the output
   constexpr int KS = DK / 16;  // k-steps of QK^T
   const int tid = threadIdx.x;
@@ -165,11 +188,16 @@ __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMa
     const uint32_t kdst = sbase + stage * C::STAGE_BYTES;
     fence_proxy_async_smem();  // this thread's view: earlier generic writes to the stage come first
     mbar_expect_tx(&full[stage], C::STAGE_BYTES);
+    if constexpr (FP8) {  // one unswizzled box each: [64 tokens x DK bytes], [64 tokens x DV bytes]
+      tma_load_3d(kdst, tm_k, 0, g, row0, &full[stage]);
+      tma_load_3d(kdst + C::K_LOAD, tm_v, 0, g, row0, &full[stage]);
+    } else {
 #pragma unroll
-    for (int kb = 0; kb < DK / 64; ++kb) tma_load_3d(kdst + kb * C::BLK, tm_k, kb * 64, g, row0, &full[stage]);
+      for (int kb = 0; kb < DK / 64; ++kb) tma_load_3d(kdst + kb * C::BLK, tm_k, kb * 64, g, row0, &full[stage]);
 #pragma unroll
-    for (int kb = 0; kb < DV / 64; ++kb)
-      tma_load_3d(kdst + C::K_TILE + kb * C::BLK, tm_v, kb * 64, g, row0, &full[stage]);
+      for (int kb = 0; kb < DV / 64; ++kb)
+        tma_load_3d(kdst + C::K_TILE + kb * C::BLK, tm_v, kb * 64, g, row0, &full[stage]);
+    }
   };
 
   // ---- online-softmax state and output accumulator (rows lane/4 and lane/4 + 8)
@@ -191,15 +219,43 @@ __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMa
 
   for (int t = 0; t < ntiles; ++t) {
     const int stage = t % C::NST;
-    const uint32_t kbase = sbase + stage * C::STAGE_BYTES;
+    const uint32_t kbase = FP8 ? sbase + C::WORK_OFF : sbase + stage * C::STAGE_BYTES;
     const uint32_t vbase = kbase + C::K_TILE;
     bool landed = mbar_wait(&full[stage], (phase >> stage) & 1u, p.wait_ns, nullptr);
     if (t == 0 && p.test_timeout) landed = mbar_wait(never, 0, kTestWaitNs, nullptr) && landed;
     phase ^= 1u << stage;
-    // V rows past the end of the segment may hold anything (NaN included): their P is 0,
-    // but 0 * NaN is NaN in P V, so they are zeroed (K rows there only feed masked scores)
     const int nvalid = kend - (kstart + t * kTileKeys);
-    if (landed && nvalid < kTileKeys) {
+    if constexpr (FP8) {
+      // widen the landed e4m3 tile pair into the bf16 work tiles (swizzled as the MMAs
+      // read them). V rows past the end are written as zeros instead: they may hold
+      // anything, NaN included (their P is 0, but 0 * NaN is NaN); K rows there only
+      // feed masked scores. Every warp is done with the previous tile's work tiles (the
+      // barrier at the end of the last iteration).
+      if (landed) {
+        const uint8_t* src = smem + stage * C::STAGE_BYTES;
+        constexpr int KCH = DK / 16, VCH = DV / 16;  // 16-byte (16-value) chunks per row
+        for (int idx = tid; idx < kTileKeys * (KCH + VCH); idx += C::THREADS) {
+          const bool isv = idx >= kTileKeys * KCH;
+          const int j = isv ? idx - kTileKeys * KCH : idx;
+          const int ch = isv ? VCH : KCH;
+          const int r = j / ch, u = j % ch;
+          uint4 w0 = make_uint4(0, 0, 0, 0), w1 = make_uint4(0, 0, 0, 0);
+          if (!isv || r < nvalid) {
+            const uint4 b = *reinterpret_cast<const uint4*>(src + (isv ? C::K_LOAD + r * DV : r * DK) + u * 16);
+            w0 = make_uint4(e4m3x2_to_bf16x2(b.x & 0xffffu), e4m3x2_to_bf16x2(b.x >> 16),
+                            e4m3x2_to_bf16x2(b.y & 0xffffu), e4m3x2_to_bf16x2(b.y >> 16));
+            w1 = make_uint4(e4m3x2_to_bf16x2(b.z & 0xffffu), e4m3x2_to_bf16x2(b.z >> 16),
+                            e4m3x2_to_bf16x2(b.w & 0xffffu), e4m3x2_to_bf16x2(b.w >> 16));
+          }
+          uint8_t* dst = smem + C::WORK_OFF + (isv ? C::K_TILE : 0);
+          *reinterpret_cast<uint4*>(dst + tile_off(r, 2 * u)) = w0;
+          *reinterpret_cast<uint4*>(dst + tile_off(r, 2 * u + 1)) = w1;
+        }
+      }
+    } else if (landed && nvalid < kTileKeys) {
+      // V rows past the end of the segment may hold anything (NaN included): their P is
+      // 0, but 0 * NaN is NaN in P V, so they are zeroed (K rows there only feed masked
+      // scores)
       for (int idx = tid; idx < (kTileKeys - nvalid) * (DV / 8); idx += C::THREADS) {
         const int r = nvalid + idx / (DV / 8);
         *reinterpret_cast<uint4*>(smem + (vbase - sbase) + tile_off(r, idx % (DV / 8))) = make_uint4(0, 0, 0, 0);
@@ -312,6 +368,7 @@ __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMa
         mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
       }
     }
+    if constexpr (FP8) __syncthreads();  // the next tile is widened into the same work tiles
   }
   __syncthreads();  // every copy has been consumed; the merge buffer below reuses the stages
 
@@ -366,7 +423,7 @@ __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMa
       acc.z += a1.x;
       acc.w += a1.y;
     }
-    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    const float inv = Lsum > 0.f ? p.v_scale / Lsum : 0.f;  // v_scale: 1 unless the cache is FP8
     acc.x *= inv;
     acc.y *= inv;
     acc.z *= inv;
@@ -416,10 +473,10 @@ __device__ __forceinline__ bool cta_setup(const GqaParams& p, const CUtensorMap*
 }
 
 // One CTA per (sequence, KV head, context chunk, block of query rows).
-template <int DK, int DV, int MT>
+template <int DK, int DV, int MT, bool FP8>
 __global__ void __launch_bounds__(128 * MT)
     gqa_split_kernel(GqaParams p, const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
-  using C = GqaCfg<DK, DV, MT>;
+  using C = GqaCfg<DK, DV, MT, FP8>;
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ float s_m[MT][kSlices][16];
   __shared__ float s_l[MT][kSlices][16];
@@ -448,8 +505,8 @@ __global__ void __launch_bounds__(128 * MT)
     return;
   }
   const int kend = min(L, kstart + p.chunk);
-  gqa_segment<DK, DV, MT>(p, &tm_k, &tm_v, full, full + C::NST, phase, smem, s_m, s_l, bi, g, rb, L, kstart, kend,
-                          p.nsplit == 1 ? kSegFinal : kSegSplit, split);
+  gqa_segment<DK, DV, MT, FP8>(p, &tm_k, &tm_v, full, full + C::NST, phase, smem, s_m, s_l, bi, g, rb, L, kstart,
+                               kend, p.nsplit == 1 ? kSegFinal : kSegSplit, split);
 }
 
 __device__ __forceinline__ long long tiles_of(int L) { return L > 0 ? (L + kTileKeys - 1) / kTileKeys : 0; }
@@ -463,11 +520,11 @@ __device__ __forceinline__ long long tiles_of(int L) { return L > 0 ? (L + kTile
 // the order) and the CTA holding the item's first tile stores {first record, count}
 // in meta for the combine kernel. Computed from seqlens on the device, so the launch
 // needs only an upper bound of the lengths.
-template <int DK, int DV, int MT>
+template <int DK, int DV, int MT, bool FP8>
 __global__ void __launch_bounds__(128 * MT)
     gqa_balanced_kernel(GqaParams p, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v) {
-  using C = GqaCfg<DK, DV, MT>;
+  using C = GqaCfg<DK, DV, MT, FP8>;
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ float s_m[MT][kSlices][16];
   __shared__ float s_l[MT][kSlices][16];
@@ -571,7 +628,7 @@ __global__ void __launch_bounds__(128 * MT)
     // tile lies in this CTA's range still gets its meta entry, so the combine reads only
     // records inside the workspace.
     if (!aborted)
-      aborted = !gqa_segment<DK, DV, MT>(p, &tm_k, &tm_v, full, full + C::NST, phase, smem, s_m, s_l, i, g, rb, L,
+      aborted = !gqa_segment<DK, DV, MT, FP8>(p, &tm_k, &tm_v, full, full + C::NST, phase, smem, s_m, s_l, i, g, rb, L,
                                          t0 * kTileKeys, min(L, t1 * kTileKeys), c0 == c1 ? kSegFinal : kSegRecord,
                                          (int)(item + blockIdx.x));
     else
@@ -586,25 +643,32 @@ __global__ void __launch_bounds__(128 * MT)
   }
 }
 
-template <int DK, int DV, int MT>
+template <int DK, int DV, int MT, bool FP8 = false>
 cudaError_t launch_gqa_dm(const GqaParams& p, int nsplit, int hkv, int b, int balanced_grid, cudaStream_t stream) {
-  using C = GqaCfg<DK, DV, MT>;
+  using C = GqaCfg<DK, DV, MT, FP8>;
   static std::atomic<unsigned long long> split_attr{0}, balanced_attr{0};
-  if (cudaError_t e = ensure_smem_limit(gqa_split_kernel<DK, DV, MT>, C::SMEM, split_attr)) return e;
-  if (cudaError_t e = ensure_smem_limit(gqa_balanced_kernel<DK, DV, MT>, C::SMEM, balanced_attr)) return e;
+  if (cudaError_t e = ensure_smem_limit(gqa_split_kernel<DK, DV, MT, FP8>, C::SMEM, split_attr)) return e;
+  if (cudaError_t e = ensure_smem_limit(gqa_balanced_kernel<DK, DV, MT, FP8>, C::SMEM, balanced_attr)) return e;
   // K and V as [tokens, KV heads, width] (contiguous: tokens = b x capacity; paged:
   // pages x 64), read in boxes of [64 tokens, 1 head, 64 dims]
   CUtensorMap tk, tv;
   {
     const uint64_t tokens = p.paged ? (uint64_t)p.num_pages * kTileKeys : (uint64_t)p.b * p.capacity;
-    const cuuint32_t box[3] = {64, 1, kTileKeys};
     const cuuint64_t kdims[3] = {(cuuint64_t)DK, (cuuint64_t)p.hkv, (cuuint64_t)tokens};
-    const cuuint64_t kstrides[2] = {(cuuint64_t)DK * 2, (cuuint64_t)p.hkv * DK * 2};
+    const cuuint64_t kstrides[2] = {(cuuint64_t)DK * C::CACHE_ELEM, (cuuint64_t)p.hkv * DK * C::CACHE_ELEM};
     const cuuint64_t vdims[3] = {(cuuint64_t)DV, (cuuint64_t)p.hkv, (cuuint64_t)tokens};
-    const cuuint64_t vstrides[2] = {(cuuint64_t)DV * 2, (cuuint64_t)p.hkv * DV * 2};
-    if (!encode_tmap_bf16_sw128(&tk, p.k, 3, kdims, kstrides, box) ||
-        !encode_tmap_bf16_sw128(&tv, p.v, 3, vdims, vstrides, box))
-      return cudaErrorInvalidValue;
+    const cuuint64_t vstrides[2] = {(cuuint64_t)DV * C::CACHE_ELEM, (cuuint64_t)p.hkv * DV * C::CACHE_ELEM};
+    if (FP8) {  // bytes, one box per tile, no swizzle (the widening pass reads rows linearly)
+      const cuuint32_t kbox[3] = {(cuuint32_t)DK, 1, kTileKeys};
+      const cuuint32_t vbox[3] = {(cuuint32_t)DV, 1, kTileKeys};
+      if (!encode_tmap_u8(&tk, p.k, 3, kdims, kstrides, kbox) || !encode_tmap_u8(&tv, p.v, 3, vdims, vstrides, vbox))
+        return cudaErrorInvalidValue;
+    } else {
+      const cuuint32_t box[3] = {64, 1, kTileKeys};
+      if (!encode_tmap_bf16_sw128(&tk, p.k, 3, kdims, kstrides, box) ||
+          !encode_tmap_bf16_sw128(&tv, p.v, 3, vdims, vstrides, box))
+        return cudaErrorInvalidValue;
+    }
   }
   // programmatic dependent launch: the CTAs may be scheduled while the previous kernel
   // finishes; they wait for it (pdl_wait) before reading anything
@@ -618,8 +682,8 @@ cudaError_t launch_gqa_dm(const GqaParams& p, int nsplit, int hkv, int b, int ba
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = balanced_grid > 0 ? cudaLaunchKernelEx(&cfg, gqa_balanced_kernel<DK, DV, MT>, p, tk, tv)
-                                          : cudaLaunchKernelEx(&cfg, gqa_split_kernel<DK, DV, MT>, p, tk, tv);
+  const cudaError_t e = balanced_grid > 0 ? cudaLaunchKernelEx(&cfg, gqa_balanced_kernel<DK, DV, MT, FP8>, p, tk, tv)
+                                          : cudaLaunchKernelEx(&cfg, gqa_split_kernel<DK, DV, MT, FP8>, p, tk, tv);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -631,16 +695,16 @@ static int gqa_mt(int rows) { return rows <= 16 ? 1 : 2; }
 int gqa_rows_per_cta(int rows) { return 16 * gqa_mt(rows); }
 
 // Resident CTAs per SM of the balanced kernel (its grid is one wave of them).
-template <int DK, int DV, int MT>
+template <int DK, int DV, int MT, bool FP8 = false>
 static int balanced_occupancy() {
-  using C = GqaCfg<DK, DV, MT>;
+  using C = GqaCfg<DK, DV, MT, FP8>;
   // (the same GPU model on every device of a process is assumed for the cached value)
   static std::atomic<int> cached{0};
   static std::atomic<unsigned long long> attr{0};
   int n = cached.load(std::memory_order_relaxed);
   if (n == 0) {
-    if (ensure_smem_limit(gqa_balanced_kernel<DK, DV, MT>, C::SMEM, attr) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_balanced_kernel<DK, DV, MT>, C::THREADS, C::SMEM) !=
+    if (ensure_smem_limit(gqa_balanced_kernel<DK, DV, MT, FP8>, C::SMEM, attr) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_balanced_kernel<DK, DV, MT, FP8>, C::THREADS, C::SMEM) !=
             cudaSuccess ||
         n <= 0)
       return 1;
@@ -649,8 +713,16 @@ static int balanced_occupancy() {
   return n;
 }
 
-int gqa_balanced_ctas_per_sm(int dk, int dv, int rows) {
+int gqa_balanced_ctas_per_sm(int dk, int dv, int rows, bool fp8) {
   const bool two = gqa_mt(rows) == 2;
+  if (fp8) {
+    switch (dk) {
+      case 64: return two ? balanced_occupancy<64, 64, 2, true>() : balanced_occupancy<64, 64, 1, true>();
+      case 128: return two ? balanced_occupancy<128, 128, 2, true>() : balanced_occupancy<128, 128, 1, true>();
+      case 256: return two ? balanced_occupancy<256, 256, 2, true>() : balanced_occupancy<256, 256, 1, true>();
+      default: return 1;
+    }
+  }
   if (dk == 192 && dv == 128) return two ? balanced_occupancy<192, 128, 2>() : balanced_occupancy<192, 128, 1>();
   if (dk != dv) return 1;
   switch (dk) {
@@ -664,7 +736,8 @@ int gqa_ctas_per_sm(int dk, int dv) {
   if (dk != dv) return 1;
   return dk <= 64 ? 3 : (dk <= 128 ? 2 : 1);
 }
-bool gqa_supported(int dk, int dv) {
+bool gqa_supported(int dk, int dv, bool fp8) {
+  if (fp8) return dk == dv && (dk == 64 || dk == 128 || dk == 256);
   return (dk == dv && (dk == 64 || dk == 128 || dk == 256)) || (dk == 192 && dv == 128);
 }
 
@@ -689,7 +762,9 @@ cudaError_t launch_gqa(const GqaLaunch& a, cudaStream_t stream) {
   p.nrb = (p.R + 16 * mt - 1) / (16 * mt);
   p.nsplit = a.nsplit;
   p.chunk = a.chunk;
-  p.scale_log2 = a.scale * kLog2e;
+  // FP8 cache: the key scale folds into the softmax scale, the value scale into the output
+  p.scale_log2 = a.scale * (a.fp8 ? a.k_scale : 1.f) * kLog2e;
+  p.v_scale = a.fp8 ? a.v_scale : 1.f;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
   p.ws_o = a.ws_o;
@@ -699,14 +774,25 @@ cudaError_t launch_gqa(const GqaLaunch& a, cudaStream_t stream) {
   p.wait_ns = a.wait_ns;
   p.test_timeout = a.test_timeout;
 #define DECATTN_GQA_CASE(DK, DV)                                                                     \
-  if (a.dk == DK && a.dv == DV)                                                                      \
+  if (!a.fp8 && a.dk == DK && a.dv == DV)                                                            \
     return mt == 1 ? launch_gqa_dm<DK, DV, 1>(p, a.nsplit, a.hkv, a.b, a.balanced_grid, stream)      \
                    : launch_gqa_dm<DK, DV, 2>(p, a.nsplit, a.hkv, a.b, a.balanced_grid, stream);
   DECATTN_GQA_CASE(64, 64)
   DECATTN_GQA_CASE(128, 128)
   DECATTN_GQA_CASE(256, 256)
+#define DECATTN_GQA_FP8_CASE(D)                                                                      \
+  if (a.dk == D && a.dv == D)                                                                        \
+    return mt == 1 ? launch_gqa_dm<D, D, 1, true>(p, a.nsplit, a.hkv, a.b, a.balanced_grid, stream)  \
+                   : launch_gqa_dm<D, D, 2, true>(p, a.nsplit, a.hkv, a.b, a.balanced_grid, stream);
+  if (a.fp8) {
+    DECATTN_GQA_FP8_CASE(64)
+    DECATTN_GQA_FP8_CASE(128)
+    DECATTN_GQA_FP8_CASE(256)
+    return cudaErrorInvalidValue;
+  }
   DECATTN_GQA_CASE(192, 128)
 #undef DECATTN_GQA_CASE
+#undef DECATTN_GQA_FP8_CASE
   return cudaErrorInvalidValue;
 }
 

@@ -17,6 +17,8 @@ struct GqaLaunch {
   int max_pages, paged, capacity, num_pages;
   int b, s, hq, hkv;
   int dk, dv;  // query/key width, value/output width
+  int fp8;     // cache in e4m3 bytes, dequantised as k_scale * K and v_scale * V
+  float k_scale, v_scale;
   int nsplit, chunk;
   float scale;
   void* out;
@@ -33,8 +35,8 @@ struct GqaLaunch {
 // rows of one grouped-head CTA (multiple of 16) for `rows` query rows per KV head
 int gqa_rows_per_cta(int rows);
 int gqa_ctas_per_sm(int dk, int dv);
-int gqa_balanced_ctas_per_sm(int dk, int dv, int rows);  // measured occupancy of the balanced kernel
-bool gqa_supported(int dk, int dv);
+int gqa_balanced_ctas_per_sm(int dk, int dv, int rows, bool fp8);  // measured occupancy of the balanced kernel
+bool gqa_supported(int dk, int dv, bool fp8);
 cudaError_t launch_gqa(const GqaLaunch& p, cudaStream_t stream);
 
 // log-sum-exp merge of split partials: rows x nsplit partials of width d (fp32, or bf16

@@ -102,6 +102,29 @@ def gqa_decode_dv(q, k, v, seqlens, *, scale, max_seqlen=None, block_table=None,
     return out, lse
 
 
+def gqa_decode_fp8(q, k8, v8, seqlens, *, k_scale, v_scale, max_seqlen=None, scale=None, block_table=None, out=None,
+                   lse=None, return_lse=True, workspace=None, stream=None):
+    """Grouped-head decode over an FP8 (E4M3) cache: k8, v8 uint8 tensors in the
+    layouts of gqa_decode (one byte per value) standing for k_scale * K and
+    v_scale * V. q [b, Hq, s, d] bf16. Returns (out [b, Hq, s, d] bf16, lse)."""
+    lib = load()
+    _need(q, "q"), _need(k8, "k8", torch.uint8), _need(v8, "v8", torch.uint8)
+    _need(seqlens, "seqlens", torch.int32)
+    b, hq, s, d = (int(x) for x in q.shape)
+    hkv = int(k8.shape[2])
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    L = _max_seqlen(seqlens, max_seqlen)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((b, hq, s), dtype=torch.float32, device=q.device)
+    ws, wsb = _workspace(lib.gqa_decode_fp8_workspace_size(b, s, hq, hkv, d, L), workspace, q.device)
+    check(lib.gqa_decode_fp8(_p(q), _p(k8), _p(v8), _kv_desc(k8, block_table), _p(seqlens), L, b, s, hq, hkv, d, scale,
+                             float(k_scale), float(v_scale), _p(out), _p(lse), _p(ws), wsb, _stream(stream)),
+          "gqa_decode_fp8")
+    return out, lse
+
+
 def mla_decompress_kv(z, k_pe, w_uk, w_uv, *, k_out=None, v_out=None, stream=None):
     """Expanded-form cache: K = [Z W_uk^T || K_pe], V = Z W_uv for every cache row.
     z [..., k] and k_pe [..., p] with the same leading (row) shape, w_uk [h, d, k],

@@ -125,6 +125,33 @@ def make_gqa(b, hq, hkv, d, s, seqlens, *, paged=False, capacity=None, seed=0,
     return q, cache
 
 
+def make_gqa_fp8(b, hq, hkv, d, s, seqlens, *, paged=False, capacity=None, seed=0, device="cpu"):
+    """Query [b, Hq, s, d] bf16 and an FP8 (OCP E4M3) K/V cache: values drawn
+    N(0, 1) in fp32, stored as E4M3 bytes of value / scale with one scale per
+    tensor (its largest magnitude maps to 448, the largest E4M3 value). Returns
+    (q, cache with uint8 k / v, k_scale, v_scale)."""
+    seqlens = [int(x) for x in seqlens]
+    g = _gen(seed, device)
+    q = randn_bf16((b, hq, s, d), g, device)
+
+    def quantised(shape):
+        x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+        scale = float(x.abs().max()) / 448.0
+        return (x / scale).to(torch.float8_e4m3fn).view(torch.uint8), scale
+
+    if paged:
+        table, total = page_layout(seqlens, seed)
+        k, ks = quantised((max(total, 1), PAGE_SIZE, hkv, d))
+        v, vs = quantised((max(total, 1), PAGE_SIZE, hkv, d))
+        cache = KVCache(k, v, seqlens, True, 0, table.to(device))
+    else:
+        cap = int(capacity if capacity is not None else max(max(seqlens), 1))
+        k, ks = quantised((b, cap, hkv, d))
+        v, vs = quantised((b, cap, hkv, d))
+        cache = KVCache(k, v, seqlens, False, cap)
+    return q, cache, ks, vs
+
+
 @dataclass
 class MLAInputs:
     q_nope: torch.Tensor      # [b, h, s, d]

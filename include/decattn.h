@@ -120,6 +120,24 @@ int gqa_decode_dv(const decattn_bf16* q, const decattn_bf16* k, const decattn_bf
                   decattn_bf16* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Grouped-head decode over an FP8 KV cache ([LESSON] Concept, the
+ * deployment paragraph: the cache may be quantised; the pages otherwise
+ * assume BF16). k and v hold OCP FP8 E4M3 bytes (1 sign, 4 exponent bits
+ * with bias 7, 3 mantissa bits; subnormals; S.1111.111 is NaN; no
+ * infinities), in the layouts of gqa_decode with one byte per value, and
+ * stand for k_scale * K8 and v_scale * V8 (per-tensor scales, finite and
+ * > 0). Queries, outputs, workspace, errors and everything else as
+ * gqa_decode; d in {64, 128, 256}. Each cache tile is widened exactly to
+ * bf16 in shared memory; the key scale multiplies the softmax scale and the
+ * value scale the output. Cache rows past each sequence's end are never
+ * used (NaN bytes there are harmless).
+ */
+size_t gqa_decode_fp8_workspace_size(int b, int s, int hq, int hkv, int d, int max_seqlen);
+int gqa_decode_fp8(const decattn_bf16* q, const uint8_t* k, const uint8_t* v, decattn_kv kv, const int32_t* seqlens,
+                   int max_seqlen, int b, int s, int hq, int hkv, int d, float scale, float k_scale, float v_scale,
+                   decattn_bf16* out, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Expanded MLA, cache decompression ([SKILL] Absorption Trick: the keys and
  * values the latent cache stands for; Cost Models - FlashAttention; Regime
  * Selection). For every cache row m < rows and head j < h:

@@ -123,6 +123,28 @@ def gqa_ref(q: np.ndarray, k_seqs, v_seqs, seqlens, scale: float):
     return out, lse
 
 
+def e4m3_to_float(codes) -> np.ndarray:
+    """Values of FP8 E4M3 bytes (the OCP 8-bit floating-point format: bit 7 sign,
+    bits 6-3 exponent E with bias 7, bits 2-0 mantissa M; E = 0 is subnormal,
+    M/8 * 2^-6; E = 15 with M = 7 is NaN; no infinities; largest value 448)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    val = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    val = np.where((e == 15) & ((c & 0x7) == 7), np.nan, val)
+    return sign * val
+
+
+def gqa_fp8_ref(q, k8_seqs, v8_seqs, seqlens, scale: float, k_scale: float, v_scale: float):
+    """Grouped-head decode over an FP8 cache ([LESSON] deployment paragraph: a
+    quantised cache): the cached bytes stand for k_scale * K and v_scale * V; the
+    attention is gqa_ref on those values (only the first L_b rows are decoded)."""
+    ks = [k_scale * e4m3_to_float(np.asarray(k)[:int(L)]) for k, L in zip(k8_seqs, seqlens)]
+    vs = [v_scale * e4m3_to_float(np.asarray(v)[:int(L)]) for v, L in zip(v8_seqs, seqlens)]
+    return gqa_ref(q, ks, vs, seqlens, scale)
+
+
 # ---------------------------------------------------------------------------
 # absorbed latent MLA ([SKILL] "Absorption Trick (FlashMLA)": scores
 # Q K^T = (Q Wk^T) Z^T = Qz Z^T, values softmax(A) V = (softmax(A) Z) Wv; the

@@ -120,6 +120,14 @@ def gqa_bytes_exact(hq, hkv, d, seqlens, s, w=BF16_BYTES):
     return w * (rows + kv)
 
 
+def gqa_fp8_bytes_exact(hq, hkv, d, seqlens, s, w=BF16_BYTES, w_cache=1):
+    """Grouped-head decode over an FP8 cache: query and output rows in bf16 (w), K
+    and V in one byte per value (w_cache)."""
+    rows = len(seqlens) * hq * s * 2 * d
+    kv = sum(seqlens) * hkv * 2 * d
+    return w * rows + w_cache * kv
+
+
 def mla_flops_exact(h, k, p, seqlens, s):
     return sum(2 * h * causal_keys(L, s) * (2 * k + p) for L in seqlens if L > 0)
 

@@ -345,3 +345,47 @@ def test_projection_gemms_brute_force():
                 for c in range(d):
                     assert out[bi, j, i, c] == pytest.approx(
                         2.0 * math.fsum(o_lat[bi, j, i, e] * wv[j, e, c] for e in range(k)), abs=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) cache
+
+
+def test_e4m3_decoding_matches_library_and_hand_values():
+    codes = np.arange(256, dtype=np.uint8)
+    got = A.e4m3_to_float(codes)
+    lib = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(lib)) and np.isnan(got).sum() == 2
+    np.testing.assert_array_equal(got[~np.isnan(got)], lib[~np.isnan(lib)])
+    # by hand: 1.0 = 0.0111.000, 448 = 0.1111.110, -1.75 = 1.0111.110, smallest subnormal 2^-9,
+    # largest subnormal 7/8 * 2^-6, smallest normal 2^-6
+    for code, val in ((0x38, 1.0), (0x7E, 448.0), (0xBE, -1.75), (0x01, 2.0 ** -9), (0x07, 7 / 8 * 2.0 ** -6),
+                      (0x08, 2.0 ** -6), (0x00, 0.0)):
+        assert A.e4m3_to_float(np.array([code], np.uint8))[0] == val
+
+
+def test_gqa_fp8_ref_is_gqa_over_the_scaled_values():
+    # values exactly representable in E4M3 (encoded by the library), times per-tensor
+    # scales: the FP8 reference equals the grouped-head definition on k_scale*K, v_scale*V
+    rng = np.random.default_rng(5)
+    b, hq, hkv, d, s = 2, 4, 2, 8, 2
+    seqlens = [9, 5]
+    grid = A.e4m3_to_float(np.arange(0, 0x7F, dtype=np.uint8))  # every finite non-negative value
+    def cache(L):
+        x = rng.choice(grid, size=(L + 3, hkv, d)) * rng.choice([-1.0, 1.0], size=(L + 3, hkv, d))
+        codes = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        codes[L:] = 0x7F  # NaN past the end: never decoded into the result
+        return x, codes
+    kc = [cache(L) for L in seqlens]
+    vc = [cache(L) for L in seqlens]
+    q = rand(b, hq, s, d)
+    ks_, vs_ = 0.03, 0.7
+    o1, l1 = A.gqa_fp8_ref(q, [c for _, c in kc], [c for _, c in vc], seqlens, 0.3, ks_, vs_)
+    o2, l2 = A.gqa_ref(q, [ks_ * x[:L] for (x, _), L in zip(kc, seqlens)], [vs_ * x[:L] for (x, _), L in zip(vc, seqlens)],
+                       seqlens, 0.3)
+    np.testing.assert_allclose(o1, o2, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(l1, l2, atol=1e-12, rtol=0)
+    # the two scales act on different tensors
+    o3, _ = A.gqa_fp8_ref(q, [c for _, c in kc], [c for _, c in vc], seqlens, 0.3, vs_, ks_)
+    assert np.abs(o3 - o1).max() > 1e-3
+

@@ -229,6 +229,19 @@ def test_expanded_exact_counts_from_tensors():
     assert cost.fa_bytes_exact(h, d, p, [7] * 4, 1) == cost.fa_bytes(4, h, 1, 7, d, p)
 
 
+def test_gqa_fp8_bytes_from_tensors():
+    import numpy as np
+
+    hq, hkv, d, s = 6, 2, 8, 3
+    seqlens = [5, 0, 9]
+    b = len(seqlens)
+    q = np.zeros((b, hq, s, d), np.float16)  # bf16-sized query and output rows
+    kv = sum(np.zeros((L, hkv, d), np.uint8).nbytes for L in seqlens) * 2
+    assert cost.gqa_fp8_bytes_exact(hq, hkv, d, seqlens, s) == 2 * q.nbytes + kv
+    # with a two-byte cache it is the bf16 count
+    assert cost.gqa_fp8_bytes_exact(hq, hkv, d, seqlens, s, w_cache=2) == cost.gqa_bytes_exact(hq, hkv, d, seqlens, s)
+
+
 def test_decompress_counts_from_tensors():
     rows, h, d, k, p = 5, 3, 4, 6, 2
     f = (_einsum_flops("mk,hdk->mhd", (rows, k), (h, d, k)) + _einsum_flops("mk,hkd->mhd", (rows, k), (h, k, d)))

@@ -53,7 +53,8 @@ def parse():
     ap.add_argument("--no-extras", action="store_true", help="skip the grouped-head and s-sweep side measurements")
     ap.add_argument("--profile", default=None, metavar="WORKLOAD",
                     help="profiling mode: run --warmup + --steps calls of one op on one input set of the named "
-                         "workload (mla_dsv3, mla_mtp_s8, gqa_64_8, gqa_paged_hkv4, ...) and exit; prints no "
+                         "workload (mla_dsv3, mla_mtp_s8, gqa_64_8, gqa_paged_hkv4, gqa_64_8_fp8, ...) and exit; "
+                         "MLA workloads run whole pipeline steps; prints no "
                          "bench line (numbers taken under a profiler are not bench values)")
     return ap.parse_args()
 
@@ -181,7 +182,7 @@ def cpu_baseline(wl, seconds_target=15.0):
 def traffic_record():
     """DRAM bytes (read + write) per launch of the latent kernel from the committed
     ncu summary, if that summary was taken on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", "mla_latent_dsv3_b32_h128_k512_t4096_s1.md")
+    path = os.path.join(ROOT, "profiles", "mla_pair_dsv3_b32_h128_k512_t4096_s1.md")
     src = os.path.join(ROOT, "decode_attention_18_b300", "csrc", "mla_decode.cu")
     if not os.path.exists(path):
         return None
@@ -482,7 +483,7 @@ def main():
             "latent_algorithmic": {"flops": f_core, "bytes": b_core, "ai": f_core / b_core},
         },
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                     "traffic": traffic_record(), "kernel": "mla_decode call (tcgen05 latent kernel + combine)",
+                     "traffic": traffic_record(), "kernel": "mla_decode call (tcgen05 CTA-pair latent kernel + combine)",
                      "peak_source": peak_src,
                      "note": "frac of measured peak; the call's roofline time is max(FLOPs/tensor peak, bytes/HBM peak)"},
         "e2e": {"value": e2e_ms * 1e3 / (e2e_steps * world), "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -513,21 +514,31 @@ def run_profile(args):
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    wl = W.WORKLOADS[args.profile]
+    fp8 = args.profile.endswith("_fp8")  # grouped-head workload over an FP8 cache
+    wl = W.WORKLOADS[args.profile[:-4] if fp8 else args.profile]
     seqlens = wl.seqlens()
     L = max(seqlens)
     sl = torch.tensor(seqlens, dtype=torch.int32, device=dev)
-    if wl.kind == "gqa":
+    if wl.kind == "gqa" and fp8:
+        q, c, ks, vs = W.make_gqa_fp8(wl.b, wl.heads, wl.hkv, wl.d, wl.s, seqlens, paged=wl.paged, seed=wl.seed,
+                                      device=dev)
+
+        def fn():
+            da.gqa_decode_fp8(q, c.k, c.v, sl, k_scale=ks, v_scale=vs, max_seqlen=L,
+                              block_table=c.block_table if wl.paged else None)
+    elif wl.kind == "gqa":
         q, c = W.make_gqa(wl.b, wl.heads, wl.hkv, wl.d, wl.s, seqlens, paged=wl.paged, seed=wl.seed, device=dev)
 
         def fn():
             da.gqa_decode(q, c.k, c.v, sl, max_seqlen=L, block_table=c.block_table if wl.paged else None)
     else:
+        # one pipeline step per call: absorb, latent attention (+ combine), W_uv
         x = W.make_mla(wl.b, wl.heads, wl.d, wl.k, wl.p, wl.s, seqlens, seed=wl.seed, device=dev)
-        qz = da.mla_absorb_q(x.q_nope, x.w_uk, sl)
 
         def fn():
-            da.mla_decode(qz, x.q_pe, x.z, x.k_pe, sl, scale=x.scale, max_seqlen=L)
+            qz = da.mla_absorb_q(x.q_nope, x.w_uk, sl)
+            o_lat, _ = da.mla_decode(qz, x.q_pe, x.z, x.k_pe, sl, scale=x.scale, max_seqlen=L)
+            da.mla_out_proj(o_lat, x.w_uv, sl)
     for _ in range(args.warmup + args.steps):
         fn()
     torch.cuda.synchronize()

@@ -68,7 +68,11 @@ constexpr unsigned long long kTestWaitNs = 1000000ull;     // 1 ms forced-timeou
 // 64 RoPE dimensions that its values lack).
 template <int DK, int DV, int MT_, bool FP8_ = false>
 struct GqaCfg {
-  static constexpr bool FP8 = FP8_;  // cache in e4m3 bytes, widened to bf16 in shared memory per tile
+  static constexpr bool FP8 = FP8_;  // cache in e4m3 bytes
+  // FP8 with 128-byte (or longer) rows: byte tiles land 128-byte swizzled and are widened
+  // in registers after ldmatrix (f16 MMAs); with 64-byte rows they are widened to a bf16
+  // work tile in shared memory each tile
+  static constexpr bool REG8 = FP8_ && DK >= 128;
   static constexpr int MT = MT_;  // 16-row m-tiles per CTA
   static constexpr int THREADS = 128 * MT;
   static constexpr int K_TILE = kTileKeys * DK * 2;  // one K tile (bf16, as the MMAs read it)
@@ -80,10 +84,11 @@ struct GqaCfg {
   // pipeline stages: 4 for small rows, 3 for 128 or 256 dims (two resp. one CTA per SM);
   // the 192/128 form takes 4 (160 KB, one CTA per SM, three tiles in flight); an FP8
   // stage is half as large, so it takes twice as many stages in the same space
-  static constexpr int NST = FP8 ? (DK <= 64 ? 6 : 4) : ((DK <= 64 || DK != DV) ? 4 : 3);
-  // FP8: the bf16 tile pair the MMAs read, written from the landed stage by all threads
+  static constexpr int NST = REG8 ? 6 : (FP8 ? (DK <= 64 ? 6 : 4) : ((DK <= 64 || DK != DV) ? 4 : 3));
+  // FP8 with a work tile: the bf16 tile pair the MMAs read, written from the landed stage
   static constexpr int WORK_OFF = NST * STAGE_BYTES;
-  static constexpr int PIPE_BYTES = NST * STAGE_BYTES + (FP8 ? K_TILE + V_TILE : 0);
+  static constexpr int PIPE_BYTES = NST * STAGE_BYTES + ((FP8 && !REG8) ? K_TILE + V_TILE : 0);
+  static constexpr int BLK8 = kTileKeys * 128;  // REG8: one [64 keys x 128 bytes] block of a byte tile
   static constexpr int OSTR = DV + 2;  // padded fp32 row stride of the merge buffer
   static constexpr int RED_BYTES = kSlices * 16 * MT * OSTR * 4;
   static constexpr int SMEM = PIPE_BYTES > RED_BYTES ? PIPE_BYTES : RED_BYTES;
@@ -99,6 +104,23 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t v) {
   lo.x = h.x;
   hi.x = h.y;
   return pack_bf16(__half2float(__half(lo)), __half2float(__half(hi)));
+}
+
+// Four e4m3 values (bytes 0..3 of v) to two f16 pairs: lo = (byte 0, byte 1),
+// hi = (byte 2, byte 3), exactly; two conversions, no shifts or masks.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t v, uint32_t& lo, uint32_t& hi) {
+  asm("{\n.reg .b16 l, h;\nmov.b32 {l, h}, %2;\ncvt.rn.f16x2.e4m3x2 %0, l;\ncvt.rn.f16x2.e4m3x2 %1, h;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(v));
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+// Shared-memory offset of 16-byte chunk u (16 values) of key row r in a byte tile of
+// [64 keys x 128 bytes] blocks, 128-byte swizzled (as TMA writes it)
+__device__ __forceinline__ uint32_t tile8_off(int r, int u) {
+  return (uint32_t)((u >> 3) * (kTileKeys * 128) + r * 128 + (((u & 7) ^ (r & 7)) << 4));
 }
 
 // Shared-memory offset of 16-byte chunk c (8 dims) of key row r in a K or V tile: the
@@ -151,12 +173,15 @@ __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMa
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int r = mrow0 + (lane >> 2) + (e & 1) * 8;
-      const int col = ks * 16 + (lane & 3) * 2 + (e >> 1) * 8;
+      // REG8: the k index of the fragment is permuted to match the byte tiles' ldmatrix
+      // layout (fragment k 2c+i is dimension 4c+i, k 2c+8+i is dimension 4c+2+i)
+      const int col = C::REG8 ? ks * 16 + (lane & 3) * 4 + (e >> 1) * 2 : ks * 16 + (lane & 3) * 2 + (e >> 1) * 8;
       uint32_t val = 0;
       if (r < p.R) {
         const int j = g * p.G + r / p.s;
         const size_t off = ((size_t)(bi * p.hq + j) * p.s + (r % p.s)) * DK + col;
         val = __ldg(reinterpret_cast<const unsigned int*>(p.q + off));
+        if constexpr (C::REG8) val = pack_f16(bf16_lo(val), bf16_hi(val));  // f16 operands
       }
       qa[ks][e] = val;
     }
@@ -188,7 +213,13 @@ __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMa
     const uint32_t kdst = sbase + stage * C::STAGE_BYTES;
     fence_proxy_async_smem();  // this thread's view: earlier generic writes to the stage come first
     mbar_expect_tx(&full[stage], C::STAGE_BYTES);
-    if constexpr (FP8) {  // one unswizzled box each: [64 tokens x DK bytes], [64 tokens x DV bytes]
+    if constexpr (C::REG8) {  // [64 tokens x 128 bytes] boxes, 128-byte swizzle
+#pragma unroll
+      for (int kb = 0; kb < DK / 128; ++kb) tma_load_3d(kdst + kb * C::BLK8, tm_k, kb * 128, g, row0, &full[stage]);
+#pragma unroll
+      for (int kb = 0; kb < DV / 128; ++kb)
+        tma_load_3d(kdst + C::K_LOAD + kb * C::BLK8, tm_v, kb * 128, g, row0, &full[stage]);
+    } else if constexpr (FP8) {  // one unswizzled box each: [64 tokens x DK bytes], [64 tokens x DV bytes]
       tma_load_3d(kdst, tm_k, 0, g, row0, &full[stage]);
       tma_load_3d(kdst + C::K_LOAD, tm_v, 0, g, row0, &full[stage]);
     } else {
@@ -219,13 +250,22 @@ __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMa
 
   for (int t = 0; t < ntiles; ++t) {
     const int stage = t % C::NST;
-    const uint32_t kbase = FP8 ? sbase + C::WORK_OFF : sbase + stage * C::STAGE_BYTES;
-    const uint32_t vbase = kbase + C::K_TILE;
+    const uint32_t kbase = (FP8 && !C::REG8) ? sbase + C::WORK_OFF : sbase + stage * C::STAGE_BYTES;
+    const uint32_t vbase = kbase + (C::REG8 ? C::K_LOAD : C::K_TILE);
     bool landed = mbar_wait(&full[stage], (phase >> stage) & 1u, p.wait_ns, nullptr);
     if (t == 0 && p.test_timeout) landed = mbar_wait(never, 0, kTestWaitNs, nullptr) && landed;
     phase ^= 1u << stage;
     const int nvalid = kend - (kstart + t * kTileKeys);
-    if constexpr (FP8) {
+    if constexpr (C::REG8) {
+      // V rows past the end may hold anything (NaN included): zero bytes there (K rows
+      // there only feed masked scores)
+      if (landed && nvalid < kTileKeys) {
+        for (int idx = tid; idx < (kTileKeys - nvalid) * (DV / 16); idx += C::THREADS) {
+          const int r = nvalid + idx / (DV / 16);
+          *reinterpret_cast<uint4*>(smem + (vbase - sbase) + tile8_off(r, idx % (DV / 16))) = make_uint4(0, 0, 0, 0);
+        }
+      }
+    } else if constexpr (FP8) {
       // widen the landed e4m3 tile pair into the bf16 work tiles (swizzled as the MMAs
       // read them). V rows past the end are written as zeros instead: they may hold
       // anything, NaN included (their P is 0, but 0 * NaN is NaN); K rows there only
@@ -292,14 +332,31 @@ __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMa
       for (int a = 0; a < NACC; ++a)
 #pragma unroll
         for (int n = 0; n < 2; ++n) sacc[a][n][0] = sacc[a][n][1] = sacc[a][n][2] = sacc[a][n][3] = 0.f;
-      const int kr = slice * 16 + (lane & 7) + ((lane >> 4) & 1) * 8;
+      if constexpr (C::REG8) {
+        // byte tile: matrices (keys 0-7 | 8-15 of the slice) x (16-dim chunks 2kp | 2kp+1);
+        // a thread's 32 bits are dimensions 4c .. 4c+3 of one key, widened to two f16 pairs
+        const int kr = slice * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        const int c = ks * 2 + ((lane >> 3) & 1);
-        uint32_t b0, b1, b2, b3;
-        ldmatrix_x4(kbase + tile_off(kr, c), b0, b1, b2, b3);
-        mma_bf16_16816(sacc[ks % NACC][0], qa[ks], b0, b1);
-        mma_bf16_16816(sacc[ks % NACC][1], qa[ks], b2, b3);
+        for (int kp = 0; kp < KS / 2; ++kp) {
+          uint32_t r[4], lo[4], hi[4];
+          ldmatrix_x4(kbase + tile8_off(kr, kp * 2 + (lane >> 4)), r[0], r[1], r[2], r[3]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(r[i], lo[i], hi[i]);
+          mma_f16_16816(sacc[(2 * kp) % NACC][0], qa[2 * kp], lo[0], hi[0]);
+          mma_f16_16816(sacc[(2 * kp) % NACC][1], qa[2 * kp], lo[1], hi[1]);
+          mma_f16_16816(sacc[(2 * kp + 1) % NACC][0], qa[2 * kp + 1], lo[2], hi[2]);
+          mma_f16_16816(sacc[(2 * kp + 1) % NACC][1], qa[2 * kp + 1], lo[3], hi[3]);
+        }
+      } else {
+        const int kr = slice * 16 + (lane & 7) + ((lane >> 4) & 1) * 8;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const int c = ks * 2 + ((lane >> 3) & 1);
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4(kbase + tile_off(kr, c), b0, b1, b2, b3);
+          mma_bf16_16816(sacc[ks % NACC][0], qa[ks], b0, b1);
+          mma_bf16_16816(sacc[ks % NACC][1], qa[ks], b2, b3);
+        }
       }
 #pragma unroll
       for (int n = 0; n < 2; ++n)
@@ -343,8 +400,8 @@ __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMa
         ps += pv[e];
       }
       l_run[h2] = l_run[h2] * alpha2[h2] + ps;
-      pa[h2 + 0] = pack_bf16(pv[0], pv[1]);  // keys 0-7 of the slice
-      pa[h2 + 2] = pack_bf16(pv[2], pv[3]);  // keys 8-15
+      pa[h2 + 0] = C::REG8 ? pack_f16(pv[0], pv[1]) : pack_bf16(pv[0], pv[1]);  // keys 0-7 of the slice
+      pa[h2 + 2] = C::REG8 ? pack_f16(pv[2], pv[3]) : pack_bf16(pv[2], pv[3]);  // keys 8-15
     }
     if (__any_sync(0xffffffffu, alpha2[0] != 1.f || alpha2[1] != 1.f)) {
 #pragma unroll
@@ -357,7 +414,25 @@ __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMa
     }
 
     // O += P V (V fragments through ldmatrix.trans)
-    {
+    if constexpr (C::REG8) {
+      // byte tile through ldmatrix.trans: a thread's 32 bits are two keys (2c, 2c+1) x two
+      // dimensions (2p, 2p+1) of a 16-dim chunk; bytes 0/2 give the even dimension's key
+      // pair, bytes 1/3 the odd one's, so each chunk feeds two n-tiles: even dimensions
+      // (accumulator 2u) and odd dimensions (2u + 1); the merge below un-permutes them
+      const int kr = slice * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+      for (int up = 0; up < DV / 32; ++up) {
+        uint32_t r[4], ev[4], od[4];
+        ldmatrix_x4_trans(vbase + tile8_off(kr, up * 2 + (lane >> 4)), r[0], r[1], r[2], r[3]);
+        // bytes (0, 2, 1, 3): the even dimension's key pair low, the odd one's high
+#pragma unroll
+        for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(__byte_perm(r[i], 0, 0x3120), ev[i], od[i]);
+        mma_f16_16816(o[4 * up + 0], pa, ev[0], ev[1]);
+        mma_f16_16816(o[4 * up + 1], pa, od[0], od[1]);
+        mma_f16_16816(o[4 * up + 2], pa, ev[2], ev[3]);
+        mma_f16_16816(o[4 * up + 3], pa, od[2], od[3]);
+      }
+    } else {
       const int kr = slice * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
       for (int dp = 0; dp < DV / 16; ++dp) {
@@ -368,7 +443,7 @@ __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMa
         mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
       }
     }
-    if constexpr (FP8) __syncthreads();  // the next tile is widened into the same work tiles
+    if constexpr (FP8 && !C::REG8) __syncthreads();  // the next tile is widened into the same work tiles
   }
   __syncthreads();  // every copy has been consumed; the merge buffer below reuses the stages
 
@@ -393,10 +468,21 @@ __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMa
 #pragma unroll
     for (int w = 1; w < kSlices; ++w) M = fmaxf(M, s_m[mt][w][r]);
     const float f = (M == -INFINITY) ? 0.f : exp2f(m_run[h2] - M);
-    float* dst = red_o + ((mt * kSlices + slice) * 16 + r) * C::OSTR + (lane & 3) * 2;
+    if constexpr (C::REG8) {
+      // accumulator 2u + parity, column n holds dimension 16u + 2n + parity
+      float* dst = red_o + ((mt * kSlices + slice) * 16 + r) * C::OSTR + (lane & 3) * 4;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-      *reinterpret_cast<float2*>(dst + nt * 8) = make_float2(o[nt][h2 * 2] * f, o[nt][h2 * 2 + 1] * f);
+      for (int u = 0; u < DV / 16; ++u) {
+        *reinterpret_cast<float2*>(dst + u * 16) = make_float2(o[2 * u][h2 * 2] * f, o[2 * u + 1][h2 * 2] * f);
+        *reinterpret_cast<float2*>(dst + u * 16 + 2) =
+            make_float2(o[2 * u][h2 * 2 + 1] * f, o[2 * u + 1][h2 * 2 + 1] * f);
+      }
+    } else {
+      float* dst = red_o + ((mt * kSlices + slice) * 16 + r) * C::OSTR + (lane & 3) * 2;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        *reinterpret_cast<float2*>(dst + nt * 8) = make_float2(o[nt][h2 * 2] * f, o[nt][h2 * 2 + 1] * f);
+    }
   }
   __syncthreads();
 
@@ -658,7 +744,12 @@ cudaError_t launch_gqa_dm(const GqaParams& p, int nsplit, int hkv, int b, int ba
     const cuuint64_t kstrides[2] = {(cuuint64_t)DK * C::CACHE_ELEM, (cuuint64_t)p.hkv * DK * C::CACHE_ELEM};
     const cuuint64_t vdims[3] = {(cuuint64_t)DV, (cuuint64_t)p.hkv, (cuuint64_t)tokens};
     const cuuint64_t vstrides[2] = {(cuuint64_t)DV * C::CACHE_ELEM, (cuuint64_t)p.hkv * DV * C::CACHE_ELEM};
-    if (FP8) {  // bytes, one box per tile, no swizzle (the widening pass reads rows linearly)
+    if (C::REG8) {  // bytes, [64 tokens x 128 bytes] boxes, 128-byte swizzle (ldmatrix reads them)
+      const cuuint32_t box[3] = {128, 1, kTileKeys};
+      if (!encode_tmap(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.k, 3, kdims, kstrides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !encode_tmap(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.v, 3, vdims, vstrides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    } else if (FP8) {  // bytes, one box per tile, no swizzle (the widening pass reads rows linearly)
       const cuuint32_t kbox[3] = {(cuuint32_t)DK, 1, kTileKeys};
       const cuuint32_t vbox[3] = {(cuuint32_t)DV, 1, kTileKeys};
       if (!encode_tmap_u8(&tk, p.k, 3, kdims, kstrides, kbox) || !encode_tmap_u8(&tv, p.v, 3, vdims, vstrides, vbox))

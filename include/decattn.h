@@ -127,10 +127,12 @@ int gqa_decode_dv(const decattn_bf16* q, const decattn_bf16* k, const decattn_bf
  * infinities), in the layouts of gqa_decode with one byte per value, and
  * stand for k_scale * K8 and v_scale * V8 (per-tensor scales, finite and
  * > 0). Queries, outputs, workspace, errors and everything else as
- * gqa_decode; d in {64, 128, 256}. Each cache tile is widened exactly to
- * bf16 in shared memory; the key scale multiplies the softmax scale and the
- * value scale the output. Cache rows past each sequence's end are never
- * used (NaN bytes there are harmless).
+ * gqa_decode; d in {64, 128, 256}. Cache values are widened exactly: for
+ * d >= 128 in registers to float16 (the MMAs then take the query and the
+ * softmax weights as float16: exact for query values of magnitude 2^-14 ..
+ * 65504), for d = 64 to bf16 in shared memory. The key scale multiplies the
+ * softmax scale and the value scale the output. Cache rows past each
+ * sequence's end are never used (NaN bytes there are harmless).
  */
 size_t gqa_decode_fp8_workspace_size(int b, int s, int hq, int hkv, int d, int max_seqlen);
 int gqa_decode_fp8(const decattn_bf16* q, const uint8_t* k, const uint8_t* v, decattn_kv kv, const int32_t* seqlens,

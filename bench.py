@@ -406,13 +406,30 @@ def main():
             sls[r].copy_(hsl, non_blocking=True)
         ev_in[r].record(h2d_stream)
 
+    # the attention step of each input set captured once from the same public API calls, as
+    # a serving loop captures its decode step; replayed every step (the copies stay eager)
+    step_graphs = []
+    with torch.cuda.stream(stream):
+        for r in range(NBUF):
+            step(r, seq=sls[r])
+    torch.cuda.synchronize()
+    for r in range(NBUF):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(r, seq=sls[r])
+        step_graphs.append(g)
+    use_graph = [True]
+
     def compute(k):
         r = k % NBUF
         stream.wait_event(ev_in[r])
         if used[r]:
             stream.wait_event(ev_out[r])  # set r's outputs of the earlier step are downloaded
         with torch.cuda.stream(stream):
-            step(r, seq=sls[r])
+            if use_graph[0]:
+                step_graphs[r].replay()
+            else:
+                step(r, seq=sls[r])
         ev_done[r].record(stream)
         used[r] = True
 
@@ -432,22 +449,87 @@ def main():
                 upload(k + 1)
             download(k)
 
-    e2e_run(5)
+    def e2e_timed(graphed):
+        use_graph[0] = graphed
+        e2e_run(5)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(h2d_stream)  # the first upload is the first timed operation
+        th0 = time.perf_counter()
+        e2e_run(e2e_steps)
+        host = time.perf_counter() - th0  # host time to enqueue every step (API calls and copies)
+        e1.record(d2h_stream)  # after the last download
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms, host
+
+    eager_ms, eager_host_s = e2e_timed(False)
+
+    # The whole pipelined step as one graph per rotation phase: step k uploads input set
+    # k+1 (h2d stream), computes set k (compute stream) and downloads set k-1's outputs
+    # (d2h stream), joined at the end; every replay copies the pinned host buffers anew.
+    # Set k was uploaded by step k-1 and set k-1 computed by it (replays on one stream run
+    # in order); set k+1 was last read by step k-2 and downloaded by step k-1.
+    def capture_phase(r):
+        nxt, prv = (r + 1) % NBUF, (r - 1) % NBUF
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fork = torch.cuda.Event()
+            fork.record(stream)
+            h2d_stream.wait_event(fork)
+            d2h_stream.wait_event(fork)
+            with torch.cuda.stream(h2d_stream):
+                sets[nxt].q_nope.copy_(hq_nope[nxt], non_blocking=True)
+                sets[nxt].q_pe.copy_(hq_pe[nxt], non_blocking=True)
+                sls[nxt].copy_(hsl, non_blocking=True)
+            step(r, seq=sls[r])
+            with torch.cuda.stream(d2h_stream):
+                hout[prv].copy_(outs[prv]["out"], non_blocking=True)
+                hlse[prv].copy_(outs[prv]["lse"], non_blocking=True)
+            j1, j2 = torch.cuda.Event(), torch.cuda.Event()
+            j1.record(h2d_stream)
+            j2.record(d2h_stream)
+            stream.wait_event(j1)
+            stream.wait_event(j2)
+        return g
+
+    torch.cuda.synchronize()
+    phase_graphs = [capture_phase(r) for r in range(NBUF)]
+
+    def piped_run(n):
+        with torch.cuda.stream(stream):
+            sets[0].q_nope.copy_(hq_nope[0], non_blocking=True)  # step 0's inputs
+            sets[0].q_pe.copy_(hq_pe[0], non_blocking=True)
+            sls[0].copy_(hsl, non_blocking=True)
+            for k in range(n):
+                phase_graphs[k % NBUF].replay()
+            last = (n - 1) % NBUF  # the last step's outputs
+            hout[last].copy_(outs[last]["out"], non_blocking=True)
+            hlse[last].copy_(outs[last]["lse"], non_blocking=True)
+
+    piped_run(6)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(h2d_stream)  # the first upload is the first timed operation
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
     th0 = time.perf_counter()
-    e2e_run(e2e_steps)
-    host_s = time.perf_counter() - th0  # host time to enqueue every step (API calls and copies)
-    e1.record(d2h_stream)  # after the last download
+    piped_run(e2e_steps)
+    host_s = time.perf_counter() - th0
+    p1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = p0.elapsed_time(p1)
     if world > 1:
         t = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
+    graph_step_ms, graph_step_host_s = e2e_timed(True)
     h2d = sum(t.numel() * t.element_size() for t in (hq_nope[0], hq_pe[0], hsl))
     d2h = hout[0].numel() * hout[0].element_size() + hlse[0].numel() * hlse[0].element_size()
 
@@ -489,8 +571,14 @@ def main():
         "e2e": {"value": e2e_ms * 1e3 / (e2e_steps * world), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "host_enqueue_us_per_step": host_s * 1e6 / e2e_steps,
-                "copies": "every step's inputs in and outputs out, on upload / download streams overlapping "
-                          "the neighbouring steps' compute (event-ordered, three input/output sets)"},
+                "step": "the public API calls and the step's copies (upload of the next input set, download "
+                        "of the previous outputs, on their own streams) captured once per rotation phase in a "
+                        "CUDA graph and replayed each step; every replay copies the pinned host buffers",
+                "graphed_compute_eager_copies_us": graph_step_ms * 1e3 / (e2e_steps * world),
+                "eager_api_us": eager_ms * 1e3 / (e2e_steps * world),
+                "eager_api_host_enqueue_us_per_step": eager_host_s * 1e6 / e2e_steps,
+                "copies": "every step's inputs in and outputs out, overlapping the neighbouring steps' compute "
+                          "(three input/output sets)"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }

@@ -17,6 +17,7 @@ from .ops import (  # noqa: F401
     mla_out_proj,
     mla_split_forward,
     set_forced_splits,
+    set_grouped_kernel,
     set_wait_limit_ns,
     test_force_timeout,
 )
@@ -24,5 +25,5 @@ from .ops import (  # noqa: F401
 __all__ = [
     "gqa_decode", "gqa_decode_dv", "gqa_decode_fp8", "mla_decompress_kv", "mla_absorb_q", "mla_decode", "mla_out_proj", "mla_forward",
     "attn_merge_lse", "mla_split_forward",
-    "check_errors", "set_forced_splits", "last_num_splits", "set_wait_limit_ns", "test_force_timeout", "DecAttnError",
+    "check_errors", "set_forced_splits", "set_grouped_kernel", "last_num_splits", "set_wait_limit_ns", "test_force_timeout", "DecAttnError",
 ]

@@ -31,6 +31,7 @@ SYMBOLS = (
     "attn_merge_lse",
     "gqa_decode_fp8_workspace_size",
     "gqa_decode_fp8",
+    "decattn_set_grouped_kernel",
 )
 
 
@@ -105,6 +106,8 @@ def load():
     lib.gqa_decode_fp8_workspace_size.argtypes = [I, I, I, I, I, I]
     lib.gqa_decode_fp8.restype = I
     lib.gqa_decode_fp8.argtypes = [P, P, P, KV, P, I, I, I, I, I, I, F, F, F, P, P, P, SZ, P]
+    lib.decattn_set_grouped_kernel.restype = None
+    lib.decattn_set_grouped_kernel.argtypes = [I]
     _lib = lib
     return lib
 

@@ -30,6 +30,7 @@ std::atomic<unsigned long long> g_wait_ns{0};
 std::atomic<int> g_forced_splits{0};
 std::atomic<int> g_last_splits{0};
 std::atomic<int> g_test_timeout{0};
+std::atomic<int> g_grouped_kernel{0};  // 0 auto, 1 split-KV kernels, 2 tensor-core kernel (where the widths allow)
 
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
 constexpr int kPage = 64;  // chunks are whole 64-key pages (and whole kernel tiles)
@@ -178,10 +179,25 @@ Plan mla_plan(int b, int s, int h, int k, int max_seqlen, int sms) {
 namespace decattn {
 namespace {
 
+// KV heads with many query rows (prefill-sized s, large groups) run the tensor-core kernel:
+// one pass over the keys per 128 rows, no split, no workspace (a forced split count keeps
+// the split-KV kernels, which is what it is for)
+// Auto: at least 32 query rows per KV head (below that the split-KV kernel's 16-row tiles
+// waste nothing) and a grid of at least half the SMs (the kernel never splits the context).
+bool use_prefill(int b, int hq, int hkv, int s, int dk, int dv, bool fp8, int sms) {
+  if (fp8 || g_forced_splits.load() > 0 || !gqa_prefill_supported(dk, dv)) return false;
+  const int mode = g_grouped_kernel.load();
+  if (mode == 1) return false;
+  if (mode == 2) return true;
+  const long long rows = (long long)(hq / hkv) * s;
+  return rows >= 32 && (long long)b * hkv * ((rows + 127) / 128) * 2 >= sms;
+}
+
 size_t gqa_workspace(int b, int s, int hq, int hkv, int dk, int dv, int max_seqlen, bool fp8) {
   if (b < 1 || s < 1 || hq < 1 || hkv < 1 || hq % hkv || dk < 1 || dv < 1) return 0;
   DeviceState* st = nullptr;
   if (device_state(&st)) return 0;
+  if (use_prefill(b, hq, hkv, s, dk, dv, fp8, st->sms)) return 0;
   const Plan pl = gqa_plan(b, s, hq, hkv, dk, dv, max_seqlen, st->sms);
   const GqaBalanced gb = gqa_balanced(pl, b, s, hq, hkv, dk, dv, st->sms, fp8);
   if (gb.grid > 0) return balanced_bytes(gb, dv);
@@ -204,6 +220,34 @@ int gqa_decode_impl(const void* q, const void* k, const void* v, decattn_kv kv, 
   if (int rc = check_kv(kv, b, max_seqlen)) return rc;
   DeviceState* st = nullptr;
   if (int rc = device_state(&st)) return rc;
+  if (use_prefill(b, hq, hkv, s, dk, dv, fp8, st->sms)) {
+    if ((long long)b * hq * s > INT_MAX / 2) return DECATTN_ERR_INVALID_ARG;
+    GqaLaunch a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.seqlens = seqlens;
+    a.block_table = kv.block_table;
+    a.max_pages = kv.max_pages;
+    a.paged = kv.paged;
+    a.capacity = kv.capacity;
+    a.num_pages = kv.num_pages;
+    a.b = b;
+    a.s = s;
+    a.hq = hq;
+    a.hkv = hkv;
+    a.dk = dk;
+    a.dv = dv;
+    a.nsplit = 1;
+    a.scale = scale;
+    a.out = out;
+    a.lse = lse;
+    a.err = st->err;
+    a.wait_ns = wait_limit();
+    a.test_timeout = g_test_timeout.load();
+    g_last_splits.store(1);
+    return launch_gqa_prefill(a, stream) == cudaSuccess ? DECATTN_OK : DECATTN_ERR_CUDA;
+  }
   const Plan pl = gqa_plan(b, s, hq, hkv, dk, dv, max_seqlen, st->sms);
   const GqaBalanced gb = gqa_balanced(pl, b, s, hq, hkv, dk, dv, st->sms, fp8);
   const long long rows = (long long)b * hq * s;
@@ -287,6 +331,7 @@ void decattn_set_wait_limit_ns(unsigned long long ns) { g_wait_ns.store(ns); }
 void decattn_set_forced_splits(int nsplit) { g_forced_splits.store(nsplit > 0 ? nsplit : 0); }
 int decattn_last_num_splits(void) { return g_last_splits.load(); }
 void decattn_test_force_timeout(int on) { g_test_timeout.store(on ? 1 : 0); }
+void decattn_set_grouped_kernel(int mode) { g_grouped_kernel.store(mode == 1 || mode == 2 ? mode : 0); }
 
 int decattn_check_errors(cudaStream_t stream) {
   DeviceState* st = nullptr;

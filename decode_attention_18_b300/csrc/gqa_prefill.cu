@@ -1,0 +1,449 @@
+// Grouped-head attention for many query rows per KV head (prefill-sized s) on the
+// tensor cores (sm_103a).
+//
+// "Mla Analysis" skill page, Regime Selection (the Prefill row: plain attention over
+// decompressed keys wins at large s) and Cost Models — FlashAttention; the grouped-head
+// rows of the summary table in "Why MLA and MTP Fight Each Other". The same computation
+// as the split-KV decode kernel (row = head_in_group * s + token, a causal window
+// aligned to the end), for KV heads with at least 64 query rows, where the mma.sync
+// kernel's 16-row tiles re-stream the cache once per row block and run out of math.
+//
+// One CTA takes 128 query rows of one (sequence, KV head) and every key they see:
+//  * Q [128 rows x DK] is loaded once by TMA and stays in shared memory (K-major, 128-byte
+//    swizzle); K and V tiles of 64 keys stream through a 3-stage TMA ring.
+//  * One thread issues tcgen05.mma: S = Q K^T (M = 128, N = 64) into one of two TMEM
+//    buffers, and O += P V (M = 128, N = DV) into a TMEM accumulator, the P V of tile
+//    t-1 issued after the S of tile t so that the softmax of tile t overlaps it.
+//  * Four softmax warps (thread = row) read S from TMEM, keep a lazy reference maximum
+//    (moved only past 2^8; the O row is then rescaled in TMEM once the previous tile's
+//    P V has completed), write P as bf16 into one of two shared-memory buffers, and at
+//    the end scale O by 1/l and store bf16 rows and the LSE.
+// Every wait is bounded; a wait that runs out sets the error word and the CTA winds
+// down (its copies and MMAs waited for, TMEM freed). V rows past the sequence end are
+// zeroed before the MMA reads them (their P is 0, but 0 * NaN is NaN).
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace decattn {
+
+namespace {
+
+constexpr int PM = 128;          // query rows per CTA (MMA M)
+constexpr int PK = 64;           // keys per tile (S MMA N)
+constexpr int PNS = 3;           // ring stages
+constexpr int PCH = PK * 128;    // one [64 keys x 64 values] bf16 chunk, 128-byte rows
+constexpr int PQCH = PM * 128;   // one [128 rows x 64 values] chunk of Q or P
+constexpr int PTHREADS = 192;    // warp 0 TMA, warp 1 MMA, warps 2-5 softmax / epilogue
+constexpr float kPLog2e = 1.4426950408889634f;
+constexpr float kPLn2 = 0.6931471805599453f;
+constexpr float kPRescale = 8.f;
+constexpr unsigned long long kPTeardownNs = 1000000000ull;
+
+template <int DK, int DV>
+struct PfCfg {
+  static constexpr int KCH = DK / 64, VCH = DV / 64;
+  static constexpr int STAGE = (KCH + VCH) * PCH;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_RING = OFF_Q + KCH * PQCH;
+  static constexpr int OFF_P = OFF_RING + PNS * STAGE;
+  static constexpr int OFF_BAR = OFF_P + 2 * PQCH;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;  // barriers + slots, + alignment slack
+  static_assert(DK % 64 == 0 && DV % 64 == 0 && DV <= 256, "widths");
+};
+
+// barriers
+enum { F_Q = 0, F_FULL = 1, F_EMPTY = F_FULL + PNS, F_SFULL = F_EMPTY + PNS, F_SEMPTY = F_SFULL + 2,
+       F_PFULL = F_SEMPTY + 2, F_PEMPTY = F_PFULL + 2, F_OFINAL = F_PEMPTY + 2, F_FIN = F_OFINAL + 1,
+       F_TEST = F_FIN + 1, F_COUNT = F_TEST + 1 };
+constexpr unsigned long long kPTestWaitNs = 1000000ull;  // forced-timeout test: 1 ms
+
+struct PfParams {
+  const __nv_bfloat16* q;
+  __nv_bfloat16* out;
+  float* lse;
+  const int32_t* seqlens;
+  const int32_t* block_table;
+  int max_pages, paged, capacity, num_pages;
+  int b, s, hq, hkv, G, R, nrb;
+  float scale_log2;
+  unsigned* err;
+  unsigned long long wait_ns;
+  int test_timeout;  // nonzero: the first softmax wait also waits on a barrier nothing signals
+};
+
+// all lanes of a warp wait (bounded); true only if every lane saw the phase complete
+__device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, unsigned long long ns, volatile int* abort_flag) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, ns, abort_flag));
+}
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(PTHREADS, 1)
+    gqa_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, PfParams p) {
+  using C = PfCfg<DK, DV>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the 128-byte swizzle wants 1024-byte aligned tiles: round the base up (slack reserved)
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + F_COUNT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + F_COUNT) + 1;
+  const int rb = blockIdx.x, g = blockIdx.y, bi = blockIdx.z;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[F_Q], 1);
+    for (int i = 0; i < PNS; ++i) {
+      mbar_init(&bars[F_FULL + i], 1);
+      mbar_init(&bars[F_EMPTY + i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[F_SFULL + i], 1);
+      mbar_init(&bars[F_SEMPTY + i], 4);
+      mbar_init(&bars[F_PFULL + i], 4);
+      mbar_init(&bars[F_PEMPTY + i], 1);
+    }
+    mbar_init(&bars[F_OFINAL], 1);
+    mbar_init(&bars[F_FIN], 1);
+    mbar_init(&bars[F_TEST], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;  // S buffers at columns 0 and PK, O at 2 * PK
+  auto fail = [&]() {
+    raise_error(p.err, kErrWaitTimeout);
+    *abort_flag = 1;
+  };
+  pdl_wait();  // queries, cache and lengths may come from the previous kernel in the stream
+  pdl_trigger();
+
+  const int L = p.seqlens[bi];
+  const int r0 = rb * PM;             // first row (within the KV head's R rows) of the block
+  const int r1 = min(p.R, r0 + PM);   // one past the last
+  // the widest causal window among the block's rows (token = row % s)
+  const int maxtok = (r1 - r0 >= p.s || r0 / p.s != (r1 - 1) / p.s) ? p.s - 1 : (r1 - 1) % p.s;
+  const int kend = L >= p.s ? min(L, L - p.s + maxtok + 1) : (L > 0 ? L : 0);
+  const int ntiles = (kend + PK - 1) / PK;
+  const int qrow0 = (bi * p.hq + g * p.G) * p.s + r0;  // first flattened [b*hq*s] query row
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (ntiles > 0 && elect_one()) {
+      mbar_expect_tx(&bars[F_Q], C::KCH * PQCH);
+      for (int c = 0; c < C::KCH; ++c) tma_load_2d(sb + C::OFF_Q + c * PQCH, &tm_q, c * 64, qrow0, &bars[F_Q]);
+      int last[PNS];
+      for (int i = 0; i < PNS; ++i) last[i] = -1;
+      for (int t = 0; t < ntiles; ++t) {
+        const int slot = t % PNS;
+        if (t >= PNS && !mbar_wait(&bars[F_EMPTY + slot], ((t / PNS) - 1) & 1, p.wait_ns, abort_flag)) {
+          if (!*abort_flag) fail();
+          break;
+        }
+        int row0;  // token row of the tile's first key in the cache tensor (a tile is one page)
+        if (p.paged) {
+          int page = __ldg(p.block_table + (size_t)bi * p.max_pages + t);
+          if (page < 0 || page >= p.num_pages) {
+            raise_error(p.err, kErrBadPage);
+            page = 0;  // stay inside the pool; the result is flagged invalid
+          }
+          row0 = page * PK;
+        } else {
+          row0 = bi * p.capacity + t * PK;
+        }
+        const uint32_t dst = sb + C::OFF_RING + slot * C::STAGE;
+        mbar_expect_tx(&bars[F_FULL + slot], C::STAGE);
+        for (int c = 0; c < C::KCH; ++c) tma_load_3d(dst + c * PCH, &tm_k, c * 64, g, row0, &bars[F_FULL + slot]);
+        for (int c = 0; c < C::VCH; ++c)
+          tma_load_3d(dst + (C::KCH + c) * PCH, &tm_v, c * 64, g, row0, &bars[F_FULL + slot]);
+        last[slot] = t;
+      }
+      // leave no copy in flight
+      mbar_wait(&bars[F_Q], 0, kPTeardownNs, nullptr);
+      for (int i = 0; i < PNS; ++i)
+        if (last[i] >= 0) mbar_wait(&bars[F_FULL + i], (last[i] / PNS) & 1, kPTeardownNs, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer (the whole warp waits; one lane issues)
+    const bool leader = elect_one();
+    constexpr uint32_t idS = idesc_bf16_f32(PM, PK, false, false);  // B = K rows, K-major
+    constexpr uint32_t idO = idesc_bf16_f32(PM, DV, false, true);   // B = V rows, N-major
+    const uint64_t dq = smem_desc(sb + C::OFF_Q, 16, 1024, kSw128);
+    const uint64_t dk = smem_desc(sb + C::OFF_RING, 16, 1024, kSw128);
+    const uint64_t dv = smem_desc(sb + C::OFF_RING, PCH, 1024, kSw128);  // chunk stride 8 KB
+    const uint64_t dp = smem_desc(sb + C::OFF_P, 16, 1024, kSw128);
+    bool ok = ntiles == 0 || pf_wait(&bars[F_Q], 0, p.wait_ns, abort_flag);
+    // O += P(u) V(u); the tail of the last tile's V rows is zeroed first
+    auto o_mma = [&](int u) -> bool {
+      const int pb = u & 1, slot = u % PNS;
+      if (!pf_wait(&bars[F_PFULL + pb], (u >> 1) & 1, p.wait_ns, abort_flag)) return false;
+      const int nvalid = kend - u * PK;
+      if (nvalid < PK) {
+        uint8_t* vt = smem + C::OFF_RING + slot * C::STAGE + C::KCH * PCH;
+        for (int idx = lane; idx < (PK - nvalid) * C::VCH * 8; idx += 32) {
+          const int row = nvalid + idx / (C::VCH * 8), rem = idx % (C::VCH * 8);
+          *reinterpret_cast<uint4*>(vt + (rem / 8) * PCH + row * 128 + (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      tc_fence_after();
+      if (leader) {
+        const uint64_t a0 = dp + (uint64_t)((pb * PQCH) >> 4);
+        const uint64_t b0 = dv + (uint64_t)((slot * C::STAGE + C::KCH * PCH) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < PK / 16; ++kk)
+          tc_mma_ss(tmem + 2 * PK, a0 + 2 * kk, b0 + (uint64_t)((kk * 16 * 128) >> 4), idO,
+                    (u > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&bars[F_EMPTY + slot]);  // the ring slot (K and V of tile u) is free
+        tc_commit(&bars[F_PEMPTY + pb]);   // P buffer pb is free; O holds tiles <= u
+      }
+      __syncwarp();
+      return true;
+    };
+    for (int t = 0; ok && t < ntiles; ++t) {
+      const int slot = t % PNS, sbuf = t & 1;
+      if (!pf_wait(&bars[F_FULL + slot], (t / PNS) & 1, p.wait_ns, abort_flag) ||
+          (t >= 2 && !pf_wait(&bars[F_SEMPTY + sbuf], ((t >> 1) - 1) & 1, p.wait_ns, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (leader) {
+        const uint64_t b0 = dk + (uint64_t)((slot * C::STAGE) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < DK / 16; ++kk)
+          tc_mma_ss(tmem + sbuf * PK, dq + (uint64_t)(((kk / 4) * PQCH + (kk % 4) * 32) >> 4),
+                    b0 + (uint64_t)(((kk / 4) * PCH + (kk % 4) * 32) >> 4), idS, kk > 0 ? 1u : 0u);
+        tc_commit(&bars[F_SFULL + sbuf]);
+      }
+      __syncwarp();
+      if (t >= 1 && !o_mma(t - 1)) ok = false;
+    }
+    if (ok && ntiles > 0) ok = o_mma(ntiles - 1);
+    if (leader) {
+      if (ok && ntiles > 0) tc_commit(&bars[F_OFINAL]);
+      if (!ok && !*abort_flag) fail();
+      // every MMA issued has completed before Tensor Memory is freed
+      tc_commit(&bars[F_FIN]);
+      mbar_wait(&bars[F_FIN], 0, kPTeardownNs, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ softmax (thread = row = TMEM lane), then the epilogue
+    const int q = warp & 3;            // TMEM lane quadrant this warp may access
+    const int r = q * 32 + lane;       // row within the block
+    const int rg = r0 + r;             // row within the KV head
+    const bool row_ok = rg < p.R;
+    const int tok = rg % p.s;
+    const int lim = row_ok ? (L >= p.s ? min(kend, L - p.s + tok + 1) : kend) : 0;  // exclusive key limit
+    const uint32_t t_lane = tmem + ((uint32_t)(q * 32) << 16);
+    float m_ref = -INFINITY, l_run = 0.f;
+    bool ok = ntiles > 0;
+    for (int t = 0; ok && t < ntiles; ++t) {
+      const int sbuf = t & 1, pb = t & 1;
+      if (!pf_wait(&bars[F_SFULL + sbuf], (t >> 1) & 1, p.wait_ns, abort_flag) ||
+          (t == 0 && p.test_timeout && !pf_wait(&bars[F_TEST], 0, kPTestWaitNs, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float x[PK];
+      {
+        uint32_t v[32];
+        tmem_ld32(t_lane + sbuf * PK, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(v[c]) * p.scale_log2;
+        tmem_ld32(t_lane + sbuf * PK + 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) x[32 + c] = __uint_as_float(v[c]) * p.scale_log2;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[F_SEMPTY + sbuf]);  // the MMA warp may overwrite this S buffer
+      const int kb = t * PK;
+      if (kb + PK > lim) {
+#pragma unroll
+        for (int c = 0; c < PK; ++c)
+          if (kb + c >= lim) x[c] = -INFINITY;
+      }
+      float mx = x[0];
+#pragma unroll
+      for (int c = 1; c < PK; ++c) mx = fmaxf(mx, x[c]);
+      // P buffer pb was last read by the P V of tile t-2
+      if (t >= 2 && !pf_wait(&bars[F_PEMPTY + pb], ((t >> 1) - 1) & 1, p.wait_ns, abort_flag)) {
+        ok = false;
+        break;
+      }
+      // lazy reference maximum: moved only past 2^8; O (tiles < t, once their P V is done)
+      // is then rescaled in TMEM row by row (the whole warp takes part in the loads)
+      float alpha = 1.f;
+      const bool move = mx > m_ref + kPRescale;
+      if (move) alpha = fast_exp2(m_ref - mx);  // 0 while nothing was seen yet
+      if (__any_sync(0xffffffffu, move && m_ref != -INFINITY) && t >= 1) {
+        if (!pf_wait(&bars[F_PEMPTY + ((t - 1) & 1)], ((t - 1) >> 1) & 1, p.wait_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c0 = 0; c0 < DV; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(t_lane + 2 * PK + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * alpha);
+          tmem_st32(t_lane + 2 * PK + c0, v);
+        }
+        tmem_st_wait();
+      }
+      if (move) {
+        m_ref = mx;
+        l_run *= alpha;
+      }
+      const float mneg = m_ref == -INFINITY ? 0.f : -m_ref;  // all keys masked so far: x = -inf -> 0
+      uint32_t pk[PK / 2];
+      float ps = 0.f;
+#pragma unroll
+      for (int e = 0; e < PK / 2; ++e) {
+        const float p0 = fast_exp2(x[2 * e] + mneg), p1 = fast_exp2(x[2 * e + 1] + mneg);
+        ps += p0 + p1;
+        pk[e] = pack_bf16(p0, p1);
+      }
+      l_run += ps;
+      // P row r into buffer pb: [128 rows x 128 bytes], 16-byte unit u at (u ^ (r & 7))
+      uint8_t* prow = smem + C::OFF_P + pb * PQCH + r * 128;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<uint4*>(prow + ((u ^ (r & 7)) << 4)) =
+            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      fence_proxy_async_smem();  // the MMA (async proxy) reads what these stores wrote
+      tc_fence_before();         // and the rescale's TMEM stores come before its P V
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[F_PFULL + pb]);
+    }
+    if (ok && ntiles > 0) ok = pf_wait(&bars[F_OFINAL], 0, p.wait_ns, abort_flag);
+    if (!ok && ntiles > 0) {
+      if (lane == 0 && !*abort_flag) fail();
+    } else {
+      tc_fence_after();
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const int j = g * p.G + rg / p.s;
+      const size_t rowflat = ((size_t)bi * p.hq + j) * p.s + tok;
+      __nv_bfloat16* dst = p.out + rowflat * DV;
+#pragma unroll 1
+      for (int c0 = 0; c0 < DV; c0 += 32) {
+        uint32_t v[32];
+        if (ntiles > 0) {
+          tmem_ld32(t_lane + 2 * PK + c0, v);  // the whole warp loads; rows past R store nothing
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] = 0u;  // no key (empty sequence): zero rows
+        }
+        if (row_ok) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            d4[u] = make_uint4(pack_bf16(__uint_as_float(v[8 * u + 0]) * inv, __uint_as_float(v[8 * u + 1]) * inv),
+                               pack_bf16(__uint_as_float(v[8 * u + 2]) * inv, __uint_as_float(v[8 * u + 3]) * inv),
+                               pack_bf16(__uint_as_float(v[8 * u + 4]) * inv, __uint_as_float(v[8 * u + 5]) * inv),
+                               pack_bf16(__uint_as_float(v[8 * u + 6]) * inv, __uint_as_float(v[8 * u + 7]) * inv));
+        }
+      }
+      if (row_ok && p.lse) p.lse[rowflat] = l_run > 0.f ? (m_ref + log2f(l_run)) * kPLn2 : -INFINITY;
+    }
+  }
+
+  // ---- teardown: nothing of this CTA is in flight
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+}  // namespace
+
+bool gqa_prefill_supported(int dk, int dv) { return dv == 128 && (dk == 128 || dk == 192); }
+
+template <int DK, int DV>
+static cudaError_t launch_pf(const GqaLaunch& a, cudaStream_t stream) {
+  using C = PfCfg<DK, DV>;
+  static std::atomic<unsigned long long> smem_limit_set{0};
+  if (cudaError_t e = ensure_smem_limit(gqa_prefill_kernel<DK, DV>, C::SMEM, smem_limit_set)) return e;
+  CUtensorMap tq, tk, tv;
+  {  // queries as [b*Hq*s rows, DK]: boxes [128 rows x 64 values]
+    const cuuint64_t dims[2] = {(cuuint64_t)DK, (cuuint64_t)a.b * a.hq * a.s};
+    const cuuint64_t strides[1] = {(cuuint64_t)DK * 2};
+    const cuuint32_t box[2] = {64, PM};
+    if (!encode_tmap_bf16_sw128(&tq, a.q, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {  // K and V as [tokens, KV heads, width]: boxes [64 tokens, 1 head, 64 values]
+    const uint64_t tokens = a.paged ? (uint64_t)a.num_pages * PK : (uint64_t)a.b * a.capacity;
+    const cuuint32_t box[3] = {64, 1, PK};
+    const cuuint64_t kdims[3] = {(cuuint64_t)DK, (cuuint64_t)a.hkv, (cuuint64_t)tokens};
+    const cuuint64_t kstrides[2] = {(cuuint64_t)DK * 2, (cuuint64_t)a.hkv * DK * 2};
+    const cuuint64_t vdims[3] = {(cuuint64_t)DV, (cuuint64_t)a.hkv, (cuuint64_t)tokens};
+    const cuuint64_t vstrides[2] = {(cuuint64_t)DV * 2, (cuuint64_t)a.hkv * DV * 2};
+    if (!encode_tmap_bf16_sw128(&tk, a.k, 3, kdims, kstrides, box) ||
+        !encode_tmap_bf16_sw128(&tv, a.v, 3, vdims, vstrides, box))
+      return cudaErrorInvalidValue;
+  }
+  PfParams p;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.lse = a.lse;
+  p.seqlens = a.seqlens;
+  p.block_table = a.block_table;
+  p.max_pages = a.max_pages;
+  p.paged = a.paged;
+  p.capacity = a.capacity;
+  p.num_pages = a.num_pages;
+  p.b = a.b;
+  p.s = a.s;
+  p.hq = a.hq;
+  p.hkv = a.hkv;
+  p.G = a.hq / a.hkv;
+  p.R = p.G * a.s;
+  p.nrb = (p.R + PM - 1) / PM;
+  p.scale_log2 = a.scale * kPLog2e;
+  p.err = a.err;
+  p.wait_ns = a.wait_ns;
+  p.test_timeout = a.test_timeout;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.nrb, a.hkv, a.b);
+  cfg.blockDim = dim3(PTHREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gqa_prefill_kernel<DK, DV>, tq, tk, tv, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_gqa_prefill(const GqaLaunch& a, cudaStream_t stream) {
+  if (a.dk == 192 && a.dv == 128) return launch_pf<192, 128>(a, stream);
+  if (a.dk == 128 && a.dv == 128) return launch_pf<128, 128>(a, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace decattn

@@ -269,5 +269,10 @@ def set_wait_limit_ns(ns: int):
     load().decattn_set_wait_limit_ns(int(ns))
 
 
+def set_grouped_kernel(mode: int):
+    """0 automatic, 1 split-KV kernels, 2 tensor-core kernel (diagnostics and tests)."""
+    load().decattn_set_grouped_kernel(int(mode))
+
+
 def test_force_timeout(on: bool):
     load().decattn_test_force_timeout(1 if on else 0)

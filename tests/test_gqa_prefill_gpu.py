@@ -1,0 +1,157 @@
+"""Parity of the tensor-core grouped-head kernel (chosen automatically for KV heads
+with many query rows: prefill-sized s, or large groups; forced here) against the
+fp64 oracle, through the C ABI.
+Row blocks of 128 rows span head boundaries when s < 128 (row = head_in_group * s +
+token), so the causal window differs from row to row inside a block."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as A
+from tests.helpers import assert_lse_close, assert_out_close, f64, gqa_rows
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from decode_attention_18_b300 import build
+
+    build.build()
+    import decode_attention_18_b300 as da
+
+    da.set_forced_splits(0)
+    da.set_grouped_kernel(2)  # the tensor-core kernel for every shape here, whatever the grid size
+    yield
+    da.set_grouped_kernel(0)
+    da.set_forced_splits(0)
+
+
+def run(b, hq, hkv, d, s, seqlens, paged=False, seed=0, poison=False):
+    import decode_attention_18_b300 as da
+    from decode_attention_18_b300 import workloads as W
+
+    q, cache = W.make_gqa(b, hq, hkv, d, s, seqlens, paged=paged, seed=seed, device=DEV)
+    if poison:  # rows past each sequence's end hold NaN: never read
+        if paged:
+            table = cache.block_table.cpu().numpy()
+            for i, L in enumerate(seqlens):
+                n = (L + 63) // 64
+                if n and L % 64:
+                    last = int(table[i, n - 1])
+                    cache.k[last, L % 64:] = float("nan")
+                    cache.v[last, L % 64:] = float("nan")
+        else:
+            for i, L in enumerate(seqlens):
+                cache.k[i, L:] = float("nan")
+                cache.v[i, L:] = float("nan")
+    sl = torch.tensor(seqlens, dtype=torch.int32, device=DEV)
+    assert da.ops.load().gqa_decode_workspace_size(b, s, hq, hkv, d, max(max(seqlens), 1)) == 0  # no split
+    out, lse = da.gqa_decode(q, cache.k, cache.v, sl, max_seqlen=max(max(seqlens), 1),
+                             block_table=cache.block_table if paged else None)
+    torch.cuda.synchronize()
+    assert da.check_errors() == 0
+    assert da.last_num_splits() == 1
+    return q, cache, out, lse
+
+
+def check(q, cache, out, lse, seqlens, d, what):
+    b = q.shape[0]
+    ks = [gqa_rows(cache, i, "k") for i in range(b)]
+    vs = [gqa_rows(cache, i, "v") for i in range(b)]
+    ro, rl = A.gqa_ref(f64(q), ks, vs, seqlens, 1 / math.sqrt(d))
+    assert_out_close(f64(out), ro, what)
+    assert_lse_close(f64(lse), rl, what + " lse")
+
+
+@pytest.mark.parametrize("b,hq,hkv,s,seqlens,paged", [
+    (2, 8, 2, 32, [300, 95], False),         # 128 rows per KV head: 4 heads x 32 tokens in one block
+    (2, 8, 8, 1, [500, 64], False),          # one row per KV head (decode): 127 idle rows per block
+    (1, 4, 4, 100, [450], False),            # MHA, 100 rows: a block with a ragged end
+    (3, 2, 1, 64, [64, 500, 0], True),       # one sequence all new tokens, one empty; paged
+    (2, 16, 1, 16, [257, 1000], True),       # 256 rows: two blocks, each spanning 8 heads
+    (1, 1, 1, 300, [700], False),            # three blocks of one head, causal across them
+])
+def test_prefill_vs_oracle(b, hq, hkv, s, seqlens, paged):
+    q, cache, out, lse = run(b, hq, hkv, 128, s, seqlens, paged=paged, seed=s + b)
+    check(q, cache, out, lse, seqlens, 128, f"prefill b{b} hq{hq} hkv{hkv} s{s}")
+
+
+def test_automatic_choice():
+    # automatic: the tensor-core kernel for >= 32 rows per KV head with a grid of at least
+    # half the SMs (no workspace), the split-KV kernels otherwise
+    import decode_attention_18_b300 as da
+
+    da.set_grouped_kernel(0)
+    try:
+        ws = da.ops.load().gqa_decode_workspace_size
+        assert ws(64, 32, 8, 8, 128, 4096) == 0          # 32 rows x 512 CTAs: tensor-core kernel
+        assert ws(2, 1, 8, 2, 128, 8192) > 0             # 4 rows: split-KV (with a split)
+        assert ws(1, 64, 8, 2, 128, 8192) > 0            # 256 rows but 4 CTAs: split-KV
+    finally:
+        da.set_grouped_kernel(2)
+
+
+def test_prefill_sharp_softmax():
+    # queries x 8: peaked rows, where the reference maximum moves and O is rescaled
+    import decode_attention_18_b300 as da
+    from decode_attention_18_b300 import workloads as W
+
+    seqlens = [600, 300]
+    q, cache = W.make_gqa(2, 4, 2, 128, 40, seqlens, seed=9, device=DEV, q_std=8.0)
+    sl = torch.tensor(seqlens, dtype=torch.int32, device=DEV)
+    out, lse = da.gqa_decode(q, cache.k, cache.v, sl, max_seqlen=600)
+    torch.cuda.synchronize()
+    assert da.check_errors() == 0
+    check(q, cache, out, lse, seqlens, 128, "prefill sharp")
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_prefill_nan_past_the_end(paged):
+    seqlens = [333, 130]
+    q, cache, out, lse = run(2, 8, 2, 128, 32, seqlens, paged=paged, seed=7, poison=True)
+    assert torch.isfinite(out).all()
+    check(q, cache, out, lse, seqlens, 128, f"prefill poisoned paged={paged}")
+
+
+def test_prefill_paged_equals_contiguous_bitwise():
+    import decode_attention_18_b300 as da
+    from decode_attention_18_b300 import workloads as W
+
+    seqlens = [300, 77, 129]
+    q, cache, out_p, lse_p = run(3, 8, 2, 128, 32, seqlens, paged=True, seed=21)
+    cap = max(seqlens)
+    k = torch.zeros((3, cap, 2, 128), dtype=torch.bfloat16, device=DEV)
+    v = torch.zeros_like(k)
+    for i, L in enumerate(seqlens):
+        k[i, :L] = torch.from_numpy(gqa_rows(cache, i, "k")).to(DEV, torch.bfloat16)
+        v[i, :L] = torch.from_numpy(gqa_rows(cache, i, "v")).to(DEV, torch.bfloat16)
+    sl = torch.tensor(seqlens, dtype=torch.int32, device=DEV)
+    out_c, lse_c = da.gqa_decode(q, k, v, sl, max_seqlen=cap)
+    torch.cuda.synchronize()
+    assert torch.equal(out_p, out_c) and torch.equal(lse_p, lse_c)
+
+
+def test_prefill_forced_timeout():
+    import decode_attention_18_b300 as da
+    from decode_attention_18_b300 import workloads as W
+
+    seqlens = [400, 200]
+    q, cache = W.make_gqa(2, 8, 2, 128, 32, seqlens, seed=5, device=DEV)
+    sl = torch.tensor(seqlens, dtype=torch.int32, device=DEV)
+    assert da.check_errors() == 0
+    da.test_force_timeout(True)
+    try:
+        da.gqa_decode(q, cache.k, cache.v, sl, max_seqlen=400)
+        rc = da.check_errors()
+    finally:
+        da.test_force_timeout(False)
+    assert rc == 5  # DECATTN_ERR_TIMEOUT
+    out, lse = da.gqa_decode(q, cache.k, cache.v, sl, max_seqlen=400)
+    torch.cuda.synchronize()
+    assert da.check_errors() == 0
+    check(q, cache, out, lse, seqlens, 128, "after timeout")

@@ -182,22 +182,33 @@ namespace {
 // KV heads with many query rows (prefill-sized s, large groups) run the tensor-core kernel:
 // one pass over the keys per 128 rows, no split, no workspace (a forced split count keeps
 // the split-KV kernels, which is what it is for)
-// Auto: at least 32 query rows per KV head (below that the split-KV kernel's 16-row tiles
-// waste nothing) and a grid of at least half the SMs (the kernel never splits the context).
+// Auto: the tensor-core kernel from 32 query rows per KV head with values 128 wide (below
+// 32 rows the split-KV kernel's 16-row tiles keep up with HBM: 0.94 vs 0.87 of it at 16
+// rows of the expanded form; at 256-wide rows only two 64 KB stages fit beside Q and P,
+// and the 24-row MQA shape measured 80 vs 61 us, so those keep the split-KV kernels).
 bool use_prefill(int b, int hq, int hkv, int s, int dk, int dv, bool fp8, int sms) {
-  if (fp8 || g_forced_splits.load() > 0 || !gqa_prefill_supported(dk, dv)) return false;
+  (void)b;
+  (void)sms;
+  if (fp8 || !gqa_prefill_supported(dk, dv)) return false;
   const int mode = g_grouped_kernel.load();
   if (mode == 1) return false;
   if (mode == 2) return true;
+  return dv == 128 && (long long)(hq / hkv) * s >= 32;
+}
+
+// the tensor-core kernel's context split: one CTA per SM, 128 rows per CTA
+Plan prefill_plan(int b, int s, int hq, int hkv, int max_seqlen, int sms) {
   const long long rows = (long long)(hq / hkv) * s;
-  return rows >= 32 && (long long)b * hkv * ((rows + 127) / 128) * 2 >= sms;
+  const long long base = (long long)b * hkv * ceil_div(rows, 128);
+  return plan_splits(base, max_seqlen, sms, 256, 512, kPage);
 }
 
 size_t gqa_workspace(int b, int s, int hq, int hkv, int dk, int dv, int max_seqlen, bool fp8) {
   if (b < 1 || s < 1 || hq < 1 || hkv < 1 || hq % hkv || dk < 1 || dv < 1) return 0;
   DeviceState* st = nullptr;
   if (device_state(&st)) return 0;
-  if (use_prefill(b, hq, hkv, s, dk, dv, fp8, st->sms)) return 0;
+  if (use_prefill(b, hq, hkv, s, dk, dv, fp8, st->sms))
+    return partial_bytes((long long)b * hq * s, prefill_plan(b, s, hq, hkv, max_seqlen, st->sms).nsplit, dv);
   const Plan pl = gqa_plan(b, s, hq, hkv, dk, dv, max_seqlen, st->sms);
   const GqaBalanced gb = gqa_balanced(pl, b, s, hq, hkv, dk, dv, st->sms, fp8);
   if (gb.grid > 0) return balanced_bytes(gb, dv);
@@ -222,6 +233,11 @@ int gqa_decode_impl(const void* q, const void* k, const void* v, decattn_kv kv, 
   if (int rc = device_state(&st)) return rc;
   if (use_prefill(b, hq, hkv, s, dk, dv, fp8, st->sms)) {
     if ((long long)b * hq * s > INT_MAX / 2) return DECATTN_ERR_INVALID_ARG;
+    const Plan pp = prefill_plan(b, s, hq, hkv, max_seqlen, st->sms);
+    const long long prow = (long long)b * hq * s;
+    const size_t pneed = partial_bytes(prow, pp.nsplit, dv);
+    if (pneed > 0 && (!workspace || workspace_bytes < pneed || !aligned16(workspace))) return DECATTN_ERR_WORKSPACE;
+    if ((long long)pp.nsplit * ceil_div((long long)(hq / hkv) * s, 128) > INT_MAX) return DECATTN_ERR_INVALID_ARG;
     GqaLaunch a{};
     a.q = q;
     a.k = k;
@@ -238,15 +254,24 @@ int gqa_decode_impl(const void* q, const void* k, const void* v, decattn_kv kv, 
     a.hkv = hkv;
     a.dk = dk;
     a.dv = dv;
-    a.nsplit = 1;
+    a.nsplit = pp.nsplit;
+    a.chunk = pp.chunk;
     a.scale = scale;
     a.out = out;
     a.lse = lse;
+    a.ws_o = pp.nsplit > 1 ? static_cast<float*>(workspace) : nullptr;
+    a.ws_lse = pp.nsplit > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                         align256((size_t)prow * pp.nsplit * dv * sizeof(float)))
+                             : nullptr;
     a.err = st->err;
     a.wait_ns = wait_limit();
     a.test_timeout = g_test_timeout.load();
-    g_last_splits.store(1);
-    return launch_gqa_prefill(a, stream) == cudaSuccess ? DECATTN_OK : DECATTN_ERR_CUDA;
+    g_last_splits.store(pp.nsplit);
+    if (launch_gqa_prefill(a, stream) != cudaSuccess) return DECATTN_ERR_CUDA;
+    if (pp.nsplit > 1 && launch_combine(a.ws_o, false, a.ws_lse, seqlens, (int)prow, hq * s, pp.nsplit, pp.chunk, dv,
+                                        out, lse, stream) != cudaSuccess)
+      return DECATTN_ERR_CUDA;
+    return DECATTN_OK;
   }
   const Plan pl = gqa_plan(b, s, hq, hkv, dk, dv, max_seqlen, st->sms);
   const GqaBalanced gb = gqa_balanced(pl, b, s, hq, hkv, dk, dv, st->sms, fp8);

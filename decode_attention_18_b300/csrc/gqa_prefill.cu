@@ -32,7 +32,7 @@ namespace {
 
 constexpr int PM = 128;          // query rows per CTA (MMA M)
 constexpr int PK = 64;           // keys per tile (S MMA N)
-constexpr int PNS = 3;           // ring stages
+constexpr int PNS_MAX = 4;       // ring stages at most
 constexpr int PCH = PK * 128;    // one [64 keys x 64 values] bf16 chunk, 128-byte rows
 constexpr int PQCH = PM * 128;   // one [128 rows x 64 values] chunk of Q or P
 constexpr int PTHREADS = 192;    // warp 0 TMA, warp 1 MMA, warps 2-5 softmax / epilogue
@@ -47,14 +47,20 @@ struct PfCfg {
   static constexpr int STAGE = (KCH + VCH) * PCH;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = OFF_Q + KCH * PQCH;
-  static constexpr int OFF_P = OFF_RING + PNS * STAGE;
+  // as many ring stages (at most PNS_MAX) as fit beside Q and the two P buffers in 227 KB
+  static constexpr int FIXED = KCH * PQCH + 2 * PQCH + 256 + 1024;
+  static constexpr int NS_FIT = (232448 - FIXED) / STAGE;
+  static constexpr int NS = NS_FIT < PNS_MAX ? NS_FIT : PNS_MAX;
+  static constexpr int OFF_P = OFF_RING + NS * STAGE;
   static constexpr int OFF_BAR = OFF_P + 2 * PQCH;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;  // barriers + slots, + alignment slack
+  static constexpr int TMEM_COLS = 2 * PK + DV <= 256 ? 256 : 512;  // two S buffers, then O
   static_assert(DK % 64 == 0 && DV % 64 == 0 && DV <= 256, "widths");
+  static_assert(NS >= 2, "ring");
 };
 
 // barriers
-enum { F_Q = 0, F_FULL = 1, F_EMPTY = F_FULL + PNS, F_SFULL = F_EMPTY + PNS, F_SEMPTY = F_SFULL + 2,
+enum { F_Q = 0, F_FULL = 1, F_EMPTY = F_FULL + PNS_MAX, F_SFULL = F_EMPTY + PNS_MAX, F_SEMPTY = F_SFULL + 2,
        F_PFULL = F_SEMPTY + 2, F_PEMPTY = F_PFULL + 2, F_OFINAL = F_PEMPTY + 2, F_FIN = F_OFINAL + 1,
        F_TEST = F_FIN + 1, F_COUNT = F_TEST + 1 };
 constexpr unsigned long long kPTestWaitNs = 1000000ull;  // forced-timeout test: 1 ms
@@ -67,6 +73,9 @@ struct PfParams {
   const int32_t* block_table;
   int max_pages, paged, capacity, num_pages;
   int b, s, hq, hkv, G, R, nrb;
+  int nsplit, chunk;  // context split: CTA x covers keys [split * chunk, (split + 1) * chunk)
+  float* ws_o;        // nsplit > 1: fp32 partials [b*Hq*s rows][nsplit][DV] (normalised O)
+  float* ws_lse;      // and their LSEs [rows][nsplit]
   float scale_log2;
   unsigned* err;
   unsigned long long wait_ns;
@@ -91,11 +100,11 @@ __global__ void __launch_bounds__(PTHREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + F_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + F_COUNT) + 1;
-  const int rb = blockIdx.x, g = blockIdx.y, bi = blockIdx.z;
+  const int rb = blockIdx.x % p.nrb, split = blockIdx.x / p.nrb, g = blockIdx.y, bi = blockIdx.z;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars[F_Q], 1);
-    for (int i = 0; i < PNS; ++i) {
+    for (int i = 0; i < C::NS; ++i) {
       mbar_init(&bars[F_FULL + i], 1);
       mbar_init(&bars[F_EMPTY + i], 1);
     }
@@ -115,7 +124,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     prefetch_tmap(&tm_v);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 256);
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -134,8 +143,10 @@ __global__ void __launch_bounds__(PTHREADS, 1)
   const int r1 = min(p.R, r0 + PM);   // one past the last
   // the widest causal window among the block's rows (token = row % s)
   const int maxtok = (r1 - r0 >= p.s || r0 / p.s != (r1 - 1) / p.s) ? p.s - 1 : (r1 - 1) % p.s;
-  const int kend = L >= p.s ? min(L, L - p.s + maxtok + 1) : (L > 0 ? L : 0);
-  const int ntiles = (kend + PK - 1) / PK;
+  const int kwin = L >= p.s ? min(L, L - p.s + maxtok + 1) : (L > 0 ? L : 0);  // keys the block sees
+  const int kstart = split * p.chunk;
+  const int kend = min(kwin, kstart + p.chunk);
+  const int ntiles = kend > kstart ? (kend - kstart + PK - 1) / PK : 0;
   const int qrow0 = (bi * p.hq + g * p.G) * p.s + r0;  // first flattened [b*hq*s] query row
 
   if (warp == 0) {
@@ -143,24 +154,24 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     if (ntiles > 0 && elect_one()) {
       mbar_expect_tx(&bars[F_Q], C::KCH * PQCH);
       for (int c = 0; c < C::KCH; ++c) tma_load_2d(sb + C::OFF_Q + c * PQCH, &tm_q, c * 64, qrow0, &bars[F_Q]);
-      int last[PNS];
-      for (int i = 0; i < PNS; ++i) last[i] = -1;
+      int last[PNS_MAX];
+      for (int i = 0; i < PNS_MAX; ++i) last[i] = -1;
       for (int t = 0; t < ntiles; ++t) {
-        const int slot = t % PNS;
-        if (t >= PNS && !mbar_wait(&bars[F_EMPTY + slot], ((t / PNS) - 1) & 1, p.wait_ns, abort_flag)) {
+        const int slot = t % C::NS;
+        if (t >= C::NS && !mbar_wait(&bars[F_EMPTY + slot], ((t / C::NS) - 1) & 1, p.wait_ns, abort_flag)) {
           if (!*abort_flag) fail();
           break;
         }
         int row0;  // token row of the tile's first key in the cache tensor (a tile is one page)
         if (p.paged) {
-          int page = __ldg(p.block_table + (size_t)bi * p.max_pages + t);
+          int page = __ldg(p.block_table + (size_t)bi * p.max_pages + kstart / PK + t);
           if (page < 0 || page >= p.num_pages) {
             raise_error(p.err, kErrBadPage);
             page = 0;  // stay inside the pool; the result is flagged invalid
           }
           row0 = page * PK;
         } else {
-          row0 = bi * p.capacity + t * PK;
+          row0 = bi * p.capacity + kstart + t * PK;
         }
         const uint32_t dst = sb + C::OFF_RING + slot * C::STAGE;
         mbar_expect_tx(&bars[F_FULL + slot], C::STAGE);
@@ -171,8 +182,8 @@ __global__ void __launch_bounds__(PTHREADS, 1)
       }
       // leave no copy in flight
       mbar_wait(&bars[F_Q], 0, kPTeardownNs, nullptr);
-      for (int i = 0; i < PNS; ++i)
-        if (last[i] >= 0) mbar_wait(&bars[F_FULL + i], (last[i] / PNS) & 1, kPTeardownNs, nullptr);
+      for (int i = 0; i < C::NS; ++i)
+        if (last[i] >= 0) mbar_wait(&bars[F_FULL + i], (last[i] / C::NS) & 1, kPTeardownNs, nullptr);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -187,9 +198,9 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     bool ok = ntiles == 0 || pf_wait(&bars[F_Q], 0, p.wait_ns, abort_flag);
     // O += P(u) V(u); the tail of the last tile's V rows is zeroed first
     auto o_mma = [&](int u) -> bool {
-      const int pb = u & 1, slot = u % PNS;
+      const int pb = u & 1, slot = u % C::NS;
       if (!pf_wait(&bars[F_PFULL + pb], (u >> 1) & 1, p.wait_ns, abort_flag)) return false;
-      const int nvalid = kend - u * PK;
+      const int nvalid = kend - (kstart + u * PK);
       if (nvalid < PK) {
         uint8_t* vt = smem + C::OFF_RING + slot * C::STAGE + C::KCH * PCH;
         for (int idx = lane; idx < (PK - nvalid) * C::VCH * 8; idx += 32) {
@@ -214,8 +225,8 @@ __global__ void __launch_bounds__(PTHREADS, 1)
       return true;
     };
     for (int t = 0; ok && t < ntiles; ++t) {
-      const int slot = t % PNS, sbuf = t & 1;
-      if (!pf_wait(&bars[F_FULL + slot], (t / PNS) & 1, p.wait_ns, abort_flag) ||
+      const int slot = t % C::NS, sbuf = t & 1;
+      if (!pf_wait(&bars[F_FULL + slot], (t / C::NS) & 1, p.wait_ns, abort_flag) ||
           (t >= 2 && !pf_wait(&bars[F_SEMPTY + sbuf], ((t >> 1) - 1) & 1, p.wait_ns, abort_flag))) {
         ok = false;
         break;
@@ -275,7 +286,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[F_SEMPTY + sbuf]);  // the MMA warp may overwrite this S buffer
-      const int kb = t * PK;
+      const int kb = kstart + t * PK;
       if (kb + PK > lim) {
 #pragma unroll
         for (int c = 0; c < PK; ++c)
@@ -342,9 +353,9 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     } else {
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const float lse_val = l_run > 0.f ? (m_ref + log2f(l_run)) * kPLn2 : -INFINITY;
       const int j = g * p.G + rg / p.s;
       const size_t rowflat = ((size_t)bi * p.hq + j) * p.s + tok;
-      __nv_bfloat16* dst = p.out + rowflat * DV;
 #pragma unroll 1
       for (int c0 = 0; c0 < DV; c0 += 32) {
         uint32_t v[32];
@@ -353,19 +364,32 @@ __global__ void __launch_bounds__(PTHREADS, 1)
           tmem_ld_wait();
         } else {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) v[c] = 0u;  // no key (empty sequence): zero rows
+          for (int c = 0; c < 32; ++c) v[c] = 0u;  // no key in this block's range: zero rows
         }
-        if (row_ok) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+        if (!row_ok) continue;
+        if (p.nsplit == 1) {  // final bf16 rows
+          uint4* d4 = reinterpret_cast<uint4*>(p.out + rowflat * DV + c0);
 #pragma unroll
           for (int u = 0; u < 4; ++u)
             d4[u] = make_uint4(pack_bf16(__uint_as_float(v[8 * u + 0]) * inv, __uint_as_float(v[8 * u + 1]) * inv),
                                pack_bf16(__uint_as_float(v[8 * u + 2]) * inv, __uint_as_float(v[8 * u + 3]) * inv),
                                pack_bf16(__uint_as_float(v[8 * u + 4]) * inv, __uint_as_float(v[8 * u + 5]) * inv),
                                pack_bf16(__uint_as_float(v[8 * u + 6]) * inv, __uint_as_float(v[8 * u + 7]) * inv));
+        } else {  // fp32 partial of this chunk, for the combine
+          float4* d4 = reinterpret_cast<float4*>(p.ws_o + (rowflat * p.nsplit + split) * DV + c0);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            d4[u] = make_float4(__uint_as_float(v[4 * u + 0]) * inv, __uint_as_float(v[4 * u + 1]) * inv,
+                                __uint_as_float(v[4 * u + 2]) * inv, __uint_as_float(v[4 * u + 3]) * inv);
         }
       }
-      if (row_ok && p.lse) p.lse[rowflat] = l_run > 0.f ? (m_ref + log2f(l_run)) * kPLn2 : -INFINITY;
+      if (row_ok) {
+        if (p.nsplit == 1) {
+          if (p.lse) p.lse[rowflat] = lse_val;
+        } else {
+          p.ws_lse[rowflat * p.nsplit + split] = lse_val;
+        }
+      }
     }
   }
 
@@ -374,13 +398,15 @@ __global__ void __launch_bounds__(PTHREADS, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
 }  // namespace
 
-bool gqa_prefill_supported(int dk, int dv) { return dv == 128 && (dk == 128 || dk == 192); }
+bool gqa_prefill_supported(int dk, int dv) {
+  return (dv == 128 && (dk == 128 || dk == 192)) || (dk == 256 && dv == 256);
+}
 
 template <int DK, int DV>
 static cudaError_t launch_pf(const GqaLaunch& a, cudaStream_t stream) {
@@ -422,12 +448,16 @@ static cudaError_t launch_pf(const GqaLaunch& a, cudaStream_t stream) {
   p.G = a.hq / a.hkv;
   p.R = p.G * a.s;
   p.nrb = (p.R + PM - 1) / PM;
+  p.nsplit = a.nsplit;
+  p.chunk = a.chunk;
+  p.ws_o = a.ws_o;
+  p.ws_lse = a.ws_lse;
   p.scale_log2 = a.scale * kPLog2e;
   p.err = a.err;
   p.wait_ns = a.wait_ns;
   p.test_timeout = a.test_timeout;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.nrb, a.hkv, a.b);
+  cfg.gridDim = dim3(p.nrb * p.nsplit, a.hkv, a.b);
   cfg.blockDim = dim3(PTHREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = stream;
@@ -443,6 +473,7 @@ static cudaError_t launch_pf(const GqaLaunch& a, cudaStream_t stream) {
 cudaError_t launch_gqa_prefill(const GqaLaunch& a, cudaStream_t stream) {
   if (a.dk == 192 && a.dv == 128) return launch_pf<192, 128>(a, stream);
   if (a.dk == 128 && a.dv == 128) return launch_pf<128, 128>(a, stream);
+  if (a.dk == 256 && a.dv == 256) return launch_pf<256, 256>(a, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -265,10 +265,11 @@ int gqa_decode_no_alloc(const decattn_bf16* q, const decattn_bf16* k, const deca
  * decattn_set_grouped_kernel: which grouped-head kernel gqa_decode and
  * gqa_decode_dv run (diagnostics and tests; 0 = automatic, the default).
  * 1 = the split-KV kernels (16-row tiles, context split over CTAs, combine);
- * 2 = the tensor-core kernel (tcgen05, 128 query rows per CTA, no split) where
- * the widths allow (dv = 128, dk in {128, 192}). Automatic takes the
- * tensor-core kernel for at least 32 query rows per KV head when its grid
- * covers at least half the SMs. Results agree within rounding.
+ * 2 = the tensor-core kernel (tcgen05, 128 query rows per CTA, the context
+ * split over CTAs where the grid is small) where the widths allow ((dk, dv) in
+ * {(128, 128), (192, 128), (256, 256)}). Automatic takes the tensor-core
+ * kernel for at least 32 query rows per KV head with 128-wide values. Results
+ * agree within rounding.
  * decattn_test_force_timeout: when nonzero, the next mla_decode and gqa_decode
  * kernels wait once on a barrier that nothing signals, with a 1 ms limit, so that
  * the timeout path runs; the kernels then wind down (no new copies, their own

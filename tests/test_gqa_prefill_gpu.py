@@ -31,7 +31,7 @@ def _built():
     da.set_forced_splits(0)
 
 
-def run(b, hq, hkv, d, s, seqlens, paged=False, seed=0, poison=False):
+def run(b, hq, hkv, d, s, seqlens, paged=False, seed=0, poison=False, nsplit=0):
     import decode_attention_18_b300 as da
     from decode_attention_18_b300 import workloads as W
 
@@ -50,12 +50,18 @@ def run(b, hq, hkv, d, s, seqlens, paged=False, seed=0, poison=False):
                 cache.k[i, L:] = float("nan")
                 cache.v[i, L:] = float("nan")
     sl = torch.tensor(seqlens, dtype=torch.int32, device=DEV)
-    assert da.ops.load().gqa_decode_workspace_size(b, s, hq, hkv, d, max(max(seqlens), 1)) == 0  # no split
-    out, lse = da.gqa_decode(q, cache.k, cache.v, sl, max_seqlen=max(max(seqlens), 1),
-                             block_table=cache.block_table if paged else None)
-    torch.cuda.synchronize()
+    da.set_forced_splits(nsplit)
+    try:
+        out, lse = da.gqa_decode(q, cache.k, cache.v, sl, max_seqlen=max(max(seqlens), 1),
+                                 block_table=cache.block_table if paged else None)
+        torch.cuda.synchronize()
+        if nsplit:  # chunks are whole 64-key pages: ceil(L / n) rounded up to 64
+            L = max(seqlens)
+            chunk = -(-(-(-L // nsplit)) // 64) * 64
+            assert da.last_num_splits() == -(-L // chunk)
+    finally:
+        da.set_forced_splits(0)
     assert da.check_errors() == 0
-    assert da.last_num_splits() == 1
     return q, cache, out, lse
 
 
@@ -81,19 +87,45 @@ def test_prefill_vs_oracle(b, hq, hkv, s, seqlens, paged):
     check(q, cache, out, lse, seqlens, 128, f"prefill b{b} hq{hq} hkv{hkv} s{s}")
 
 
-def test_automatic_choice():
-    # automatic: the tensor-core kernel for >= 32 rows per KV head with a grid of at least
-    # half the SMs (no workspace), the split-KV kernels otherwise
-    import decode_attention_18_b300 as da
+@pytest.mark.parametrize("nsplit", [1, 3, 7])
+def test_prefill_context_split(nsplit):
+    # the context cut into chunks (one CTA each), partials merged by the combine kernel;
+    # chunks past a row block's causal window carry LSE = -inf
+    seqlens = [700, 300]
+    q, cache, out, lse = run(2, 8, 2, 128, 32, seqlens, seed=17, nsplit=nsplit)
+    check(q, cache, out, lse, seqlens, 128, f"prefill split {nsplit}")
 
-    da.set_grouped_kernel(0)
-    try:
-        ws = da.ops.load().gqa_decode_workspace_size
-        assert ws(64, 32, 8, 8, 128, 4096) == 0          # 32 rows x 512 CTAs: tensor-core kernel
-        assert ws(2, 1, 8, 2, 128, 8192) > 0             # 4 rows: split-KV (with a split)
-        assert ws(1, 64, 8, 2, 128, 8192) > 0            # 256 rows but 4 CTAs: split-KV
-    finally:
-        da.set_grouped_kernel(2)
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_prefill_mqa_d256(paged):
+    # 24 query heads on one KV head, d = 256 (the ragged MQA geometry, shorter contexts)
+    seqlens = [1500, 700, 64]
+    q, cache, out, lse = run(3, 24, 1, 256, 1, seqlens, paged=paged, seed=23)
+    check(q, cache, out, lse, seqlens, 256, f"prefill MQA d256 paged={paged}")
+
+
+@pytest.mark.parametrize("hq,hkv,d,s,seqlens", [
+    (8, 2, 128, 32, [900, 300]),      # 128 rows per KV head
+    (24, 1, 256, 1, [2000, 333]),     # 24-row MQA, d = 256
+])
+def test_both_grouped_kernels_agree(hq, hkv, d, s, seqlens):
+    # automatic choice, the split-KV kernels and the tensor-core kernel: the same result
+    # within rounding on the same inputs
+    import decode_attention_18_b300 as da
+    from decode_attention_18_b300 import workloads as W
+
+    q, cache = W.make_gqa(2, hq, hkv, d, s, seqlens, seed=29, device=DEV)
+    sl = torch.tensor(seqlens, dtype=torch.int32, device=DEV)
+    res = {}
+    for mode in (0, 1, 2):
+        da.set_grouped_kernel(mode)
+        res[mode] = da.gqa_decode(q, cache.k, cache.v, sl, max_seqlen=max(seqlens))
+    da.set_grouped_kernel(2)
+    torch.cuda.synchronize()
+    assert da.check_errors() == 0
+    for mode in (0, 1):
+        assert_out_close(f64(res[mode][0]), f64(res[2][0]), f"mode {mode} vs 2", max_abs=1e-2, mean_abs=1e-3)
+        np.testing.assert_allclose(f64(res[mode][1]), f64(res[2][1]), atol=2e-4, rtol=0)
 
 
 def test_prefill_sharp_softmax():

@@ -84,3 +84,37 @@ def test_invalid_arguments_rejected_without_launch(lib):
     assert lib.mla_out_proj(null, null, null, null, 1, 1, 8, 512, 128, 1.0, null) == 1
     # b = 0 is a no-op
     assert lib.gqa_decode(null, null, null, kv, null, 0, 0, 1, 8, 8, 128, 1.0, null, null, null, 0, null) == 0
+
+
+def test_new_entry_points_refuse_bad_arguments_without_launch(lib):
+    from decode_attention_18_b300._native import KV
+
+    kv = KV(0, 16, None, 0, 0, 0)
+    null = ctypes.c_void_p(0)
+    # grouped-head with its own value width: null pointers, bad head counts, s out of range
+    assert lib.gqa_decode_dv(null, null, null, kv, null, 16, 1, 1, 8, 8, 192, 128, 1.0, null, null, null, 0,
+                             null) == 1
+    assert lib.gqa_decode_dv(null, null, null, kv, null, 16, 1, 1, 8, 3, 192, 128, 1.0, null, null, null, 0,
+                             null) == 1
+    assert lib.gqa_decode_dv(null, null, null, kv, null, 16, 1, 1025, 8, 8, 192, 128, 1.0, null, null, null, 0,
+                             null) == 1
+    assert lib.gqa_decode_dv(null, null, null, kv, null, 0, 0, 1, 8, 8, 192, 128, 1.0, null, null, null, 0,
+                             null) == 0  # b = 0: nothing to do
+    # FP8 cache: null pointers; scales that are not finite and positive
+    for ks in (1.0, 0.0, -1.0, float("inf"), float("nan")):
+        assert lib.gqa_decode_fp8(null, null, null, kv, null, 16, 1, 1, 8, 8, 128, 1.0, ks, 1.0, null, null, null,
+                                  0, null) == 1
+    # decompression: negative rows, null pointers; zero rows is a no-op
+    assert lib.mla_decompress_kv(null, null, null, null, -1, 8, 128, 512, 64, null, null, null) == 1
+    assert lib.mla_decompress_kv(null, null, null, null, 64, 8, 128, 512, 64, null, null, null) == 1
+    assert lib.mla_decompress_kv(null, null, null, null, 0, 8, 128, 512, 64, null, null, null) == 0
+    # LSE merge: a width that is not a multiple of 8, null pointers; zero rows is a no-op
+    assert lib.attn_merge_lse(null, null, null, null, 4, 12, null, null, null) == 1
+    assert lib.attn_merge_lse(null, null, null, null, 4, 128, null, null, null) == 1
+    assert lib.attn_merge_lse(null, null, null, null, 0, 128, null, null, null) == 0
+
+
+def test_workspace_queries_refuse_bad_shapes(lib):
+    assert lib.gqa_decode_dv_workspace_size(1, 1, 8, 3, 192, 128, 64) == 0  # Hq % Hkv != 0
+    assert lib.gqa_decode_fp8_workspace_size(0, 1, 8, 8, 128, 64) == 0     # b = 0
+    assert lib.mla_decode_workspace_size(1, 0, 8, 512, 64) == 0             # s = 0

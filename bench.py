@@ -602,6 +602,20 @@ def run_profile(args):
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
+    if args.profile == "mla_expanded_s128_b4":
+        # the expanded form's attention at s = 128 (tensor-core grouped-head kernel) on 4
+        # sequences of 4096 + 128 keys, 128 heads (decompressed cache 1.4 GB, > L2)
+        b, h, s, L = 4, 128, 128, 4096 + 128
+        x = W.make_mla(b, h, 128, 512, 64, s, [L] * b, capacity=L, seed=5, device=dev)
+        kf, vf = da.mla_decompress_kv(x.z, x.k_pe, x.w_uk, x.w_uv)
+        q = torch.cat([x.q_nope, x.q_pe], dim=-1).contiguous()
+        sl = torch.tensor([L] * b, dtype=torch.int32, device=dev)
+        for _ in range(args.warmup + args.steps):
+            da.gqa_decode_dv(q, kf, vf, sl, scale=x.scale, max_seqlen=L)
+        torch.cuda.synchronize()
+        assert da.check_errors() == 0
+        print(f"profiled {args.profile}: {args.warmup + args.steps} calls, splits {da.last_num_splits()}", flush=True)
+        return 0
     fp8 = args.profile.endswith("_fp8")  # grouped-head workload over an FP8 cache
     wl = W.WORKLOADS[args.profile[:-4] if fp8 else args.profile]
     seqlens = wl.seqlens()

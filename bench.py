@@ -53,7 +53,8 @@ def parse():
     ap.add_argument("--no-extras", action="store_true", help="skip the grouped-head and s-sweep side measurements")
     ap.add_argument("--profile", default=None, metavar="WORKLOAD",
                     help="profiling mode: run --warmup + --steps calls of one op on one input set of the named "
-                         "workload (mla_dsv3, mla_mtp_s8, gqa_64_8, gqa_paged_hkv4, gqa_64_8_fp8, ...) and exit; "
+                         "workload (mla_dsv3, mla_mtp_s8, gqa_64_8, gqa_paged_hkv4, gqa_64_8_fp8, gqa_paged_hkv1_tc ...: _tc pins "
+                         "the tensor-core grouped-head kernel) and exit; "
                          "MLA workloads run whole pipeline steps; prints no "
                          "bench line (numbers taken under a profiler are not bench values)")
     return ap.parse_args()
@@ -616,8 +617,12 @@ def run_profile(args):
         assert da.check_errors() == 0
         print(f"profiled {args.profile}: {args.warmup + args.steps} calls, splits {da.last_num_splits()}", flush=True)
         return 0
-    fp8 = args.profile.endswith("_fp8")  # grouped-head workload over an FP8 cache
-    wl = W.WORKLOADS[args.profile[:-4] if fp8 else args.profile]
+    name = args.profile
+    if name.endswith("_tc"):  # grouped-head workload pinned to the tensor-core kernel
+        da.set_grouped_kernel(2)
+        name = name[:-3]
+    fp8 = name.endswith("_fp8")  # grouped-head workload over an FP8 cache
+    wl = W.WORKLOADS[name[:-4] if fp8 else name]
     seqlens = wl.seqlens()
     L = max(seqlens)
     sl = torch.tensor(seqlens, dtype=torch.int32, device=dev)

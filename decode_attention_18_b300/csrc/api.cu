@@ -186,6 +186,11 @@ namespace {
 // 32 rows the split-KV kernel's 16-row tiles keep up with HBM: 0.94 vs 0.87 of it at 16
 // rows of the expanded form; at 256-wide rows only two 64 KB stages fit beside Q and P,
 // and the 24-row MQA shape measured 80 vs 61 us, so those keep the split-KV kernels).
+// Automatic choice, from same-box graph-replay measurements of both kernels (rows R =
+// query rows per KV head): 192 / 128 (expanded MLA) from R = 1 up (s = 1: 1723 vs 1742 us,
+// s = 16: 1747 vs 1925, s = 128: 1747 vs 8632); 256 / 256 from R = 24 (ragged paged MQA:
+// 54 vs 60 us; R = 48: 51 vs 76); 128 / 128 from R = 32 (R = 16: 123 vs 86 us; R = 32:
+// 121 vs 133). Below those the split-KV mma.sync kernel's 16-row tiles waste less.
 bool use_prefill(int b, int hq, int hkv, int s, int dk, int dv, bool fp8, int sms) {
   (void)b;
   (void)sms;
@@ -193,7 +198,9 @@ bool use_prefill(int b, int hq, int hkv, int s, int dk, int dv, bool fp8, int sm
   const int mode = g_grouped_kernel.load();
   if (mode == 1) return false;
   if (mode == 2) return true;
-  return dv == 128 && (long long)(hq / hkv) * s >= 32;
+  const long long rows = (long long)(hq / hkv) * s;
+  if (dk == 192) return true;
+  return rows >= (dk == 256 ? 24 : 32);
 }
 
 // the tensor-core kernel's context split: one CTA per SM, 128 rows per CTA
@@ -202,13 +209,28 @@ Plan prefill_plan(int b, int s, int hq, int hkv, int max_seqlen, int sms) {
   const long long base = (long long)b * hkv * ceil_div(rows, 128);
   return plan_splits(base, max_seqlen, sms, 256, 512, kPage);
 }
+// Its balanced split (planned on the device from the actual lengths) whenever the work
+// items are fewer than the CTAs of one wave and no split count is forced; 0: fixed chunks.
+long long prefill_items(int b, int s, int hq, int hkv) {
+  return (long long)b * hkv * ceil_div((long long)(hq / hkv) * s, 128);
+}
+int prefill_balanced_grid(int b, int s, int hq, int hkv, int sms) {
+  if (g_forced_splits.load() > 0) return 0;
+  return prefill_items(b, s, hq, hkv) < sms ? sms : 0;
+}
+size_t prefill_balanced_bytes(int b, int s, int hq, int hkv, int dv, int grid) {
+  return align256((size_t)grid * 128 * dv * sizeof(float)) + align256((size_t)grid * 128 * sizeof(float)) +
+         align256((size_t)prefill_items(b, s, hq, hkv) * 2 * sizeof(int));
+}
 
 size_t gqa_workspace(int b, int s, int hq, int hkv, int dk, int dv, int max_seqlen, bool fp8) {
   if (b < 1 || s < 1 || hq < 1 || hkv < 1 || hq % hkv || dk < 1 || dv < 1) return 0;
   DeviceState* st = nullptr;
   if (device_state(&st)) return 0;
-  if (use_prefill(b, hq, hkv, s, dk, dv, fp8, st->sms))
+  if (use_prefill(b, hq, hkv, s, dk, dv, fp8, st->sms)) {
+    if (const int grid = prefill_balanced_grid(b, s, hq, hkv, st->sms)) return prefill_balanced_bytes(b, s, hq, hkv, dv, grid);
     return partial_bytes((long long)b * hq * s, prefill_plan(b, s, hq, hkv, max_seqlen, st->sms).nsplit, dv);
+  }
   const Plan pl = gqa_plan(b, s, hq, hkv, dk, dv, max_seqlen, st->sms);
   const GqaBalanced gb = gqa_balanced(pl, b, s, hq, hkv, dk, dv, st->sms, fp8);
   if (gb.grid > 0) return balanced_bytes(gb, dv);
@@ -235,7 +257,8 @@ int gqa_decode_impl(const void* q, const void* k, const void* v, decattn_kv kv, 
     if ((long long)b * hq * s > INT_MAX / 2) return DECATTN_ERR_INVALID_ARG;
     const Plan pp = prefill_plan(b, s, hq, hkv, max_seqlen, st->sms);
     const long long prow = (long long)b * hq * s;
-    const size_t pneed = partial_bytes(prow, pp.nsplit, dv);
+    const int bgrid = prefill_balanced_grid(b, s, hq, hkv, st->sms);
+    const size_t pneed = bgrid > 0 ? prefill_balanced_bytes(b, s, hq, hkv, dv, bgrid) : partial_bytes(prow, pp.nsplit, dv);
     if (pneed > 0 && (!workspace || workspace_bytes < pneed || !aligned16(workspace))) return DECATTN_ERR_WORKSPACE;
     if ((long long)pp.nsplit * ceil_div((long long)(hq / hkv) * s, 128) > INT_MAX) return DECATTN_ERR_INVALID_ARG;
     GqaLaunch a{};
@@ -263,14 +286,28 @@ int gqa_decode_impl(const void* q, const void* k, const void* v, decattn_kv kv, 
     a.ws_lse = pp.nsplit > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                                          align256((size_t)prow * pp.nsplit * dv * sizeof(float)))
                              : nullptr;
+    a.meta = nullptr;
+    a.balanced_grid = bgrid;
+    if (bgrid > 0) {
+      char* w = static_cast<char*>(workspace);
+      const size_t o_bytes = align256((size_t)bgrid * 128 * dv * sizeof(float));
+      a.ws_o = reinterpret_cast<float*>(w);
+      a.ws_lse = reinterpret_cast<float*>(w + o_bytes);
+      a.meta = reinterpret_cast<int*>(w + o_bytes + align256((size_t)bgrid * 128 * sizeof(float)));
+    }
     a.err = st->err;
     a.wait_ns = wait_limit();
     a.test_timeout = g_test_timeout.load();
-    g_last_splits.store(pp.nsplit);
+    g_last_splits.store(bgrid > 0 ? 0 : pp.nsplit);  // 0: pieces planned on the device
     if (launch_gqa_prefill(a, stream) != cudaSuccess) return DECATTN_ERR_CUDA;
-    if (pp.nsplit > 1 && launch_combine(a.ws_o, false, a.ws_lse, seqlens, (int)prow, hq * s, pp.nsplit, pp.chunk, dv,
-                                        out, lse, stream) != cudaSuccess)
+    if (bgrid > 0) {
+      if (launch_combine_balanced(a.ws_o, a.ws_lse, a.meta, seqlens, b, hq, s, hkv, dv, 128, bgrid, out, lse,
+                                  stream) != cudaSuccess)
+        return DECATTN_ERR_CUDA;
+    } else if (pp.nsplit > 1 && launch_combine(a.ws_o, false, a.ws_lse, seqlens, (int)prow, hq * s, pp.nsplit,
+                                               pp.chunk, dv, out, lse, stream) != cudaSuccess) {
       return DECATTN_ERR_CUDA;
+    }
     return DECATTN_OK;
   }
   const Plan pl = gqa_plan(b, s, hq, hkv, dk, dv, max_seqlen, st->sms);
@@ -322,8 +359,8 @@ int gqa_decode_impl(const void* q, const void* k, const void* v, decattn_kv kv, 
   g_last_splits.store(pl.nsplit);
   if (launch_gqa(a, stream) != cudaSuccess) return DECATTN_ERR_CUDA;
   if (gb.grid > 0) {
-    if (launch_combine_balanced(a.ws_o, a.ws_lse, a.meta, seqlens, b, hq, s, hkv, dv, gb.items + gb.grid, out, lse,
-                                stream) != cudaSuccess)
+    if (launch_combine_balanced(a.ws_o, a.ws_lse, a.meta, seqlens, b, hq, s, hkv, dv, gb.rpb, gb.items + gb.grid,
+                                out, lse, stream) != cudaSuccess)
       return DECATTN_ERR_CUDA;
   } else if (pl.nsplit > 1) {
     if (launch_combine(a.ws_o, false, a.ws_lse, seqlens, (int)rows, hq * s, pl.nsplit, pl.chunk, dv, out, lse,

@@ -1078,10 +1078,9 @@ cudaError_t launch_combine(const void* ws_o, bool bf16_partials, const float* ws
 }
 
 cudaError_t launch_combine_balanced(const float* ws_o, const float* ws_lse, const int* meta, const int32_t* seqlens,
-                                    int b, int hq, int s, int hkv, int d, long long records, void* out, float* lse,
-                                    cudaStream_t stream) {
+                                    int b, int hq, int s, int hkv, int d, int rpb, long long records, void* out,
+                                    float* lse, cudaStream_t stream) {
   const int rows_kv = (hq / hkv) * s;
-  const int rpb = gqa_rows_per_cta(rows_kv);
   const int nrb = (rows_kv + rpb - 1) / rpb;
   const int rows = b * hq * s;
   auto* o = static_cast<__nv_bfloat16*>(out);

@@ -8,12 +8,16 @@
 // aligned to the end), for KV heads with at least 64 query rows, where the mma.sync
 // kernel's 16-row tiles re-stream the cache once per row block and run out of math.
 //
-// One CTA takes 128 query rows of one (sequence, KV head) and every key they see:
-//  * Q [128 rows x DK] is loaded once by TMA and stays in shared memory (K-major, 128-byte
-//    swizzle); K and V tiles of 64 keys stream through a 3-stage TMA ring.
-//  * One thread issues tcgen05.mma: S = Q K^T (M = 128, N = 64) into one of two TMEM
-//    buffers, and O += P V (M = 128, N = DV) into a TMEM accumulator, the P V of tile
-//    t-1 issued after the S of tile t so that the softmax of tile t overlaps it.
+// One CTA takes 128 query rows of one (sequence, KV head) and every key they see, or a
+// piece of those keys:
+//  * Q [128 rows x DK] comes by TMA through the ring's first lap and is moved into Tensor
+//    Memory by the softmax warps (lane = row, two bf16 per column), where it stays as the
+//    A operand of the score MMAs; the ring's shared memory is then all K and V: 64-key
+//    tiles in 3 (DK = DV = 256), 4 (192 / 128) or 6 (128 / 128) stages.
+//  * One thread issues tcgen05.mma: S = Q K^T (M = 128, N = 64, A from Tensor Memory)
+//    into one of two TMEM buffers, and O += P V (M = 128, N = DV) into a TMEM
+//    accumulator, the P V of tile t-1 issued after the S of tile t so that the softmax of
+//    tile t overlaps it.
 //  * Four softmax warps (thread = row) read S from TMEM, keep a lazy reference maximum
 //    (moved only past 2^8; the O row is then rescaled in TMEM once the previous tile's
 //    P V has completed), write P as bf16 into one of two shared-memory buffers, and at
@@ -21,6 +25,15 @@
 // Every wait is bounded; a wait that runs out sets the error word and the CTA winds
 // down (its copies and MMAs waited for, TMEM freed). V rows past the sequence end are
 // zeroed before the MMA reads them (their P is 0, but 0 * NaN is NaN).
+//
+// Work split. Either a fixed chunk count planned on the host from the longest sequence
+// (CTA (rb + nrb * split, KV head, sequence)), or, when the work items (sequence, KV head,
+// row block) are fewer than the CTAs of one wave, a balanced split planned on the device
+// from the actual lengths: with T key tiles over all items and a grid of C CTAs, every
+// item is cut into ceil(tiles / W) near-equal pieces, W = ceil(T / (C - items)), so that
+// the pieces fit one wave and none is longer than W tiles. A piece that is a whole item
+// writes final rows; the pieces of a cut item write fp32 partial records (record = CTA
+// index) merged by the balanced combine.
 #include <cstring>
 
 #include "common.cuh"
@@ -32,7 +45,7 @@ namespace {
 
 constexpr int PM = 128;          // query rows per CTA (MMA M)
 constexpr int PK = 64;           // keys per tile (S MMA N)
-constexpr int PNS_MAX = 4;       // ring stages at most
+constexpr int PNS_MAX = 6;       // ring stages at most
 constexpr int PCH = PK * 128;    // one [64 keys x 64 values] bf16 chunk, 128-byte rows
 constexpr int PQCH = PM * 128;   // one [128 rows x 64 values] chunk of Q or P
 constexpr int PTHREADS = 192;    // warp 0 TMA, warp 1 MMA, warps 2-5 softmax / epilogue
@@ -45,24 +58,29 @@ template <int DK, int DV>
 struct PfCfg {
   static constexpr int KCH = DK / 64, VCH = DV / 64;
   static constexpr int STAGE = (KCH + VCH) * PCH;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_RING = OFF_Q + KCH * PQCH;
-  // as many ring stages (at most PNS_MAX) as fit beside Q and the two P buffers in 227 KB
-  static constexpr int FIXED = KCH * PQCH + 2 * PQCH + 256 + 1024;
+  static constexpr int OFF_RING = 0;
+  // as many ring stages (at most PNS_MAX) as fit beside the two P buffers in 227 KB
+  static constexpr int FIXED = 2 * PQCH + 256 + 1024;
   static constexpr int NS_FIT = (232448 - FIXED) / STAGE;
   static constexpr int NS = NS_FIT < PNS_MAX ? NS_FIT : PNS_MAX;
+  static constexpr int QS = (KCH * PQCH + STAGE - 1) / STAGE;  // ring slots the query lap covers
   static constexpr int OFF_P = OFF_RING + NS * STAGE;
   static constexpr int OFF_BAR = OFF_P + 2 * PQCH;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;  // barriers + slots, + alignment slack
-  static constexpr int TMEM_COLS = 2 * PK + DV <= 256 ? 256 : 512;  // two S buffers, then O
+  // Tensor Memory: two S buffers (columns 0 and PK), O (2 PK), Q (2 PK + DV, DK / 2 columns)
+  static constexpr int OCOL = 2 * PK, QCOL = 2 * PK + DV;
+  static constexpr int TMEM_COLS = 512;
   static_assert(DK % 64 == 0 && DV % 64 == 0 && DV <= 256, "widths");
-  static_assert(NS >= 2, "ring");
+  static_assert(QCOL + DK / 2 <= TMEM_COLS, "tensor memory");
+  static_assert(NS >= 2 && QS < NS, "ring");
 };
 
 // barriers
-enum { F_Q = 0, F_FULL = 1, F_EMPTY = F_FULL + PNS_MAX, F_SFULL = F_EMPTY + PNS_MAX, F_SEMPTY = F_SFULL + 2,
+enum { F_QREADY = 0, F_FULL = 1, F_EMPTY = F_FULL + PNS_MAX, F_SFULL = F_EMPTY + PNS_MAX, F_SEMPTY = F_SFULL + 2,
        F_PFULL = F_SEMPTY + 2, F_PEMPTY = F_PFULL + 2, F_OFINAL = F_PEMPTY + 2, F_FIN = F_OFINAL + 1,
        F_TEST = F_FIN + 1, F_COUNT = F_TEST + 1 };
+static_assert(F_COUNT * 8 + 8 <= 256, "barrier region");
+constexpr int kPBarQ = 1;  // named barrier of the four softmax warps
 constexpr unsigned long long kPTestWaitNs = 1000000ull;  // forced-timeout test: 1 ms
 
 struct PfParams {
@@ -74,8 +92,11 @@ struct PfParams {
   int max_pages, paged, capacity, num_pages;
   int b, s, hq, hkv, G, R, nrb;
   int nsplit, chunk;  // context split: CTA x covers keys [split * chunk, (split + 1) * chunk)
-  float* ws_o;        // nsplit > 1: fp32 partials [b*Hq*s rows][nsplit][DV] (normalised O)
-  float* ws_lse;      // and their LSEs [rows][nsplit]
+  float* ws_o;        // nsplit > 1: fp32 partials [b*Hq*s rows][nsplit][DV] (normalised O);
+                      // balanced: records [grid][PM rows][DV]
+  float* ws_lse;      // and their LSEs [rows][nsplit] / [grid][PM]
+  int balanced;       // nonzero: the device-planned balanced split over a 1-D grid
+  int* meta;          // balanced: [work items][2] {first record, count}
   float scale_log2;
   unsigned* err;
   unsigned long long wait_ns;
@@ -85,6 +106,69 @@ struct PfParams {
 // all lanes of a warp wait (bounded); true only if every lane saw the phase complete
 __device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, unsigned long long ns, volatile int* abort_flag) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, ns, abort_flag));
+}
+
+// keys seen by row block rb of a sequence of L keys: the widest causal window among the
+// block's rows (row = head_in_group * s + token)
+__device__ __forceinline__ int pf_kwin(const PfParams& p, int L, int rb) {
+  const int r0 = rb * PM, r1 = min(p.R, r0 + PM);
+  const int maxtok = (r1 - r0 >= p.s || r0 / p.s != (r1 - 1) / p.s) ? p.s - 1 : (r1 - 1) % p.s;
+  return L >= p.s ? min(L, L - p.s + maxtok + 1) : (L > 0 ? L : 0);
+}
+
+// this CTA's work: item (sequence bi, KV head g, row block rb) and key range; n = pieces
+// of the item (1: final rows), first = its first record; valid = false: no work
+struct PfPiece {
+  int bi, g, rb, kstart, kend, n, first;
+  long long item;
+  bool valid;
+};
+__device__ PfPiece pf_piece(const PfParams& p) {
+  PfPiece w{};
+  if (!p.balanced) {
+    w.rb = blockIdx.x % p.nrb;
+    const int split = blockIdx.x / p.nrb;
+    w.g = blockIdx.y;
+    w.bi = blockIdx.z;
+    w.kstart = split * p.chunk;
+    w.kend = min(pf_kwin(p, p.seqlens[w.bi], w.rb), w.kstart + p.chunk);
+    w.n = p.nsplit;
+    w.first = split;
+    w.valid = true;
+    return w;
+  }
+  const long long items = (long long)p.b * p.hkv * p.nrb;
+  auto tiles_of = [&](long long it) -> long long {
+    const int bi = (int)(it / ((long long)p.hkv * p.nrb));
+    return (pf_kwin(p, __ldg(p.seqlens + bi), (int)(it % p.nrb)) + PK - 1) / PK;
+  };
+  long long total = 0;
+  for (long long it = 0; it < items; ++it) total += tiles_of(it);
+  const long long spare = (long long)gridDim.x - items;  // > 0 (the host checks)
+  const long long W = spare > 0 ? max(1ll, (total + spare - 1) / spare) : max(1ll, total);
+  const long long c = blockIdx.x;
+  long long prefix = 0;
+  for (long long it = 0; it < items; ++it) {
+    const long long tiles = tiles_of(it);
+    const long long n = (tiles + W - 1) / W;
+    if (c < prefix + n) {
+      const long long j = c - prefix;
+      const int L = __ldg(p.seqlens + (int)(it / ((long long)p.hkv * p.nrb)));
+      w.item = it;
+      w.rb = (int)(it % p.nrb);
+      w.g = (int)((it / p.nrb) % p.hkv);
+      w.bi = (int)(it / ((long long)p.hkv * p.nrb));
+      w.kstart = (int)((j * tiles / n) * PK);
+      w.kend = min(pf_kwin(p, L, w.rb), (int)(((j + 1) * tiles / n) * PK));
+      w.n = (int)n;
+      w.first = (int)prefix;
+      w.valid = true;
+      return w;
+    }
+    prefix += n;
+  }
+  w.valid = false;  // beyond the last piece: nothing to do
+  return w;
 }
 
 template <int DK, int DV>
@@ -100,10 +184,9 @@ __global__ void __launch_bounds__(PTHREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + F_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + F_COUNT) + 1;
-  const int rb = blockIdx.x % p.nrb, split = blockIdx.x / p.nrb, g = blockIdx.y, bi = blockIdx.z;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars[F_Q], 1);
+    mbar_init(&bars[F_QREADY], 1);
     for (int i = 0; i < C::NS; ++i) {
       mbar_init(&bars[F_FULL + i], 1);
       mbar_init(&bars[F_EMPTY + i], 1);
@@ -130,7 +213,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;  // S buffers at columns 0 and PK, O at 2 * PK
+  const uint32_t tmem = *tmem_slot;  // S buffers at columns 0 and PK, O at 2 PK, Q after O
   auto fail = [&]() {
     raise_error(p.err, kErrWaitTimeout);
     *abort_flag = 1;
@@ -138,27 +221,37 @@ __global__ void __launch_bounds__(PTHREADS, 1)
   pdl_wait();  // queries, cache and lengths may come from the previous kernel in the stream
   pdl_trigger();
 
-  const int L = p.seqlens[bi];
-  const int r0 = rb * PM;             // first row (within the KV head's R rows) of the block
-  const int r1 = min(p.R, r0 + PM);   // one past the last
-  // the widest causal window among the block's rows (token = row % s)
-  const int maxtok = (r1 - r0 >= p.s || r0 / p.s != (r1 - 1) / p.s) ? p.s - 1 : (r1 - 1) % p.s;
-  const int kwin = L >= p.s ? min(L, L - p.s + maxtok + 1) : (L > 0 ? L : 0);  // keys the block sees
-  const int kstart = split * p.chunk;
-  const int kend = min(kwin, kstart + p.chunk);
-  const int ntiles = kend > kstart ? (kend - kstart + PK - 1) / PK : 0;
+  const PfPiece w = pf_piece(p);
+  const int rb = w.rb, g = w.g, bi = w.bi;
+  const int L = w.valid ? p.seqlens[bi] : 0;
+  const int r0 = rb * PM;  // first row (within the KV head's R rows) of the block
+  const int kstart = w.kstart, kend = w.kend;
+  const int ntiles = w.valid && kend > kstart ? (kend - kstart + PK - 1) / PK : 0;
   const int qrow0 = (bi * p.hq + g * p.G) * p.s + r0;  // first flattened [b*hq*s] query row
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (ntiles > 0 && elect_one()) {
-      mbar_expect_tx(&bars[F_Q], C::KCH * PQCH);
-      for (int c = 0; c < C::KCH; ++c) tma_load_2d(sb + C::OFF_Q + c * PQCH, &tm_q, c * 64, qrow0, &bars[F_Q]);
+      // the query lap: Q boxes [128 rows x 64] (16 KB each) laid end to end from the ring's
+      // start over its first QS slots; a box completes on the barrier of the slot it starts
+      // in, and a slot in which no box starts gets a plain arrival
+      uint32_t qbytes[C::QS];
+      for (int i = 0; i < C::QS; ++i) qbytes[i] = 0;
+      for (int c = 0; c < C::KCH; ++c) qbytes[(c * PQCH) / C::STAGE] += PQCH;
+      for (int i = 0; i < C::QS; ++i) {
+        if (qbytes[i])
+          mbar_expect_tx(&bars[F_FULL + i], qbytes[i]);
+        else
+          mbar_arrive(&bars[F_FULL + i]);
+      }
+      for (int c = 0; c < C::KCH; ++c)
+        tma_load_2d(sb + C::OFF_RING + c * PQCH, &tm_q, c * 64, qrow0, &bars[F_FULL + (c * PQCH) / C::STAGE]);
+      // tile t takes ring position u = QS + t: slot u % NS, its (u / NS)-th use
       int last[PNS_MAX];
-      for (int i = 0; i < PNS_MAX; ++i) last[i] = -1;
+      for (int i = 0; i < PNS_MAX; ++i) last[i] = i < C::QS ? i : -1;
       for (int t = 0; t < ntiles; ++t) {
-        const int slot = t % C::NS;
-        if (t >= C::NS && !mbar_wait(&bars[F_EMPTY + slot], ((t / C::NS) - 1) & 1, p.wait_ns, abort_flag)) {
+        const int u = C::QS + t, slot = u % C::NS;
+        if (u >= C::NS && !mbar_wait(&bars[F_EMPTY + slot], ((u / C::NS) - 1) & 1, p.wait_ns, abort_flag)) {
           if (!*abort_flag) fail();
           break;
         }
@@ -173,15 +266,16 @@ __global__ void __launch_bounds__(PTHREADS, 1)
         } else {
           row0 = bi * p.capacity + kstart + t * PK;
         }
+        // one box for K and one for V: [chunks][64 keys][64 values], chunk-major as the
+        // MMAs read them (the TMA engine serves about one box per few hundred cycles per SM
+        // whatever its size, so a tile is not cut into per-chunk boxes)
         const uint32_t dst = sb + C::OFF_RING + slot * C::STAGE;
         mbar_expect_tx(&bars[F_FULL + slot], C::STAGE);
-        for (int c = 0; c < C::KCH; ++c) tma_load_3d(dst + c * PCH, &tm_k, c * 64, g, row0, &bars[F_FULL + slot]);
-        for (int c = 0; c < C::VCH; ++c)
-          tma_load_3d(dst + (C::KCH + c) * PCH, &tm_v, c * 64, g, row0, &bars[F_FULL + slot]);
-        last[slot] = t;
+        tma_load_4d(dst, &tm_k, 0, row0, 0, g, &bars[F_FULL + slot]);
+        tma_load_4d(dst + C::KCH * PCH, &tm_v, 0, row0, 0, g, &bars[F_FULL + slot]);
+        last[slot] = u;
       }
       // leave no copy in flight
-      mbar_wait(&bars[F_Q], 0, kPTeardownNs, nullptr);
       for (int i = 0; i < C::NS; ++i)
         if (last[i] >= 0) mbar_wait(&bars[F_FULL + i], (last[i] / C::NS) & 1, kPTeardownNs, nullptr);
     }
@@ -191,14 +285,14 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     const bool leader = elect_one();
     constexpr uint32_t idS = idesc_bf16_f32(PM, PK, false, false);  // B = K rows, K-major
     constexpr uint32_t idO = idesc_bf16_f32(PM, DV, false, true);   // B = V rows, N-major
-    const uint64_t dq = smem_desc(sb + C::OFF_Q, 16, 1024, kSw128);
     const uint64_t dk = smem_desc(sb + C::OFF_RING, 16, 1024, kSw128);
     const uint64_t dv = smem_desc(sb + C::OFF_RING, PCH, 1024, kSw128);  // chunk stride 8 KB
     const uint64_t dp = smem_desc(sb + C::OFF_P, 16, 1024, kSw128);
-    bool ok = ntiles == 0 || pf_wait(&bars[F_Q], 0, p.wait_ns, abort_flag);
+    bool ok = ntiles == 0 || pf_wait(&bars[F_QREADY], 0, p.wait_ns, abort_flag);
+    tc_fence_after();  // Q was written to Tensor Memory by the softmax warps
     // O += P(u) V(u); the tail of the last tile's V rows is zeroed first
     auto o_mma = [&](int u) -> bool {
-      const int pb = u & 1, slot = u % C::NS;
+      const int pb = u & 1, slot = (C::QS + u) % C::NS;
       if (!pf_wait(&bars[F_PFULL + pb], (u >> 1) & 1, p.wait_ns, abort_flag)) return false;
       const int nvalid = kend - (kstart + u * PK);
       if (nvalid < PK) {
@@ -216,7 +310,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
         const uint64_t b0 = dv + (uint64_t)((slot * C::STAGE + C::KCH * PCH) >> 4);
 #pragma unroll
         for (int kk = 0; kk < PK / 16; ++kk)
-          tc_mma_ss(tmem + 2 * PK, a0 + 2 * kk, b0 + (uint64_t)((kk * 16 * 128) >> 4), idO,
+          tc_mma_ss(tmem + C::OCOL, a0 + 2 * kk, b0 + (uint64_t)((kk * 16 * 128) >> 4), idO,
                     (u > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&bars[F_EMPTY + slot]);  // the ring slot (K and V of tile u) is free
         tc_commit(&bars[F_PEMPTY + pb]);   // P buffer pb is free; O holds tiles <= u
@@ -225,8 +319,8 @@ __global__ void __launch_bounds__(PTHREADS, 1)
       return true;
     };
     for (int t = 0; ok && t < ntiles; ++t) {
-      const int slot = t % C::NS, sbuf = t & 1;
-      if (!pf_wait(&bars[F_FULL + slot], (t / C::NS) & 1, p.wait_ns, abort_flag) ||
+      const int slot = (C::QS + t) % C::NS, sbuf = t & 1;
+      if (!pf_wait(&bars[F_FULL + slot], ((C::QS + t) / C::NS) & 1, p.wait_ns, abort_flag) ||
           (t >= 2 && !pf_wait(&bars[F_SEMPTY + sbuf], ((t >> 1) - 1) & 1, p.wait_ns, abort_flag))) {
         ok = false;
         break;
@@ -236,8 +330,8 @@ __global__ void __launch_bounds__(PTHREADS, 1)
         const uint64_t b0 = dk + (uint64_t)((slot * C::STAGE) >> 4);
 #pragma unroll
         for (int kk = 0; kk < DK / 16; ++kk)
-          tc_mma_ss(tmem + sbuf * PK, dq + (uint64_t)(((kk / 4) * PQCH + (kk % 4) * 32) >> 4),
-                    b0 + (uint64_t)(((kk / 4) * PCH + (kk % 4) * 32) >> 4), idS, kk > 0 ? 1u : 0u);
+          tc_mma_ts(tmem + sbuf * PK, tmem + C::QCOL + kk * 8, b0 + (uint64_t)(((kk / 4) * PCH + (kk % 4) * 32) >> 4),
+                    idS, kk > 0 ? 1u : 0u);
         tc_commit(&bars[F_SFULL + sbuf]);
       }
       __syncwarp();
@@ -263,6 +357,40 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     const uint32_t t_lane = tmem + ((uint32_t)(q * 32) << 16);
     float m_ref = -INFINITY, l_run = 0.f;
     bool ok = ntiles > 0;
+    if (ntiles > 0) {
+      // Q row r into Tensor Memory (A operand of the score MMAs: lane = row, two bf16 per
+      // column, even index low); chunk j of the query lap is [128 rows x 64] with 128-byte
+      // swizzled rows. Then the query lap's ring slots go back to the producer.
+      bool okq = true;
+      for (int i = 0; i < C::QS; ++i) okq = okq && pf_wait(&bars[F_FULL + i], 0, p.wait_ns, abort_flag);
+      if (okq) {
+#pragma unroll 1
+        for (int j = 0; j < C::KCH; ++j) {
+          const uint8_t* bx = smem + C::OFF_RING + j * PQCH + r * 128;
+          uint32_t v[32];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint4 x = *reinterpret_cast<const uint4*>(bx + ((u ^ (r & 7)) << 4));
+            v[4 * u] = x.x;
+            v[4 * u + 1] = x.y;
+            v[4 * u + 2] = x.z;
+            v[4 * u + 3] = x.w;
+          }
+          tmem_st32(t_lane + C::QCOL + j * 32, v);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      ok = named_bar_and(kPBarQ, 128, okq && !*abort_flag);
+      if (threadIdx.x == 64) {
+        if (ok) {
+          for (int i = 0; i < C::QS; ++i) mbar_arrive(&bars[F_EMPTY + i]);
+          mbar_arrive(&bars[F_QREADY]);
+        } else if (!*abort_flag) {
+          fail();
+        }
+      }
+    }
     for (int t = 0; ok && t < ntiles; ++t) {
       const int sbuf = t & 1, pb = t & 1;
       if (!pf_wait(&bars[F_SFULL + sbuf], (t >> 1) & 1, p.wait_ns, abort_flag) ||
@@ -314,11 +442,11 @@ __global__ void __launch_bounds__(PTHREADS, 1)
 #pragma unroll 1
         for (int c0 = 0; c0 < DV; c0 += 32) {
           uint32_t v[32];
-          tmem_ld32(t_lane + 2 * PK + c0, v);
+          tmem_ld32(t_lane + C::OCOL + c0, v);
           tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * alpha);
-          tmem_st32(t_lane + 2 * PK + c0, v);
+          tmem_st32(t_lane + C::OCOL + c0, v);
         }
         tmem_st_wait();
       }
@@ -350,24 +478,41 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     if (ok && ntiles > 0) ok = pf_wait(&bars[F_OFINAL], 0, p.wait_ns, abort_flag);
     if (!ok && ntiles > 0) {
       if (lane == 0 && !*abort_flag) fail();
-    } else {
+    } else if (w.valid) {
+      // final rows when the item is whole (one piece or no split), else a partial: fp32
+      // normalised O and its LSE, by split (fixed chunks) or in record blockIdx.x (balanced)
+      const bool whole = w.n <= 1;
+      float* part_o = nullptr;
+      float* part_l = nullptr;
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       const float lse_val = l_run > 0.f ? (m_ref + log2f(l_run)) * kPLn2 : -INFINITY;
       const int j = g * p.G + rg / p.s;
       const size_t rowflat = ((size_t)bi * p.hq + j) * p.s + tok;
+      if (!whole) {
+        const size_t rec = p.balanced ? ((size_t)blockIdx.x * PM + r) : (rowflat * p.nsplit + w.first);
+        part_o = p.ws_o + rec * DV;
+        part_l = p.ws_lse + rec;
+        if (p.balanced && w.kstart == 0 && threadIdx.x == 64) {  // the item's first piece
+          p.meta[2 * w.item] = w.first;
+          p.meta[2 * w.item + 1] = w.n;
+        }
+      } else if (p.balanced && threadIdx.x == 64) {
+        p.meta[2 * w.item] = (int)blockIdx.x;
+        p.meta[2 * w.item + 1] = 1;
+      }
 #pragma unroll 1
       for (int c0 = 0; c0 < DV; c0 += 32) {
         uint32_t v[32];
         if (ntiles > 0) {
-          tmem_ld32(t_lane + 2 * PK + c0, v);  // the whole warp loads; rows past R store nothing
+          tmem_ld32(t_lane + C::OCOL + c0, v);  // the whole warp loads; rows past R store nothing
           tmem_ld_wait();
         } else {
 #pragma unroll
           for (int c = 0; c < 32; ++c) v[c] = 0u;  // no key in this block's range: zero rows
         }
         if (!row_ok) continue;
-        if (p.nsplit == 1) {  // final bf16 rows
+        if (whole) {  // final bf16 rows
           uint4* d4 = reinterpret_cast<uint4*>(p.out + rowflat * DV + c0);
 #pragma unroll
           for (int u = 0; u < 4; ++u)
@@ -375,8 +520,8 @@ __global__ void __launch_bounds__(PTHREADS, 1)
                                pack_bf16(__uint_as_float(v[8 * u + 2]) * inv, __uint_as_float(v[8 * u + 3]) * inv),
                                pack_bf16(__uint_as_float(v[8 * u + 4]) * inv, __uint_as_float(v[8 * u + 5]) * inv),
                                pack_bf16(__uint_as_float(v[8 * u + 6]) * inv, __uint_as_float(v[8 * u + 7]) * inv));
-        } else {  // fp32 partial of this chunk, for the combine
-          float4* d4 = reinterpret_cast<float4*>(p.ws_o + (rowflat * p.nsplit + split) * DV + c0);
+        } else {  // fp32 partial of this piece, for the combine
+          float4* d4 = reinterpret_cast<float4*>(part_o + c0);
 #pragma unroll
           for (int u = 0; u < 8; ++u)
             d4[u] = make_float4(__uint_as_float(v[4 * u + 0]) * inv, __uint_as_float(v[4 * u + 1]) * inv,
@@ -384,10 +529,10 @@ __global__ void __launch_bounds__(PTHREADS, 1)
         }
       }
       if (row_ok) {
-        if (p.nsplit == 1) {
+        if (whole) {
           if (p.lse) p.lse[rowflat] = lse_val;
         } else {
-          p.ws_lse[rowflat * p.nsplit + split] = lse_val;
+          *part_l = lse_val;
         }
       }
     }
@@ -420,15 +565,18 @@ static cudaError_t launch_pf(const GqaLaunch& a, cudaStream_t stream) {
     const cuuint32_t box[2] = {64, PM};
     if (!encode_tmap_bf16_sw128(&tq, a.q, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  {  // K and V as [tokens, KV heads, width]: boxes [64 tokens, 1 head, 64 values]
+  {  // K and V [tokens, KV heads, width] viewed as {64 values, tokens, width / 64 chunks, KV
+     // heads} (strides: token hkv*width*2 B, chunk 128 B, head width*2 B): a box {64, 64
+     // tokens, all chunks, 1 head} lands chunk-major, each 128-byte row swizzled
     const uint64_t tokens = a.paged ? (uint64_t)a.num_pages * PK : (uint64_t)a.b * a.capacity;
-    const cuuint32_t box[3] = {64, 1, PK};
-    const cuuint64_t kdims[3] = {(cuuint64_t)DK, (cuuint64_t)a.hkv, (cuuint64_t)tokens};
-    const cuuint64_t kstrides[2] = {(cuuint64_t)DK * 2, (cuuint64_t)a.hkv * DK * 2};
-    const cuuint64_t vdims[3] = {(cuuint64_t)DV, (cuuint64_t)a.hkv, (cuuint64_t)tokens};
-    const cuuint64_t vstrides[2] = {(cuuint64_t)DV * 2, (cuuint64_t)a.hkv * DV * 2};
-    if (!encode_tmap_bf16_sw128(&tk, a.k, 3, kdims, kstrides, box) ||
-        !encode_tmap_bf16_sw128(&tv, a.v, 3, vdims, vstrides, box))
+    const cuuint32_t kbox[4] = {64, PK, (cuuint32_t)C::KCH, 1};
+    const cuuint32_t vbox[4] = {64, PK, (cuuint32_t)C::VCH, 1};
+    const cuuint64_t kdims[4] = {64, (cuuint64_t)tokens, (cuuint64_t)C::KCH, (cuuint64_t)a.hkv};
+    const cuuint64_t kstrides[3] = {(cuuint64_t)a.hkv * DK * 2, 128, (cuuint64_t)DK * 2};
+    const cuuint64_t vdims[4] = {64, (cuuint64_t)tokens, (cuuint64_t)C::VCH, (cuuint64_t)a.hkv};
+    const cuuint64_t vstrides[3] = {(cuuint64_t)a.hkv * DV * 2, 128, (cuuint64_t)DV * 2};
+    if (!encode_tmap_bf16_sw128(&tk, a.k, 4, kdims, kstrides, kbox) ||
+        !encode_tmap_bf16_sw128(&tv, a.v, 4, vdims, vstrides, vbox))
       return cudaErrorInvalidValue;
   }
   PfParams p;
@@ -452,12 +600,14 @@ static cudaError_t launch_pf(const GqaLaunch& a, cudaStream_t stream) {
   p.chunk = a.chunk;
   p.ws_o = a.ws_o;
   p.ws_lse = a.ws_lse;
+  p.balanced = a.balanced_grid > 0 ? 1 : 0;
+  p.meta = a.meta;
   p.scale_log2 = a.scale * kPLog2e;
   p.err = a.err;
   p.wait_ns = a.wait_ns;
   p.test_timeout = a.test_timeout;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.nrb * p.nsplit, a.hkv, a.b);
+  cfg.gridDim = p.balanced ? dim3(a.balanced_grid) : dim3(p.nrb * p.nsplit, a.hkv, a.b);
   cfg.blockDim = dim3(PTHREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = stream;

@@ -26,7 +26,7 @@ struct GqaLaunch {
   float* ws_o;    // [b*hq*s, nsplit, dv] (nsplit > 1), or balanced: [records, rows per CTA, dv]
   float* ws_lse;  // [b*hq*s, nsplit], or balanced: [records, rows per CTA]
   int* meta;      // balanced: [work items][2] {first record, count}
-  int balanced_grid;  // > 0: balanced schedule over this many CTAs (mma.sync kernel)
+  int balanced_grid;  // > 0: balanced schedule over this many CTAs
   unsigned* err;
   unsigned long long wait_ns;  // limit of the bounded tile waits
   int test_timeout;            // forced-timeout test: one wait on a barrier nothing signals
@@ -47,10 +47,11 @@ cudaError_t launch_gqa_prefill(const GqaLaunch& p, cudaStream_t stream);
 // when bf16_partials) and their fp32 LSEs
 cudaError_t launch_combine(const void* ws_o, bool bf16_partials, const float* ws_lse, const int32_t* seqlens, int rows,
                            int rows_per_seq, int nsplit, int chunk, int d, void* out, float* lse, cudaStream_t stream);
-// combine of the balanced grouped-head schedule (see gqa_balanced_kernel)
+// combine of the balanced grouped-head schedules (gqa_balanced_kernel, rpb = its rows per
+// CTA; the tensor-core kernel's balanced split, rpb = 128): records [records][rpb][d]
 cudaError_t launch_combine_balanced(const float* ws_o, const float* ws_lse, const int* meta, const int32_t* seqlens,
-                                    int b, int hq, int s, int hkv, int d, long long records, void* out, float* lse,
-                                    cudaStream_t stream);
+                                    int b, int hq, int s, int hkv, int d, int rpb, long long records, void* out,
+                                    float* lse, cudaStream_t stream);
 
 struct ProjLaunch {
   unsigned* err;     // device error word

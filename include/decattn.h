@@ -261,15 +261,20 @@ int gqa_decode_no_alloc(const decattn_bf16* q, const decattn_bf16* k, const deca
  * 2 s). decattn_set_forced_splits: 0 = let the planner choose the number of
  * context chunks; n > 0 forces n (for split-invariance tests); it also
  * changes the workspace sizes returned afterwards.
- * decattn_last_num_splits: number of chunks the last attention call used.
+ * decattn_last_num_splits: number of chunks the last attention call used (0:
+ * the tensor-core grouped-head kernel's balanced split, whose pieces are
+ * planned on the device from the actual lengths).
  * decattn_set_grouped_kernel: which grouped-head kernel gqa_decode and
  * gqa_decode_dv run (diagnostics and tests; 0 = automatic, the default).
  * 1 = the split-KV kernels (16-row tiles, context split over CTAs, combine);
- * 2 = the tensor-core kernel (tcgen05, 128 query rows per CTA, the context
- * split over CTAs where the grid is small) where the widths allow ((dk, dv) in
+ * 2 = the tensor-core kernel (tcgen05, 128 query rows per CTA; the context cut
+ * into chunks planned from max_seqlen, or, when the work items are fewer than
+ * the SMs, into pieces balanced over one wave from the actual lengths, merged
+ * by a combine kernel) where the widths allow ((dk, dv) in
  * {(128, 128), (192, 128), (256, 256)}). Automatic takes the tensor-core
- * kernel for at least 32 query rows per KV head with 128-wide values. Results
- * agree within rounding.
+ * kernel for (dk, dv) = (192, 128) at any row count, for (256, 256) from 24
+ * and for (128, 128) from 32 query rows per KV head. Results agree within
+ * rounding.
  * decattn_test_force_timeout: when nonzero, the next mla_decode and gqa_decode
  * kernels wait once on a barrier that nothing signals, with a 1 ms limit, so that
  * the timeout path runs; the kernels then wind down (no new copies, their own

@@ -187,3 +187,30 @@ def test_prefill_forced_timeout():
     torch.cuda.synchronize()
     assert da.check_errors() == 0
     check(q, cache, out, lse, seqlens, 128, "after timeout")
+
+
+def test_prefill_balanced_pieces_ragged():
+    # fewer work items than SMs: each item is cut into near-equal pieces planned on the
+    # device from the actual lengths (empty, one-key and sub-tile sequences included), the
+    # pieces of an item merged by the balanced combine; the plan depends on the lengths only
+    import decode_attention_18_b300 as da
+
+    seqlens = [5000, 0, 64, 1, 3100, 777]
+    q, cache, out, lse = run(6, 24, 1, 256, 1, seqlens, paged=True, seed=41)
+    assert da.last_num_splits() == 0
+    check(q, cache, out, lse, seqlens, 256, "prefill balanced ragged")
+    sl = torch.tensor(seqlens, dtype=torch.int32, device=DEV)
+    out2, lse2 = da.gqa_decode(q, cache.k, cache.v, sl, max_seqlen=max(seqlens), block_table=cache.block_table)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
+def test_prefill_many_items_fixed_chunks():
+    # at least as many work items (sequence, KV head, row block) as SMs: chunks planned from
+    # max_seqlen instead of the balanced pieces
+    import decode_attention_18_b300 as da
+
+    seqlens = [(i * 331) % 900 + 70 for i in range(40)]
+    q, cache, out, lse = run(40, 16, 4, 128, 8, seqlens, seed=43)  # 32 rows per KV head, 160 items
+    assert da.last_num_splits() >= 1
+    check(q, cache, out, lse, seqlens, 128, "prefill fixed chunks, 160 items")

@@ -106,7 +106,8 @@ def test_gqa_graph_replays(hkv, d, paged):
                       stream=stream)
 
     g = _capture(step, stream)
-    assert da.last_num_splits() > 1
+    # the context was cut: fixed chunks (> 1), or the tensor-core kernel's balanced pieces (0)
+    assert da.last_num_splits() != 1
     results = []
     with torch.cuda.stream(stream):
         for q, c in sets:

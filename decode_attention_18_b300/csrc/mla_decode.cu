@@ -111,7 +111,6 @@ struct MlaCfg {
   static constexpr int NH = KL / ON;                    // O column blocks
   static constexpr int O_ITEM = HK * ON * 2;            // [64 keys x ON columns]
   static constexpr int OCOLS = KL / 2;                  // O columns per row warp (rescale, epilogue)
-  static constexpr int PASS = OCOLS < 128 ? OCOLS : 128;  // epilogue staging pass (columns)
   // S CTA: one P staging slot, q_pe, the S-ring
   static constexpr int OFF_STG = 0;
   static constexpr int OFF_QPE = MSG_STRIDE;
@@ -127,8 +126,8 @@ struct MlaCfg {
   static_assert(KL % 64 == 0 && KL / 2 <= SB0 && KL % ON == 0 && ON % 16 == 0 && ON <= 256, "latent width");
   static_assert(NCH % CPI == 0 && 2 * CPI <= 8 && QS <= S_NR && LATL >= 1, "S-ring items");
   static_assert(P % 16 == 0 && PE_ROW <= 128, "rope width");
-  static_assert(OCOLS % 32 == 0 && OCOLS % PASS == 0, "row-warp columns");
-  static_assert(NSMW * 32 * PASS * 4 <= O_NR * O_ITEM, "epilogue staging");
+  static_assert(OCOLS % 32 == 0 && (OCOLS / 8 <= 32) && 32 % (OCOLS / 8) == 0, "row-warp columns");
+  static_assert(NSMW * 32 * OCOLS * 2 <= O_NR * O_ITEM, "epilogue staging");
   static_assert(OFF_SRING % 1024 == 0 && OFF_ORING % 1024 == 0 && O_ITEM % 1024 == 0 && OFF_QPE % 1024 == 0,
                 "swizzle alignment");
   static_assert(SMEM <= 232448, "shared memory");
@@ -835,39 +834,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         } else {
           tc_fence_after();
           const float inv = reinterpret_cast<const float*>(smem + C::OFF_FIN)[r];
-          // O / l of this warp's 32 rows x OCOLS columns is staged through shared memory (the
-          // O-ring, idle once every MMA has completed) in passes of PASS columns and stored as
-          // whole row segments; staged rows are 16-byte units XOR-swizzled by (row & 7).
-          constexpr int F4 = C::PASS / 4;  // 16-byte units per staged row
-          constexpr int ROWB = C::PASS * 4;
-          constexpr int RPI = 32 / F4;     // rows per store instruction
+          // O / l of this warp's 32 rows x OCOLS columns: Tensor Memory -> registers (up to
+          // four 32-column loads in flight per wait) -> bf16 rows staged in shared memory (the
+          // O-ring, idle once every MMA has completed; 16-byte units XOR-swizzled by the row,
+          // so that neither the row-per-lane writes nor the unit-per-lane reads conflict) ->
+          // whole row segments stored to global memory, 16 bytes per lane.
+          constexpr int UNITS = C::OCOLS / 8;  // 16-byte bf16 units per row of this warp
+          constexpr int ROWB = C::OCOLS * 2;
+          constexpr int RPI = 32 / UNITS;      // rows per store instruction
+          constexpr int GRP = C::OCOLS / 32 < 4 ? C::OCOLS / 32 : 4;  // 32-column loads per wait
           uint8_t* stg = smem + C::OFF_ORING + (warp - 2) * 32 * ROWB;
 #pragma unroll 1
-          for (int c0 = c_lo; c0 < c_lo + C::OCOLS; c0 += C::PASS) {
-#pragma unroll 1
-            for (int cc = 0; cc < C::PASS; cc += 32) {
-              uint32_t v[32];
-              tmem_ld32(t_lane + c0 + cc, v);
-              tmem_ld_wait();
+          for (int g0 = 0; g0 < C::OCOLS; g0 += 32 * GRP) {
+            uint32_t v[GRP][32];
 #pragma unroll
-              for (int e = 0; e < 8; ++e)
-                *reinterpret_cast<float4*>(stg + lane * ROWB + (((cc / 4 + e) ^ (lane & 7)) * 16)) =
-                    make_float4(__uint_as_float(v[4 * e + 0]) * inv, __uint_as_float(v[4 * e + 1]) * inv,
-                                __uint_as_float(v[4 * e + 2]) * inv, __uint_as_float(v[4 * e + 3]) * inv);
+            for (int gi = 0; gi < GRP; ++gi) tmem_ld32(t_lane + c_lo + g0 + gi * 32, v[gi]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int gi = 0; gi < GRP; ++gi) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int u = (g0 + gi * 32) / 8 + e;
+                const uint32_t* w = v[gi] + 8 * e;
+                *reinterpret_cast<uint4*>(stg + lane * ROWB + ((u ^ (lane % UNITS)) << 4)) =
+                    make_uint4(pack_bf16(__uint_as_float(w[0]) * inv, __uint_as_float(w[1]) * inv),
+                               pack_bf16(__uint_as_float(w[2]) * inv, __uint_as_float(w[3]) * inv),
+                               pack_bf16(__uint_as_float(w[4]) * inv, __uint_as_float(w[5]) * inv),
+                               pack_bf16(__uint_as_float(w[6]) * inv, __uint_as_float(w[7]) * inv));
+              }
             }
-            __syncwarp();
-            const int jl = lane % F4;
+          }
+          __syncwarp();
+          const int ju = lane % UNITS;
 #pragma unroll 4
-            for (int rr = lane / F4; rr < 32; rr += RPI) {
-              const int rs = q * 32 + rr;  // row within the tile
-              if (mt * BM + rs >= p.rows) continue;
-              const float4 xv = *reinterpret_cast<const float4*>(stg + rr * ROWB + ((jl ^ (rr & 7)) * 16));
-              const size_t g = (size_t)qrow0 + rs;
-              const int col = c0 + jl * 4;
-              __nv_bfloat16* dst = p.nsplit == 1 ? p.o_lat + g * KL : p.ws_ob + (g * p.nsplit + split) * KL;
-              *reinterpret_cast<uint2*>(dst + col) = make_uint2(pack_bf16(xv.x, xv.y), pack_bf16(xv.z, xv.w));
-            }
-            __syncwarp();
+          for (int rr = lane / UNITS; rr < 32; rr += RPI) {
+            const int rs = q * 32 + rr;  // row within the tile
+            if (mt * BM + rs >= p.rows) continue;
+            const uint4 xv = *reinterpret_cast<const uint4*>(stg + rr * ROWB + ((ju ^ (rr % UNITS)) << 4));
+            const size_t g = (size_t)qrow0 + rs;
+            __nv_bfloat16* dst = p.nsplit == 1 ? p.o_lat + g * KL : p.ws_ob + (g * p.nsplit + split) * KL;
+            *reinterpret_cast<uint4*>(dst + c_lo + ju * 8) = xv;
           }
         }
       }

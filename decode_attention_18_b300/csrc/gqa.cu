@@ -1022,6 +1022,111 @@ __global__ void __launch_bounds__(256) combine_balanced_kernel(const float* __re
                lse_out ? lse_out + row : nullptr, threadIdx.x % M::TPR);
 }
 
+// The same merge for few rows with many partials each (the tensor-core kernel's balanced
+// pieces give about SMs / items partials per row): one block per row. The partials are
+// split over NG = 256 / (D / 8) groups of threads, each group merging its share with four
+// partials' loads in flight per round; the groups' (maximum, weight sum, weighted row)
+// are then combined through shared memory. A row of a whole item returns at once.
+template <int D>
+__global__ void __launch_bounds__(256) combine_wide_kernel(const float* __restrict__ ws_o,
+                                                           const float* __restrict__ ws_lse,
+                                                           const int* __restrict__ meta,
+                                                           const int32_t* __restrict__ seqlens, int hq, int s, int hkv,
+                                                           int G, int rpb, int nrb, long long records,
+                                                           __nv_bfloat16* __restrict__ out,
+                                                           float* __restrict__ lse_out) {
+  constexpr int TPR = D / 8, NG = 256 / TPR;
+  __shared__ float s_m[NG], s_w[NG];
+  __shared__ __align__(16) float s_acc[NG][D];
+  pdl_wait();  // the partials come from the attention kernel just before
+  pdl_trigger();
+  const int row = blockIdx.x;
+  const int bi = row / (hq * s);
+  const int j = (row / s) % hq;
+  const int r = (j % G) * s + row % s;  // row within the KV head's rows
+  const long long item = ((long long)bi * hkv + j / G) * nrb + r / rpb;
+  int first = 0, n = 0;
+  if (seqlens[bi] > 0) {
+    first = meta[2 * item];
+    n = meta[2 * item + 1];
+    if (n <= 1) return;  // written directly by its CTA
+    if (first < 0 || first >= records) return;  // only a corrupted entry: stay inside the workspace
+    n = (int)min((long long)n, records - first);
+  }
+  const int g = threadIdx.x / TPR, t = threadIdx.x % TPR;
+  const size_t rec_row = (size_t)first * rpb + r % rpb;
+  const float* o0 = ws_o + rec_row * D + 8 * t;
+  const float* l0 = ws_lse + rec_row;
+  float M = -INFINITY, wsum = 0.f;
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  for (int c0 = g; c0 < n; c0 += 4 * NG) {
+    float lv[4];
+    float x[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + u * NG;
+      lv[u] = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[u][e] = 0.f;
+      if (c < n) {
+        lv[u] = l0[(size_t)c * rpb];
+        load8(o0 + (size_t)c * rpb * D, x[u]);
+      }
+    }
+    float mn = M;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) mn = fmaxf(mn, lv[u]);
+    if (mn == -INFINITY) continue;
+    const float f = expf(M - mn);  // 0 while nothing was merged yet
+    wsum *= f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] *= f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (lv[u] == -INFINITY) continue;
+      const float w = expf(lv[u] - mn);
+      wsum += w;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += w * x[u][e];
+    }
+    M = mn;
+  }
+  if (t == 0) {
+    s_m[g] = M;
+    s_w[g] = wsum;
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) s_acc[g][8 * t + e] = acc[e];
+  __syncthreads();
+  if (g != 0) return;
+  float mx = -INFINITY;
+#pragma unroll 4
+  for (int gg = 0; gg < NG; ++gg) mx = fmaxf(mx, s_m[gg]);
+  float W = 0.f;
+  float a[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) a[e] = 0.f;
+  if (mx != -INFINITY) {
+    for (int gg = 0; gg < NG; ++gg) {
+      if (s_m[gg] == -INFINITY) continue;
+      const float f = expf(s_m[gg] - mx);
+      W += f * s_w[gg];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) a[e] += f * s_acc[gg][8 * t + e];
+    }
+  }
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+  uint4 pk;
+  pk.x = pack_bf16(a[0] * inv, a[1] * inv);
+  pk.y = pack_bf16(a[2] * inv, a[3] * inv);
+  pk.z = pack_bf16(a[4] * inv, a[5] * inv);
+  pk.w = pack_bf16(a[6] * inv, a[7] * inv);
+  *reinterpret_cast<uint4*>(out + (size_t)row * D + 8 * t) = pk;
+  if (lse_out && t == 0) lse_out[row] = W > 0.f ? mx + logf(W) : -INFINITY;
+}
+
 template <int D>
 static int merge_blocks(int rows) {
   return (rows + MergeCfg<D>::ROWS - 1) / MergeCfg<D>::ROWS;
@@ -1085,11 +1190,16 @@ cudaError_t launch_combine_balanced(const float* ws_o, const float* ws_lse, cons
   const int rows = b * hq * s;
   auto* o = static_cast<__nv_bfloat16*>(out);
   const int G = hq / hkv;
-#define DECATTN_COMBINE_CASE(D)                                                                              \
-  case D:                                                                                                    \
-    if (cudaError_t e = launch_dependent(combine_balanced_kernel<D>, merge_blocks<D>(rows), stream, ws_o,      \
-                                         ws_lse, meta, seqlens, rows, hq, s, hkv, G, rpb, nrb, records, o, lse)) \
-      return e;                                                                                              \
+  // few rows: one block per row, its partials merged by groups of threads in parallel
+  const bool wide = rows <= 4096;
+#define DECATTN_COMBINE_CASE(D)                                                                                  \
+  case D:                                                                                                        \
+    if (cudaError_t e = wide ? launch_dependent(combine_wide_kernel<D>, rows, stream, ws_o, ws_lse, meta, seqlens,  \
+                                                hq, s, hkv, G, rpb, nrb, records, o, lse)                         \
+                             : launch_dependent(combine_balanced_kernel<D>, merge_blocks<D>(rows), stream, ws_o,  \
+                                                ws_lse, meta, seqlens, rows, hq, s, hkv, G, rpb, nrb, records, o, \
+                                                lse))                                                             \
+      return e;                                                                                                  \
     break;
   switch (d) {
     DECATTN_COMBINE_CASE(64)

@@ -10,18 +10,22 @@
 //
 // One CTA takes 128 query rows of one (sequence, KV head) and every key they see, or a
 // piece of those keys:
-//  * Q [128 rows x DK] comes by TMA through the ring's first lap and is moved into Tensor
-//    Memory by the softmax warps (lane = row, two bf16 per column), where it stays as the
-//    A operand of the score MMAs; the ring's shared memory is then all K and V: 64-key
-//    tiles in 3 (DK = DV = 256), 4 (192 / 128) or 6 (128 / 128) stages.
+//  * Q [128 rows x DK] comes by TMA through the K ring's first two slots and is moved into
+//    Tensor Memory by the softmax warps (lane = row, two bf16 per column), where it stays
+//    as the A operand of the score MMAs; shared memory is then all K and V: 64-key tiles
+//    in 3 K + 4 V slots (DK = DV = 256), 4 + 8 (192 / 128) or 7 + 7 (128 / 128).
 //  * One thread issues tcgen05.mma: S = Q K^T (M = 128, N = 64, A from Tensor Memory)
 //    into one of two TMEM buffers, and O += P V (M = 128, N = DV) into a TMEM
 //    accumulator, the P V of tile t-1 issued after the S of tile t so that the softmax of
 //    tile t overlaps it.
 //  * Four softmax warps (thread = row) read S from TMEM, keep a lazy reference maximum
 //    (moved only past 2^8; the O row is then rescaled in TMEM once the previous tile's
-//    P V has completed), write P as bf16 into one of two shared-memory buffers, and at
-//    the end scale O by 1/l and store bf16 rows and the LSE.
+//    P V has completed), write P as bf16 back into Tensor Memory over its own S columns
+//    (the P V takes A from there), and at the end scale O by 1/l and store bf16 rows and
+//    the LSE.
+//  * K and V have rings of their own, fed by two producer warps: a K slot is free once
+//    its score MMA completes, a V slot once its P V has, so the K stream runs ahead of
+//    the V stream and more of both is in flight than a shared K+V stage allows.
 // Every wait is bounded; a wait that runs out sets the error word and the CTA winds
 // down (its copies and MMAs waited for, TMEM freed). V rows past the sequence end are
 // zeroed before the MMA reads them (their P is 0, but 0 * NaN is NaN).
@@ -45,10 +49,11 @@ namespace {
 
 constexpr int PM = 128;          // query rows per CTA (MMA M)
 constexpr int PK = 64;           // keys per tile (S MMA N)
-constexpr int PNS_MAX = 6;       // ring stages at most
+constexpr int PNS_MAX = 8;       // slots of either ring at most
 constexpr int PCH = PK * 128;    // one [64 keys x 64 values] bf16 chunk, 128-byte rows
 constexpr int PQCH = PM * 128;   // one [128 rows x 64 values] chunk of Q or P
-constexpr int PTHREADS = 192;    // warp 0 TMA, warp 1 MMA, warps 2-5 softmax / epilogue
+constexpr int PTHREADS = 224;    // warp 0 K (and Q) loads, 1 MMA, 2-5 softmax / epilogue, 6 V loads
+constexpr int kPWarpV = 6;
 constexpr float kPLog2e = 1.4426950408889634f;
 constexpr float kPLn2 = 0.6931471805599453f;
 constexpr float kPRescale = 8.f;
@@ -57,29 +62,35 @@ constexpr unsigned long long kPTeardownNs = 1000000000ull;
 template <int DK, int DV>
 struct PfCfg {
   static constexpr int KCH = DK / 64, VCH = DV / 64;
-  static constexpr int STAGE = (KCH + VCH) * PCH;
-  static constexpr int OFF_RING = 0;
-  // as many ring stages (at most PNS_MAX) as fit beside the two P buffers in 227 KB
-  static constexpr int FIXED = 2 * PQCH + 256 + 1024;
-  static constexpr int NS_FIT = (232448 - FIXED) / STAGE;
-  static constexpr int NS = NS_FIT < PNS_MAX ? NS_FIT : PNS_MAX;
-  static constexpr int QS = (KCH * PQCH + STAGE - 1) / STAGE;  // ring slots the query lap covers
-  static constexpr int OFF_P = OFF_RING + NS * STAGE;
-  static constexpr int OFF_BAR = OFF_P + 2 * PQCH;
-  static constexpr int SMEM = OFF_BAR + 256 + 1024;  // barriers + slots, + alignment slack
-  // Tensor Memory: two S buffers (columns 0 and PK), O (2 PK), Q (2 PK + DV, DK / 2 columns)
+  static constexpr int KT = KCH * PCH, VT = VCH * PCH;  // one 64-key K / V tile
+  // Separate K and V rings: a K slot is free once its score MMA completes, a V slot only
+  // once the P V that reads it has. Half the shared memory goes to K (the query lap takes
+  // its first two slots), the rest to V.
+  static constexpr int BUDGET = 232448 - 512 - 1024;  // barriers + slots, alignment slack
+  static constexpr int NK_FIT = (BUDGET / 2) / KT;
+  static constexpr int NK = NK_FIT < PNS_MAX ? NK_FIT : PNS_MAX;
+  static constexpr int NV_FIT = (BUDGET - NK * KT) / VT;
+  static constexpr int NV = NV_FIT < PNS_MAX ? NV_FIT : PNS_MAX;
+  static constexpr int QS = (KCH * PQCH + KT - 1) / KT;  // K slots the query lap covers (2)
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + NK * KT;
+  static constexpr int OFF_BAR = OFF_V + NV * VT;
+  static constexpr int SMEM = OFF_BAR + 512 + 1024;
+  // Tensor Memory: two S buffers (columns 0 and PK; P is written over the first PK / 2
+  // columns of its own S), O (2 PK), Q (2 PK + DV, DK / 2 columns)
   static constexpr int OCOL = 2 * PK, QCOL = 2 * PK + DV;
   static constexpr int TMEM_COLS = 512;
   static_assert(DK % 64 == 0 && DV % 64 == 0 && DV <= 256, "widths");
   static_assert(QCOL + DK / 2 <= TMEM_COLS, "tensor memory");
-  static_assert(NS >= 2 && QS < NS, "ring");
+  static_assert(NK >= 3 && NV >= 2 && QS < NK && OFF_V % 1024 == 0 && KT % 1024 == 0, "rings");
+  static_assert(SMEM <= 232448, "shared memory");
 };
 
 // barriers
-enum { F_QREADY = 0, F_FULL = 1, F_EMPTY = F_FULL + PNS_MAX, F_SFULL = F_EMPTY + PNS_MAX, F_SEMPTY = F_SFULL + 2,
-       F_PFULL = F_SEMPTY + 2, F_PEMPTY = F_PFULL + 2, F_OFINAL = F_PEMPTY + 2, F_FIN = F_OFINAL + 1,
-       F_TEST = F_FIN + 1, F_COUNT = F_TEST + 1 };
-static_assert(F_COUNT * 8 + 8 <= 256, "barrier region");
+enum { F_QREADY = 0, F_KFULL = 1, F_KEMPTY = F_KFULL + PNS_MAX, F_VFULL = F_KEMPTY + PNS_MAX,
+       F_VEMPTY = F_VFULL + PNS_MAX, F_SFULL = F_VEMPTY + PNS_MAX, F_PFULL = F_SFULL + 2, F_PVDONE = F_PFULL + 2,
+       F_OFINAL = F_PVDONE + 2, F_FIN = F_OFINAL + 1, F_TEST = F_FIN + 1, F_COUNT = F_TEST + 1 };
+static_assert(F_COUNT * 8 + 8 <= 512, "barrier region");
 constexpr int kPBarQ = 1;  // named barrier of the four softmax warps
 constexpr unsigned long long kPTestWaitNs = 1000000ull;  // forced-timeout test: 1 ms
 
@@ -187,15 +198,18 @@ __global__ void __launch_bounds__(PTHREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars[F_QREADY], 1);
-    for (int i = 0; i < C::NS; ++i) {
-      mbar_init(&bars[F_FULL + i], 1);
-      mbar_init(&bars[F_EMPTY + i], 1);
+    for (int i = 0; i < C::NK; ++i) {
+      mbar_init(&bars[F_KFULL + i], 1);
+      mbar_init(&bars[F_KEMPTY + i], 1);
+    }
+    for (int i = 0; i < C::NV; ++i) {
+      mbar_init(&bars[F_VFULL + i], 1);
+      mbar_init(&bars[F_VEMPTY + i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[F_SFULL + i], 1);
-      mbar_init(&bars[F_SEMPTY + i], 4);
       mbar_init(&bars[F_PFULL + i], 4);
-      mbar_init(&bars[F_PEMPTY + i], 1);
+      mbar_init(&bars[F_PVDONE + i], 1);
     }
     mbar_init(&bars[F_OFINAL], 1);
     mbar_init(&bars[F_FIN], 1);
@@ -229,55 +243,73 @@ __global__ void __launch_bounds__(PTHREADS, 1)
   const int ntiles = w.valid && kend > kstart ? (kend - kstart + PK - 1) / PK : 0;
   const int qrow0 = (bi * p.hq + g * p.G) * p.s + r0;  // first flattened [b*hq*s] query row
 
+  // token row of tile t's first key in the cache tensor (a tile is one page)
+  auto tile_row = [&](int t) -> int {
+    if (p.paged) {
+      int page = __ldg(p.block_table + (size_t)bi * p.max_pages + kstart / PK + t);
+      if (page < 0 || page >= p.num_pages) {
+        raise_error(p.err, kErrBadPage);
+        page = 0;  // stay inside the pool; the result is flagged invalid
+      }
+      return page * PK;
+    }
+    return bi * p.capacity + kstart + t * PK;
+  };
+
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer
+    // ------------------------------------------------ TMA producer: the query lap, then K tiles
     if (ntiles > 0 && elect_one()) {
-      // the query lap: Q boxes [128 rows x 64] (16 KB each) laid end to end from the ring's
+      // the query lap: Q boxes [128 rows x 64] (16 KB each) laid end to end from the K ring's
       // start over its first QS slots; a box completes on the barrier of the slot it starts
       // in, and a slot in which no box starts gets a plain arrival
       uint32_t qbytes[C::QS];
       for (int i = 0; i < C::QS; ++i) qbytes[i] = 0;
-      for (int c = 0; c < C::KCH; ++c) qbytes[(c * PQCH) / C::STAGE] += PQCH;
+      for (int c = 0; c < C::KCH; ++c) qbytes[(c * PQCH) / C::KT] += PQCH;
       for (int i = 0; i < C::QS; ++i) {
         if (qbytes[i])
-          mbar_expect_tx(&bars[F_FULL + i], qbytes[i]);
+          mbar_expect_tx(&bars[F_KFULL + i], qbytes[i]);
         else
-          mbar_arrive(&bars[F_FULL + i]);
+          mbar_arrive(&bars[F_KFULL + i]);
       }
       for (int c = 0; c < C::KCH; ++c)
-        tma_load_2d(sb + C::OFF_RING + c * PQCH, &tm_q, c * 64, qrow0, &bars[F_FULL + (c * PQCH) / C::STAGE]);
-      // tile t takes ring position u = QS + t: slot u % NS, its (u / NS)-th use
+        tma_load_2d(sb + C::OFF_K + c * PQCH, &tm_q, c * 64, qrow0, &bars[F_KFULL + (c * PQCH) / C::KT]);
+      // K of tile t takes K-ring position u = QS + t: slot u % NK, its (u / NK)-th use. One
+      // box per tile ([chunks][64 keys][64 values], chunk-major as the MMAs read it: the
+      // TMA engine serves about one box per few hundred cycles per SM whatever its size).
       int last[PNS_MAX];
       for (int i = 0; i < PNS_MAX; ++i) last[i] = i < C::QS ? i : -1;
       for (int t = 0; t < ntiles; ++t) {
-        const int u = C::QS + t, slot = u % C::NS;
-        if (u >= C::NS && !mbar_wait(&bars[F_EMPTY + slot], ((u / C::NS) - 1) & 1, p.wait_ns, abort_flag)) {
+        const int u = C::QS + t, slot = u % C::NK;
+        if (u >= C::NK && !mbar_wait(&bars[F_KEMPTY + slot], ((u / C::NK) - 1) & 1, p.wait_ns, abort_flag)) {
           if (!*abort_flag) fail();
           break;
         }
-        int row0;  // token row of the tile's first key in the cache tensor (a tile is one page)
-        if (p.paged) {
-          int page = __ldg(p.block_table + (size_t)bi * p.max_pages + kstart / PK + t);
-          if (page < 0 || page >= p.num_pages) {
-            raise_error(p.err, kErrBadPage);
-            page = 0;  // stay inside the pool; the result is flagged invalid
-          }
-          row0 = page * PK;
-        } else {
-          row0 = bi * p.capacity + kstart + t * PK;
-        }
-        // one box for K and one for V: [chunks][64 keys][64 values], chunk-major as the
-        // MMAs read them (the TMA engine serves about one box per few hundred cycles per SM
-        // whatever its size, so a tile is not cut into per-chunk boxes)
-        const uint32_t dst = sb + C::OFF_RING + slot * C::STAGE;
-        mbar_expect_tx(&bars[F_FULL + slot], C::STAGE);
-        tma_load_4d(dst, &tm_k, 0, row0, 0, g, &bars[F_FULL + slot]);
-        tma_load_4d(dst + C::KCH * PCH, &tm_v, 0, row0, 0, g, &bars[F_FULL + slot]);
+        mbar_expect_tx(&bars[F_KFULL + slot], C::KT);
+        tma_load_4d(sb + C::OFF_K + slot * C::KT, &tm_k, 0, tile_row(t), 0, g, &bars[F_KFULL + slot]);
         last[slot] = u;
       }
       // leave no copy in flight
-      for (int i = 0; i < C::NS; ++i)
-        if (last[i] >= 0) mbar_wait(&bars[F_FULL + i], (last[i] / C::NS) & 1, kPTeardownNs, nullptr);
+      for (int i = 0; i < C::NK; ++i)
+        if (last[i] >= 0) mbar_wait(&bars[F_KFULL + i], (last[i] / C::NK) & 1, kPTeardownNs, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == kPWarpV) {
+    // ------------------------------------------------ TMA producer: V tiles (slot t % NV)
+    if (ntiles > 0 && elect_one()) {
+      int last[PNS_MAX];
+      for (int i = 0; i < PNS_MAX; ++i) last[i] = -1;
+      for (int t = 0; t < ntiles; ++t) {
+        const int slot = t % C::NV;
+        if (t >= C::NV && !mbar_wait(&bars[F_VEMPTY + slot], ((t / C::NV) - 1) & 1, p.wait_ns, abort_flag)) {
+          if (!*abort_flag) fail();
+          break;
+        }
+        mbar_expect_tx(&bars[F_VFULL + slot], C::VT);
+        tma_load_4d(sb + C::OFF_V + slot * C::VT, &tm_v, 0, tile_row(t), 0, g, &bars[F_VFULL + slot]);
+        last[slot] = t;
+      }
+      for (int i = 0; i < C::NV; ++i)
+        if (last[i] >= 0) mbar_wait(&bars[F_VFULL + i], (last[i] / C::NV) & 1, kPTeardownNs, nullptr);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -285,18 +317,20 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     const bool leader = elect_one();
     constexpr uint32_t idS = idesc_bf16_f32(PM, PK, false, false);  // B = K rows, K-major
     constexpr uint32_t idO = idesc_bf16_f32(PM, DV, false, true);   // B = V rows, N-major
-    const uint64_t dk = smem_desc(sb + C::OFF_RING, 16, 1024, kSw128);
-    const uint64_t dv = smem_desc(sb + C::OFF_RING, PCH, 1024, kSw128);  // chunk stride 8 KB
-    const uint64_t dp = smem_desc(sb + C::OFF_P, 16, 1024, kSw128);
+    const uint64_t dk = smem_desc(sb + C::OFF_K, 16, 1024, kSw128);
+    const uint64_t dv = smem_desc(sb + C::OFF_V, PCH, 1024, kSw128);  // chunk stride 8 KB
     bool ok = ntiles == 0 || pf_wait(&bars[F_QREADY], 0, p.wait_ns, abort_flag);
     tc_fence_after();  // Q was written to Tensor Memory by the softmax warps
-    // O += P(u) V(u); the tail of the last tile's V rows is zeroed first
+    // O += P(u) V(u), P(u) from Tensor Memory (over S buffer u & 1); the tail of the last
+    // tile's V rows is zeroed first
     auto o_mma = [&](int u) -> bool {
-      const int pb = u & 1, slot = (C::QS + u) % C::NS;
-      if (!pf_wait(&bars[F_PFULL + pb], (u >> 1) & 1, p.wait_ns, abort_flag)) return false;
+      const int pb = u & 1, slot = u % C::NV;
+      if (!pf_wait(&bars[F_PFULL + pb], (u >> 1) & 1, p.wait_ns, abort_flag) ||
+          !pf_wait(&bars[F_VFULL + slot], (u / C::NV) & 1, p.wait_ns, abort_flag))
+        return false;
       const int nvalid = kend - (kstart + u * PK);
       if (nvalid < PK) {
-        uint8_t* vt = smem + C::OFF_RING + slot * C::STAGE + C::KCH * PCH;
+        uint8_t* vt = smem + C::OFF_V + slot * C::VT;
         for (int idx = lane; idx < (PK - nvalid) * C::VCH * 8; idx += 32) {
           const int row = nvalid + idx / (C::VCH * 8), rem = idx % (C::VCH * 8);
           *reinterpret_cast<uint4*>(vt + (rem / 8) * PCH + row * 128 + (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
@@ -306,32 +340,33 @@ __global__ void __launch_bounds__(PTHREADS, 1)
       }
       tc_fence_after();
       if (leader) {
-        const uint64_t a0 = dp + (uint64_t)((pb * PQCH) >> 4);
-        const uint64_t b0 = dv + (uint64_t)((slot * C::STAGE + C::KCH * PCH) >> 4);
+        const uint64_t b0 = dv + (uint64_t)((slot * C::VT) >> 4);
 #pragma unroll
         for (int kk = 0; kk < PK / 16; ++kk)
-          tc_mma_ss(tmem + C::OCOL, a0 + 2 * kk, b0 + (uint64_t)((kk * 16 * 128) >> 4), idO,
+          tc_mma_ts(tmem + C::OCOL, tmem + pb * PK + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), idO,
                     (u > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&bars[F_EMPTY + slot]);  // the ring slot (K and V of tile u) is free
-        tc_commit(&bars[F_PEMPTY + pb]);   // P buffer pb is free; O holds tiles <= u
+        tc_commit(&bars[F_VEMPTY + slot]);  // the V slot is free
+        tc_commit(&bars[F_PVDONE + pb]);    // S/P buffer pb is free; O holds tiles <= u
       }
       __syncwarp();
       return true;
     };
     for (int t = 0; ok && t < ntiles; ++t) {
-      const int slot = (C::QS + t) % C::NS, sbuf = t & 1;
-      if (!pf_wait(&bars[F_FULL + slot], ((C::QS + t) / C::NS) & 1, p.wait_ns, abort_flag) ||
-          (t >= 2 && !pf_wait(&bars[F_SEMPTY + sbuf], ((t >> 1) - 1) & 1, p.wait_ns, abort_flag))) {
+      const int u = C::QS + t, slot = u % C::NK, sbuf = t & 1;
+      // K of tile t landed; S buffer sbuf (P of tile t - 2) has been read by its P V
+      if (!pf_wait(&bars[F_KFULL + slot], (u / C::NK) & 1, p.wait_ns, abort_flag) ||
+          (t >= 2 && !pf_wait(&bars[F_PVDONE + sbuf], ((t >> 1) - 1) & 1, p.wait_ns, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
       if (leader) {
-        const uint64_t b0 = dk + (uint64_t)((slot * C::STAGE) >> 4);
+        const uint64_t b0 = dk + (uint64_t)((slot * C::KT) >> 4);
 #pragma unroll
         for (int kk = 0; kk < DK / 16; ++kk)
           tc_mma_ts(tmem + sbuf * PK, tmem + C::QCOL + kk * 8, b0 + (uint64_t)(((kk / 4) * PCH + (kk % 4) * 32) >> 4),
                     idS, kk > 0 ? 1u : 0u);
+        tc_commit(&bars[F_KEMPTY + slot]);  // the K slot is free once these MMAs complete
         tc_commit(&bars[F_SFULL + sbuf]);
       }
       __syncwarp();
@@ -362,11 +397,11 @@ __global__ void __launch_bounds__(PTHREADS, 1)
       // column, even index low); chunk j of the query lap is [128 rows x 64] with 128-byte
       // swizzled rows. Then the query lap's ring slots go back to the producer.
       bool okq = true;
-      for (int i = 0; i < C::QS; ++i) okq = okq && pf_wait(&bars[F_FULL + i], 0, p.wait_ns, abort_flag);
+      for (int i = 0; i < C::QS; ++i) okq = okq && pf_wait(&bars[F_KFULL + i], 0, p.wait_ns, abort_flag);
       if (okq) {
 #pragma unroll 1
         for (int j = 0; j < C::KCH; ++j) {
-          const uint8_t* bx = smem + C::OFF_RING + j * PQCH + r * 128;
+          const uint8_t* bx = smem + C::OFF_K + j * PQCH + r * 128;
           uint32_t v[32];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
@@ -384,7 +419,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
       ok = named_bar_and(kPBarQ, 128, okq && !*abort_flag);
       if (threadIdx.x == 64) {
         if (ok) {
-          for (int i = 0; i < C::QS; ++i) mbar_arrive(&bars[F_EMPTY + i]);
+          for (int i = 0; i < C::QS; ++i) mbar_arrive(&bars[F_KEMPTY + i]);
           mbar_arrive(&bars[F_QREADY]);
         } else if (!*abort_flag) {
           fail();
@@ -392,7 +427,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
       }
     }
     for (int t = 0; ok && t < ntiles; ++t) {
-      const int sbuf = t & 1, pb = t & 1;
+      const int sbuf = t & 1;
       if (!pf_wait(&bars[F_SFULL + sbuf], (t >> 1) & 1, p.wait_ns, abort_flag) ||
           (t == 0 && p.test_timeout && !pf_wait(&bars[F_TEST], 0, kPTestWaitNs, abort_flag))) {
         ok = false;
@@ -411,9 +446,6 @@ __global__ void __launch_bounds__(PTHREADS, 1)
 #pragma unroll
         for (int c = 0; c < 32; ++c) x[32 + c] = __uint_as_float(v[c]) * p.scale_log2;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[F_SEMPTY + sbuf]);  // the MMA warp may overwrite this S buffer
       const int kb = kstart + t * PK;
       if (kb + PK > lim) {
 #pragma unroll
@@ -423,18 +455,13 @@ __global__ void __launch_bounds__(PTHREADS, 1)
       float mx = x[0];
 #pragma unroll
       for (int c = 1; c < PK; ++c) mx = fmaxf(mx, x[c]);
-      // P buffer pb was last read by the P V of tile t-2
-      if (t >= 2 && !pf_wait(&bars[F_PEMPTY + pb], ((t >> 1) - 1) & 1, p.wait_ns, abort_flag)) {
-        ok = false;
-        break;
-      }
       // lazy reference maximum: moved only past 2^8; O (tiles < t, once their P V is done)
       // is then rescaled in TMEM row by row (the whole warp takes part in the loads)
       float alpha = 1.f;
       const bool move = mx > m_ref + kPRescale;
       if (move) alpha = fast_exp2(m_ref - mx);  // 0 while nothing was seen yet
       if (__any_sync(0xffffffffu, move && m_ref != -INFINITY) && t >= 1) {
-        if (!pf_wait(&bars[F_PEMPTY + ((t - 1) & 1)], ((t - 1) >> 1) & 1, p.wait_ns, abort_flag)) {
+        if (!pf_wait(&bars[F_PVDONE + ((t - 1) & 1)], ((t - 1) >> 1) & 1, p.wait_ns, abort_flag)) {
           ok = false;
           break;
         }
@@ -464,16 +491,13 @@ __global__ void __launch_bounds__(PTHREADS, 1)
         pk[e] = pack_bf16(p0, p1);
       }
       l_run += ps;
-      // P row r into buffer pb: [128 rows x 128 bytes], 16-byte unit u at (u ^ (r & 7))
-      uint8_t* prow = smem + C::OFF_P + pb * PQCH + r * 128;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        *reinterpret_cast<uint4*>(prow + ((u ^ (r & 7)) << 4)) =
-            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-      fence_proxy_async_smem();  // the MMA (async proxy) reads what these stores wrote
-      tc_fence_before();         // and the rescale's TMEM stores come before its P V
+      // P row r into Tensor Memory over the first PK / 2 columns of its own S buffer (the A
+      // operand of the P V: lane = row, two bf16 per column, even key low); S is in x[]
+      tmem_st32(t_lane + sbuf * PK, pk);
+      tmem_st_wait();
+      tc_fence_before();  // P and the rescale's TMEM stores come before the P V
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[F_PFULL + pb]);
+      if (lane == 0) mbar_arrive(&bars[F_PFULL + sbuf]);
     }
     if (ok && ntiles > 0) ok = pf_wait(&bars[F_OFINAL], 0, p.wait_ns, abort_flag);
     if (!ok && ntiles > 0) {

@@ -172,6 +172,35 @@ Plan mla_plan(int b, int s, int h, int k, int max_seqlen, int sms) {
   const int per = mla_ctas_per_row_tile();
   return plan_splits(base, max_seqlen, sms / per > 0 ? sms / per : 1, 384, 512, mla_tile_keys());
 }
+// Tail split: with one chunk per (sequence, row tile) unit and U units on P cluster slots,
+// the last wave holds only U mod P units. Those units are cut into k = P / (U mod P) >= 2
+// chunks each, so that the last wave runs k times shorter; the other units stay whole.
+struct MlaTail {
+  int whole = 0, units = 0, k = 0, chunk = 0;
+};
+MlaTail mla_tail(int b, int s, int h, int max_seqlen, int sms, const Plan& pl) {
+  MlaTail t;
+  if (g_forced_splits.load() > 0 || pl.nsplit != 1 || max_seqlen <= 0) return t;
+  const long long U = (long long)b * ceil_div((long long)h * s, 128);
+  const long long P = sms / mla_ctas_per_row_tile();
+  if (P <= 0 || U <= P) return t;
+  const long long rm = U % P;
+  if (rm == 0 || P / rm < 2 || U > INT_MAX) return t;
+  const int k = (int)(P / rm);
+  const int tk = mla_tile_keys();
+  const int chunk = (int)(ceil_div(ceil_div(max_seqlen, k), tk) * tk);
+  if (chunk >= max_seqlen) return t;
+  t.whole = (int)(U - rm);
+  t.units = (int)rm;
+  t.k = k;
+  t.chunk = chunk;
+  return t;
+}
+size_t mla_tail_bytes(const MlaTail& t, int k_lat) {
+  if (t.k == 0) return 0;
+  const size_t rows = (size_t)t.units * 128 * t.k;
+  return align256(rows * k_lat * kMlaPartialBytes) + align256(rows * sizeof(float));
+}
 
 }  // namespace
 }  // namespace decattn
@@ -512,6 +541,8 @@ size_t mla_decode_workspace_size(int b, int s, int h, int k, int max_seqlen) {
   DeviceState* st = nullptr;
   if (device_state(&st)) return 0;
   const Plan pl = mla_plan(b, s, h, k, max_seqlen, st->sms);
+  const MlaTail tail = mla_tail(b, s, h, max_seqlen, st->sms, pl);
+  if (tail.k > 0) return mla_tail_bytes(tail, k);
   return partial_bytes((long long)b * h * s, pl.nsplit, k, kMlaPartialBytes);
 }
 
@@ -531,7 +562,8 @@ int mla_decode(const decattn_bf16* qz, const decattn_bf16* q_pe, const decattn_b
   if (int rc = device_state(&st)) return rc;
   const Plan pl = mla_plan(b, s, h, k, max_seqlen, st->sms);
   const long long rows = (long long)b * h * s;
-  const size_t need = partial_bytes(rows, pl.nsplit, k, kMlaPartialBytes);
+  const MlaTail tail = mla_tail(b, s, h, max_seqlen, st->sms, pl);
+  const size_t need = tail.k > 0 ? mla_tail_bytes(tail, k) : partial_bytes(rows, pl.nsplit, k, kMlaPartialBytes);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return DECATTN_ERR_WORKSPACE;
   MlaLaunch a;
   a.qz = qz;
@@ -558,12 +590,25 @@ int mla_decode(const decattn_bf16* qz, const decattn_bf16* q_pe, const decattn_b
   a.ws_lse = pl.nsplit > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                                        align256((size_t)rows * pl.nsplit * k * kMlaPartialBytes))
                            : nullptr;
+  a.tail_whole = tail.whole;
+  a.tail_units = tail.units;
+  a.tail_k = tail.k;
+  a.tail_chunk = tail.chunk;
+  if (tail.k > 0) {
+    const size_t trows = (size_t)tail.units * 128 * tail.k;
+    a.ws_o = workspace;
+    a.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(trows * k * kMlaPartialBytes));
+  }
   a.err = st->err;
   a.wait_ns = wait_limit();
   a.test_timeout = g_test_timeout.load();
-  g_last_splits.store(pl.nsplit);
+  g_last_splits.store(tail.k > 0 ? tail.k : pl.nsplit);  // the tail units' chunk count
   if (launch_mla_latent(a, stream) != cudaSuccess) return DECATTN_ERR_CUDA;
-  if (pl.nsplit > 1) {
+  if (tail.k > 0) {
+    if (launch_combine_tail(a.ws_o, a.ws_lse, seqlens, tail.units, tail.whole, (int)ceil_div((long long)h * s, 128),
+                            h * s, tail.k, tail.chunk, k, o_lat, lse, stream) != cudaSuccess)
+      return DECATTN_ERR_CUDA;
+  } else if (pl.nsplit > 1) {
     if (launch_combine(a.ws_o, true, a.ws_lse, seqlens, (int)rows, h * s, pl.nsplit, pl.chunk, k, o_lat, lse, stream) !=
         cudaSuccess)
       return DECATTN_ERR_CUDA;

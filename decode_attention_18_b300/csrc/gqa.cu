@@ -1127,6 +1127,31 @@ __global__ void __launch_bounds__(256) combine_wide_kernel(const float* __restri
   if (lse_out && t == 0) lse_out[row] = W > 0.f ? mx + logf(W) : -INFINITY;
 }
 
+// Combine of the latent MLA kernel's tail split: partial row rp belongs to unit
+// tail_whole + rp / 128 (row tile mt of sequence bi), row rp % 128 of it; its k bf16
+// partials cover chunks of `chunk` keys, of which ceil(L / chunk) saw keys.
+template <int D>
+__global__ void __launch_bounds__(256) combine_tail_kernel(const __nv_bfloat16* __restrict__ ws_o,
+                                                           const float* __restrict__ ws_lse,
+                                                           const int32_t* __restrict__ seqlens, int tail_rows,
+                                                           int tail_whole, int mtiles, int rows_per_seq, int k, int chunk,
+                                                           __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
+  using M = MergeCfg<D>;
+  pdl_wait();  // the partials come from the attention kernel just before
+  pdl_trigger();
+  const int rp = blockIdx.x * M::ROWS + threadIdx.x / M::TPR;
+  if (rp >= tail_rows) return;
+  const int u = tail_whole + rp / 128;
+  const int bi = u / mtiles;
+  const int rin = (u % mtiles) * 128 + rp % 128;  // row within the sequence
+  if (rin >= rows_per_seq) return;
+  const size_t row = (size_t)bi * rows_per_seq + rin;
+  const int L = seqlens[bi];
+  const int nv = L > 0 ? min(k, (L + chunk - 1) / chunk) : 0;
+  merge_row<D, 2, __nv_bfloat16>(ws_o + (size_t)rp * k * D, D, ws_lse + (size_t)rp * k, 1, nv, out + row * D,
+                                 lse_out ? lse_out + row : nullptr, threadIdx.x % M::TPR);
+}
+
 template <int D>
 static int merge_blocks(int rows) {
   return (rows + MergeCfg<D>::ROWS - 1) / MergeCfg<D>::ROWS;
@@ -1179,6 +1204,28 @@ cudaError_t launch_combine(const void* ws_o, bool bf16_partials, const float* ws
                                        nsplit, chunk, d, o, lse, stream)
                     : launch_combine_t(static_cast<const float*>(ws_o), ws_lse, seqlens, rows, rows_per_seq, nsplit,
                                        chunk, d, o, lse, stream);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_combine_tail(const void* ws_o, const float* ws_lse, const int32_t* seqlens, int tail_units,
+                                int tail_whole, int mtiles, int rows_per_seq, int k, int chunk, int d, void* out,
+                                float* lse, cudaStream_t stream) {
+  const int tail_rows = tail_units * 128;
+  const auto* o = static_cast<const __nv_bfloat16*>(ws_o);
+  auto* dst = static_cast<__nv_bfloat16*>(out);
+  cudaError_t e;
+  switch (d) {
+    case 512:
+      e = launch_dependent(combine_tail_kernel<512>, merge_blocks<512>(tail_rows), stream, o, ws_lse, seqlens,
+                           tail_rows, tail_whole, mtiles, rows_per_seq, k, chunk, dst, lse);
+      break;
+    case 64:
+      e = launch_dependent(combine_tail_kernel<64>, merge_blocks<64>(tail_rows), stream, o, ws_lse, seqlens, tail_rows,
+                           tail_whole, mtiles, rows_per_seq, k, chunk, dst, lse);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

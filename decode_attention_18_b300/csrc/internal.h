@@ -47,6 +47,11 @@ cudaError_t launch_gqa_prefill(const GqaLaunch& p, cudaStream_t stream);
 // when bf16_partials) and their fp32 LSEs
 cudaError_t launch_combine(const void* ws_o, bool bf16_partials, const float* ws_lse, const int32_t* seqlens, int rows,
                            int rows_per_seq, int nsplit, int chunk, int d, void* out, float* lse, cudaStream_t stream);
+// combine of the latent kernel's tail split: tail_units * 128 partial rows of k bf16
+// partials each (unit tail_whole + i, rows i * 128 ..), merged into their rows of out
+cudaError_t launch_combine_tail(const void* ws_o, const float* ws_lse, const int32_t* seqlens, int tail_units,
+                                int tail_whole, int mtiles, int rows_per_seq, int k, int chunk, int d, void* out,
+                                float* lse, cudaStream_t stream);
 // combine of the balanced grouped-head schedules (gqa_balanced_kernel, rpb = its rows per
 // CTA; the tensor-core kernel's balanced split, rpb = 128): records [records][rpb][d]
 cudaError_t launch_combine_balanced(const float* ws_o, const float* ws_lse, const int* meta, const int32_t* seqlens,
@@ -78,8 +83,9 @@ struct MlaLaunch {
   float scale;
   void* o_lat;
   float* lse;
-  void* ws_o;     // [b*h*s, nsplit, k] bf16 O / l partials
-  float* ws_lse;  // [b*h*s, nsplit]
+  void* ws_o;     // [b*h*s, nsplit, k] bf16 O / l partials (tail split: [tail rows, tail_k, k])
+  float* ws_lse;  // [b*h*s, nsplit] (tail split: [tail rows, tail_k])
+  int tail_whole, tail_units, tail_k, tail_chunk;  // tail split (tail_k > 0): whole units, split units
   unsigned* err;
   unsigned long long wait_ns;
   int test_timeout;

@@ -53,6 +53,8 @@
 //     after it.
 #include <cuda.h>
 
+#include <climits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -160,6 +162,8 @@ struct MlaParams {
   const int32_t* block_table;
   int max_pages, paged, capacity, num_pages;
   int b, s, h, rows, nsplit, chunk;
+  int mtiles;                             // 128-row tiles per sequence
+  int tail_whole, tail_k, tail_chunk;     // tail split (tail_k > 0), see the kernel
   float scale_log2;
   __nv_bfloat16* o_lat;
   float* lse;
@@ -226,10 +230,43 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt = blockIdx.x >> 1;  // row tile (one cluster each)
-  const int split = blockIdx.y;
-  const int bi = blockIdx.z;
-  const int kstart = split * p.chunk;
+  // This cluster's work: row tile mt of sequence bi over keys [kstart, kstart + chunk).
+  //  * Fixed chunks: grid (2 * mtiles, nsplit, b).
+  //  * Tail split (a 1-D grid): the units u = bi * mtiles + mt that fill whole waves of
+  //    clusters run whole (u < tail_whole); each unit of the last, partial wave is cut into
+  //    tail_k chunks of tail_chunk keys, so that wave takes 1 / tail_k of the time.
+  // Partials go to record row (part_row0 + r) * part_n + split.
+  int mt, split, bi, chunk, part_n;
+  bool whole;
+  size_t part_row0;
+  if (p.tail_k > 0) {
+    const int c = blockIdx.x >> 1;
+    int u;
+    if (c < p.tail_whole) {
+      u = c;
+      split = 0;
+      whole = true;
+      chunk = INT_MAX;
+    } else {
+      u = p.tail_whole + (c - p.tail_whole) / p.tail_k;
+      split = (c - p.tail_whole) % p.tail_k;
+      whole = false;
+      chunk = p.tail_chunk;
+    }
+    bi = u / p.mtiles;
+    mt = u % p.mtiles;
+    part_n = p.tail_k;
+    part_row0 = (size_t)(u - p.tail_whole) * BM;
+  } else {
+    mt = blockIdx.x >> 1;
+    split = blockIdx.y;
+    bi = blockIdx.z;
+    chunk = p.chunk;
+    whole = p.nsplit == 1;
+    part_n = p.nsplit;
+    part_row0 = (size_t)bi * p.rows + mt * BM;
+  }
+  const int kstart = split * chunk;
   const int qrow0 = bi * p.rows + mt * BM;  // first flattened [b*h*s] query row of the tile
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -305,7 +342,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   pdl_trigger();
   const int L = p.seqlens[bi];
   const bool active = kstart < L && setup_ok && !*abort_flag;
-  if (kstart >= L && L <= 0 && p.nsplit == 1) {  // empty sequence without a combine pass
+  if (L <= 0 && whole) {  // empty sequence without a combine pass
     for (int idx = threadIdx.x; idx < BM * (KL / 8); idx += NTHREADS) {
       const int r = idx / (KL / 8);
       if (mt * BM + r >= p.rows) continue;
@@ -316,7 +353,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         p.lse[grow] = -INFINITY;
     }
   }
-  const int kend = min(L, kstart + p.chunk);
+  const int kend = chunk > L - kstart ? L : kstart + chunk;
   const int ntiles = active ? (kend - kstart + TK - 1) / TK : 0;
   constexpr uint32_t tmem = 0;
 
@@ -636,10 +673,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (ok && hh == 0) {
         if (row_ok) {
           const float lse = l_tot > 0.f ? (m_ref + log2f(l_tot)) * kLn2 : -INFINITY;
-          if (p.nsplit == 1) {
+          if (whole) {
             if (p.lse) p.lse[grow] = lse;
           } else {
-            p.ws_lse[grow * p.nsplit + split] = lse;
+            p.ws_lse[(part_row0 + r) * part_n + split] = lse;
           }
         }
         reinterpret_cast<float*>(smem + C::OFF_FIN)[r] = l_tot > 0.f ? 1.f / l_tot : 0.f;
@@ -872,7 +909,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (mt * BM + rs >= p.rows) continue;
             const uint4 xv = *reinterpret_cast<const uint4*>(stg + rr * ROWB + ((ju ^ (rr % UNITS)) << 4));
             const size_t g = (size_t)qrow0 + rs;
-            __nv_bfloat16* dst = p.nsplit == 1 ? p.o_lat + g * KL : p.ws_ob + (g * p.nsplit + split) * KL;
+            __nv_bfloat16* dst = whole ? p.o_lat + g * KL : p.ws_ob + ((part_row0 + rs) * part_n + split) * KL;
             *reinterpret_cast<uint4*>(dst + c_lo + ju * 8) = xv;
           }
         }
@@ -957,9 +994,13 @@ cudaError_t launch_klp(const MlaLaunch& a, cudaStream_t stream) {
   p.wait_ns = a.wait_ns;
   p.test_timeout = a.test_timeout;
   const int mtiles = (p.rows + BM - 1) / BM;
+  p.mtiles = mtiles;
+  p.tail_whole = a.tail_whole;
+  p.tail_k = a.tail_k;
+  p.tail_chunk = a.tail_chunk;
   // a cluster of two CTAs per row tile, launched as a programmatic dependent
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * mtiles, a.nsplit, a.b);
+  cfg.gridDim = a.tail_k > 0 ? dim3(2 * (a.tail_whole + a.tail_units * a.tail_k)) : dim3(2 * mtiles, a.nsplit, a.b);
   cfg.blockDim = dim3(NTHREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = stream;

@@ -191,6 +191,22 @@ def test_projection_gemms_alone():
     assert_out_close(f64(qz), A.mla_absorb_ref(f64(q), f64(wk), 2.0), "absorb", max_abs=4e-2, mean_abs=4e-3)
 
 
+def test_tail_split_last_wave():
+    # more (sequence, row tile) units than cluster slots, with a short last wave: the
+    # units of that wave are cut into chunks (merged by their own combine), the others run
+    # whole; an empty sequence and several lengths fall in the cut units
+    import decode_attention_18_b300 as da
+
+    seqlens = [1500 - 37 * i for i in range(19)] + [0]
+    inp = make(20, 128, 128, 512, 64, 4, seqlens, seed=13)
+    res = forward(inp)
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    units = 20 * 4  # 512 rows per sequence: 4 row tiles
+    if units > pairs and units % pairs and pairs // (units % pairs) >= 2:
+        assert da.last_num_splits() == pairs // (units % pairs)
+    check(inp, res, seqs=[0, 17, 18, 19], what="tail split")
+
+
 def test_full_size_dsv3_sampled():
     # b=32, h=128, d=128, k=512, p=64, t=4096, s=1: the headline workload
     from decode_attention_18_b300 import workloads as W

@@ -106,17 +106,6 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t v) {
   return pack_bf16(__half2float(__half(lo)), __half2float(__half(hi)));
 }
 
-// Four e4m3 values (bytes 0..3 of v) to two f16 pairs: lo = (byte 0, byte 1),
-// hi = (byte 2, byte 3), exactly; two conversions, no shifts or masks.
-__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t v, uint32_t& lo, uint32_t& hi) {
-  asm("{\n.reg .b16 l, h;\nmov.b32 {l, h}, %2;\ncvt.rn.f16x2.e4m3x2 %0, l;\ncvt.rn.f16x2.e4m3x2 %1, h;\n}\n"
-      : "=r"(lo), "=r"(hi)
-      : "r"(v));
-}
-__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
-  const __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
 // Shared-memory offset of 16-byte chunk u (16 values) of key row r in a byte tile of
 // [64 keys x 128 bytes] blocks, 128-byte swizzled (as TMA writes it)
 __device__ __forceinline__ uint32_t tile8_off(int r, int u) {

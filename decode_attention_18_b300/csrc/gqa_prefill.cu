@@ -52,35 +52,43 @@ constexpr int PK = 64;           // keys per tile (S MMA N)
 constexpr int PNS_MAX = 8;       // slots of either ring at most
 constexpr int PCH = PK * 128;    // one [64 keys x 64 values] bf16 chunk, 128-byte rows
 constexpr int PQCH = PM * 128;   // one [128 rows x 64 values] chunk of Q or P
-constexpr int PTHREADS = 224;    // warp 0 K (and Q) loads, 1 MMA, 2-5 softmax / epilogue, 6 V loads
-constexpr int kPWarpV = 6;
+// warp 0 K (and Q) loads, 1 MMA, 2-5 softmax / epilogue, 6 V loads; FP8: 7 and 8 widen the
+// landed K and V bytes to f16
+constexpr int kPWarpV = 6, kPWarpCK = 7, kPWarpCV = 8;
+__host__ __device__ constexpr int pf_threads(bool fp8) { return fp8 ? 288 : 224; }
 constexpr float kPLog2e = 1.4426950408889634f;
 constexpr float kPLn2 = 0.6931471805599453f;
 constexpr float kPRescale = 8.f;
 constexpr unsigned long long kPTeardownNs = 1000000000ull;
 
-template <int DK, int DV>
+template <int DK, int DV, bool FP8>
 struct PfCfg {
   static constexpr int KCH = DK / 64, VCH = DV / 64;
-  static constexpr int KT = KCH * PCH, VT = VCH * PCH;  // one 64-key K / V tile
+  static constexpr int KT = KCH * PCH, VT = VCH * PCH;  // one 64-key K / V tile (16-bit values)
   // Separate K and V rings: a K slot is free once its score MMA completes, a V slot only
-  // once the P V that reads it has. Half the shared memory goes to K (the query lap takes
-  // its first two slots), the rest to V.
-  static constexpr int BUDGET = 232448 - 512 - 1024;  // barriers + slots, alignment slack
+  // once the P V that reads it has. bf16: half the shared memory goes to K (the query lap
+  // takes its first two slots), the rest to V. FP8: E4M3 tiles land by TMA in rings of
+  // their own (LK / LV bytes a tile) and are widened to f16 into the K and V rings.
+  static constexpr int BUDGET = 232448 - 1024 - 1024;  // barriers + slots, alignment slack
+  static constexpr int LK = FP8 ? PK * DK : 0, LV = FP8 ? PK * DV : 0;
+  static constexpr int NLK = FP8 ? (DK == 256 ? 2 : 4) : 0, NLV = NLK;
   static constexpr int NK_FIT = (BUDGET / 2) / KT;
-  static constexpr int NK = NK_FIT < PNS_MAX ? NK_FIT : PNS_MAX;
+  static constexpr int NK = FP8 ? (DK == 256 ? 3 : 4) : (NK_FIT < PNS_MAX ? NK_FIT : PNS_MAX);
   static constexpr int NV_FIT = (BUDGET - NK * KT) / VT;
-  static constexpr int NV = NV_FIT < PNS_MAX ? NV_FIT : PNS_MAX;
+  static constexpr int NV = FP8 ? (DK == 256 ? 2 : 6) : (NV_FIT < PNS_MAX ? NV_FIT : PNS_MAX);
   static constexpr int QS = (KCH * PQCH + KT - 1) / KT;  // K slots the query lap covers (2)
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + NK * KT;
-  static constexpr int OFF_BAR = OFF_V + NV * VT;
-  static constexpr int SMEM = OFF_BAR + 512 + 1024;
+  static constexpr int OFF_LK = OFF_V + NV * VT;
+  static constexpr int OFF_LV = OFF_LK + NLK * LK;
+  static constexpr int OFF_BAR = OFF_LV + NLV * LV;
+  static constexpr int SMEM = OFF_BAR + 1024 + 1024;
   // Tensor Memory: two S buffers (columns 0 and PK; P is written over the first PK / 2
   // columns of its own S), O (2 PK), Q (2 PK + DV, DK / 2 columns)
   static constexpr int OCOL = 2 * PK, QCOL = 2 * PK + DV;
   static constexpr int TMEM_COLS = 512;
   static_assert(DK % 64 == 0 && DV % 64 == 0 && DV <= 256, "widths");
+  static_assert(!FP8 || (DK == DV && (DK == 128 || DK == 256)), "FP8 widths");
   static_assert(QCOL + DK / 2 <= TMEM_COLS, "tensor memory");
   static_assert(NK >= 3 && NV >= 2 && QS < NK && OFF_V % 1024 == 0 && KT % 1024 == 0, "rings");
   static_assert(SMEM <= 232448, "shared memory");
@@ -89,8 +97,10 @@ struct PfCfg {
 // barriers
 enum { F_QREADY = 0, F_KFULL = 1, F_KEMPTY = F_KFULL + PNS_MAX, F_VFULL = F_KEMPTY + PNS_MAX,
        F_VEMPTY = F_VFULL + PNS_MAX, F_SFULL = F_VEMPTY + PNS_MAX, F_PFULL = F_SFULL + 2, F_PVDONE = F_PFULL + 2,
-       F_OFINAL = F_PVDONE + 2, F_FIN = F_OFINAL + 1, F_TEST = F_FIN + 1, F_COUNT = F_TEST + 1 };
-static_assert(F_COUNT * 8 + 8 <= 512, "barrier region");
+       F_OFINAL = F_PVDONE + 2, F_FIN = F_OFINAL + 1, F_TEST = F_FIN + 1,
+       F_LKFULL = F_TEST + 1, F_LKEMPTY = F_LKFULL + PNS_MAX, F_LVFULL = F_LKEMPTY + PNS_MAX,
+       F_LVEMPTY = F_LVFULL + PNS_MAX, F_COUNT = F_LVEMPTY + PNS_MAX };
+static_assert(F_COUNT * 8 + 8 <= 1024, "barrier region");
 constexpr int kPBarQ = 1;  // named barrier of the four softmax warps
 constexpr unsigned long long kPTestWaitNs = 1000000ull;  // forced-timeout test: 1 ms
 
@@ -108,7 +118,8 @@ struct PfParams {
   float* ws_lse;      // and their LSEs [rows][nsplit] / [grid][PM]
   int balanced;       // nonzero: the device-planned balanced split over a 1-D grid
   int* meta;          // balanced: [work items][2] {first record, count}
-  float scale_log2;
+  float scale_log2;  // softmax scale x log2(e) (FP8: x k_scale)
+  float v_scale;     // FP8: dequantisation scale of V (1 for bf16)
   unsigned* err;
   unsigned long long wait_ns;
   int test_timeout;  // nonzero: the first softmax wait also waits on a barrier nothing signals
@@ -182,11 +193,34 @@ __device__ PfPiece pf_piece(const PfParams& p) {
   return w;
 }
 
-template <int DK, int DV>
-__global__ void __launch_bounds__(PTHREADS, 1)
+// Widen one landed tile of 64 rows x W E4M3 bytes ([row][W]) to f16 in the chunk-major,
+// 128-byte swizzled layout of the K / V rings ([W/64 chunks][64 rows][64 values]); the
+// lanes of one warp share the work, 16 bytes (16 values) each.
+template <int W>
+__device__ __forceinline__ void widen_e4m3_tile(const uint8_t* land, uint8_t* dst, int lane) {
+  constexpr int UPR = W / 16;  // 16-byte units of a landed row
+#pragma unroll 4
+  for (int idx = lane; idx < PK * UPR; idx += 32) {
+    const int row = idx / UPR, v = idx % UPR;
+    const uint4 x = *reinterpret_cast<const uint4*>(land + row * W + v * 16);
+    uint32_t lo[4], hi[4];
+    e4m3x4_to_f16x2x2(x.x, lo[0], hi[0]);
+    e4m3x4_to_f16x2x2(x.y, lo[1], hi[1]);
+    e4m3x4_to_f16x2x2(x.z, lo[2], hi[2]);
+    e4m3x4_to_f16x2x2(x.w, lo[3], hi[3]);
+    // values 16v .. 16v+15: chunk v / 4, 16-byte units 2 (v % 4) and the next
+    const int u0 = (v & 3) * 2;
+    uint8_t* rowp = dst + (v >> 2) * PCH + row * 128;
+    *reinterpret_cast<uint4*>(rowp + ((u0 ^ (row & 7)) << 4)) = make_uint4(lo[0], hi[0], lo[1], hi[1]);
+    *reinterpret_cast<uint4*>(rowp + (((u0 + 1) ^ (row & 7)) << 4)) = make_uint4(lo[2], hi[2], lo[3], hi[3]);
+  }
+}
+
+template <int DK, int DV, bool FP8>
+__global__ void __launch_bounds__(pf_threads(FP8), 1)
     gqa_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, PfParams p) {
-  using C = PfCfg<DK, DV>;
+  using C = PfCfg<DK, DV, FP8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // the 128-byte swizzle wants 1024-byte aligned tiles: round the base up (slack reserved)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -210,6 +244,14 @@ __global__ void __launch_bounds__(PTHREADS, 1)
       mbar_init(&bars[F_SFULL + i], 1);
       mbar_init(&bars[F_PFULL + i], 4);
       mbar_init(&bars[F_PVDONE + i], 1);
+    }
+    for (int i = 0; i < C::NLK; ++i) {
+      mbar_init(&bars[F_LKFULL + i], 1);
+      mbar_init(&bars[F_LKEMPTY + i], 1);
+    }
+    for (int i = 0; i < C::NLV; ++i) {
+      mbar_init(&bars[F_LVFULL + i], 1);
+      mbar_init(&bars[F_LVEMPTY + i], 1);
     }
     mbar_init(&bars[F_OFINAL], 1);
     mbar_init(&bars[F_FIN], 1);
@@ -278,19 +320,48 @@ __global__ void __launch_bounds__(PTHREADS, 1)
       // TMA engine serves about one box per few hundred cycles per SM whatever its size).
       int last[PNS_MAX];
       for (int i = 0; i < PNS_MAX; ++i) last[i] = i < C::QS ? i : -1;
+      int lastl[PNS_MAX];
+      for (int i = 0; i < PNS_MAX; ++i) lastl[i] = -1;
       for (int t = 0; t < ntiles; ++t) {
-        const int u = C::QS + t, slot = u % C::NK;
-        if (u >= C::NK && !mbar_wait(&bars[F_KEMPTY + slot], ((u / C::NK) - 1) & 1, p.wait_ns, abort_flag)) {
-          if (!*abort_flag) fail();
-          break;
+        if constexpr (FP8) {  // E4M3 bytes [64 rows x DK] into landing slot t % NLK
+          const int ls = t % C::NLK;
+          if (t >= C::NLK && !mbar_wait(&bars[F_LKEMPTY + ls], ((t / C::NLK) - 1) & 1, p.wait_ns, abort_flag)) {
+            if (!*abort_flag) fail();
+            break;
+          }
+          mbar_expect_tx(&bars[F_LKFULL + ls], C::LK);
+          tma_load_3d(sb + C::OFF_LK + ls * C::LK, &tm_k, 0, g, tile_row(t), &bars[F_LKFULL + ls]);
+          lastl[ls] = t;
+          if (t == (ntiles < C::NLK ? ntiles : C::NLK) - 1) {
+            // The widening warp reuses the query lap's slots once the softmax warps have
+            // moved Q, and their barriers then run past the lap's phase: wait for the lap
+            // here (with the first landings already requested), not at teardown.
+            bool qok = true;
+            for (int i = 0; i < C::QS; ++i) qok = qok && mbar_wait(&bars[F_KFULL + i], 0, p.wait_ns, abort_flag);
+            if (!qok) {
+              if (!*abort_flag) fail();
+              break;
+            }
+            for (int i = 0; i < C::QS; ++i) last[i] = -1;
+          }
+        } else {
+          const int u = C::QS + t, slot = u % C::NK;
+          if (u >= C::NK && !mbar_wait(&bars[F_KEMPTY + slot], ((u / C::NK) - 1) & 1, p.wait_ns, abort_flag)) {
+            if (!*abort_flag) fail();
+            break;
+          }
+          mbar_expect_tx(&bars[F_KFULL + slot], C::KT);
+          tma_load_4d(sb + C::OFF_K + slot * C::KT, &tm_k, 0, tile_row(t), 0, g, &bars[F_KFULL + slot]);
+          last[slot] = u;
         }
-        mbar_expect_tx(&bars[F_KFULL + slot], C::KT);
-        tma_load_4d(sb + C::OFF_K + slot * C::KT, &tm_k, 0, tile_row(t), 0, g, &bars[F_KFULL + slot]);
-        last[slot] = u;
       }
-      // leave no copy in flight
+      // leave no copy in flight (FP8: the query lap's slots here, the landings below)
       for (int i = 0; i < C::NK; ++i)
         if (last[i] >= 0) mbar_wait(&bars[F_KFULL + i], (last[i] / C::NK) & 1, kPTeardownNs, nullptr);
+      if constexpr (FP8) {
+        for (int i = 0; i < C::NLK; ++i)
+          if (lastl[i] >= 0) mbar_wait(&bars[F_LKFULL + i], (lastl[i] / C::NLK) & 1, kPTeardownNs, nullptr);
+      }
     }
     __syncwarp();
   } else if (warp == kPWarpV) {
@@ -298,25 +369,65 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     if (ntiles > 0 && elect_one()) {
       int last[PNS_MAX];
       for (int i = 0; i < PNS_MAX; ++i) last[i] = -1;
+      constexpr int NR = FP8 ? C::NLV : C::NV;  // FP8: V lands in its own ring first
       for (int t = 0; t < ntiles; ++t) {
-        const int slot = t % C::NV;
-        if (t >= C::NV && !mbar_wait(&bars[F_VEMPTY + slot], ((t / C::NV) - 1) & 1, p.wait_ns, abort_flag)) {
+        const int slot = t % NR;
+        uint64_t* full = &bars[(FP8 ? F_LVFULL : F_VFULL) + slot];
+        if (t >= NR && !mbar_wait(&bars[(FP8 ? F_LVEMPTY : F_VEMPTY) + slot], ((t / NR) - 1) & 1, p.wait_ns, abort_flag)) {
           if (!*abort_flag) fail();
           break;
         }
-        mbar_expect_tx(&bars[F_VFULL + slot], C::VT);
-        tma_load_4d(sb + C::OFF_V + slot * C::VT, &tm_v, 0, tile_row(t), 0, g, &bars[F_VFULL + slot]);
+        if constexpr (FP8) {
+          mbar_expect_tx(full, C::LV);
+          tma_load_3d(sb + C::OFF_LV + slot * C::LV, &tm_v, 0, g, tile_row(t), full);
+        } else {
+          mbar_expect_tx(full, C::VT);
+          tma_load_4d(sb + C::OFF_V + slot * C::VT, &tm_v, 0, tile_row(t), 0, g, full);
+        }
         last[slot] = t;
       }
-      for (int i = 0; i < C::NV; ++i)
-        if (last[i] >= 0) mbar_wait(&bars[F_VFULL + i], (last[i] / C::NV) & 1, kPTeardownNs, nullptr);
+      for (int i = 0; i < NR; ++i)
+        if (last[i] >= 0) mbar_wait(&bars[(FP8 ? F_LVFULL : F_VFULL) + i], (last[i] / NR) & 1, kPTeardownNs, nullptr);
     }
     __syncwarp();
+  } else if (warp == kPWarpCK || warp == kPWarpCV) {  // FP8 instances only (bf16 has 7 warps)
+    // ------------------------------------------------ widen landed E4M3 tiles to f16 (K: warp 7, V: warp 8)
+    // K tile t goes to K-ring position QS + t (after the query lap), V tile t to V-ring
+    // slot t % NV; a ring slot is taken once the MMA that read it last has completed, and
+    // the landing slot is released once its bytes have been read.
+    if constexpr (FP8) {
+    const bool isk = warp == kPWarpCK;
+    const int NL = isk ? C::NLK : C::NLV;
+    bool ok = true;
+    for (int t = 0; ok && t < ntiles; ++t) {
+      const int ls = t % NL;
+      const int u = isk ? C::QS + t : t;
+      const int NR = isk ? C::NK : C::NV;
+      const int rs = u % NR;
+      if (!pf_wait(&bars[(isk ? F_LKFULL : F_LVFULL) + ls], (t / NL) & 1, p.wait_ns, abort_flag) ||
+          (u >= NR && !pf_wait(&bars[(isk ? F_KEMPTY : F_VEMPTY) + rs], ((u / NR) - 1) & 1, p.wait_ns, abort_flag))) {
+        ok = false;
+        break;
+      }
+      if (isk)
+        widen_e4m3_tile<DK>(smem + C::OFF_LK + ls * C::LK, smem + C::OFF_K + rs * C::KT, lane);
+      else
+        widen_e4m3_tile<DV>(smem + C::OFF_LV + ls * C::LV, smem + C::OFF_V + rs * C::VT, lane);
+      fence_proxy_async_smem();  // the MMAs and the next landing copy (async proxy) come after these accesses
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars[(isk ? F_KFULL : F_VFULL) + rs]);
+        mbar_arrive(&bars[(isk ? F_LKEMPTY : F_LVEMPTY) + ls]);
+      }
+    }
+    if (!ok && lane == 0 && !*abort_flag) fail();
+    }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer (the whole warp waits; one lane issues)
     const bool leader = elect_one();
-    constexpr uint32_t idS = idesc_bf16_f32(PM, PK, false, false);  // B = K rows, K-major
-    constexpr uint32_t idO = idesc_bf16_f32(PM, DV, false, true);   // B = V rows, N-major
+    // bf16 operands, or f16 (FP8 cache widened exactly to f16; Q and P in f16 too)
+    constexpr uint32_t idS = FP8 ? idesc_f16_f32(PM, PK, false, false) : idesc_bf16_f32(PM, PK, false, false);
+    constexpr uint32_t idO = FP8 ? idesc_f16_f32(PM, DV, false, true) : idesc_bf16_f32(PM, DV, false, true);
     const uint64_t dk = smem_desc(sb + C::OFF_K, 16, 1024, kSw128);
     const uint64_t dv = smem_desc(sb + C::OFF_V, PCH, 1024, kSw128);  // chunk stride 8 KB
     bool ok = ntiles == 0 || pf_wait(&bars[F_QREADY], 0, p.wait_ns, abort_flag);
@@ -411,6 +522,10 @@ __global__ void __launch_bounds__(PTHREADS, 1)
             v[4 * u + 2] = x.z;
             v[4 * u + 3] = x.w;
           }
+          if constexpr (FP8) {  // f16 queries for the f16 MMAs (range 2^-14 .. 65504)
+#pragma unroll
+            for (int c = 0; c < 32; ++c) v[c] = pack_f16(bf16_lo(v[c]), bf16_hi(v[c]));
+          }
           tmem_st32(t_lane + C::QCOL + j * 32, v);
         }
         tmem_st_wait();
@@ -488,7 +603,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
       for (int e = 0; e < PK / 2; ++e) {
         const float p0 = fast_exp2(x[2 * e] + mneg), p1 = fast_exp2(x[2 * e + 1] + mneg);
         ps += p0 + p1;
-        pk[e] = pack_bf16(p0, p1);
+        pk[e] = FP8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
       }
       l_run += ps;
       // P row r into Tensor Memory over the first PK / 2 columns of its own S buffer (the A
@@ -509,7 +624,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
       float* part_o = nullptr;
       float* part_l = nullptr;
       tc_fence_after();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const float inv = l_run > 0.f ? p.v_scale / l_run : 0.f;  // FP8: V's dequantisation scale too
       const float lse_val = l_run > 0.f ? (m_ref + log2f(l_run)) * kPLn2 : -INFINITY;
       const int j = g * p.G + rg / p.s;
       const size_t rowflat = ((size_t)bi * p.hq + j) * p.s + tok;
@@ -573,15 +688,16 @@ __global__ void __launch_bounds__(PTHREADS, 1)
 
 }  // namespace
 
-bool gqa_prefill_supported(int dk, int dv) {
+bool gqa_prefill_supported(int dk, int dv, bool fp8) {
+  if (fp8) return dk == dv && (dk == 128 || dk == 256);
   return (dv == 128 && (dk == 128 || dk == 192)) || (dk == 256 && dv == 256);
 }
 
-template <int DK, int DV>
+template <int DK, int DV, bool FP8>
 static cudaError_t launch_pf(const GqaLaunch& a, cudaStream_t stream) {
-  using C = PfCfg<DK, DV>;
+  using C = PfCfg<DK, DV, FP8>;
   static std::atomic<unsigned long long> smem_limit_set{0};
-  if (cudaError_t e = ensure_smem_limit(gqa_prefill_kernel<DK, DV>, C::SMEM, smem_limit_set)) return e;
+  if (cudaError_t e = ensure_smem_limit(gqa_prefill_kernel<DK, DV, FP8>, C::SMEM, smem_limit_set)) return e;
   CUtensorMap tq, tk, tv;
   {  // queries as [b*Hq*s rows, DK]: boxes [128 rows x 64 values]
     const cuuint64_t dims[2] = {(cuuint64_t)DK, (cuuint64_t)a.b * a.hq * a.s};
@@ -589,10 +705,22 @@ static cudaError_t launch_pf(const GqaLaunch& a, cudaStream_t stream) {
     const cuuint32_t box[2] = {64, PM};
     if (!encode_tmap_bf16_sw128(&tq, a.q, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  {  // K and V [tokens, KV heads, width] viewed as {64 values, tokens, width / 64 chunks, KV
-     // heads} (strides: token hkv*width*2 B, chunk 128 B, head width*2 B): a box {64, 64
-     // tokens, all chunks, 1 head} lands chunk-major, each 128-byte row swizzled
-    const uint64_t tokens = a.paged ? (uint64_t)a.num_pages * PK : (uint64_t)a.b * a.capacity;
+  const uint64_t tokens = a.paged ? (uint64_t)a.num_pages * PK : (uint64_t)a.b * a.capacity;
+  if constexpr (FP8) {
+    // E4M3 K and V [tokens, KV heads, width] bytes: a box {width, 1 head, 64 tokens} lands
+    // as [64 rows][width bytes], unswizzled (the widening warps read it row by row)
+    const cuuint32_t kbox[3] = {(cuuint32_t)DK, 1, PK};
+    const cuuint32_t vbox[3] = {(cuuint32_t)DV, 1, PK};
+    const cuuint64_t kdims[3] = {(cuuint64_t)DK, (cuuint64_t)a.hkv, (cuuint64_t)tokens};
+    const cuuint64_t kstrides[2] = {(cuuint64_t)DK, (cuuint64_t)a.hkv * DK};
+    const cuuint64_t vdims[3] = {(cuuint64_t)DV, (cuuint64_t)a.hkv, (cuuint64_t)tokens};
+    const cuuint64_t vstrides[2] = {(cuuint64_t)DV, (cuuint64_t)a.hkv * DV};
+    if (!encode_tmap_u8(&tk, a.k, 3, kdims, kstrides, kbox) || !encode_tmap_u8(&tv, a.v, 3, vdims, vstrides, vbox))
+      return cudaErrorInvalidValue;
+  } else {
+    // K and V [tokens, KV heads, width] viewed as {64 values, tokens, width / 64 chunks, KV
+    // heads} (strides: token hkv*width*2 B, chunk 128 B, head width*2 B): a box {64, 64
+    // tokens, all chunks, 1 head} lands chunk-major, each 128-byte row swizzled
     const cuuint32_t kbox[4] = {64, PK, (cuuint32_t)C::KCH, 1};
     const cuuint32_t vbox[4] = {64, PK, (cuuint32_t)C::VCH, 1};
     const cuuint64_t kdims[4] = {64, (cuuint64_t)tokens, (cuuint64_t)C::KCH, (cuuint64_t)a.hkv};
@@ -626,13 +754,14 @@ static cudaError_t launch_pf(const GqaLaunch& a, cudaStream_t stream) {
   p.ws_lse = a.ws_lse;
   p.balanced = a.balanced_grid > 0 ? 1 : 0;
   p.meta = a.meta;
-  p.scale_log2 = a.scale * kPLog2e;
+  p.scale_log2 = a.scale * (FP8 ? a.k_scale : 1.f) * kPLog2e;
+  p.v_scale = FP8 ? a.v_scale : 1.f;
   p.err = a.err;
   p.wait_ns = a.wait_ns;
   p.test_timeout = a.test_timeout;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = p.balanced ? dim3(a.balanced_grid) : dim3(p.nrb * p.nsplit, a.hkv, a.b);
-  cfg.blockDim = dim3(PTHREADS);
+  cfg.blockDim = dim3(pf_threads(FP8));
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -640,14 +769,19 @@ static cudaError_t launch_pf(const GqaLaunch& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gqa_prefill_kernel<DK, DV>, tq, tk, tv, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gqa_prefill_kernel<DK, DV, FP8>, tq, tk, tv, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_gqa_prefill(const GqaLaunch& a, cudaStream_t stream) {
-  if (a.dk == 192 && a.dv == 128) return launch_pf<192, 128>(a, stream);
-  if (a.dk == 128 && a.dv == 128) return launch_pf<128, 128>(a, stream);
-  if (a.dk == 256 && a.dv == 256) return launch_pf<256, 256>(a, stream);
+  if (a.fp8) {
+    if (a.dk == 128 && a.dv == 128) return launch_pf<128, 128, true>(a, stream);
+    if (a.dk == 256 && a.dv == 256) return launch_pf<256, 256, true>(a, stream);
+    return cudaErrorInvalidValue;
+  }
+  if (a.dk == 192 && a.dv == 128) return launch_pf<192, 128, false>(a, stream);
+  if (a.dk == 128 && a.dv == 128) return launch_pf<128, 128, false>(a, stream);
+  if (a.dk == 256 && a.dv == 256) return launch_pf<256, 256, false>(a, stream);
   return cudaErrorInvalidValue;
 }
 

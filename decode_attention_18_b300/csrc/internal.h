@@ -40,7 +40,7 @@ bool gqa_supported(int dk, int dv, bool fp8);
 cudaError_t launch_gqa(const GqaLaunch& p, cudaStream_t stream);
 // tensor-core grouped-head kernel for KV heads with many query rows (no split: one CTA
 // per 128 query rows of a KV head, every key in one pass)
-bool gqa_prefill_supported(int dk, int dv);
+bool gqa_prefill_supported(int dk, int dv, bool fp8);
 cudaError_t launch_gqa_prefill(const GqaLaunch& p, cudaStream_t stream);
 
 // log-sum-exp merge of split partials: rows x nsplit partials of width d (fp32, or bf16

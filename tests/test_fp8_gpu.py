@@ -1,6 +1,7 @@
 """Parity of grouped-head decode over an FP8 (E4M3) cache against the fp64
 oracle (oracle.gqa_fp8_ref: gqa_ref on k_scale * K8 and v_scale * V8), through
-the C ABI. The kernel widens each cache tile to bf16 exactly, so the usual
+the C ABI. Both kernels widen each cache tile exactly (to f16 for 128- and
+256-wide rows, where the MMAs run in f16; to bf16 at d = 64), so the usual
 output and LSE tolerances apply. The checker reads the cache bytes itself (a
 paged pool through the oracle's gather_paged)."""
 import math
@@ -40,6 +41,9 @@ def byte_rows(t, cache, i, kv_head=None):
     L = cache.seqlens[i]
     if not cache.paged:
         x = t[i, :L]
+        return (x if kv_head is None else x[:, kv_head:kv_head + 1]).cpu().numpy()
+    if L == 0:  # an empty sequence owns no page
+        x = t[0, :0]
         return (x if kv_head is None else x[:, kv_head:kv_head + 1]).cpu().numpy()
     table = cache.block_table[i].cpu().numpy()
     n = (L + 63) // 64
@@ -157,3 +161,51 @@ def test_fp8_full_size_gqa_64_8_sampled():
         ro, rl = A.gqa_fp8_ref(f64(q[i:i + 1, heads]), [k8], [v8], [4096], 1 / math.sqrt(128), ks, vs)
         assert_out_close(f64(out[i:i + 1, heads]), ro, f"seq {i} kv head {g}")
         assert_lse_close(f64(lse[i:i + 1, heads]), rl, f"seq {i} kv head {g} lse")
+
+
+@pytest.mark.parametrize("hq,hkv,d,s,seqlens,paged,nsplit", [
+    (24, 1, 256, 1, [1500, 333, 0, 64], True, 0),   # ragged MQA with an empty sequence: balanced pieces
+    (16, 2, 128, 4, [700, 65], False, 0),           # 32 rows per KV head, causal s = 4
+    (8, 8, 128, 16, [300, 129], True, 0),           # 16 rows per KV head, paged
+    (24, 1, 256, 1, [1000, 700], False, 3),         # forced chunks: fixed split and its combine
+])
+def test_fp8_tensor_core_kernel(hq, hkv, d, s, seqlens, paged, nsplit):
+    # the tensor-core kernel over an FP8 cache: E4M3 tiles land by TMA, two warps widen
+    # them to f16, and the score and P V MMAs run in f16
+    import decode_attention_18_b300 as da
+
+    b = len(seqlens)
+    q, cache, ks, vs = make(b, hq, hkv, d, s, seqlens, paged=paged, seed=7 + d + s)
+    da.set_grouped_kernel(2)
+    da.set_forced_splits(nsplit)
+    try:
+        out, lse = run(q, cache, ks, vs, seqlens, d)
+    finally:
+        da.set_grouped_kernel(0)
+        da.set_forced_splits(0)
+    check(q, cache, ks, vs, out, lse, seqlens, d, f"fp8 tensor-core hq{hq} hkv{hkv} d{d} s{s} n{nsplit}")
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_fp8_tensor_core_nan_past_the_end(paged):
+    # E4M3 NaN bytes (0x7f) in every cache row past each sequence's end: never read into a result
+    import decode_attention_18_b300 as da
+
+    seqlens = [333, 130]
+    q, cache, ks, vs = make(2, 24, 1, 256, 1, seqlens, paged=paged, seed=31)
+    for t in (cache.k, cache.v):
+        for i, L in enumerate(seqlens):
+            if paged:
+                n = (L + 63) // 64
+                last = int(cache.block_table[i, n - 1])
+                if L % 64:
+                    t[last, L % 64:] = 0x7F
+            else:
+                t[i, L:] = 0x7F
+    da.set_grouped_kernel(2)
+    try:
+        out, lse = run(q, cache, ks, vs, seqlens, 256)
+    finally:
+        da.set_grouped_kernel(0)
+    assert torch.isfinite(out.float()).all()
+    check(q, cache, ks, vs, out, lse, seqlens, 256, f"fp8 tensor-core poisoned paged={paged}")

@@ -218,8 +218,9 @@ namespace {
 // Automatic choice, from same-box graph-replay measurements of both kernels (rows R =
 // query rows per KV head): 192 / 128 (expanded MLA) from R = 1 up (s = 1: 1723 vs 1742 us,
 // s = 16: 1747 vs 1925, s = 128: 1747 vs 8632); 256 / 256 from R = 24 (ragged paged MQA:
-// 54 vs 60 us; R = 48: 51 vs 76); 128 / 128 from R = 32 (R = 16: 123 vs 86 us; R = 32:
-// 121 vs 133). Below those the split-KV mma.sync kernel's 16-row tiles waste less.
+// 54 vs 60 us; R = 48: 51 vs 76; over an FP8 cache 45 vs 64 us, and at R = 6 144 vs 127);
+// 128 / 128 from R = 32 (R = 16: 123 vs 86 us; R = 32: 121 vs 133). Below those the
+// split-KV mma.sync kernel's 16-row tiles waste less.
 bool use_prefill(int b, int hq, int hkv, int s, int dk, int dv, bool fp8, int sms) {
   (void)b;
   (void)sms;
@@ -227,10 +228,6 @@ bool use_prefill(int b, int hq, int hkv, int s, int dk, int dv, bool fp8, int sm
   const int mode = g_grouped_kernel.load();
   if (mode == 1) return false;
   if (mode == 2) return true;
-  // an FP8 cache stays on the split-KV kernel, which widens in registers: the tensor-core
-  // kernel widens into shared memory, which halves the bytes it can keep in flight
-  // (ragged paged MQA: 67.2 against 63.7 us)
-  if (fp8) return false;
   const long long rows = (long long)(hq / hkv) * s;
   if (dk == 192) return true;
   return rows >= (dk == 256 ? 24 : 32);

@@ -52,10 +52,10 @@ constexpr int PK = 64;           // keys per tile (S MMA N)
 constexpr int PNS_MAX = 8;       // slots of either ring at most
 constexpr int PCH = PK * 128;    // one [64 keys x 64 values] bf16 chunk, 128-byte rows
 constexpr int PQCH = PM * 128;   // one [128 rows x 64 values] chunk of Q or P
-// warp 0 K (and Q) loads, 1 MMA, 2-5 softmax / epilogue, 6 V loads; FP8: 7 and 8 widen the
-// landed K and V bytes to f16
-constexpr int kPWarpV = 6, kPWarpCK = 7, kPWarpCV = 8;
-__host__ __device__ constexpr int pf_threads(bool fp8) { return fp8 ? 288 : 224; }
+// warp 0 K (and Q) loads, 1 MMA, 2-5 softmax / epilogue, 6 V loads; FP8: warps 7-10 widen
+// the landed K bytes to f16, warps 11-14 the V bytes
+constexpr int kPWarpV = 6, kPWarpC0 = 7, kPNCW = 4;
+__host__ __device__ constexpr int pf_threads(bool fp8) { return fp8 ? 32 * (7 + 2 * kPNCW) : 224; }
 constexpr float kPLog2e = 1.4426950408889634f;
 constexpr float kPLn2 = 0.6931471805599453f;
 constexpr float kPRescale = 8.f;
@@ -70,13 +70,17 @@ struct PfCfg {
   // takes its first two slots), the rest to V. FP8: E4M3 tiles land by TMA in rings of
   // their own (LK / LV bytes a tile) and are widened to f16 into the K and V rings.
   static constexpr int BUDGET = 232448 - 1024 - 1024;  // barriers + slots, alignment slack
+  // FP8: the query lap lands in the V ring (free until the first P V), so the K ring is
+  // two or three slots and the landing rings take the rest.
   static constexpr int LK = FP8 ? PK * DK : 0, LV = FP8 ? PK * DV : 0;
-  static constexpr int NLK = FP8 ? (DK == 256 ? 2 : 4) : 0, NLV = NLK;
+  static constexpr int NLK = FP8 ? (DK == 256 ? 3 : 7) : 0, NLV = NLK;
   static constexpr int NK_FIT = (BUDGET / 2) / KT;
-  static constexpr int NK = FP8 ? (DK == 256 ? 3 : 4) : (NK_FIT < PNS_MAX ? NK_FIT : PNS_MAX);
+  static constexpr int NK = FP8 ? (DK == 256 ? 2 : 3) : (NK_FIT < PNS_MAX ? NK_FIT : PNS_MAX);
   static constexpr int NV_FIT = (BUDGET - NK * KT) / VT;
-  static constexpr int NV = FP8 ? (DK == 256 ? 2 : 6) : (NV_FIT < PNS_MAX ? NV_FIT : PNS_MAX);
-  static constexpr int QS = (KCH * PQCH + KT - 1) / KT;  // K slots the query lap covers (2)
+  static constexpr int NV = FP8 ? (DK == 256 ? 2 : 4) : (NV_FIT < PNS_MAX ? NV_FIT : PNS_MAX);
+  static constexpr int QBYTES = KCH * PQCH;                      // Q [128 rows x DK] bf16
+  static constexpr int QS = FP8 ? 0 : (QBYTES + KT - 1) / KT;    // K slots the query lap covers
+  static constexpr int QSV = FP8 ? (QBYTES + VT - 1) / VT : 0;   // V slots the query lap covers
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + NK * KT;
   static constexpr int OFF_LK = OFF_V + NV * VT;
@@ -90,7 +94,9 @@ struct PfCfg {
   static_assert(DK % 64 == 0 && DV % 64 == 0 && DV <= 256, "widths");
   static_assert(!FP8 || (DK == DV && (DK == 128 || DK == 256)), "FP8 widths");
   static_assert(QCOL + DK / 2 <= TMEM_COLS, "tensor memory");
-  static_assert(NK >= 3 && NV >= 2 && QS < NK && OFF_V % 1024 == 0 && KT % 1024 == 0, "rings");
+  static_assert(NK >= 2 && NV >= 2 && QS < NK && QSV <= NV && QBYTES <= (FP8 ? NV * VT : NK * KT) &&
+                    OFF_V % 1024 == 0 && KT % 1024 == 0,
+                "rings");
   static_assert(SMEM <= 232448, "shared memory");
 };
 
@@ -99,7 +105,7 @@ enum { F_QREADY = 0, F_KFULL = 1, F_KEMPTY = F_KFULL + PNS_MAX, F_VFULL = F_KEMP
        F_VEMPTY = F_VFULL + PNS_MAX, F_SFULL = F_VEMPTY + PNS_MAX, F_PFULL = F_SFULL + 2, F_PVDONE = F_PFULL + 2,
        F_OFINAL = F_PVDONE + 2, F_FIN = F_OFINAL + 1, F_TEST = F_FIN + 1,
        F_LKFULL = F_TEST + 1, F_LKEMPTY = F_LKFULL + PNS_MAX, F_LVFULL = F_LKEMPTY + PNS_MAX,
-       F_LVEMPTY = F_LVFULL + PNS_MAX, F_COUNT = F_LVEMPTY + PNS_MAX };
+       F_LVEMPTY = F_LVFULL + PNS_MAX, F_QLAND = F_LVEMPTY + PNS_MAX, F_COUNT = F_QLAND + 1 };
 static_assert(F_COUNT * 8 + 8 <= 1024, "barrier region");
 constexpr int kPBarQ = 1;  // named barrier of the four softmax warps
 constexpr unsigned long long kPTestWaitNs = 1000000ull;  // forced-timeout test: 1 ms
@@ -195,12 +201,12 @@ __device__ PfPiece pf_piece(const PfParams& p) {
 
 // Widen one landed tile of 64 rows x W E4M3 bytes ([row][W]) to f16 in the chunk-major,
 // 128-byte swizzled layout of the K / V rings ([W/64 chunks][64 rows][64 values]); the
-// lanes of one warp share the work, 16 bytes (16 values) each.
+// threads of one group of kPNCW warps share the work, 16 bytes (16 values) each.
 template <int W>
-__device__ __forceinline__ void widen_e4m3_tile(const uint8_t* land, uint8_t* dst, int lane) {
+__device__ __forceinline__ void widen_e4m3_tile(const uint8_t* land, uint8_t* dst, int tid) {
   constexpr int UPR = W / 16;  // 16-byte units of a landed row
 #pragma unroll 4
-  for (int idx = lane; idx < PK * UPR; idx += 32) {
+  for (int idx = tid; idx < PK * UPR; idx += 32 * kPNCW) {
     const int row = idx / UPR, v = idx % UPR;
     const uint4 x = *reinterpret_cast<const uint4*>(land + row * W + v * 16);
     uint32_t lo[4], hi[4];
@@ -232,12 +238,15 @@ __global__ void __launch_bounds__(pf_threads(FP8), 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars[F_QREADY], 1);
+    mbar_init(&bars[F_QLAND], 1);
+    // FP8: the K / V rings are filled by the widening warps (one arrival each), the
+    // landing rings emptied by them
     for (int i = 0; i < C::NK; ++i) {
-      mbar_init(&bars[F_KFULL + i], 1);
+      mbar_init(&bars[F_KFULL + i], FP8 ? kPNCW : 1);
       mbar_init(&bars[F_KEMPTY + i], 1);
     }
     for (int i = 0; i < C::NV; ++i) {
-      mbar_init(&bars[F_VFULL + i], 1);
+      mbar_init(&bars[F_VFULL + i], FP8 ? kPNCW : 1);
       mbar_init(&bars[F_VEMPTY + i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -247,11 +256,11 @@ __global__ void __launch_bounds__(pf_threads(FP8), 1)
     }
     for (int i = 0; i < C::NLK; ++i) {
       mbar_init(&bars[F_LKFULL + i], 1);
-      mbar_init(&bars[F_LKEMPTY + i], 1);
+      mbar_init(&bars[F_LKEMPTY + i], kPNCW);
     }
     for (int i = 0; i < C::NLV; ++i) {
       mbar_init(&bars[F_LVFULL + i], 1);
-      mbar_init(&bars[F_LVEMPTY + i], 1);
+      mbar_init(&bars[F_LVEMPTY + i], kPNCW);
     }
     mbar_init(&bars[F_OFINAL], 1);
     mbar_init(&bars[F_FIN], 1);
@@ -304,17 +313,23 @@ __global__ void __launch_bounds__(pf_threads(FP8), 1)
       // the query lap: Q boxes [128 rows x 64] (16 KB each) laid end to end from the K ring's
       // start over its first QS slots; a box completes on the barrier of the slot it starts
       // in, and a slot in which no box starts gets a plain arrival
-      uint32_t qbytes[C::QS];
-      for (int i = 0; i < C::QS; ++i) qbytes[i] = 0;
-      for (int c = 0; c < C::KCH; ++c) qbytes[(c * PQCH) / C::KT] += PQCH;
-      for (int i = 0; i < C::QS; ++i) {
-        if (qbytes[i])
-          mbar_expect_tx(&bars[F_KFULL + i], qbytes[i]);
-        else
-          mbar_arrive(&bars[F_KFULL + i]);
+      if constexpr (FP8) {
+        // FP8: the whole lap completes on its own barrier, in the V ring's first QSV slots
+        mbar_expect_tx(&bars[F_QLAND], C::QBYTES);
+        for (int c = 0; c < C::KCH; ++c) tma_load_2d(sb + C::OFF_V + c * PQCH, &tm_q, c * 64, qrow0, &bars[F_QLAND]);
+      } else {
+        uint32_t qbytes[C::QS > 0 ? C::QS : 1];
+        for (int i = 0; i < C::QS; ++i) qbytes[i] = 0;
+        for (int c = 0; c < C::KCH; ++c) qbytes[(c * PQCH) / C::KT] += PQCH;
+        for (int i = 0; i < C::QS; ++i) {
+          if (qbytes[i])
+            mbar_expect_tx(&bars[F_KFULL + i], qbytes[i]);
+          else
+            mbar_arrive(&bars[F_KFULL + i]);
+        }
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_2d(sb + C::OFF_K + c * PQCH, &tm_q, c * 64, qrow0, &bars[F_KFULL + (c * PQCH) / C::KT]);
       }
-      for (int c = 0; c < C::KCH; ++c)
-        tma_load_2d(sb + C::OFF_K + c * PQCH, &tm_q, c * 64, qrow0, &bars[F_KFULL + (c * PQCH) / C::KT]);
       // K of tile t takes K-ring position u = QS + t: slot u % NK, its (u / NK)-th use. One
       // box per tile ([chunks][64 keys][64 values], chunk-major as the MMAs read it: the
       // TMA engine serves about one box per few hundred cycles per SM whatever its size).
@@ -332,18 +347,6 @@ __global__ void __launch_bounds__(pf_threads(FP8), 1)
           mbar_expect_tx(&bars[F_LKFULL + ls], C::LK);
           tma_load_3d(sb + C::OFF_LK + ls * C::LK, &tm_k, 0, g, tile_row(t), &bars[F_LKFULL + ls]);
           lastl[ls] = t;
-          if (t == (ntiles < C::NLK ? ntiles : C::NLK) - 1) {
-            // The widening warp reuses the query lap's slots once the softmax warps have
-            // moved Q, and their barriers then run past the lap's phase: wait for the lap
-            // here (with the first landings already requested), not at teardown.
-            bool qok = true;
-            for (int i = 0; i < C::QS; ++i) qok = qok && mbar_wait(&bars[F_KFULL + i], 0, p.wait_ns, abort_flag);
-            if (!qok) {
-              if (!*abort_flag) fail();
-              break;
-            }
-            for (int i = 0; i < C::QS; ++i) last[i] = -1;
-          }
         } else {
           const int u = C::QS + t, slot = u % C::NK;
           if (u >= C::NK && !mbar_wait(&bars[F_KEMPTY + slot], ((u / C::NK) - 1) & 1, p.wait_ns, abort_flag)) {
@@ -361,6 +364,7 @@ __global__ void __launch_bounds__(pf_threads(FP8), 1)
       if constexpr (FP8) {
         for (int i = 0; i < C::NLK; ++i)
           if (lastl[i] >= 0) mbar_wait(&bars[F_LKFULL + i], (lastl[i] / C::NLK) & 1, kPTeardownNs, nullptr);
+        mbar_wait(&bars[F_QLAND], 0, kPTeardownNs, nullptr);
       }
     }
     __syncwarp();
@@ -390,18 +394,19 @@ __global__ void __launch_bounds__(pf_threads(FP8), 1)
         if (last[i] >= 0) mbar_wait(&bars[(FP8 ? F_LVFULL : F_VFULL) + i], (last[i] / NR) & 1, kPTeardownNs, nullptr);
     }
     __syncwarp();
-  } else if (warp == kPWarpCK || warp == kPWarpCV) {  // FP8 instances only (bf16 has 7 warps)
-    // ------------------------------------------------ widen landed E4M3 tiles to f16 (K: warp 7, V: warp 8)
+  } else if (warp >= kPWarpC0) {  // FP8 instances only (bf16 has 7 warps)
+    // ------------------------------------------------ widen landed E4M3 tiles to f16 (K: warps 7-10, V: 11-14)
     // K tile t goes to K-ring position QS + t (after the query lap), V tile t to V-ring
     // slot t % NV; a ring slot is taken once the MMA that read it last has completed, and
     // the landing slot is released once its bytes have been read.
     if constexpr (FP8) {
-    const bool isk = warp == kPWarpCK;
+    const bool isk = warp < kPWarpC0 + kPNCW;
+    const int tid = ((warp - kPWarpC0) % kPNCW) * 32 + lane;  // thread within the group
     const int NL = isk ? C::NLK : C::NLV;
     bool ok = true;
     for (int t = 0; ok && t < ntiles; ++t) {
       const int ls = t % NL;
-      const int u = isk ? C::QS + t : t;
+      const int u = isk ? C::QS + t : C::QSV + t;  // ring position after the query lap
       const int NR = isk ? C::NK : C::NV;
       const int rs = u % NR;
       if (!pf_wait(&bars[(isk ? F_LKFULL : F_LVFULL) + ls], (t / NL) & 1, p.wait_ns, abort_flag) ||
@@ -410,9 +415,9 @@ __global__ void __launch_bounds__(pf_threads(FP8), 1)
         break;
       }
       if (isk)
-        widen_e4m3_tile<DK>(smem + C::OFF_LK + ls * C::LK, smem + C::OFF_K + rs * C::KT, lane);
+        widen_e4m3_tile<DK>(smem + C::OFF_LK + ls * C::LK, smem + C::OFF_K + rs * C::KT, tid);
       else
-        widen_e4m3_tile<DV>(smem + C::OFF_LV + ls * C::LV, smem + C::OFF_V + rs * C::VT, lane);
+        widen_e4m3_tile<DV>(smem + C::OFF_LV + ls * C::LV, smem + C::OFF_V + rs * C::VT, tid);
       fence_proxy_async_smem();  // the MMAs and the next landing copy (async proxy) come after these accesses
       __syncwarp();
       if (lane == 0) {
@@ -435,9 +440,14 @@ __global__ void __launch_bounds__(pf_threads(FP8), 1)
     // O += P(u) V(u), P(u) from Tensor Memory (over S buffer u & 1); the tail of the last
     // tile's V rows is zeroed first
     auto o_mma = [&](int u) -> bool {
-      const int pb = u & 1, slot = u % C::NV;
+      // V of tile u sits at V-ring position QSV + u (FP8: the query lap took the first QSV
+      // positions without completing their full barriers, so those slots' completions lag
+      // one lap)
+      const int pv = C::QSV + u;
+      const int pb = u & 1, slot = pv % C::NV;
+      const int vph = (pv / C::NV - (slot < C::QSV ? 1 : 0)) & 1;
       if (!pf_wait(&bars[F_PFULL + pb], (u >> 1) & 1, p.wait_ns, abort_flag) ||
-          !pf_wait(&bars[F_VFULL + slot], (u / C::NV) & 1, p.wait_ns, abort_flag))
+          !pf_wait(&bars[F_VFULL + slot], vph, p.wait_ns, abort_flag))
         return false;
       const int nvalid = kend - (kstart + u * PK);
       if (nvalid < PK) {
@@ -508,11 +518,14 @@ __global__ void __launch_bounds__(pf_threads(FP8), 1)
       // column, even index low); chunk j of the query lap is [128 rows x 64] with 128-byte
       // swizzled rows. Then the query lap's ring slots go back to the producer.
       bool okq = true;
-      for (int i = 0; i < C::QS; ++i) okq = okq && pf_wait(&bars[F_KFULL + i], 0, p.wait_ns, abort_flag);
+      if constexpr (FP8)
+        okq = pf_wait(&bars[F_QLAND], 0, p.wait_ns, abort_flag);
+      else
+        for (int i = 0; i < C::QS; ++i) okq = okq && pf_wait(&bars[F_KFULL + i], 0, p.wait_ns, abort_flag);
       if (okq) {
 #pragma unroll 1
         for (int j = 0; j < C::KCH; ++j) {
-          const uint8_t* bx = smem + C::OFF_K + j * PQCH + r * 128;
+          const uint8_t* bx = smem + (FP8 ? C::OFF_V : C::OFF_K) + j * PQCH + r * 128;
           uint32_t v[32];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
@@ -535,6 +548,7 @@ __global__ void __launch_bounds__(pf_threads(FP8), 1)
       if (threadIdx.x == 64) {
         if (ok) {
           for (int i = 0; i < C::QS; ++i) mbar_arrive(&bars[F_KEMPTY + i]);
+          for (int i = 0; i < C::QSV; ++i) mbar_arrive(&bars[F_VEMPTY + i]);
           mbar_arrive(&bars[F_QREADY]);
         } else if (!*abort_flag) {
           fail();

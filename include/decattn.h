@@ -273,9 +273,8 @@ int gqa_decode_no_alloc(const decattn_bf16* q, const decattn_bf16* k, const deca
  * by a combine kernel) where the widths allow ((dk, dv) in
  * {(128, 128), (192, 128), (256, 256)}). Automatic takes the tensor-core
  * kernel for (dk, dv) = (192, 128) at any row count, for (256, 256) from 24
- * and for (128, 128) from 32 query rows per KV head, over a bf16 cache; an FP8
- * cache stays on the split-KV kernel unless 2 pins the tensor-core kernel's
- * FP8 form (d = 128 or 256). Results agree within rounding.
+ * and for (128, 128) from 32 query rows per KV head, over a bf16 or (d = 128
+ * or 256) an FP8 cache. Results agree within rounding.
  * decattn_test_force_timeout: when nonzero, the next mla_decode and gqa_decode
  * kernels wait once on a barrier that nothing signals, with a 1 ms limit, so that
  * the timeout path runs; the kernels then wind down (no new copies, their own

@@ -56,6 +56,7 @@ struct GqaParams {
 };
 
 constexpr int kTileKeys = 64;
+constexpr int kTileBlk = kTileKeys * 128;  // one [64 keys x 128 bytes] block of a tile (64 bf16 dims or 128 E4M3)
 constexpr int kSlices = 4;  // warps (key slices of 16) per m-tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -88,11 +89,9 @@ struct GqaCfg {
   // FP8 with a work tile: the bf16 tile pair the MMAs read, written from the landed stage
   static constexpr int WORK_OFF = NST * STAGE_BYTES;
   static constexpr int PIPE_BYTES = NST * STAGE_BYTES + ((FP8 && !REG8) ? K_TILE + V_TILE : 0);
-  static constexpr int BLK8 = kTileKeys * 128;  // REG8: one [64 keys x 128 bytes] block of a byte tile
   static constexpr int OSTR = DV + 2;  // padded fp32 row stride of the merge buffer
   static constexpr int RED_BYTES = kSlices * 16 * MT * OSTR * 4;
   static constexpr int SMEM = PIPE_BYTES > RED_BYTES ? PIPE_BYTES : RED_BYTES;
-  static constexpr int BLK = kTileKeys * 128;  // one [64 keys x 64 dims] block of a tile
   static_assert(DK % 64 == 0 && DV % 64 == 0, "tiles are 64-dim blocks");
 };
 
@@ -204,19 +203,19 @@ __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMa
     mbar_expect_tx(&full[stage], C::STAGE_BYTES);
     if constexpr (C::REG8) {  // [64 tokens x 128 bytes] boxes, 128-byte swizzle
 #pragma unroll
-      for (int kb = 0; kb < DK / 128; ++kb) tma_load_3d(kdst + kb * C::BLK8, tm_k, kb * 128, g, row0, &full[stage]);
+      for (int kb = 0; kb < DK / 128; ++kb) tma_load_3d(kdst + kb * kTileBlk, tm_k, kb * 128, g, row0, &full[stage]);
 #pragma unroll
       for (int kb = 0; kb < DV / 128; ++kb)
-        tma_load_3d(kdst + C::K_LOAD + kb * C::BLK8, tm_v, kb * 128, g, row0, &full[stage]);
+        tma_load_3d(kdst + C::K_LOAD + kb * kTileBlk, tm_v, kb * 128, g, row0, &full[stage]);
     } else if constexpr (FP8) {  // one unswizzled box each: [64 tokens x DK bytes], [64 tokens x DV bytes]
       tma_load_3d(kdst, tm_k, 0, g, row0, &full[stage]);
       tma_load_3d(kdst + C::K_LOAD, tm_v, 0, g, row0, &full[stage]);
     } else {
 #pragma unroll
-      for (int kb = 0; kb < DK / 64; ++kb) tma_load_3d(kdst + kb * C::BLK, tm_k, kb * 64, g, row0, &full[stage]);
+      for (int kb = 0; kb < DK / 64; ++kb) tma_load_3d(kdst + kb * kTileBlk, tm_k, kb * 64, g, row0, &full[stage]);
 #pragma unroll
       for (int kb = 0; kb < DV / 64; ++kb)
-        tma_load_3d(kdst + C::K_TILE + kb * C::BLK, tm_v, kb * 64, g, row0, &full[stage]);
+        tma_load_3d(kdst + C::K_TILE + kb * kTileBlk, tm_v, kb * 64, g, row0, &full[stage]);
     }
   };
 

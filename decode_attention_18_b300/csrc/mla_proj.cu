@@ -46,8 +46,11 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) { return (uint32_t)(
 // is BN/64 TMA boxes of [64 k x 64 n] (box-major, 128-byte swizzle); otherwise (narrow
 // outputs) 16-byte cp.async copies with the same swizzle over BN*2-byte rows.
 // Stage t holds k-tile t (t < NST) and then every NST-th one after it; all NST stages
-// are requested before the first is consumed.
-template <int BM, int BN, int NST, bool TMA_W>
+// are requested before the first is consumed. SLAB (TMA_W, every k-tile fits its stage at
+// once): the W stages are one slab [BN/64 chunks][NST*64 k][64 n] requested as boxes of
+// up to 256 k-rows (one box per CTA at BN = 128, two at BN = 64 and 512 rows), since the
+// TMA engine serves about one box per few hundred cycles per SM whatever its size.
+template <int BM, int BN, int NST, bool TMA_W, bool SLAB>
 __global__ void __launch_bounds__(128) proj_kernel(const __grid_constant__ CUtensorMap tm_w, ProjParams p) {
   constexpr int WMW = BM / 32;               // warps along M
   constexpr int WNW = 4 / WMW;               // warps along N
@@ -57,10 +60,14 @@ __global__ void __launch_bounds__(128) proj_kernel(const __grid_constant__ CUten
   constexpr int B_ROW = BN * 2;              // bytes per k row of the W tile
   constexpr int B_BYTES = BK * B_ROW;        // [64 k][BN n]
   constexpr int STAGE = A_BYTES + B_BYTES;
+  // slab boxes: KB k-rows each, NBOX of them
+  constexpr int KB = NST * BK < 256 ? NST * BK : 256;
+  constexpr int NBOX = (NST * BK + KB - 1) / KB;
   static_assert(NTW % 2 == 0 && (BM * 8) % 128 == 0 && (BK * (BN / 8)) % 128 == 0, "tile shape");
   static_assert(!TMA_W || (BN % 64 == 0 && A_BYTES % 1024 == 0 && STAGE % 1024 == 0), "TMA tile shape");
+  static_assert(!SLAB || (TMA_W && (BN == 64 || NBOX == 1) && (NST * BK) % KB == 0), "slab boxes");
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ uint64_t wbar[NST];  // stage's W landed (TMA)
+  __shared__ uint64_t wbar[NST];  // stage's (SLAB: box's) W landed (TMA)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wm = warp / WNW, wn = warp % WNW;
@@ -75,8 +82,10 @@ __global__ void __launch_bounds__(128) proj_kernel(const __grid_constant__ CUten
     return p.a + ((size_t)(bi * p.h + j) * p.s + i) * p.kin;
   };
 
+  // SLAB: A stages [NST][A_BYTES], then the W slab; else stage t = A tile then W tile
+  auto a_base = [&](int stage) -> uint32_t { return SLAB ? sbase + stage * A_BYTES : sbase + stage * STAGE; };
   auto load_a = [&](int kt, int stage) {
-    const uint32_t adst = sbase + stage * STAGE;
+    const uint32_t adst = a_base(stage);
 #pragma unroll
     for (int n = 0; n < (BM * 8) / 128; ++n) {
       const int idx = tid + n * 128;
@@ -89,13 +98,22 @@ __global__ void __launch_bounds__(128) proj_kernel(const __grid_constant__ CUten
   };
   // shared-memory offset of 16-byte chunk c (8 columns) of k-row r of a stage's W tile
   auto w_off = [&](int r, int c) -> uint32_t {
-    if constexpr (TMA_W) return (uint32_t)((c >> 3) * (BK * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+    if constexpr (SLAB) return (uint32_t)((c >> 3) * (NST * BK * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+    else if constexpr (TMA_W) return (uint32_t)((c >> 3) * (BK * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
     else return (uint32_t)(r * B_ROW + swz(r, c) * 16);
   };
   uint32_t wphase = 0;  // parity of each stage's next W completion (TMA_W)
   auto load_w = [&](int kt, int stage) {
     const uint32_t bdst = sbase + stage * STAGE + A_BYTES;
-    if constexpr (TMA_W) {
+    if constexpr (SLAB) {
+      (void)bdst;
+      if (tid == 0 && kt * BK % KB == 0) {  // the box that starts at this k-tile
+        const int bx = kt * BK / KB;
+        mbar_expect_tx(&wbar[bx], KB * BN * 2);
+        tma_load_3d(sbase + NST * A_BYTES + bx * KB * 128, &tm_w, 0, j * p.kin + kt * BK, n0 / 64, &wbar[bx]);
+      }
+      return;
+    } else if constexpr (TMA_W) {
       if (tid == 0) {
         mbar_expect_tx(&wbar[stage], B_BYTES);
         tma_load_3d(bdst, &tm_w, 0, j * p.kin + kt * BK, n0 / 64, &wbar[stage]);
@@ -127,7 +145,7 @@ __global__ void __launch_bounds__(128) proj_kernel(const __grid_constant__ CUten
     }
     if (tid == 0) {
 #pragma unroll
-      for (int i = 0; i < NST; ++i) mbar_init(&wbar[i], 1);
+      for (int i = 0; i < (SLAB ? NBOX : NST); ++i) mbar_init(&wbar[i], 1);
       fence_mbar_init();
       prefetch_tmap(&tm_w);
     }
@@ -152,7 +170,15 @@ __global__ void __launch_bounds__(128) proj_kernel(const __grid_constant__ CUten
     // groups 0 .. kt+1 complete: k-tile t < NST is group t, a later one is group t + 1
     // (the iteration that refills it commits after the empty commit of iteration 0)
     cp_async_wait<NST - 2>();
-    if constexpr (TMA_W) {
+    if constexpr (SLAB) {
+      if (kt * BK % KB == 0) {  // the first k-tile of a box: wait for the box
+        const int bx = kt * BK / KB;
+        if (!mbar_wait(&wbar[bx], 0, p.wait_ns, nullptr)) {
+          w_ok = false;  // recorded below; the box is waited for before the CTA leaves
+          mbar_wait(&wbar[bx], 0, 1000000000ull, nullptr);
+        }
+      }
+    } else if constexpr (TMA_W) {
       const int stage = kt % NST;
       if (!mbar_wait(&wbar[stage], (wphase >> stage) & 1u, p.wait_ns, nullptr)) {
         w_ok = false;  // recorded below; the stage's copy is waited for before the CTA leaves
@@ -166,8 +192,9 @@ __global__ void __launch_bounds__(128) proj_kernel(const __grid_constant__ CUten
       load_w(kt - 1 + NST, (kt - 1) % NST);
     }
     cp_async_commit();  // group NST + kt (k-tile kt - 1 + NST when kt >= 1, else empty)
-    const uint32_t abase = sbase + (kt % NST) * STAGE;
-    const uint32_t bbase = abase + A_BYTES;
+    const uint32_t abase = a_base(kt % NST);
+    // SLAB: the k-tile's 64 rows inside the slab (chunk stride NST*64 rows, see w_off)
+    const uint32_t bbase = SLAB ? sbase + NST * A_BYTES + (kt % NST) * BK * 128 : abase + A_BYTES;
 #pragma unroll
     for (int kk = 0; kk < BK / 16; ++kk) {
       uint32_t af[2][4];
@@ -211,11 +238,11 @@ __global__ void __launch_bounds__(128) proj_kernel(const __grid_constant__ CUten
     }
 }
 
-template <int BM, int BN, int NST, bool TMA_W>
+template <int BM, int BN, int NST, bool TMA_W, bool SLAB = false>
 cudaError_t launch_tile(const ProjParams& p, cudaStream_t stream) {
   constexpr int SMEM = NST * (BM * BK * 2 + BK * BN * 2);
   static std::atomic<unsigned long long> smem_limit_set{0};
-  if (cudaError_t e = ensure_smem_limit(proj_kernel<BM, BN, NST, TMA_W>, SMEM, smem_limit_set)) return e;
+  if (cudaError_t e = ensure_smem_limit(proj_kernel<BM, BN, NST, TMA_W, SLAB>, SMEM, smem_limit_set)) return e;
   // W viewed as [h * kin rows, nout columns] in 64-column chunks: dims {64 columns, rows,
   // nout/64 chunks}, so one box {64, BK, BN/64} lands chunk-major, [chunk][k row][128 B]
   // swizzled. k-rows of a stage past kin read the next head's rows (their A columns are
@@ -224,7 +251,8 @@ cudaError_t launch_tile(const ProjParams& p, cudaStream_t stream) {
   if (TMA_W) {
     const cuuint64_t dims[3] = {64, (cuuint64_t)p.h * p.kin, (cuuint64_t)p.nout / 64};
     const cuuint64_t strides[2] = {(cuuint64_t)p.nout * 2, 128};
-    const cuuint32_t box[3] = {64, BK, BN / 64};
+    constexpr int KB = SLAB ? (NST * BK < 256 ? NST * BK : 256) : BK;
+    const cuuint32_t box[3] = {64, KB, BN / 64};
     if (!encode_tmap_bf16_sw128(&tw, p.w, 3, dims, strides, box)) return cudaErrorInvalidValue;
   } else {
     memset(&tw, 0, sizeof(tw));
@@ -240,7 +268,7 @@ cudaError_t launch_tile(const ProjParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, proj_kernel<BM, BN, NST, TMA_W>, tw, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, proj_kernel<BM, BN, NST, TMA_W, SLAB>, tw, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -273,10 +301,10 @@ cudaError_t launch_proj(const ProjLaunch& a, int num_sms, cudaStream_t stream) {
   // 16-byte aligned and rows are nout*2 bytes, a multiple of 16, as the API checks)
   const bool tma = a.nout % 64 == 0;
   if (p.M <= 32) {
-    if (a.nout >= 256 && kiters <= 2)  // 4 column tiles per head
-      return tma ? launch_tile<32, 128, 2, true>(p, stream) : launch_tile<32, 128, 2, false>(p, stream);
-    if (kiters <= 8)  // every k-stage in flight (96 KB)
-      return tma ? launch_tile<32, 64, 8, true>(p, stream) : launch_tile<32, 64, 8, false>(p, stream);
+    if (a.nout >= 256 && kiters <= 2)  // 4 column tiles per head; the weight slab in one box
+      return tma ? launch_tile<32, 128, 2, true, true>(p, stream) : launch_tile<32, 128, 2, false>(p, stream);
+    if (kiters <= 8)  // every k-stage in flight (96 KB); the weight slab in boxes of 256 rows
+      return tma ? launch_tile<32, 64, 8, true, true>(p, stream) : launch_tile<32, 64, 8, false>(p, stream);
     return tma ? launch_tile<32, 64, 4, true>(p, stream) : launch_tile<32, 64, 4, false>(p, stream);
   }
   if (a.nout >= 128)

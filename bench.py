@@ -54,7 +54,7 @@ def parse():
     ap.add_argument("--profile", default=None, metavar="WORKLOAD",
                     help="profiling mode: run --warmup + --steps calls of one op on one input set of the named "
                          "workload (mla_dsv3, mla_mtp_s8, gqa_64_8, gqa_paged_hkv4, gqa_64_8_fp8, gqa_paged_hkv1_tc ...: _tc pins "
-                         "the tensor-core grouped-head kernel) and exit; "
+                         "the tensor-core grouped-head kernel, _split the split-KV kernels) and exit; "
                          "MLA workloads run whole pipeline steps; prints no "
                          "bench line (numbers taken under a profiler are not bench values)")
     return ap.parse_args()
@@ -621,6 +621,9 @@ def run_profile(args):
     if name.endswith("_tc"):  # grouped-head workload pinned to the tensor-core kernel
         da.set_grouped_kernel(2)
         name = name[:-3]
+    elif name.endswith("_split"):  # grouped-head workload pinned to the split-KV kernels
+        da.set_grouped_kernel(1)
+        name = name[:-6]
     fp8 = name.endswith("_fp8")  # grouped-head workload over an FP8 cache
     wl = W.WORKLOADS[name[:-4] if fp8 else name]
     seqlens = wl.seqlens()

@@ -79,7 +79,6 @@ constexpr int MSG_STRIDE = 34 * 1024;      // 1024-byte aligned message slots
 constexpr int FIN_BYTES = BM * 4;          // [128] float 1/l, sent once at the end
 constexpr int S_NR = 3;                    // S-ring slots (CPI chunks each)
 constexpr int O_NR = 4;                    // O-ring slots
-constexpr int PF = 2;                      // S CTA: L2 prefetch distance in tiles
 constexpr int SB0 = 256;                   // first S buffer column (Qz holds columns 0 .. k/2-1)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -364,37 +363,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // ------------------------------------------------ producer: query tile, then cache chunks
       // The whole warp walks the items (warp-uniform values, block-table entries read by
       // every lane); one lane arms an item's barrier and one lane per box requests it. The
-      // issuing lanes rotate (independent request streams), and tiles PF ahead are
-      // prefetched into L2, which keeps more of the cache stream in flight than the ring
-      // itself can hold.
+      // issuing lanes rotate (independent request streams). No L2 prefetch: its requests
+      // share this SM's TMA queue with the ring's loads and the P copies, and removing
+      // them measured faster (s = 8: 296 -> 270 us; s = 1: 55.0 -> 53.7 us).
       RingPos<S_NR> rp;
       int ic = 0;
       int last[S_NR];
       for (int i = 0; i < S_NR; ++i) last[i] = -1;
       bool ok = true;
-      auto prefetch_tile = [&](int t) {
-        const int key0 = kstart + t * TK;
-        if (t >= ntiles || key0 >= kend) return;
-        if constexpr (PAGED) {
-          const bool two = kend - key0 > HK;
-          const int k = lane;  // box k: chunk k / 2, page k % 2
-          if (k < 2 * C::NCH && (two || (k & 1) == 0)) {
-            const int row = cache_row(p, bi, key0 + (k & 1) * HK);
-            if (k / 2 == C::NBL)
-              tma_prefetch_l2_2d(&tm_kpe, 0, row);
-            else
-              tma_prefetch_l2_2d(&tm_za, (k / 2) * 64, row);
-          }
-        } else {
-          const int row = cache_row(p, bi, key0);
-          if (lane < C::NITEM - 1)
-            tma_prefetch_l2_3d(&tm_za, 0, row, lane * C::CPI);
-          else if (lane == C::NITEM - 1)
-            tma_prefetch_l2_3d(&tm_zb, 0, row, lane * C::CPI);
-          else if (lane == C::NITEM)
-            tma_prefetch_l2_2d(&tm_kpe, 0, row);
-        }
-      };
       if (ntiles > 0) {
         // first lap: the query tile (chunk-major boxes of CPI chunks, moved into Tensor
         // Memory by the softmax warps, which then free the slots) and q_pe in its own region
@@ -412,14 +388,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           __syncwarp();
         }
-        for (int t = 0; t < PF; ++t) prefetch_tile(t);
       }
       for (int t = 0; ok && t < ntiles; ++t) {
         const int key0 = kstart + t * TK;
         const bool two = kend - key0 > HK;  // the tile's second page holds keys of the chunk
         const int row0 = cache_row(p, bi, key0);
         const int row1 = (PAGED && two) ? cache_row(p, bi, key0 + HK) : 0;
-        prefetch_tile(t + PF);
         for (int it = 0; it < C::NITEM; ++it) {
           const int slot = rp.slot;
           const uint32_t prev = rp.phase ^ 1u;

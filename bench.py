@@ -326,6 +326,16 @@ def main():
         with torch.cuda.graph(g2, stream=stream):
             step(r, ("decode",))
         dgraphs.append(g2)
+    # the same steps back to back: one graph per rotation (a step on each input set in
+    # turn), so that programmatic dependent launch also overlaps consecutive steps, as
+    # inside a graph of a whole decode step; reported beside the one-step graphs
+    rot, drot = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(rot, stream=stream):
+        for r in range(NBUF):
+            step(r)
+    with torch.cuda.graph(drot, stream=stream):
+        for r in range(NBUF):
+            step(r, ("decode",))
     launches_per_step = 3 + (1 if nsplit > 1 else 0)
 
     def timed(gs, k_steps, w_steps):
@@ -357,6 +367,9 @@ def main():
         total_ms = timed(graphs, args.steps, args.warmup)
     dec_steps = max(args.steps, 500)
     dec_ms = timed(dgraphs, dec_steps, max(3, args.warmup // 4))
+    b2b_reps = max(dec_steps // NBUF, 100)
+    b2b_ms = timed([rot] * NBUF, b2b_reps, 3) / (b2b_reps * NBUF)
+    dec_b2b_ms = timed([drot] * NBUF, b2b_reps, 3) / (b2b_reps * NBUF)
 
     def per_call(gs, n):
         """Per-replay durations (an event pair around each replay): median, p10, p90."""
@@ -555,6 +568,8 @@ def main():
         "step_breakdown": {
             "pipeline_us": ms_per_step * 1e3,
             "latent_call_us": dec_s * 1e6,
+            "back_to_back": {"pipeline_us": b2b_ms * 1e3, "latent_call_us": dec_b2b_ms * 1e3,
+                             "graphs": f"one graph of {NBUF} steps (one per input set), replayed {b2b_reps} times"},
             "pipeline_per_call": step_dist,
             "latent_per_call": dec_dist,
             "pipeline_tflops": (f_core + 2 * f_proj) / step_s / 1e12,
@@ -671,7 +686,8 @@ def extras(dev, stream, hbm, tfl):
     def time_calls(fns, n=100, w=6):
         """Seconds per call: one CUDA graph per input set (captured after an eager
         warm-up call), replayed round-robin, an event pair around every replay on
-        the stream. Returns the mean; the per-call median, p10 and p90 are kept in
+        the stream. Returns the mean; the per-call median, p10 and p90, and the mean
+        per call with all input sets' calls back to back in one graph, are kept in
         `dist` for the caller's record."""
         with torch.cuda.stream(stream):
             for f in fns:
@@ -697,6 +713,23 @@ def extras(dev, stream, hbm, tfl):
         per = [ev[i].elapsed_time(ev[i + 1]) * 1e-3 for i in range(n)]
         dist.clear()
         dist.update(distribution_us(per))
+        # the same calls back to back in one graph (one call per input set), so that
+        # programmatic dependent launch overlaps consecutive calls as inside a larger graph
+        g_all = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_all, stream=stream):
+            for f in fns:
+                f()
+        reps = max(2, n // len(fns))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g_all.replay()
+            e0.record(stream)
+            for _ in range(reps):
+                g_all.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        dist["back_to_back_us"] = e0.elapsed_time(e1) * 1e3 / (reps * len(fns))
+        del g_all
         return ev[0].elapsed_time(ev[n]) / n * 1e-3
 
     dist = {}

@@ -211,11 +211,8 @@ __device__ __forceinline__ bool gqa_segment(const GqaParams& p, const CUtensorMa
       tma_load_3d(kdst, tm_k, 0, g, row0, &full[stage]);
       tma_load_3d(kdst + C::K_LOAD, tm_v, 0, g, row0, &full[stage]);
     } else {
-#pragma unroll
-      for (int kb = 0; kb < DK / 64; ++kb) tma_load_3d(kdst + kb * kTileBlk, tm_k, kb * 64, g, row0, &full[stage]);
-#pragma unroll
-      for (int kb = 0; kb < DV / 64; ++kb)
-        tma_load_3d(kdst + C::K_TILE + kb * kTileBlk, tm_v, kb * 64, g, row0, &full[stage]);
+      tma_load_4d(kdst, tm_k, 0, row0, 0, g, &full[stage]);
+      tma_load_4d(kdst + C::K_TILE, tm_v, 0, row0, 0, g, &full[stage]);
     }
   };
 
@@ -724,7 +721,11 @@ cudaError_t launch_gqa_dm(const GqaParams& p, int nsplit, int hkv, int b, int ba
   if (cudaError_t e = ensure_smem_limit(gqa_split_kernel<DK, DV, MT, FP8>, C::SMEM, split_attr)) return e;
   if (cudaError_t e = ensure_smem_limit(gqa_balanced_kernel<DK, DV, MT, FP8>, C::SMEM, balanced_attr)) return e;
   // K and V as [tokens, KV heads, width] (contiguous: tokens = b x capacity; paged:
-  // pages x 64), read in boxes of [64 tokens, 1 head, 64 dims]
+  // pages x 64). bf16: viewed as {64 values, tokens, width / 64 chunks, KV heads}
+  // (strides: token hkv*width*2 B, chunk 128 B, head width*2 B), so that one box {64, 64
+  // tokens, all chunks, 1 head} per tile lands chunk-major with 128-byte swizzled rows
+  // (one request per tile instead of one per 64-dim chunk: 0.5-0.7 % faster on the
+  // paged d = 256 shapes). FP8: byte boxes of one head's 64 tokens, as set out below.
   CUtensorMap tk, tv;
   {
     const uint64_t tokens = p.paged ? (uint64_t)p.num_pages * kTileKeys : (uint64_t)p.b * p.capacity;
@@ -743,9 +744,14 @@ cudaError_t launch_gqa_dm(const GqaParams& p, int nsplit, int hkv, int b, int ba
       if (!encode_tmap_u8(&tk, p.k, 3, kdims, kstrides, kbox) || !encode_tmap_u8(&tv, p.v, 3, vdims, vstrides, vbox))
         return cudaErrorInvalidValue;
     } else {
-      const cuuint32_t box[3] = {64, 1, kTileKeys};
-      if (!encode_tmap_bf16_sw128(&tk, p.k, 3, kdims, kstrides, box) ||
-          !encode_tmap_bf16_sw128(&tv, p.v, 3, vdims, vstrides, box))
+      const cuuint32_t kbox4[4] = {64, kTileKeys, (cuuint32_t)(DK / 64), 1};
+      const cuuint32_t vbox4[4] = {64, kTileKeys, (cuuint32_t)(DV / 64), 1};
+      const cuuint64_t kdims4[4] = {64, (cuuint64_t)tokens, (cuuint64_t)(DK / 64), (cuuint64_t)p.hkv};
+      const cuuint64_t kstrides4[3] = {(cuuint64_t)p.hkv * DK * 2, 128, (cuuint64_t)DK * 2};
+      const cuuint64_t vdims4[4] = {64, (cuuint64_t)tokens, (cuuint64_t)(DV / 64), (cuuint64_t)p.hkv};
+      const cuuint64_t vstrides4[3] = {(cuuint64_t)p.hkv * DV * 2, 128, (cuuint64_t)DV * 2};
+      if (!encode_tmap_bf16_sw128(&tk, p.k, 4, kdims4, kstrides4, kbox4) ||
+          !encode_tmap_bf16_sw128(&tv, p.v, 4, vdims4, vstrides4, vbox4))
         return cudaErrorInvalidValue;
     }
   }

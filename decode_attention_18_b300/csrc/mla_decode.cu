@@ -77,7 +77,7 @@ constexpr int MSG_FLAGS = MSG_ALPHA + BM * 4;  // [4] per-quadrant "a row was re
 constexpr int MSG_BYTES = MSG_FLAGS + 16;
 constexpr int MSG_STRIDE = 34 * 1024;      // 1024-byte aligned message slots
 constexpr int FIN_BYTES = BM * 4;          // [128] float 1/l, sent once at the end
-constexpr int S_NR = 3;                    // S-ring slots (CPI chunks each)
+constexpr int S_NR = 5;                    // S-ring slots (CPI chunks each)
 constexpr int O_NR = 4;                    // O-ring slots
 constexpr int SB0 = 256;                   // first S buffer column (Qz holds columns 0 .. k/2-1)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -97,14 +97,17 @@ template <int KL, int P>
 struct MlaCfg {
   static constexpr int NBL = KL / 64;                   // latent chunks per tile (= query boxes)
   static constexpr int NCH = NBL + 1;                   // + the RoPE chunk
-  // chunks per S-ring item: each wait / commit of the ring costs ~250 cycles of the issuing
-  // warp, so an item carries 12 MMAs (3 chunks x 4 k-steps) where the tile allows
-  static constexpr int CPI = NCH % 3 == 0 ? 3 : NCH;
-  static constexpr int NITEM = NCH / CPI;               // S-ring items per tile
+  // chunks per S-ring item: two, in five 32 KB slots. Each wait / commit of the ring costs
+  // ~250 cycles of the issuing warp, but finer items keep more of the ring in flight:
+  // against three chunks in three slots this measured 52.7 vs 53.5 us at s = 1 (267 vs
+  // 268 us at s = 8), and one 80 KB item of five chunks in two slots 55.4 / 295 us. At
+  // k = 512 the RoPE chunk forms the tile's last item on its own.
+  static constexpr int CPI = 2;
+  static constexpr int NITEM = (NCH + CPI - 1) / CPI;   // S-ring items per tile
   static constexpr int S_ITEM = CPI * CHUNK;
   static constexpr int QS = (NBL + CPI - 1) / CPI;      // ring slots of the query lap
   static constexpr int LAT0 = NBL < CPI ? NBL : CPI;    // latent chunks of a full S-ring item
-  static constexpr int LATL = NBL - (NITEM - 1) * CPI;  // latent chunks of a tile's last item (+ RoPE)
+  static constexpr int LATL = NBL - (NITEM - 1) * CPI;  // latent chunks of a tile's last item (+ RoPE; may be 0)
   static constexpr int PE_ROW = P * 2;                  // bytes per RoPE row
   static constexpr uint32_t PE_SWZ = PE_ROW == 128 ? kSw128 : (PE_ROW == 64 ? kSw64 : kSw32);
   static constexpr int PE_HALF = HK * PE_ROW;           // one RoPE box (64 keys)
@@ -125,7 +128,7 @@ struct MlaCfg {
   static constexpr int OFF_BAR = OFF_RED + 6 * BM * 4;  // same offset in both CTAs
   static constexpr int SMEM = OFF_BAR + 512;
   static_assert(KL % 64 == 0 && KL / 2 <= SB0 && KL % ON == 0 && ON % 16 == 0 && ON <= 256, "latent width");
-  static_assert(NCH % CPI == 0 && 2 * CPI <= 8 && QS <= S_NR && LATL >= 1, "S-ring items");
+  static_assert(2 * CPI <= 16 && QS <= S_NR && LATL >= 0, "S-ring items");
   static_assert(P % 16 == 0 && PE_ROW <= 128, "rope width");
   static_assert(OCOLS % 32 == 0 && (OCOLS / 8 <= 32) && 32 % (OCOLS / 8) == 0, "row-warp columns");
   static_assert(NSMW * 32 * OCOLS * 2 <= O_NR * O_ITEM, "epilogue staging");
@@ -210,7 +213,8 @@ struct RingPos {
 //           box {64, 128, LAT0}: one box per query-lap slot, chunk-major as the MMAs read it
 //   tm_qpe  q_pe [rows, p], box [128 rows, p]
 //   tm_za / tm_zb   contiguous cache: Z viewed like Qz, boxes {64, 128, LAT0} / {64, 128, LATL}
-//           (one box per S-ring item); paged pool: Z [rows, k] with boxes [64 rows, 64] (one
+//           (one box per S-ring item; tm_zb unused when the last item is the RoPE chunk
+//           alone); paged pool: Z [rows, k] with boxes [64 rows, 64] (one
 //           box per chunk and page), tm_zb unused
 //   tm_kpe  K_pe [rows, p], box [128 rows, p] (contiguous) or [64 rows, p] (paged)
 //   tm_zo   Z viewed like Qz, box {64, 64, ON/64}: one [64 keys x ON columns] O-ring item
@@ -405,14 +409,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const bool has_pe = it == C::NITEM - 1;  // the RoPE chunk is the tile's last
           const uint32_t base = sb + C::OFF_SRING + slot * C::S_ITEM;
           if constexpr (PAGED) {
-            const int lb = (ic & 3) * 8;  // first issuing lane of this item
+            const int lb = (ic & 1) * 16;  // first issuing lane of this item
             last[slot] = ic++;
             const uint32_t bytes =
-                ((has_pe ? (C::CPI - 1) * HALF_BOX + C::PE_HALF : C::CPI * HALF_BOX)) * (two ? 2 : 1);
+                ((has_pe ? C::LATL * HALF_BOX + C::PE_HALF : C::CPI * HALF_BOX)) * (two ? 2 : 1);
             if (lane == lb) mbar_expect_tx(&bars[B_FULL + slot], bytes);
             __syncwarp();
             const int k = lane - lb;  // box k: chunk it*CPI + k/2 of the tile, page k % 2
-            if (k >= 0 && k < 2 * C::CPI && (two || (k & 1) == 0)) {
+            if (k >= 0 && k < 2 * C::CPI && (two || (k & 1) == 0) && it * C::CPI + k / 2 <= C::NBL) {
               const int c = it * C::CPI + k / 2;
               const bool pe = c == C::NBL;
               const uint32_t dst = base + (k / 2) * CHUNK + (k & 1) * (pe ? C::PE_HALF : HALF_BOX);
@@ -430,7 +434,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int lat = has_pe ? C::LATL : C::LAT0;
             if (lane == lb) {
               mbar_expect_tx(&bars[B_FULL + slot], lat * CHUNK + (has_pe ? BM * C::PE_ROW : 0));
-              tma_load_3d(base, has_pe ? &tm_zb : &tm_za, 0, row0, it * C::CPI, &bars[B_FULL + slot]);
+              if (lat > 0) tma_load_3d(base, has_pe ? &tm_zb : &tm_za, 0, row0, it * C::CPI, &bars[B_FULL + slot]);
             }
             __syncwarp();
             if (has_pe && lane == lb + 1) tma_load_2d(base + lat * CHUNK, &tm_kpe, 0, row0, &bars[B_FULL + slot]);
@@ -479,7 +483,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int cc = 0; cc < C::CPI; ++cc) {
               const int j = it * C::CPI + cc;
               const uint64_t so = (uint64_t)((slot * C::S_ITEM + cc * CHUNK) >> 4);
-              if (j < C::NBL) {
+              if (j > C::NBL) {
+                // past the RoPE chunk: nothing in this part of the item
+              } else if (j < C::NBL) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                   tc_mma_ts(d_s, tmem + j * 32 + kk * 8, dring + so + 2 * kk, idS, (j | kk) ? 1u : 0u);
@@ -942,7 +948,7 @@ cudaError_t launch_klp(const MlaLaunch& a, cudaStream_t stream) {
     ok = ok && make_map(&tza, a.z, krows, KL, HK, 64) && make_map(&tkpe, a.k_pe, krows, P, HK, P);
     tzb = tza;
   } else {
-    ok = ok && make_chunk_map(&tza, a.z, krows, KL, TK, C::LAT0) && make_chunk_map(&tzb, a.z, krows, KL, TK, C::LATL) &&
+    ok = ok && make_chunk_map(&tza, a.z, krows, KL, TK, C::LAT0) && make_chunk_map(&tzb, a.z, krows, KL, TK, C::LATL > 0 ? C::LATL : 1) &&
          make_map(&tkpe, a.k_pe, krows, P, TK, P);
   }
   if (!ok) return cudaErrorInvalidValue;

@@ -99,9 +99,10 @@ struct MlaCfg {
   static constexpr int NCH = NBL + 1;                   // + the RoPE chunk
   // chunks per S-ring item: two, in five 32 KB slots. Each wait / commit of the ring costs
   // ~250 cycles of the issuing warp, but finer items keep more of the ring in flight:
-  // against three chunks in three slots this measured 52.7 vs 53.5 us at s = 1 (267 vs
-  // 268 us at s = 8), and one 80 KB item of five chunks in two slots 55.4 / 295 us. At
-  // k = 512 the RoPE chunk forms the tile's last item on its own.
+  // against three chunks in three slots this measured 52.9 vs 53.5 us at s = 1 and 268
+  // vs 269 us at s = 8 (s = 4, 32 and 64 lose 1.5-4 %), and one 80 KB item of five
+  // chunks in two slots 55.4 / 295 us. At k = 512 the RoPE chunk forms the tile's last
+  // item on its own.
   static constexpr int CPI = 2;
   static constexpr int NITEM = (NCH + CPI - 1) / CPI;   // S-ring items per tile
   static constexpr int S_ITEM = CPI * CHUNK;

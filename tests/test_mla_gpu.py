@@ -119,6 +119,17 @@ def test_edge_lengths():
     assert torch.all(torch.isneginf(lse[0]))
 
 
+@pytest.mark.parametrize("b,h,s,seqlens", [
+    (2, 64, 2, [190, 66]),        # two row tiles per sequence; a last tile of 2 keys (one page)
+    (3, 16, 8, [129, 64, 300]),   # s=8: a page-sized sequence and a 1-key last tile
+])
+def test_paged_mtp(b, h, s, seqlens):
+    """Paged latent cache with s > 1 new tokens (causal among them): the producer's
+    per-page boxes, the RoPE chunk's own ring item and the causal limits together."""
+    inp = make(b, h, 128, 512, 64, s, seqlens, paged=True, seed=21)
+    check(inp, forward(inp), what=f"paged b{b} h{h} s{s}")
+
+
 def test_paged_vs_oracle_and_bitwise_contiguous():
     import decode_attention_18_b300 as da
 
